@@ -1,0 +1,129 @@
+"""CPU oracle for the complex SSD — TEST INFRASTRUCTURE ONLY.
+
+Plain double-precision C (``cssd_oracle.c``) behind a ctypes wrapper.  Only the
+tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg may
+import this package; the CUDA library and its Python binding never do.
+
+Inputs are the float32 / complex64 arrays of ``complex_valued_state_gb300.workloads``
+(promoted exactly to double here); outputs are complex128 / float64.
+
+Pins: every function here is checked in ``tests/test_oracle.py`` against
+results fixed independently of this code (closed forms, brute-force sums,
+special cases and the numbers the pages print).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "cssd_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc (OpenMP over independent (batch, head) pairs)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-std=c11", "-fcx-limited-range", "-fPIC", "-shared", "-fopenmp",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            build()
+            lib = ctypes.CDLL(_LIB)
+            i64, dp = ctypes.c_int64, ctypes.c_void_p
+            lib.oracle_threads.restype = ctypes.c_int
+            lib.oracle_cssd_naive.argtypes = [i64] * 5 + [dp] * 9
+            lib.oracle_cssd_step.argtypes = [i64] * 4 + [dp] * 8
+            lib.oracle_cssd_chunked.argtypes = [i64] * 6 + [dp] * 8
+            lib.oracle_geom_closed_form.argtypes = [i64] * 5 + [dp] * 10
+            for f in (lib.oracle_cssd_naive, lib.oracle_cssd_step, lib.oracle_cssd_chunked,
+                      lib.oracle_geom_closed_form):
+                f.restype = None
+            _lib = lib
+    return _lib
+
+
+def _c(a):
+    return np.ascontiguousarray(a, dtype=np.complex128)
+
+
+def _r(a):
+    return np.ascontiguousarray(a, dtype=np.float64)
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data
+
+
+def threads() -> int:
+    """OpenMP threads the oracle uses (OMP_NUM_THREADS, else all cores)."""
+    return int(_load().oracle_threads())
+
+
+def cssd_naive(x, dt, A, B, C, D, h0=None, want_state=True):
+    """Sequential recurrence; returns (y [Bz,T,H,P], h_final [Bz,H,N,P])."""
+    lib = _load()
+    x, dt, A, B, C, D = _c(x), _r(dt), _c(A), _c(B), _c(C), _r(D)
+    Bz, T, H, P = x.shape
+    N = B.shape[-1]
+    h0 = None if h0 is None else _c(h0)
+    y = np.empty((Bz, T, H, P), np.complex128)
+    hf = np.empty((Bz, H, N, P), np.complex128) if want_state else None
+    lib.oracle_cssd_naive(Bz, T, H, N, P, _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(h0),
+                          _p(y), _p(hf))
+    return y, hf
+
+
+def cssd_step(h, x, dt, A, B, C, D):
+    """One decode token; returns (h_new [Bz,H,N,P], y [Bz,H,P])."""
+    lib = _load()
+    h = _c(h).copy()
+    x, dt, A, B, C, D = _c(x), _r(dt), _c(A), _c(B), _c(C), _r(D)
+    Bz, H, N, P = h.shape
+    y = np.empty((Bz, H, P), np.complex128)
+    lib.oracle_cssd_step(Bz, H, N, P, _p(h), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(y))
+    return h, y
+
+
+def cssd_chunked(x, dt, A, B, C, D, chunk: int):
+    """Chunkwise decomposition (theorem form); returns (y, h_final)."""
+    lib = _load()
+    x, dt, A, B, C, D = _c(x), _r(dt), _c(A), _c(B), _c(C), _r(D)
+    Bz, T, H, P = x.shape
+    N = B.shape[-1]
+    y = np.empty((Bz, T, H, P), np.complex128)
+    hf = np.empty((Bz, H, N, P), np.complex128)
+    lib.oracle_cssd_chunked(Bz, T, H, N, P, int(chunk), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D),
+                            _p(y), _p(hf))
+    return y, hf
+
+
+def geom_closed_form(h0, x, dt, A, B, C, D, nsteps: int):
+    """Constant input held for `nsteps` decode steps from h0, in closed form.
+
+    Returns (h_n [Bz,H,N,P], y_n [Bz,H,P], y_inf [Bz,H,P])."""
+    lib = _load()
+    h0 = _c(h0)
+    x, dt, A, B, C, D = _c(x), _r(dt), _c(A), _c(B), _c(C), _r(D)
+    Bz, H, N, P = h0.shape
+    hn = np.empty_like(h0)
+    yn = np.empty((Bz, H, P), np.complex128)
+    yinf = np.empty((Bz, H, P), np.complex128)
+    lib.oracle_geom_closed_form(Bz, H, N, P, int(nsteps), _p(h0), _p(x), _p(dt), _p(A), _p(B), _p(C),
+                                _p(D), _p(hn), _p(yn), _p(yinf))
+    return hn, yn, yinf
