@@ -1,0 +1,422 @@
+#!/usr/bin/env python
+"""Benchmark: complex SSD tokens/s (B*T*H) on GB300.
+
+One step = one pass of the whole hot path on the mamba2_layer workload
+(batch 4, T 2048, 24 heads, N = P = 64, chunk 64): the chunked forward over
+the batch (discretise, chunk decays, intra-chunk contraction, chunk states,
+inter-chunk scan, output combine) followed by one decode step that continues
+from the forward's final state.  Units per step: Bz*T*H + Bz*H token-heads.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+N > 1 runs under torch.distributed.run, one independent replica per rank
+(weak scaling, no collective on the data path).  Rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "complex SSD scan tokens/s (B·T·H) at 1 GB300; % tensor-pipe / % HBM roofline"
+UNIT = "tokens/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+            time.sleep(0.25)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[4:8]):
+                if v.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------- traffic record
+def kernel_source_sha() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "complex_valued_state_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, units: int):
+    """DRAM bytes per launch from a committed ncu summary, if taken on this source."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec or rec.get("source_sha") != kernel_source_sha():
+        return None
+    return float(rec["bytes_per_unit"]) * units
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local):
+    import torch
+
+    from complex_valued_state_gb300 import build as cbuild
+    from complex_valued_state_gb300 import cssd
+    from complex_valued_state_gb300 import workloads as wl
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+    if rank == 0 or world == 1:
+        cbuild.build()
+    if pg:
+        pg.barrier()
+    cssd.load()
+
+    w = wl.MAMBA2_LAYER
+    Bz, T, H, N, P, ch = w.batch, w.seqlen, w.nheads, w.dstate, w.headdim, w.chunk
+    host = wl.make_inputs(w, seed=w.seed + rank)
+    tok = wl.decode_token(w.with_(kind="decode"), rank)
+    keys = ("x", "dt", "A", "B", "C", "D")
+    g = {k: torch.from_numpy(host[k]).to(dev) for k in keys}
+    gt = {k: torch.from_numpy(tok[k]).to(dev) for k in ("x", "dt", "B", "C")}
+    y = torch.empty((Bz, T, H, P), dtype=torch.complex64, device=dev)
+    h = torch.empty((Bz, H, N, P), dtype=torch.complex64, device=dev)
+    y1 = torch.empty((Bz, H, P), dtype=torch.complex64, device=dev)
+    ws = torch.empty(cssd.workspace_bytes(Bz, T, H, N, P, ch), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    units = Bz * T * H + Bz * H
+    launches = cssd.forward_launches(Bz, T, H, N, P, ch) + 1
+
+    def step():
+        cssd.chunked_forward(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk=ch, y=y, h_final=h, workspace=ws)
+        cssd.step(h, gt["x"], gt["dt"], g["A"], gt["B"], gt["C"], g["D"], y=y1)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    # Per-launch events around the dominant kernel (recorded by the library on
+    # this stream), plus events around the whole timed region.
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for e in kb + ke:  # creates the events; the library re-records them later
+        e.record(stream)
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        if pg:
+            pg.barrier()
+        torch.cuda.synchronize(dev)
+        t0.record(stream)
+        for i in range(args.steps):
+            cssd.profile_events(kb[i], ke[i])
+            step()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        cssd.profile_events(None, None)
+        if pg:
+            pg.barrier()
+    ms = t0.elapsed_time(t1) / args.steps
+    k_ms = sum(kb[i].elapsed_time(ke[i]) for i in range(args.steps)) / args.steps
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    value = world * units / (ms / 1e3)
+
+    # end to end: pinned host inputs in, results out, every step
+    pin = {k: torch.from_numpy(host[k]).pin_memory() for k in ("x", "dt", "B", "C")}
+    pint = {k: torch.from_numpy(tok[k]).pin_memory() for k in ("x", "dt", "B", "C")}
+    y_host = torch.empty(y.shape, dtype=y.dtype).pin_memory()
+    y1_host = torch.empty(y1.shape, dtype=y1.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in list(pin.values()) + list(pint.values()))
+    d2h = y_host.numel() * y_host.element_size() + y1_host.numel() * y1_host.element_size()
+
+    def e2e_step():
+        for k in pin:
+            g[k].copy_(pin[k], non_blocking=True)
+        for k in pint:
+            gt[k].copy_(pint[k], non_blocking=True)
+        step()
+        y_host.copy_(y, non_blocking=True)
+        y1_host.copy_(y1, non_blocking=True)
+
+    for _ in range(max(1, args.warmup // 2)):
+        e2e_step()
+    torch.cuda.synchronize(dev)
+    if pg:
+        pg.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(3, args.steps // 2)
+    e0.record(stream)
+    for _ in range(e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    e_ms = e0.elapsed_time(e1) / e_steps
+    if pg:
+        t = torch.tensor([e_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        e_ms = float(t.item())
+
+    decode = None
+    if not args.no_decode:
+        decode = bench_decode(args, dev)
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    hbm, peak_kind = peaks()
+    fwd_units = Bz * T * H
+    alg_bytes = fwd_units * (8 * P + 16 * N + 4 + 8 * P)  # x, B, C, dt in; y out
+    achieved = alg_bytes / (k_ms / 1e3) / 1e9
+    roof = {"bound": "hbm", "kernel": "chunk_output", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
+            "traffic": recorded_traffic("chunk_output", fwd_units), "kernel_ms": round(k_ms, 5),
+            "alg_bytes_per_launch": alg_bytes}
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": f"mamba2_layer prefill Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch} + 1 decode token",
+                   "batch": Bz, "seqlen": T, "nheads": H, "dstate": N, "headdim": P, "chunk": ch,
+                   "units_per_step": units, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (%.2f GB read+written per step)" % (alg_bytes / 1e9)},
+        "roofline": roof,
+        "e2e": {"value": round(world * units / (e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 5)},
+        "gpu_launches": launches * args.steps,
+        "clocks": clk.summary(),
+    }
+    if decode:
+        out["decode"] = decode
+    if world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(host, tok)
+    print(json.dumps(out), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def bench_decode(args, dev):
+    """Decode workload (batch 256, 32 heads, N 128, P 64): one token per call."""
+    import torch
+
+    from complex_valued_state_gb300 import cssd
+    from complex_valued_state_gb300 import workloads as wl
+
+    w = wl.DECODE
+    fx = wl.decode_fixed(w)
+    h = torch.from_numpy(fx["h"]).to(dev)
+    A, D = torch.from_numpy(fx["A"]).to(dev), torch.from_numpy(fx["D"]).to(dev)
+    toks = []
+    for s in range(4):
+        t = wl.decode_token(w, s)
+        toks.append({k: torch.from_numpy(t[k]).to(dev) for k in t})
+    y = torch.empty((w.batch, w.nheads, w.headdim), dtype=torch.complex64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for i in range(max(3, args.warmup)):
+        t = toks[i % 4]
+        cssd.step(h, t["x"], t["dt"], A, t["B"], t["C"], D, y=y)
+    torch.cuda.synchronize(dev)
+    n = max(20, 5 * args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n):
+        t = toks[i % 4]
+        cssd.step(h, t["x"], t["dt"], A, t["B"], t["C"], D, y=y)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    us = e0.elapsed_time(e1) * 1e3 / n
+    units = w.batch * w.nheads
+    N, P = w.dstate, w.headdim
+    alg = units * (2 * 8 * N * P + 8 * P + 16 * N + 4 + 8 * P)  # state read+write, x, B, C, dt, y
+    hbm, kind = peaks()
+    gbs = alg / (us / 1e6) / 1e9
+    return {"workload": f"decode Bz{w.batch} H{w.nheads} N{N} P{P}, one token per call",
+            "value": round(units / (us / 1e6), 1), "unit": UNIT, "us_per_step": round(us, 3), "steps": n,
+            "roofline": {"bound": "hbm", "kernel": "step", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+                         "frac": round(gbs / hbm, 4), "peak_kind": kind,
+                         "traffic": recorded_traffic("step", units), "alg_bytes_per_launch": alg}}
+
+
+# ---------------------------------------------------------------- CPU oracle
+def _oracle_step(o, arrays, tok_arrays):
+    y, hf = o.cssd_naive(*arrays)
+    o.cssd_step(hf, *tok_arrays)
+
+
+def _oracle_inputs(host, tok):
+    c = lambda a: np.ascontiguousarray(a, dtype=np.complex128)
+    r = lambda a: np.ascontiguousarray(a, dtype=np.float64)
+    arrays = (c(host["x"]), r(host["dt"]), c(host["A"]), c(host["B"]), c(host["C"]), r(host["D"]))
+    tok_arrays = (c(tok["x"]), r(tok["dt"]), c(host["A"]), c(tok["B"]), c(tok["C"]), r(host["D"]))
+    return arrays, tok_arrays
+
+
+def cpu_baseline(host, tok, budget_s: float = 12.0):
+    """The oracle as it stands on this host's cores, on the same workload."""
+    import oracle
+
+    oracle.build()
+    arrays, tok_arrays = _oracle_inputs(host, tok)
+    Bz, T, H, _ = host["x"].shape
+    units = Bz * T * H + Bz * H
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _oracle_step(oracle, arrays, tok_arrays)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 50:
+            break
+    return {"value": round(reps * units / el, 1), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"full mamba2_layer step (prefill + 1 decode token) x{reps}, {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """Reference arm: the CPU oracle, timed as it stands on the host cores."""
+    if rank != 0:
+        return
+    import oracle
+
+    from complex_valued_state_gb300 import workloads as wl
+
+    oracle.build()
+    w = wl.MAMBA2_LAYER
+    host = wl.make_inputs(w)
+    tok = wl.decode_token(w.with_(kind="decode"), 0)
+    arrays, tok_arrays = _oracle_inputs(host, tok)
+    Bz, T, H = w.batch, w.seqlen, w.nheads
+    # bounded sample per step: a slice of heads, sized to keep the run to minutes
+    hs = max(1, H // 6)
+    sub = tuple(a[:, :, :hs] if a.ndim == 4 or a.ndim == 3 else a[:hs] for a in arrays)
+    sub_tok = tuple(a[:, :hs] if a.ndim >= 2 else a[:hs] for a in tok_arrays)
+    sub = tuple(np.ascontiguousarray(a) for a in sub)
+    sub_tok = tuple(np.ascontiguousarray(a) for a in sub_tok)
+    units = Bz * T * hs + Bz * hs
+    for _ in range(args.warmup):
+        _oracle_step(oracle, sub, sub_tok)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(oracle, sub, sub_tok)
+    el = time.perf_counter() - t0
+    ms = el * 1e3 / args.steps
+    value = units / (ms / 1e3)
+    out = {"impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+           "config": {"workload": f"mamba2_layer prefill Bz{Bz} T{T} H{H} N{w.dstate} P{w.headdim} chunk{w.chunk} "
+                                  f"+ 1 decode token", "parallelism": "host cores"},
+           "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+                            "sample": f"{hs} of {H} heads, all {Bz} batch rows and {T} tokens, per step"},
+           "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(out), flush=True)
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        run_ours(args, rank, world, local)
+
+
+if __name__ == "__main__":
+    main()

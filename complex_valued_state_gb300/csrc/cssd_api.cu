@@ -1,0 +1,179 @@
+// C ABI entry points of libcssd: argument validation on the host, workspace
+// handling, and the launches.  See include/cssd.h for the contract.
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/cssd.h"
+#include "cssd_internal.h"
+
+namespace {
+
+bool supported_n(int64_t n) { return n == 16 || n == 32 || n == 64 || n == 128; }
+bool supported_p(int64_t p) { return p == 16 || p == 32 || p == 64; }
+bool supported_chunk(int c) { return c == 64 || c == 128; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+constexpr int64_t kMaxGridYZ = 65535;
+constexpr int64_t kMaxInt = 2147483647;
+
+int check_dims(const cssd_dims* d, bool need_seq) {
+    if (!d) return CSSD_ERR_NULL;
+    if (d->batch <= 0 || d->nheads <= 0 || d->dstate <= 0 || d->headdim <= 0) return CSSD_ERR_DIMS;
+    if (need_seq && d->seqlen <= 0) return CSSD_ERR_DIMS;
+    if (!supported_n(d->dstate) || !supported_p(d->headdim)) return CSSD_ERR_UNSUPPORTED;
+    if (d->batch > kMaxGridYZ || d->nheads > kMaxGridYZ) return CSSD_ERR_DIMS;
+    if (d->batch * d->nheads > kMaxInt) return CSSD_ERR_DIMS;
+    if (need_seq && d->seqlen > kMaxInt) return CSSD_ERR_DIMS;
+    return CSSD_OK;
+}
+
+// Device of the stream (or the current device for the default stream).
+int stream_device(cudaStream_t s, int* dev) {
+    if (s == nullptr) return cudaGetDevice(dev) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+    return cudaStreamGetDevice(s, dev) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+}
+
+// The pointer must be device (or managed) memory usable on `dev`.
+int check_device_ptr(const void* p, int dev) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();  // clear the sticky-free error this query may set
+        return CSSD_ERR_DEVICE;
+    }
+    if (at.type == cudaMemoryTypeManaged) return CSSD_OK;
+    if (at.type != cudaMemoryTypeDevice || at.device != dev) return CSSD_ERR_DEVICE;
+    return CSSD_OK;
+}
+
+template <typename... Ts>
+int check_all_device(int dev, Ts... ptrs) {
+    const void* arr[] = {ptrs...};
+    for (const void* p : arr) {
+        if (!p) continue;
+        const int s = check_device_ptr(p, dev);
+        if (s != CSSD_OK) return s;
+    }
+    return CSSD_OK;
+}
+
+}  // namespace
+
+namespace cssd {
+// Measurement hook: events recorded around the dominant kernel of the next
+// forward calls made from this host thread (both NULL = off).
+thread_local cudaEvent_t g_prof_begin = nullptr;
+thread_local cudaEvent_t g_prof_end = nullptr;
+}  // namespace cssd
+
+extern "C" {
+
+int cssd_profile_events(void* ev_begin, void* ev_end) {
+    if ((ev_begin == nullptr) != (ev_end == nullptr)) return CSSD_ERR_NULL;
+    cssd::g_prof_begin = static_cast<cudaEvent_t>(ev_begin);
+    cssd::g_prof_end = static_cast<cudaEvent_t>(ev_end);
+    return CSSD_OK;
+}
+
+const char* cssd_status_string(int status) {
+    switch (status) {
+        case CSSD_OK: return "ok";
+        case CSSD_ERR_NULL: return "a required pointer is NULL";
+        case CSSD_ERR_DIMS: return "a size is zero, negative or too large";
+        case CSSD_ERR_UNSUPPORTED: return "dstate, headdim or chunk outside the supported set";
+        case CSSD_ERR_ALIGN: return "a pointer breaks the alignment rule";
+        case CSSD_ERR_WORKSPACE: return "workspace too small or its allocation failed";
+        case CSSD_ERR_CUDA: return "a CUDA runtime call or kernel launch failed";
+        case CSSD_ERR_DEVICE: return "a pointer is not device memory of the stream's device";
+    }
+    return "unknown status";
+}
+
+size_t cssd_workspace_bytes(const cssd_dims* d, int chunk) {
+    if (check_dims(d, true) != CSSD_OK || !supported_chunk(chunk)) return 0;
+    return cssd::forward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
+}
+
+int cssd_forward_launches(const cssd_dims* d, int chunk) {
+    if (check_dims(d, true) != CSSD_OK || !supported_chunk(chunk)) return 0;
+    return cssd::forward_launches(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
+}
+
+int cssd_chunked_forward(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B,
+                         const void* C, const float* D, void* y, void* h_final, int chunk, void* workspace,
+                         size_t workspace_bytes, cssd_stream_t stream_) {
+    int s = check_dims(d, true);
+    if (s != CSSD_OK) return s;
+    if (!supported_chunk(chunk)) return CSSD_ERR_UNSUPPORTED;
+    if (!x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+        (h_final && !aligned(h_final, 16)) || (workspace && !aligned(workspace, 16)) || !aligned(A, 8) ||
+        !aligned(dt, 4) || !aligned(D, 4))
+        return CSSD_ERR_ALIGN;
+    const size_t need = cssd::forward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
+    if (workspace && workspace_bytes < need) return CSSD_ERR_WORKSPACE;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    if ((s = stream_device(stream, &dev)) != CSSD_OK) return s;
+    if ((s = check_all_device(dev, x, (const void*)dt, A, B, C, (const void*)D, (const void*)y, (const void*)h_final,
+                              (const void*)workspace)) != CSSD_OK)
+        return s;
+
+    void* ws = workspace;
+    if (!ws) {
+        if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return CSSD_ERR_WORKSPACE;
+        }
+    }
+    cssd::FwdArgs a;
+    a.Bz = d->batch;
+    a.T = d->seqlen;
+    a.H = d->nheads;
+    a.N = d->dstate;
+    a.P = d->headdim;
+    a.chunk = chunk;
+    a.x = static_cast<const float2*>(x);
+    a.dt = dt;
+    a.A = static_cast<const float2*>(A);
+    a.B = static_cast<const float2*>(B);
+    a.C = static_cast<const float2*>(C);
+    a.D = D;
+    a.y = static_cast<float2*>(y);
+    a.h_final = static_cast<float2*>(h_final);
+    const cudaError_t e = cssd::launch_forward(a, ws, stream);
+    if (!workspace) cudaFreeAsync(ws, stream);
+    return e == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+}
+
+int cssd_step(const cssd_dims* d, void* h, const void* x, const float* dt, const void* A, const void* B,
+              const void* C, const float* D, void* y, cssd_stream_t stream_) {
+    int s = check_dims(d, false);
+    if (s != CSSD_OK) return s;
+    if (!h || !x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
+    if (!aligned(h, 16) || !aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+        !aligned(A, 8) || !aligned(dt, 4) || !aligned(D, 4))
+        return CSSD_ERR_ALIGN;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    if ((s = stream_device(stream, &dev)) != CSSD_OK) return s;
+    if ((s = check_all_device(dev, (const void*)h, x, (const void*)dt, A, B, C, (const void*)D, (const void*)y)) !=
+        CSSD_OK)
+        return s;
+    cssd::StepArgs a;
+    a.Bz = d->batch;
+    a.H = d->nheads;
+    a.N = d->dstate;
+    a.P = d->headdim;
+    a.h = static_cast<float2*>(h);
+    a.x = static_cast<const float2*>(x);
+    a.dt = dt;
+    a.A = static_cast<const float2*>(A);
+    a.B = static_cast<const float2*>(B);
+    a.C = static_cast<const float2*>(C);
+    a.D = D;
+    a.y = static_cast<float2*>(y);
+    return cssd::launch_step(a, stream) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,53 @@
+// Launchers behind the C ABI (host side).  Arguments are validated by the
+// entry points in cssd_api.cu before any of these is called.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/cssd.h"
+
+namespace cssd {
+
+struct FwdArgs {
+    int64_t Bz, T, H, N, P;
+    int chunk;
+    const float2* x;
+    const float* dt;
+    const float2* A;
+    const float2* B;
+    const float2* C;
+    const float* D;
+    float2* y;
+    float2* h_final;  // may be null
+};
+
+struct StepArgs {
+    int64_t Bz, H, N, P;
+    float2* h;
+    const float2* x;
+    const float* dt;
+    const float2* A;
+    const float2* B;
+    const float2* C;
+    const float* D;
+    float2* y;
+};
+
+// Events the forward records around its dominant kernel (null = off); set by
+// cssd_profile_events for the calling host thread.
+extern thread_local cudaEvent_t g_prof_begin;
+extern thread_local cudaEvent_t g_prof_end;
+
+// Workspace layout of the chunked forward.
+size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
+
+// Kernel launches one forward makes.
+int forward_launches(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
+
+// Each returns cudaSuccess or the launch error.
+cudaError_t launch_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
+cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
+
+}  // namespace cssd

@@ -1,0 +1,196 @@
+"""ctypes binding of libcssd (argument marshalling only).
+
+Every function here takes torch tensors that already live on a CUDA device,
+checks dtype / shape / contiguity, and passes raw pointers and sizes to the C
+ABI declared in ``include/cssd.h``.  All arithmetic runs in the library's
+kernels.  If ``libcssd.so`` is missing the first call raises: there is no CPU
+fallback.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libcssd.so")
+
+CSSD_OK = 0
+STATUS = {
+    0: "CSSD_OK",
+    -1: "CSSD_ERR_NULL",
+    -2: "CSSD_ERR_DIMS",
+    -3: "CSSD_ERR_UNSUPPORTED",
+    -4: "CSSD_ERR_ALIGN",
+    -5: "CSSD_ERR_WORKSPACE",
+    -6: "CSSD_ERR_CUDA",
+    -7: "CSSD_ERR_DEVICE",
+}
+
+# Every symbol include/cssd.h declares.
+EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward", "cssd_step",
+           "cssd_profile_events", "cssd_status_string")
+
+
+class Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int64) for n in ("batch", "seqlen", "nheads", "dstate", "headdim")]
+
+
+class CssdError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({status_string(status)})")
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def load(path: str = LIB_PATH):
+    """Load libcssd.so and declare its signatures (raises if it is not built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(path):
+                raise RuntimeError(f"{path} is not built; run complex_valued_state_gb300.build.build() first")
+            lib = ctypes.CDLL(path)
+            vp, dims_p = ctypes.c_void_p, ctypes.POINTER(Dims)
+            lib.cssd_workspace_bytes.argtypes = [dims_p, ctypes.c_int]
+            lib.cssd_workspace_bytes.restype = ctypes.c_size_t
+            lib.cssd_forward_launches.argtypes = [dims_p, ctypes.c_int]
+            lib.cssd_forward_launches.restype = ctypes.c_int
+            lib.cssd_chunked_forward.argtypes = [dims_p] + [vp] * 8 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
+            lib.cssd_chunked_forward.restype = ctypes.c_int
+            lib.cssd_step.argtypes = [dims_p] + [vp] * 8 + [vp]
+            lib.cssd_step.restype = ctypes.c_int
+            lib.cssd_profile_events.argtypes = [vp, vp]
+            lib.cssd_profile_events.restype = ctypes.c_int
+            lib.cssd_status_string.argtypes = [ctypes.c_int]
+            lib.cssd_status_string.restype = ctypes.c_char_p
+            _lib = lib
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return load().cssd_status_string(int(status)).decode()
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _check(t, name, dtype, shape, device):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.device != device:
+        raise ValueError(f"{name} must be on {device}, got {t.device}")
+
+
+def _stream_handle(stream, device):
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def profile_events(begin=None, end=None):
+    """Record `begin` / `end` (torch.cuda.Event, created with enable_timing and
+    recorded once so that they exist) around the dominant kernel of later
+    forward calls from this thread; None, None = off."""
+
+    def h(e):
+        if e is None:
+            return None
+        if not e.cuda_event:
+            raise ValueError("event not created yet: record it once first")
+        return ctypes.c_void_p(e.cuda_event)
+
+    st = load().cssd_profile_events(h(begin), h(end))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_profile_events")
+
+
+def workspace_bytes(batch: int, seqlen: int, nheads: int, dstate: int, headdim: int, chunk: int) -> int:
+    d = Dims(batch, seqlen, nheads, dstate, headdim)
+    return int(load().cssd_workspace_bytes(ctypes.byref(d), int(chunk)))
+
+
+def forward_launches(batch: int, seqlen: int, nheads: int, dstate: int, headdim: int, chunk: int) -> int:
+    d = Dims(batch, seqlen, nheads, dstate, headdim)
+    return int(load().cssd_forward_launches(ctypes.byref(d), int(chunk)))
+
+
+def chunked_forward(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None, want_state: bool = True,
+                    workspace=None, stream=None):
+    """cssd_chunked_forward on device tensors; returns (y, h_final or None).
+
+    x complex64 [Bz,T,H,P]; dt float32 [Bz,T,H]; A complex64 [H];
+    B, C complex64 [Bz,T,H,N]; D float32 [H].  `workspace` is an optional
+    uint8 device tensor of at least workspace_bytes(...) bytes.
+    """
+    lib = load()
+    dev = x.device
+    Bz, T, H, P = x.shape
+    N = B.shape[-1]
+    c64, f32 = torch.complex64, torch.float32
+    _check(x, "x", c64, (Bz, T, H, P), dev)
+    _check(dt, "dt", f32, (Bz, T, H), dev)
+    _check(A, "A", c64, (H,), dev)
+    _check(B, "B", c64, (Bz, T, H, N), dev)
+    _check(C, "C", c64, (Bz, T, H, N), dev)
+    _check(D, "D", f32, (H,), dev)
+    if y is None:
+        y = torch.empty((Bz, T, H, P), dtype=c64, device=dev)
+    _check(y, "y", c64, (Bz, T, H, P), dev)
+    if h_final is None and want_state:
+        h_final = torch.empty((Bz, H, N, P), dtype=c64, device=dev)
+    if h_final is not None:
+        _check(h_final, "h_final", c64, (Bz, H, N, P), dev)
+    ws_bytes = 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    d = Dims(Bz, T, H, N, P)
+    st = lib.cssd_chunked_forward(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y),
+                                  _ptr(h_final), int(chunk), _ptr(workspace), ctypes.c_size_t(ws_bytes),
+                                  _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_chunked_forward")
+    return y, h_final
+
+
+def step(h, x, dt, A, B, C, D, *, y=None, stream=None):
+    """cssd_step on device tensors: h updated in place; returns y.
+
+    h complex64 [Bz,H,N,P]; x complex64 [Bz,H,P]; dt float32 [Bz,H];
+    A complex64 [H]; B, C complex64 [Bz,H,N]; D float32 [H].
+    """
+    lib = load()
+    dev = h.device
+    Bz, H, N, P = h.shape
+    c64, f32 = torch.complex64, torch.float32
+    _check(h, "h", c64, (Bz, H, N, P), dev)
+    _check(x, "x", c64, (Bz, H, P), dev)
+    _check(dt, "dt", f32, (Bz, H), dev)
+    _check(A, "A", c64, (H,), dev)
+    _check(B, "B", c64, (Bz, H, N), dev)
+    _check(C, "C", c64, (Bz, H, N), dev)
+    _check(D, "D", f32, (H,), dev)
+    if y is None:
+        y = torch.empty((Bz, H, P), dtype=c64, device=dev)
+    _check(y, "y", c64, (Bz, H, P), dev)
+    d = Dims(Bz, 1, H, N, P)
+    st = lib.cssd_step(ctypes.byref(d), _ptr(h), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y),
+                       _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_step")
+    return y

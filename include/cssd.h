@@ -1,0 +1,132 @@
+/*
+ * cssd.h — C ABI of libcssd, the complex SSD (complex-valued diagonal state
+ * space) forward and decode step for NVIDIA GB300 (sm_103a).
+ *
+ * The operation (per batch b and head h, state h_t in C^{N x P}):
+ *     a_t = exp(softplus(dt_t) * A)          softplus on the real dt, then the
+ *                                            complex exponential
+ *     h_t = a_t h_{t-1} + B_t x_t^T          outer product, no conjugate
+ *     y_t = C_t^T h_t + D x_t                readout after the update, sum over
+ *                                            the N state rows, no conjugate
+ * Sources: "Complex-Valued State Spaces" (Mamba-3-Lite docs), sections
+ * "Discretization" and "The discretization" (the sequential loop and
+ * exp(softplus(dt) A)); "SSD Theory" section 2 (the recurrence) and the
+ * readout C^T h + D x of the workload statement.  The forward evaluates it in
+ * the chunkwise form of "The Chunkwise Complex SSD Algorithm" sections 4.1-4.5
+ * (pad, within-chunk cumsum, segment matrix, per-chunk states, inter-chunk
+ * scan, output combine), with the inter-chunk state taken from the theorem of
+ * "SSD Theory" section 4.5.
+ *
+ * Conventions shared by every entry point:
+ *   - Complex numbers are complex64: interleaved [re, im] float32 pairs.
+ *   - Arrays are dense and row-major with the shapes given per argument.
+ *   - Every array pointer is a DEVICE pointer on the device that `stream`
+ *     belongs to (the current device when stream is NULL).  The caller owns
+ *     all memory; apart from the measurement hook cssd_profile_events the
+ *     library keeps no state between calls.
+ *   - Execution is asynchronous on `stream`.  Argument errors are detected on
+ *     the host before anything is launched and leave every output untouched.
+ *     A launch failure returns CSSD_ERR_CUDA.  Faults during execution surface
+ *     at the caller's next synchronisation.  Nothing aborts or traps.
+ *   - Alignment: x, B, C, y, h, h_final and the workspace must be 16-byte
+ *     aligned; A 8-byte; dt and D 4-byte.
+ *   - Supported sizes: dstate N in {16, 32, 64, 128}; headdim P in {16, 32, 64};
+ *     chunk in {64, 128}; seqlen >= 1 (any length; the last chunk is padded
+ *     internally); batch >= 1; nheads >= 1.  Other values return
+ *     CSSD_ERR_UNSUPPORTED (or CSSD_ERR_DIMS for non-positive sizes).
+ *   - y must not alias any input.
+ */
+#ifndef CSSD_H
+#define CSSD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); NULL is the legacy default stream. */
+typedef struct CUstream_st* cssd_stream_t;
+
+typedef enum {
+    CSSD_OK = 0,
+    CSSD_ERR_NULL = -1,        /* a required pointer is NULL */
+    CSSD_ERR_DIMS = -2,        /* a size is zero/negative or too large */
+    CSSD_ERR_UNSUPPORTED = -3, /* N, P or chunk outside the supported set */
+    CSSD_ERR_ALIGN = -4,       /* a pointer breaks the alignment rule */
+    CSSD_ERR_WORKSPACE = -5,   /* workspace too small, or allocating it failed */
+    CSSD_ERR_CUDA = -6,        /* a CUDA runtime call or launch failed */
+    CSSD_ERR_DEVICE = -7       /* a pointer is not device memory of the stream's device */
+} cssd_status;
+
+/* Problem sizes.  seqlen is ignored by cssd_step. */
+typedef struct {
+    int64_t batch;   /* Bz */
+    int64_t seqlen;  /* T  */
+    int64_t nheads;  /* H  */
+    int64_t dstate;  /* N  (state rows) */
+    int64_t headdim; /* P  (state columns, the pages' head dimension D) */
+} cssd_dims;
+
+/* Bytes of device workspace cssd_chunked_forward needs for these sizes.
+ * Returns 0 when the sizes or the chunk are invalid. */
+size_t cssd_workspace_bytes(const cssd_dims* dims, int chunk);
+
+/* Chunkwise forward over a whole sequence from a zero initial state.
+ *   x       complex64 [batch, seqlen, nheads, headdim]   token content
+ *   dt      float32   [batch, seqlen, nheads]            raw step (softplus applied inside)
+ *   A       complex64 [nheads]                           per-head rate
+ *   B       complex64 [batch, seqlen, nheads, dstate]    input coupling
+ *   C       complex64 [batch, seqlen, nheads, dstate]    readout
+ *   D       float32   [nheads]                           skip, broadcast over headdim
+ *   y       complex64 [batch, seqlen, nheads, headdim]   output (written)
+ *   h_final complex64 [batch, nheads, dstate, headdim]   state after the last
+ *           token (written); may be NULL.  It is the h that cssd_step
+ *           continues from.
+ *   chunk   chunk length of the decomposition (64 or 128).  The result does
+ *           not depend on it beyond rounding.
+ *   workspace, workspace_bytes: device scratch of at least
+ *           cssd_workspace_bytes(dims, chunk) bytes, owned by the caller and
+ *           not read before it is written.  With workspace == NULL the
+ *           library allocates and frees it stream-ordered on `stream`
+ *           (cudaMallocAsync / cudaFreeAsync).
+ * Returns a cssd_status. */
+int cssd_chunked_forward(const cssd_dims* dims, const void* x, const float* dt, const void* A,
+                         const void* B, const void* C, const float* D, void* y, void* h_final,
+                         int chunk, void* workspace, size_t workspace_bytes, cssd_stream_t stream);
+
+/* Number of kernel launches one cssd_chunked_forward call makes for these
+ * sizes (0 when they are invalid).  Informational, for launch accounting. */
+int cssd_forward_launches(const cssd_dims* dims, int chunk);
+
+/* One decode token for every (batch, head): the same recurrence, one step.
+ *   h   complex64 [batch, nheads, dstate, headdim]  state, read then updated in place
+ *   x   complex64 [batch, nheads, headdim]
+ *   dt  float32   [batch, nheads]
+ *   A   complex64 [nheads]
+ *   B   complex64 [batch, nheads, dstate]
+ *   C   complex64 [batch, nheads, dstate]
+ *   D   float32   [nheads]
+ *   y   complex64 [batch, nheads, headdim]          output (written)
+ * Returns a cssd_status. */
+int cssd_step(const cssd_dims* dims, void* h, const void* x, const float* dt, const void* A,
+              const void* B, const void* C, const float* D, void* y, cssd_stream_t stream);
+
+/* Measurement hook.  ev_begin / ev_end are cudaEvent_t handles created by
+ * the caller on the device in use; every later cssd_chunked_forward call made
+ * from the same host thread records ev_begin on its stream just before the
+ * launch of its dominant kernel and ev_end just after it, so that the caller
+ * can time that kernel alone with cudaEventElapsedTime.  Pass (NULL, NULL) to
+ * turn it off.  This per-thread setting is the library's only state.
+ * Returns CSSD_ERR_NULL if exactly one of the two is NULL. */
+int cssd_profile_events(void* ev_begin, void* ev_end);
+
+/* Static, NUL-terminated description of a status code. */
+const char* cssd_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CSSD_H */

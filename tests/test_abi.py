@@ -1,0 +1,104 @@
+"""The C ABI library on the host: it loads, exports every declared symbol, and
+rejects bad arguments before touching CUDA (no GPU needed, nothing launched)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from complex_valued_state_gb300 import build as cbuild
+from complex_valued_state_gb300 import cssd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "cssd.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cbuild.build()
+    return cssd.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(cssd_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert set(cssd.EXPORTS) <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+        assert ctypes.cast(getattr(lib, n), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for code in cssd.STATUS:
+        s = cssd.status_string(code)
+        assert isinstance(s, str) and s and s != "unknown status"
+    assert cssd.status_string(12345) == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    # states (Bz*H*nc*N*P complex64) plus the per-chunk decay totals, 256-byte rounded
+    got = cssd.workspace_bytes(4, 2048, 24, 64, 64, 64)
+    nc = 32
+    assert got >= 4 * 24 * nc * 64 * 64 * 8
+    assert cssd.workspace_bytes(1, 65, 1, 16, 16, 64) > cssd.workspace_bytes(1, 64, 1, 16, 16, 64)
+    assert cssd.workspace_bytes(1, 64, 1, 16, 16, 96) == 0  # unsupported chunk
+    assert cssd.workspace_bytes(1, 0, 1, 16, 16, 64) == 0  # empty sequence
+    assert cssd.workspace_bytes(1, 64, 1, 48, 16, 64) == 0  # unsupported N
+
+
+def _fwd(lib, dims, ptrs=None, chunk=64, ws=None, ws_bytes=0):
+    p = ptrs or {}
+    args = [p.get(k, 0x10000 + 0x100 * i) for i, k in enumerate(("x", "dt", "A", "B", "C", "D", "y", "h"))]
+    d = None if dims is None else ctypes.byref(cssd.Dims(*dims))
+    return lib.cssd_chunked_forward(d, *[ctypes.c_void_p(a) if a else None for a in args], chunk,
+                                    ctypes.c_void_p(ws) if ws else None, ctypes.c_size_t(ws_bytes), None)
+
+
+def _step(lib, dims, ptrs=None):
+    p = ptrs or {}
+    args = [p.get(k, 0x10000 + 0x100 * i) for i, k in enumerate(("h", "x", "dt", "A", "B", "C", "D", "y"))]
+    d = None if dims is None else ctypes.byref(cssd.Dims(*dims))
+    return lib.cssd_step(d, *[ctypes.c_void_p(a) if a else None for a in args], None)
+
+
+def test_argument_errors_are_caught_on_the_host(lib):
+    ok = (1, 64, 1, 16, 16)
+    assert _fwd(lib, None) == -1
+    assert _fwd(lib, (0, 64, 1, 16, 16)) == -2
+    assert _fwd(lib, (1, 0, 1, 16, 16)) == -2
+    assert _fwd(lib, (1, 64, -3, 16, 16)) == -2
+    assert _fwd(lib, (1, 64, 1, 24, 16)) == -3
+    assert _fwd(lib, (1, 64, 1, 16, 128)) == -3
+    assert _fwd(lib, ok, chunk=32) == -3
+    assert _fwd(lib, ok, {"x": 0}) == -1
+    assert _fwd(lib, ok, {"D": 0}) == -1
+    assert _fwd(lib, ok, {"x": 0x10008}) == -4  # complex64 arrays want 16-byte alignment
+    assert _fwd(lib, ok, {"dt": 0x10102}) == -4
+    assert _fwd(lib, ok, ws=0x900000, ws_bytes=16) == -5
+    assert _fwd(lib, (70000, 64, 1, 16, 16)) == -2  # beyond the grid limit
+    assert _step(lib, None) == -1
+    assert _step(lib, (1, 1, 1, 16, 16), {"h": 0}) == -1
+    assert _step(lib, (1, 1, 1, 16, 8)) == -3
+    assert _step(lib, (1, 1, 1, 16, 16), {"y": 0x10004}) == -4
+
+
+def test_binding_rejects_wrong_dtypes_and_shapes():
+    import torch
+
+    x = torch.zeros((1, 8, 1, 16), dtype=torch.complex64)
+    dt = torch.zeros((1, 8, 1))
+    A = torch.zeros(1, dtype=torch.complex64)
+    B = torch.zeros((1, 8, 1, 16), dtype=torch.complex64)
+    D = torch.zeros(1)
+    with pytest.raises(TypeError):
+        cssd.chunked_forward(x, dt.double(), A, B, B, D)
+    with pytest.raises(ValueError):
+        cssd.chunked_forward(x, dt[:, :4], A, B, B, D)
+    with pytest.raises(ValueError):
+        cssd.chunked_forward(x, dt, A, B.transpose(1, 3), B, D)
