@@ -40,14 +40,22 @@ struct StepArgs {
 extern thread_local cudaEvent_t g_prof_begin;
 extern thread_local cudaEvent_t g_prof_end;
 
-// Workspace layout of the chunked forward.
+// The chunked forward: the fused tensor-core kernel where its shape applies
+// (chunk = dstate = headdim = 64), else the CUDA-core chunk kernels.
 size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
-
-// Kernel launches one forward makes.
 int forward_launches(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
-
-// Each returns cudaSuccess or the launch error.
 cudaError_t launch_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
+
+// CUDA-core chunk kernels (forward_seq.cu).
+size_t seq_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
+cudaError_t launch_seq_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
+
+// Fused tensor-core kernel (forward_tc.cu).
+bool tc_forward_supported(int64_t N, int64_t P, int chunk);
+size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H);
+cudaError_t launch_tc_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
+
+// Decode step (step.cu).
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
 
 }  // namespace cssd

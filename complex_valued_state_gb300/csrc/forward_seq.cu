@@ -182,16 +182,14 @@ cudaError_t launch_n(const FwdArgs& a, float2* S, float2* E, cudaStream_t st) {
 
 }  // namespace
 
-size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
+size_t seq_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
     const int64_t nc = (T + chunk - 1) / chunk;
     const size_t states = (size_t)(Bz * H * nc) * (size_t)(N * P) * sizeof(float2);
     const size_t totals = (size_t)(Bz * H * nc) * sizeof(float2);
     return states + ((totals + 255) / 256) * 256;
 }
 
-int forward_launches(int64_t, int64_t, int64_t, int64_t, int64_t, int) { return 3; }
-
-cudaError_t launch_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
+cudaError_t launch_seq_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     const int64_t nc = (a.T + a.chunk - 1) / a.chunk;
     float2* S = static_cast<float2*>(ws);
     float2* E = S + (size_t)(a.Bz * a.H * nc) * (size_t)(a.N * a.P);

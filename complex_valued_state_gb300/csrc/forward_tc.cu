@@ -1,0 +1,543 @@
+// Fused chunkwise forward on the tcgen05 tensor cores (TF32, fp32 accumulate),
+// for chunk = dstate = headdim = 64.
+//
+// Method ("The Chunkwise Complex SSD Algorithm", Mamba-3-Lite docs, sections
+// 4.2-4.5; "SSD Theory" section 4.5).  For one (batch, head) with
+// A_log_t = softplus(dt_t) A = sp_t (alpha + i beta), write the cumulative
+// log-step inside chunk c as rho_l + i theta_l (inclusive cumsum over the
+// chunk's tokens) and the phase accumulated before the chunk as Phi_c.  With
+// the global phase Theta_t = Phi_c + theta_l, rotate the couplings,
+//     Bt_t = e^{-i Theta_t} B_t,    Ct_t = e^{+i Theta_t} C_t,
+// and the recurrence becomes one with a REAL per-step decay e^{sp_t alpha} on
+// the rotated state ht_t = e^{-i Theta_t} h_t (multiplying through by the
+// unit phase is exact).  Then every decay factor of the chunkwise form is real:
+//     L[l,s]       = exp(rho_l - rho_s) 1[l >= s]        (segment matrix)
+//     Y_diag       = (L o Ct Bt^T) X                      (intra-chunk)
+//     S_c          = sum_l exp(rho_end - rho_l) Bt_l x_l^T (chunk state)
+//     H_{c+1}      = exp(rho_end) H_c + S_c               (inter-chunk)
+//     Y_off        = exp(rho_l) Ct_l H_c                  (carried-in state)
+//     y            = Y_diag + Y_off + D x,   h_final = e^{i Theta_last} H_final
+// so the epilogues scale real and imaginary parts independently.
+//
+// One CTA per (chunk, batch*head), dispatched in chunk-major order through an
+// atomic ticket so that the CTA owning chunk c-1 of a sequence has always
+// started before the CTA owning chunk c waits for its state.  The state is
+// handed over through a two-slot ring in global memory (L2 resident) with a
+// per-sequence release/acquire counter; the wait is bounded.
+//
+// Complex GEMMs run as real ones on stacked operands: with A = Ar + i Ai
+// stored as the three row blocks [-Ai; Ar; Ai] and B as planes Br, Bi,
+//     [Ar; Ai] Br^T + [-Ai; Ar] Bi^T = [Re(A B^T); Im(A B^T)]
+// so one M = 128 accumulator holds the real part in TMEM lanes 0-63 and the
+// imaginary part in lanes 64-127.
+
+#include "cssd_common.cuh"
+#include "cssd_internal.h"
+#include "tcgen05.cuh"
+
+namespace cssd {
+namespace {
+
+constexpr int CH = 64;    // chunk length
+constexpr int NS = 64;    // dstate
+constexpr int PD = 64;    // headdim
+constexpr int NT = 256;   // threads per CTA
+constexpr int RING = 2;   // state slots per sequence
+
+// Shared memory regions (bytes).
+constexpr int STACK_BYTES = 3 * 64 * 64 * 4;  // [-Ai; Ar; Ai], 192 rows x 64 K
+constexpr int PLANE_BYTES = 64 * 64 * 4;      // one 64 x 64 fp32 plane
+constexpr int S1 = 0;                          // F, then Ct, then M, then y staging
+constexpr int S2 = S1 + STACK_BYTES;           // X planes (Xr, Xi)
+constexpr int S3 = S2 + 2 * PLANE_BYTES;       // Bt planes, then H planes
+constexpr int SMEM_BYTES = S3 + 2 * PLANE_BYTES;  // 112 KB
+constexpr int STAGE_LD = 2 * PD + 1;           // y staging row stride (floats)
+static_assert(CH * STAGE_LD * 4 <= STACK_BYTES, "y staging fits in S1");
+
+// TMEM columns of the four accumulators (each 128 lanes x 64 columns).
+constexpr uint32_t COL_S = 0, COL_G = 64, COL_OFF = 128, COL_Y = 192, TMEM_COLS = 256;
+
+// Descriptor strides: stacks have 24 row groups, planes 8.
+constexpr uint32_t STACK_LBO = 24 * 128, PLANE_LBO = 8 * 128, SBO = 128;
+
+constexpr long long kWaitCycles = 4000000000LL;  // ~2 s at 2 GHz
+
+// Byte offset of element (row, k) in a K-major, non-swizzled operand whose
+// row count is `rows`.
+__device__ __forceinline__ uint32_t koff(int row, int k, int rows) {
+    return (uint32_t)((((k >> 2) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + ((k & 3) << 2));
+}
+
+__device__ __forceinline__ float tf32r(float v) {
+    uint32_t u;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(v));
+    return __uint_as_float(u);
+}
+
+__device__ __forceinline__ void st_f32(unsigned char* base, uint32_t off, float v) {
+    *reinterpret_cast<float*>(base + off) = v;
+}
+__device__ __forceinline__ void st_f32x2(unsigned char* base, uint32_t off, float a, float b) {
+    *reinterpret_cast<float2*>(base + off) = make_float2(a, b);
+}
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+struct TcParams {
+    const float4* x;   // [Bz,T,H,P] complex as float4 pairs
+    const float* dt;   // [Bz,T,H]
+    const float2* A;   // [H]
+    const float4* B;   // [Bz,T,H,N]
+    const float4* C;   // [Bz,T,H,N]
+    const float* D;    // [H]
+    float2* y;         // [Bz,T,H,P]
+    float2* h_final;   // [Bz,H,N,P] or null
+    float* ring;       // [BH][RING][2][P][N]
+    int* flags;        // [BH] published chunk count
+    int* ticket;       // [1]
+    float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
+    int* err;          // [1] error bits
+    int T, H, BH, nc;
+};
+
+// ------------------------------------------------------------------ prep
+// Per sequence: the phase accumulated before each chunk, Phi_c =
+// beta * sum_{t < c*CH} softplus(dt_t) (mod 2 pi, accumulated in double), and
+// reset of the hand-off counters.
+__global__ void __launch_bounds__(256) phase_prep_kernel(TcParams p) {
+    const int bh = blockIdx.x;
+    const int b = bh / p.H, h = bh % p.H;
+    const float beta = p.A[h].y;
+    __shared__ double wsum[8];
+    __shared__ double carry;
+    if (threadIdx.x == 0) {
+        carry = 0.0;
+        p.flags[bh] = 0;
+        if (bh == 0) {
+            *p.ticket = 0;
+            *p.err = 0;
+        }
+    }
+    __syncthreads();
+    const double two_pi = 6.283185307179586476925286766559;
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    for (int c0 = 0; c0 < p.nc; c0 += 256) {
+        const int c = c0 + threadIdx.x;
+        double th = 0.0;
+        if (c < p.nc) {
+            float s = 0.f;
+            const int t0 = c * CH, t1 = min(t0 + CH, p.T);
+            for (int t = t0; t < t1; ++t) s += softplusf(p.dt[((size_t)b * p.T + t) * p.H + h]);
+            th = (double)(s * beta);
+        }
+        // block-wide inclusive scan of th
+        double v = th;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        if (lane == 31) wsum[wid] = v;
+        __syncthreads();
+        double before = carry;
+        for (int w = 0; w < wid; ++w) before += wsum[w];
+        const double excl = before + v - th;
+        if (c < p.nc) {
+            double r = fmod(excl, two_pi);
+            if (r > 3.141592653589793) r -= two_pi;
+            if (r < -3.141592653589793) r += two_pi;
+            p.phi[(size_t)bh * p.nc + c] = (float)r;
+        }
+        __syncthreads();
+        if (threadIdx.x == 255) carry = fmod(excl + th, two_pi);
+        __syncthreads();
+    }
+}
+
+// ------------------------------------------------------------------ main
+__global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ float s_rho[CH];
+    __shared__ float2 s_rot[CH];  // (cos, sin) of Theta_l; first used as scan scratch
+    __shared__ float2 s_rot_last;
+    __shared__ __align__(8) uint64_t mbar[4];  // S, G, OFF, Y
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_ticket;
+    __shared__ int s_bad;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned char* sm1 = smem + S1;
+    unsigned char* sm2 = smem + S2;
+    unsigned char* sm3 = smem + S3;
+
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        s_ticket = atomicAdd(p.ticket, 1);
+        s_bad = 0;
+        for (int i = 0; i < 4; ++i) tc::mbar_init(&mbar[i], 1);
+        tc::mbar_fence_init();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    const int ticket = s_ticket;
+    const int c = ticket / p.BH, bh = ticket - c * p.BH;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const float2 Ah = p.A[h];
+    const int t0 = c * CH;
+    const size_t row0 = ((size_t)b * p.T + t0) * p.H + h;  // token row of l = 0
+    const size_t rstride = (size_t)p.H;                    // rows between tokens
+    const float phi_c = p.phi[(size_t)bh * p.nc + c];
+
+    // ---- 1. per-token log-steps, their inclusive cumsums, and the rotations
+    if (tid < CH) {
+        const int t = t0 + tid;
+        float sp = 0.f;
+        if (t < p.T) sp = softplusf(p.dt[row0 + (size_t)tid * rstride]);
+        float v = sp;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v, o);
+            if (lane >= o) v += u;
+        }
+        reinterpret_cast<float*>(s_rot)[tid] = v;  // per-warp partial sums
+    }
+    __syncthreads();
+    float th_mine = 0.f;
+    if (tid < CH) {
+        float v = reinterpret_cast<float*>(s_rot)[tid];
+        if (tid >= 32) v += reinterpret_cast<float*>(s_rot)[31];
+        s_rho[tid] = v * Ah.x;
+        th_mine = v * Ah.y;
+    }
+    __syncthreads();
+    if (tid < CH) {
+        float sn, cs;
+        sincosf(phi_c + th_mine, &sn, &cs);  // Theta_l = Phi_c + theta_l
+        s_rot[tid] = make_float2(cs, sn);
+        if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
+    }
+    __syncthreads();
+    const float rho_end = s_rho[CH - 1];
+
+    // ---- 2. B and X: Bt planes (S3), F stack (S1), X planes (S2)
+    // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
+    // mapped so that 16 consecutive items fill one 8-row core matrix.
+    {
+        float4 bv[8], xv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + NT * i;
+            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+            const int l = g * 8 + r8, n = kc * 4 + half * 2;
+            const bool ok = t0 + l < p.T;
+            const size_t row = row0 + (size_t)l * rstride;
+            bv[i] = ok ? __ldg(p.B + row * (NS / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+            xv[i] = ok ? __ldg(p.x + row * (PD / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + NT * i;
+            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+            const int l = g * 8 + r8, n = kc * 4 + half * 2;
+            const float cs = s_rot[l].x, sn = s_rot[l].y;
+            // Bt = e^{-i Theta} B
+            const float b0r = cs * bv[i].x + sn * bv[i].y, b0i = cs * bv[i].y - sn * bv[i].x;
+            const float b1r = cs * bv[i].z + sn * bv[i].w, b1i = cs * bv[i].w - sn * bv[i].z;
+            st_f32x2(sm3, koff(l, n, 64), tf32r(b0r), tf32r(b1r));
+            st_f32x2(sm3 + PLANE_BYTES, koff(l, n, 64), tf32r(b0i), tf32r(b1i));
+            // F[n][l] = exp(rho_end - rho_l) Bt[l][n]
+            const float ds = __expf(rho_end - s_rho[l]);
+            const float f0r = tf32r(ds * b0r), f0i = tf32r(ds * b0i), f1r = tf32r(ds * b1r), f1i = tf32r(ds * b1i);
+            st_f32(sm1, koff(n, l, 192), -f0i);
+            st_f32(sm1, koff(n + 1, l, 192), -f1i);
+            st_f32(sm1, koff(64 + n, l, 192), f0r);
+            st_f32(sm1, koff(64 + n + 1, l, 192), f1r);
+            st_f32(sm1, koff(128 + n, l, 192), f0i);
+            st_f32(sm1, koff(128 + n + 1, l, 192), f1i);
+            // X planes, rows p (= n here), K = l
+            st_f32(sm2, koff(n, l, 64), tf32r(xv[i].x));
+            st_f32(sm2, koff(n + 1, l, 64), tf32r(xv[i].z));
+            st_f32(sm2 + PLANE_BYTES, koff(n, l, 64), tf32r(xv[i].y));
+            st_f32(sm2 + PLANE_BYTES, koff(n + 1, l, 64), tf32r(xv[i].w));
+        }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
+    const uint32_t ID = tc::idesc_tf32(128, 64);
+    // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`.
+    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs) {
+        for (int ks = 0; ks < 8; ++ks)
+            tc::mma_tf32(d, tc::make_desc(as + ks * 2 * STACK_LBO + 8 * SBO, STACK_LBO, SBO),
+                         tc::make_desc(bs + ks * 2 * PLANE_LBO, PLANE_LBO, SBO), ID, ks > 0);
+        for (int ks = 0; ks < 8; ++ks)
+            tc::mma_tf32(d, tc::make_desc(as + ks * 2 * STACK_LBO, STACK_LBO, SBO),
+                         tc::make_desc(bs + PLANE_BYTES + ks * 2 * PLANE_LBO, PLANE_LBO, SBO), ID, 1);
+    };
+    if (tid == 0) {
+        tc::fence_after_sync();
+        cgemm(tmem + COL_S, a1, a2);  // S' = F X
+        tc::commit(&mbar[0]);
+    }
+
+    // ---- 3. C: Ct stack into S1 once the state GEMM has read F
+    {
+        float4 cv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + NT * i;
+            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+            const int l = g * 8 + r8, n = kc * 4 + half * 2;
+            const bool ok = t0 + l < p.T;
+            const size_t row = row0 + (size_t)l * rstride;
+            cv[i] = ok ? __ldg(p.C + row * (NS / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+        if (!tc::mbar_wait_bounded(&mbar[0], 0, kWaitCycles)) s_bad = 1;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + NT * i;
+            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+            const int l = g * 8 + r8, n = kc * 4 + half * 2;
+            const float cs = s_rot[l].x, sn = s_rot[l].y;
+            // Ct = e^{+i Theta} C
+            const float c0r = tf32r(cs * cv[i].x - sn * cv[i].y), c0i = tf32r(cs * cv[i].y + sn * cv[i].x);
+            const float c1r = tf32r(cs * cv[i].z - sn * cv[i].w), c1i = tf32r(cs * cv[i].w + sn * cv[i].z);
+            st_f32x2(sm1, koff(l, n, 192), -c0i, -c1i);
+            st_f32x2(sm1, koff(64 + l, n, 192), c0r, c1r);
+            st_f32x2(sm1, koff(128 + l, n, 192), c0i, c1i);
+        }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        tc::fence_after_sync();
+        cgemm(tmem + COL_G, a1, a3);  // G = Ct Bt^T
+        tc::commit(&mbar[1]);
+    }
+
+    // ---- 4. inter-chunk hand-off: H_c in, H_{c+1} = e^{rho_end} H_c + S' out
+    if (tid == 0 && c > 0) {
+        const long long w0 = clock64();
+        while (ld_acquire(p.flags + bh) < c) {
+            if (clock64() - w0 > kWaitCycles) {
+                atomicOr(p.err, 1);
+                s_bad = 1;
+                break;
+            }
+            __nanosleep(64);
+        }
+    }
+    __syncthreads();
+    const float* slot_in = p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS);
+    float* slot_out = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS);
+    // (a) H_c as the B operand of Y_off: planes (part), rows p, K = n.
+    if (!tc::mbar_wait_bounded(&mbar[1], 0, kWaitCycles)) s_bad = 1;  // Bt planes consumed
+    {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + NT * i;  // [part][p][n/4]
+            const int part = e >> 10, r8 = e & 7, kc = (e >> 3) & 15, g = (e >> 7) & 7;
+            const int pp = g * 8 + r8, n = kc * 4;
+            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (c > 0) v = __ldcg(reinterpret_cast<const float4*>(slot_in + (part * PD + pp) * NS + n));
+            *reinterpret_cast<float4*>(sm3 + part * PLANE_BYTES + koff(pp, n, 64)) =
+                make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
+        }
+    }
+    // (b) the state update, thread = (TMEM lane quarter, column half)
+    {
+        const int q = warp & 3, chalf = warp >> 2;
+        const int L = q * 32 + lane;          // accumulator row (lane)
+        const int part = L >> 6, n = L & 63;  // real rows 0-63, imaginary 64-127
+        const int p0 = chalf * 32;
+        uint32_t r[32];
+        tc::fence_after_sync();
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_S + p0, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_S + p0 + 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tc::tmem_wait_ld();
+        const float eend = __expf(rho_end);
+        const float* src = slot_in + (size_t)part * PD * NS + n;
+        float* dst = slot_out + (size_t)part * PD * NS + n;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float hv = (c > 0) ? __ldcg(src + (p0 + j) * NS) : 0.f;
+            __stcg(dst + (p0 + j) * NS, fmaf(eend, hv, __uint_as_float(r[j])));
+        }
+    }
+    __threadfence();
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        st_release(p.flags + bh, c + 1);
+        tc::fence_after_sync();
+        cgemm(tmem + COL_OFF, a1, a3);  // Y_off' = Ct H_c
+        tc::commit(&mbar[2]);
+    }
+
+    // ---- 5. masked scores M = L o G into S1 (after Y_off has read Ct)
+    {
+        const int q = warp & 3, chalf = warp >> 2;
+        const int L = q * 32 + lane;
+        const int part = L >> 6, l = L & 63;
+        const int s0 = chalf * 32;
+        uint32_t r[32];
+        tc::fence_after_sync();
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_G + s0, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_G + s0 + 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tc::tmem_wait_ld();
+        const float rl = s_rho[l];
+        float m[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const int s = s0 + j;
+            m[j] = (s <= l) ? tf32r(__expf(rl - s_rho[s]) * __uint_as_float(r[j])) : 0.f;
+        }
+        if (!tc::mbar_wait_bounded(&mbar[2], 0, kWaitCycles)) s_bad = 1;
+        if (part == 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) st_f32(sm1, koff(64 + l, s0 + j, 192), m[j]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                st_f32(sm1, koff(128 + l, s0 + j, 192), m[j]);
+                st_f32(sm1, koff(l, s0 + j, 192), -m[j]);
+            }
+        }
+    }
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        tc::fence_after_sync();
+        cgemm(tmem + COL_Y, a1, a2);  // Y_diag = M X
+        tc::commit(&mbar[3]);
+    }
+
+    // ---- 6. y = Y_diag + e^{rho_l} Y_off' + D x
+    {
+        const int q = warp & 3, chalf = warp >> 2;
+        const int L = q * 32 + lane;
+        const int part = L >> 6, l = L & 63;
+        const int p0 = chalf * 32;
+        if (!tc::mbar_wait_bounded(&mbar[3], 0, kWaitCycles)) s_bad = 1;
+        tc::fence_after_sync();
+        uint32_t ry[32], ro[32];
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_Y + p0, *reinterpret_cast<uint32_t(*)[16]>(ry));
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_Y + p0 + 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(ry + 16));
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_OFF + p0, *reinterpret_cast<uint32_t(*)[16]>(ro));
+        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_OFF + p0 + 16,
+                      *reinterpret_cast<uint32_t(*)[16]>(ro + 16));
+        tc::tmem_wait_ld();
+        const float el = __expf(s_rho[l]);
+        float* stage = reinterpret_cast<float*>(sm1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j)
+            stage[l * STAGE_LD + 2 * (p0 + j) + part] = fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
+    }
+    __syncthreads();
+    {
+        const float Dh = p.D[h];
+        const float* stage = reinterpret_cast<const float*>(sm1);
+        const float2* x2 = reinterpret_cast<const float2*>(p.x);
+#pragma unroll 4
+        for (int i = tid; i < CH * PD; i += NT) {
+            const int l = i >> 6, pp = i & 63;
+            if (t0 + l < p.T) {
+                const size_t row = row0 + (size_t)l * rstride;
+                const float2 xv = __ldg(x2 + row * PD + pp);
+                const float yr = stage[l * STAGE_LD + 2 * pp], yi = stage[l * STAGE_LD + 2 * pp + 1];
+                p.y[row * PD + pp] = make_float2(fmaf(Dh, xv.x, yr), fmaf(Dh, xv.y, yi));
+            }
+        }
+    }
+
+    // ---- 7. final state of the sequence, rotated back
+    if (c == p.nc - 1 && p.h_final) {
+        const float cs = s_rot_last.x, sn = s_rot_last.y;
+        for (int i = tid; i < NS * PD; i += NT) {
+            const int n = i >> 6, pp = i & 63;
+            const float hr = __ldcg(slot_out + (size_t)pp * NS + n);
+            const float hi = __ldcg(slot_out + (size_t)PD * NS + (size_t)pp * NS + n);
+            p.h_final[(size_t)bh * NS * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
+        }
+    }
+
+    if (s_bad && tid == 0) atomicOr(p.err, 2);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
+}  // namespace
+
+bool tc_forward_supported(int64_t N, int64_t P, int chunk) { return N == NS && P == PD && chunk == CH; }
+
+size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H) {
+    const int64_t BH = Bz * H, nc = (T + CH - 1) / CH;
+    size_t off = (size_t)BH * RING * 2 * PD * NS * sizeof(float);  // ring
+    off += 256 + ((size_t)BH * sizeof(int) + 255) / 256 * 256;      // ticket+err, flags
+    off += ((size_t)BH * nc * sizeof(float) + 255) / 256 * 256;     // phi
+    return off;
+}
+
+cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
+    TcParams p;
+    const int64_t BH = a.Bz * a.H, nc = (a.T + CH - 1) / CH;
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    p.ring = reinterpret_cast<float*>(w);
+    w += (size_t)BH * RING * 2 * PD * NS * sizeof(float);
+    p.ticket = reinterpret_cast<int*>(w);
+    p.err = reinterpret_cast<int*>(w) + 1;
+    w += 256;
+    p.flags = reinterpret_cast<int*>(w);
+    w += ((size_t)BH * sizeof(int) + 255) / 256 * 256;
+    p.phi = reinterpret_cast<float*>(w);
+    p.x = reinterpret_cast<const float4*>(a.x);
+    p.dt = a.dt;
+    p.A = a.A;
+    p.B = reinterpret_cast<const float4*>(a.B);
+    p.C = reinterpret_cast<const float4*>(a.C);
+    p.D = a.D;
+    p.y = a.y;
+    p.h_final = a.h_final;
+    p.T = (int)a.T;
+    p.H = (int)a.H;
+    p.BH = (int)BH;
+    p.nc = (int)nc;
+    phase_prep_kernel<<<(unsigned)BH, 256, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static bool attr_set[128] = {};
+    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
+        e = cudaFuncSetAttribute(fused_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 128) attr_set[dev] = true;
+    }
+    if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
+    fused_chunk_kernel<<<(unsigned)(BH * nc), NT, SMEM_BYTES, st>>>(p);
+    e = cudaGetLastError();
+    if (g_prof_end) cudaEventRecord(g_prof_end, st);
+    return e;
+}
+
+}  // namespace cssd

@@ -42,10 +42,14 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    # states (Bz*H*nc*N*P complex64) plus the per-chunk decay totals, 256-byte rounded
+    # fused tensor-core path: a two-slot state ring per sequence plus per-chunk phases
     got = cssd.workspace_bytes(4, 2048, 24, 64, 64, 64)
-    nc = 32
-    assert got >= 4 * 24 * nc * 64 * 64 * 8
+    assert got >= 4 * 24 * 2 * 64 * 64 * 8 + 4 * 24 * 32 * 4
+    # CUDA-core path: every chunk's end state plus per-chunk decay totals
+    got = cssd.workspace_bytes(1, 65536, 32, 128, 64, 128)
+    assert got >= 32 * 512 * 128 * 64 * 8
+    assert cssd.forward_launches(4, 2048, 24, 64, 64, 64) == 2
+    assert cssd.forward_launches(1, 65536, 32, 128, 64, 128) == 3
     assert cssd.workspace_bytes(1, 65, 1, 16, 16, 64) > cssd.workspace_bytes(1, 64, 1, 16, 16, 64)
     assert cssd.workspace_bytes(1, 64, 1, 16, 16, 96) == 0  # unsupported chunk
     assert cssd.workspace_bytes(1, 0, 1, 16, 16, 64) == 0  # empty sequence
