@@ -200,6 +200,21 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     const size_t rstride = (size_t)p.H;                    // rows between tokens
     const float phi_c = p.phi[(size_t)bh * p.nc + c];
 
+    // ---- 0. issue the B and X tile loads; they land while the scalars are made.
+    // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
+    // mapped so that 16 consecutive items fill one 8-row core matrix.
+    float4 bv[8], xv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int e = tid + NT * i;
+        const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+        const int l = g * 8 + r8, n = kc * 4 + half * 2;
+        const bool ok = t0 + l < p.T;
+        const size_t row = row0 + (size_t)l * rstride;
+        bv[i] = ok ? __ldg(p.B + row * (NS / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        xv[i] = ok ? __ldg(p.x + row * (PD / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+
     // ---- 1. per-token log-steps, their inclusive cumsums, and the rotations
     if (tid < CH) {
         const int t = t0 + tid;
@@ -232,20 +247,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     const float rho_end = s_rho[CH - 1];
 
     // ---- 2. B and X: Bt planes (S3), F stack (S1), X planes (S2)
-    // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
-    // mapped so that 16 consecutive items fill one 8-row core matrix.
     {
-        float4 bv[8], xv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + NT * i;
-            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-            const int l = g * 8 + r8, n = kc * 4 + half * 2;
-            const bool ok = t0 + l < p.T;
-            const size_t row = row0 + (size_t)l * rstride;
-            bv[i] = ok ? __ldg(p.B + row * (NS / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
-            xv[i] = ok ? __ldg(p.x + row * (PD / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = tid + NT * i;
@@ -373,11 +375,11 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         const float eend = __expf(rho_end);
         const float* src = slot_in + (size_t)part * PD * NS + n;
         float* dst = slot_out + (size_t)part * PD * NS + n;
+        float hv[32];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-            const float hv = (c > 0) ? __ldcg(src + (p0 + j) * NS) : 0.f;
-            __stcg(dst + (p0 + j) * NS, fmaf(eend, hv, __uint_as_float(r[j])));
-        }
+        for (int j = 0; j < 32; ++j) hv[j] = (c > 0) ? __ldcg(src + (p0 + j) * NS) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) __stcg(dst + (p0 + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j])));
     }
     __threadfence();
     tc::fence_proxy_async();
