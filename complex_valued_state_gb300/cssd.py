@@ -31,8 +31,11 @@ STATUS = {
 }
 
 # Every symbol include/cssd.h declares.
-EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward", "cssd_step",
-           "cssd_profile_events", "cssd_status_string")
+EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward",
+           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_profile_events", "cssd_status_string")
+
+# Scratch array size of cssd_chunked_forward_noalloc (bytes).
+NOALLOC_SCRATCH_BYTES = 16 << 20
 
 
 class Dims(ctypes.Structure):
@@ -64,6 +67,8 @@ def load(path: str = LIB_PATH):
             lib.cssd_forward_launches.restype = ctypes.c_int
             lib.cssd_chunked_forward.argtypes = [dims_p] + [vp] * 8 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
             lib.cssd_chunked_forward.restype = ctypes.c_int
+            lib.cssd_chunked_forward_noalloc.argtypes = [dims_p] + [vp] * 8 + [ctypes.c_int, vp]
+            lib.cssd_chunked_forward_noalloc.restype = ctypes.c_int
             lib.cssd_step.argtypes = [dims_p] + [vp] * 8 + [vp]
             lib.cssd_step.restype = ctypes.c_int
             lib.cssd_profile_events.argtypes = [vp, vp]
@@ -165,6 +170,40 @@ def chunked_forward(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None,
                                   _stream_handle(stream, dev))
     if st != CSSD_OK:
         raise CssdError(st, "cssd_chunked_forward")
+    return y, h_final
+
+
+def chunked_forward_noalloc(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None, want_state: bool = True,
+                            stream=None):
+    """cssd_chunked_forward_noalloc: the forward on the library's fixed scratch
+    array, for callers that cannot allocate device memory; returns (y, h_final).
+
+    The outputs must be passed in (y, h_final) for the call itself to allocate
+    nothing; when they are omitted this wrapper creates them with torch first.
+    """
+    lib = load()
+    dev = x.device
+    Bz, T, H, P = x.shape
+    N = B.shape[-1]
+    c64, f32 = torch.complex64, torch.float32
+    _check(x, "x", c64, (Bz, T, H, P), dev)
+    _check(dt, "dt", f32, (Bz, T, H), dev)
+    _check(A, "A", c64, (H,), dev)
+    _check(B, "B", c64, (Bz, T, H, N), dev)
+    _check(C, "C", c64, (Bz, T, H, N), dev)
+    _check(D, "D", f32, (H,), dev)
+    if y is None:
+        y = torch.empty((Bz, T, H, P), dtype=c64, device=dev)
+    _check(y, "y", c64, (Bz, T, H, P), dev)
+    if h_final is None and want_state:
+        h_final = torch.empty((Bz, H, N, P), dtype=c64, device=dev)
+    if h_final is not None:
+        _check(h_final, "h_final", c64, (Bz, H, N, P), dev)
+    d = Dims(Bz, T, H, N, P)
+    st = lib.cssd_chunked_forward_noalloc(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                          _ptr(y), _ptr(h_final), int(chunk), _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_chunked_forward_noalloc")
     return y, h_final
 
 

@@ -100,6 +100,27 @@ int cssd_chunked_forward(const cssd_dims* dims, const void* x, const float* dt, 
  * sizes (0 when they are invalid).  Informational, for launch accounting. */
 int cssd_forward_launches(const cssd_dims* dims, int chunk);
 
+/* cssd_chunked_forward for callers that cannot allocate device memory when
+ * they call it: callers whose device heap is owned outright by another
+ * allocator (a host framework's caching allocator, an embedding runtime that
+ * forbids allocation after start-up) or that must not wait on an allocator on
+ * a latency-critical path.  The paper has no counterpart to this entry point.
+ * Arguments and results are those of cssd_chunked_forward without the
+ * workspace: the scratch the kernels need lives in a 16 MiB array that is
+ * part of the library's device image, so the call allocates nothing.
+ *   - Every device that loads the library holds those 16 MiB until exit.
+ *   - Sizes whose workspace (cssd_workspace_bytes) exceeds 16 MiB return
+ *     CSSD_ERR_WORKSPACE without launching.
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and caches it; make that first call before any
+ *     stream capture.
+ *   - All calls share the array and it keeps the last call's contents; the
+ *     kernels clear what must start at zero on every call, but calls whose
+ *     executions overlap on the GPU race on it and must be serialised. */
+int cssd_chunked_forward_noalloc(const cssd_dims* dims, const void* x, const float* dt, const void* A,
+                                 const void* B, const void* C, const float* D, void* y, void* h_final,
+                                 int chunk, cssd_stream_t stream);
+
 /* One decode token for every (batch, head): the same recurrence, one step.
  *   h   complex64 [batch, nheads, dstate, headdim]  state, read then updated in place
  *   x   complex64 [batch, nheads, headdim]
