@@ -81,15 +81,6 @@ __device__ __forceinline__ void st_f32x2(unsigned char* base, uint32_t off, floa
     *reinterpret_cast<float2*>(base + off) = make_float2(a, b);
 }
 
-__device__ __forceinline__ int ld_acquire(const int* p) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-    return v;
-}
-__device__ __forceinline__ void st_release(int* p, int v) {
-    asm volatile("st.release.gpu.global.b32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
-}
-
 struct TcParams {
     const float4* x;   // [Bz,T,H,P] complex as float4 pairs
     const float* dt;   // [Bz,T,H]
@@ -99,27 +90,56 @@ struct TcParams {
     const float* D;    // [H]
     float2* y;         // [Bz,T,H,P]
     float2* h_final;   // [Bz,H,N,P] or null
-    float* ring;       // [BH][RING][2][P][N]
-    int* flags;        // [BH] published chunk count
+    unsigned long long* ring;  // [BH][RING][2][P][N] tagged cells
     int* ticket;       // [1]
     float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
     int* err;          // [1] error bits
     int T, H, BH, nc;
 };
 
+// ------------------------------------------------------------------ helpers
+// Raw 64 x 64 complex tiles land in shared memory row by row (512 bytes per
+// token); 16-byte chunk j of row l is stored at chunk j ^ (l & 7) so that the
+// transform's reads spread over the banks.
+__device__ __forceinline__ uint32_t raw_off(int l, int j) { return (uint32_t)(l * 512 + ((j ^ (l & 7)) << 4)); }
+
+__device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gptr), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
+// State hand-off cells: one 8-byte word per state element, the fp32 value in
+// the low half and the chunk count it belongs to in the high half, written and
+// read as single 8-byte accesses so a reader sees a value only together with
+// its own tag.  Tag 0 never names a published state.
+__device__ __forceinline__ unsigned long long ld_cell(const unsigned long long* q) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(v) : "l"(q) : "memory");
+    return v;
+}
+__device__ __forceinline__ void st_cell(unsigned long long* q, float v, uint32_t tag) {
+    const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
+    asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(q), "l"(w) : "memory");
+}
+
 // ------------------------------------------------------------------ prep
 // Per sequence: the phase accumulated before each chunk, Phi_c =
-// beta * sum_{t < c*CH} softplus(dt_t) (mod 2 pi, accumulated in double), and
-// reset of the hand-off counters.
+// beta * sum_{t < c*CH} softplus(dt_t) (mod 2 pi, accumulated in double),
+// clearing of the sequence's hand-off cells, and reset of the ticket.
 __global__ void __launch_bounds__(256) phase_prep_kernel(TcParams p) {
     const int bh = blockIdx.x;
     const int b = bh / p.H, h = bh % p.H;
     const float beta = p.A[h].y;
     __shared__ double wsum[8];
     __shared__ double carry;
+    {
+        ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring + (size_t)bh * RING * 2 * PD * NS);
+        for (int i = threadIdx.x; i < RING * PD * NS; i += 256) cells[i] = make_ulonglong2(0ull, 0ull);
+    }
     if (threadIdx.x == 0) {
         carry = 0.0;
-        p.flags[bh] = 0;
         if (bh == 0) {
             *p.ticket = 0;
             *p.err = 0;
@@ -199,27 +219,57 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     const size_t row0 = ((size_t)b * p.T + t0) * p.H + h;  // token row of l = 0
     const size_t rstride = (size_t)p.H;                    // rows between tokens
     const float phi_c = p.phi[(size_t)bh * p.nc + c];
+    const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
 
-    // ---- 0. issue the B and X tile loads; they land while the scalars are made.
-    // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
-    // mapped so that 16 consecutive items fill one 8-row core matrix.
-    float4 bv[8], xv[8];
+    // ---- 0. every input of the chunk in flight at once: dt first (the
+    // rotations depend on it), raw B and X rows by cp.async into S3 and S2,
+    // the C tile into registers.
+    float dt_raw = 0.f;
+    if (tid < CH && t0 + tid < p.T) dt_raw = __ldg(p.dt + row0 + (size_t)tid * rstride);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
-        const int e = tid + NT * i;
-        const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-        const int l = g * 8 + r8, n = kc * 4 + half * 2;
+        const int e = tid + NT * i;  // row l = e / 32, 16-byte chunk j = e % 32
+        const int l = e >> 5, j = e & 31;
         const bool ok = t0 + l < p.T;
-        const size_t row = row0 + (size_t)l * rstride;
-        bv[i] = ok ? __ldg(p.B + row * (NS / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        xv[i] = ok ? __ldg(p.x + row * (PD / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const size_t row = row0 + (ok ? (size_t)l * rstride : 0);
+        cp_async16(a3 + raw_off(l, j), p.B + row * (NS / 2) + j, ok);
+        cp_async16(a2 + raw_off(l, j), p.x + row * (PD / 2) + j, ok);
     }
+    cp_async_commit();
+    // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
+    // mapped so that 16 consecutive items fill one 8-row core matrix.
+    float4 cv[8];
+    auto load_c = [&]() {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + NT * i;
+            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+            const int l = g * 8 + r8, n = kc * 4 + half * 2;
+            const bool ok = t0 + l < p.T;
+            const size_t row = row0 + (size_t)l * rstride;
+            cv[i] = ok ? __ldg(p.C + row * (NS / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+    // Ct = e^{+i Theta} C as the stack [-Ct_i; Ct_r; Ct_i] in S1 (rows l, K = n).
+    auto store_ct = [&]() {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + NT * i;
+            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+            const int l = g * 8 + r8, n = kc * 4 + half * 2;
+            const float cs = s_rot[l].x, sn = s_rot[l].y;
+            const float c0r = tf32r(cs * cv[i].x - sn * cv[i].y), c0i = tf32r(cs * cv[i].y + sn * cv[i].x);
+            const float c1r = tf32r(cs * cv[i].z - sn * cv[i].w), c1i = tf32r(cs * cv[i].w + sn * cv[i].z);
+            st_f32x2(sm1, koff(l, n, 192), -c0i, -c1i);
+            st_f32x2(sm1, koff(64 + l, n, 192), c0r, c1r);
+            st_f32x2(sm1, koff(128 + l, n, 192), c0i, c1i);
+        }
+    };
+    load_c();
 
     // ---- 1. per-token log-steps, their inclusive cumsums, and the rotations
     if (tid < CH) {
-        const int t = t0 + tid;
-        float sp = 0.f;
-        if (t < p.T) sp = softplusf(p.dt[row0 + (size_t)tid * rstride]);
+        const float sp = (t0 + tid < p.T) ? softplusf(dt_raw) : 0.f;
         float v = sp;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -243,11 +293,22 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         s_rot[tid] = make_float2(cs, sn);
         if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
     }
+    cp_async_wait_all();
     __syncthreads();
     const float rho_end = s_rho[CH - 1];
 
-    // ---- 2. B and X: Bt planes (S3), F stack (S1), X planes (S2)
+    // ---- 2. B and X: Bt planes (S3, over raw B), F stack (S1), X planes (S2, over raw X)
     {
+        float4 bv[8], xv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = tid + NT * i;
+            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+            const int l = g * 8 + r8, j = kc * 2 + half;
+            bv[i] = *reinterpret_cast<const float4*>(sm3 + raw_off(l, j));
+            xv[i] = *reinterpret_cast<const float4*>(sm2 + raw_off(l, j));
+        }
+        __syncthreads();  // raw tiles are overwritten below
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
             const int e = tid + NT * i;
@@ -278,7 +339,6 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
-    const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
     const uint32_t ID = tc::idesc_tf32(128, 64);
     // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`.
     auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs) {
@@ -295,131 +355,51 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         tc::commit(&mbar[0]);
     }
 
-    // ---- 3. C: Ct stack into S1 once the state GEMM has read F
-    {
-        float4 cv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + NT * i;
-            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-            const int l = g * 8 + r8, n = kc * 4 + half * 2;
-            const bool ok = t0 + l < p.T;
-            const size_t row = row0 + (size_t)l * rstride;
-            cv[i] = ok ? __ldg(p.C + row * (NS / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-        if (!tc::mbar_wait_bounded(&mbar[0], 0, kWaitCycles)) s_bad = 1;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + NT * i;
-            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-            const int l = g * 8 + r8, n = kc * 4 + half * 2;
-            const float cs = s_rot[l].x, sn = s_rot[l].y;
-            // Ct = e^{+i Theta} C
-            const float c0r = tf32r(cs * cv[i].x - sn * cv[i].y), c0i = tf32r(cs * cv[i].y + sn * cv[i].x);
-            const float c1r = tf32r(cs * cv[i].z - sn * cv[i].w), c1i = tf32r(cs * cv[i].w + sn * cv[i].z);
-            st_f32x2(sm1, koff(l, n, 192), -c0i, -c1i);
-            st_f32x2(sm1, koff(64 + l, n, 192), c0r, c1r);
-            st_f32x2(sm1, koff(128 + l, n, 192), c0i, c1i);
-        }
-    }
+    // ---- 3. Ct stack into S1 once the state GEMM has read F; G = Ct Bt^T
+    if (!tc::mbar_wait_bounded(&mbar[0], 0, kWaitCycles)) s_bad = 1;
+    store_ct();
     tc::fence_proxy_async();
     tc::fence_before_sync();
     __syncthreads();
     if (tid == 0) {
         tc::fence_after_sync();
-        cgemm(tmem + COL_G, a1, a3);  // G = Ct Bt^T
+        cgemm(tmem + COL_G, a1, a3);
         tc::commit(&mbar[1]);
     }
 
-    // ---- 4. inter-chunk hand-off: H_c in, H_{c+1} = e^{rho_end} H_c + S' out
-    if (tid == 0 && c > 0) {
-        const long long w0 = clock64();
-        while (ld_acquire(p.flags + bh) < c) {
-            if (clock64() - w0 > kWaitCycles) {
-                atomicOr(p.err, 1);
-                s_bad = 1;
-                break;
-            }
-            __nanosleep(64);
-        }
-    }
-    __syncthreads();
-    const float* slot_in = p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS);
-    float* slot_out = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS);
-    // (a) H_c as the B operand of Y_off: planes (part), rows p, K = n.
-    if (!tc::mbar_wait_bounded(&mbar[1], 0, kWaitCycles)) s_bad = 1;  // Bt planes consumed
-    {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + NT * i;  // [part][p][n/4]
-            const int part = e >> 10, r8 = e & 7, kc = (e >> 3) & 15, g = (e >> 7) & 7;
-            const int pp = g * 8 + r8, n = kc * 4;
-            float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (c > 0) v = __ldcg(reinterpret_cast<const float4*>(slot_in + (part * PD + pp) * NS + n));
-            *reinterpret_cast<float4*>(sm3 + part * PLANE_BYTES + koff(pp, n, 64)) =
-                make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
-        }
-    }
-    // (b) the state update, thread = (TMEM lane quarter, column half)
-    {
-        const int q = warp & 3, chalf = warp >> 2;
-        const int L = q * 32 + lane;          // accumulator row (lane)
-        const int part = L >> 6, n = L & 63;  // real rows 0-63, imaginary 64-127
-        const int p0 = chalf * 32;
-        uint32_t r[32];
-        tc::fence_after_sync();
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_S + p0, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_S + p0 + 16,
-                      *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-        tc::tmem_wait_ld();
-        const float eend = __expf(rho_end);
-        const float* src = slot_in + (size_t)part * PD * NS + n;
-        float* dst = slot_out + (size_t)part * PD * NS + n;
-        float hv[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) hv[j] = (c > 0) ? __ldcg(src + (p0 + j) * NS) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) __stcg(dst + (p0 + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j])));
-    }
-    __threadfence();
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        st_release(p.flags + bh, c + 1);
-        tc::fence_after_sync();
-        cgemm(tmem + COL_OFF, a1, a3);  // Y_off' = Ct H_c
-        tc::commit(&mbar[2]);
-    }
+    // Thread roles for the TMEM epilogues: lane quarter q, column half chalf;
+    // accumulator row L = 32 q + lane is the real part (L < 64) or the
+    // imaginary part (L >= 64) of row lrow = L mod 64.
+    const int q = warp & 3, chalf = warp >> 2;
+    const int L = q * 32 + lane;
+    const int part = L >> 6, lrow = L & 63;
+    const int c0col = chalf * 32;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
 
-    // ---- 5. masked scores M = L o G into S1 (after Y_off has read Ct)
+    // ---- 4. masked scores M = L o G into S1 (G has read Ct); Y_diag = M X
+    if (!tc::mbar_wait_bounded(&mbar[1], 0, kWaitCycles)) s_bad = 1;
     {
-        const int q = warp & 3, chalf = warp >> 2;
-        const int L = q * 32 + lane;
-        const int part = L >> 6, l = L & 63;
-        const int s0 = chalf * 32;
         uint32_t r[32];
         tc::fence_after_sync();
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_G + s0, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_G + s0 + 16,
-                      *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tc::tmem_ld16(tmem + lane_base + COL_G + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tc::tmem_ld16(tmem + lane_base + COL_G + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
         tc::tmem_wait_ld();
-        const float rl = s_rho[l];
+        const float rl = s_rho[lrow];
         float m[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-            const int s = s0 + j;
-            m[j] = (s <= l) ? tf32r(__expf(rl - s_rho[s]) * __uint_as_float(r[j])) : 0.f;
+            const int sidx = c0col + j;
+            m[j] = (sidx <= lrow) ? tf32r(__expf(rl - s_rho[sidx]) * __uint_as_float(r[j])) : 0.f;
         }
-        if (!tc::mbar_wait_bounded(&mbar[2], 0, kWaitCycles)) s_bad = 1;
-        if (part == 0) {
+        // 16-byte stores: four consecutive K of one row fill one core-matrix row
 #pragma unroll
-            for (int j = 0; j < 32; ++j) st_f32(sm1, koff(64 + l, s0 + j, 192), m[j]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                st_f32(sm1, koff(128 + l, s0 + j, 192), m[j]);
-                st_f32(sm1, koff(l, s0 + j, 192), -m[j]);
+        for (int k4 = 0; k4 < 8; ++k4) {
+            const float4 v = make_float4(m[4 * k4], m[4 * k4 + 1], m[4 * k4 + 2], m[4 * k4 + 3]);
+            if (part == 0) {
+                *reinterpret_cast<float4*>(sm1 + koff(64 + lrow, c0col + 4 * k4, 192)) = v;
+            } else {
+                *reinterpret_cast<float4*>(sm1 + koff(128 + lrow, c0col + 4 * k4, 192)) = v;
+                *reinterpret_cast<float4*>(sm1 + koff(lrow, c0col + 4 * k4, 192)) = make_float4(-v.x, -v.y, -v.z, -v.w);
             }
         }
     }
@@ -429,55 +409,163 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     if (tid == 0) {
         tc::fence_after_sync();
         cgemm(tmem + COL_Y, a1, a2);  // Y_diag = M X
+        tc::commit(&mbar[2]);
+    }
+
+    // ---- 5. inter-chunk hand-off.  This thread owns state row lrow of part
+    // `part` and 32 columns; it takes H_c from the cells the same thread
+    // position of chunk c-1 wrote and writes H_{c+1} = e^{rho_end} H_c + S'.
+    float hv[32];
+    {
+        const unsigned long long* cin =
+            p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
+        unsigned long long* cout =
+            p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
+        if (c > 0) {
+            const uint32_t want = (uint32_t)c;
+            const long long w0 = clock64();
+            // one lane per warp watches one cell, then every lane reads its own
+            if (lane == 0) {
+                while ((uint32_t)(ld_cell(cin + c0col * NS) >> 32) != want) {
+                    if (clock64() - w0 > kWaitCycles) break;
+                    __nanosleep(128);
+                }
+            }
+            __syncwarp();
+            bool late = false;
+            while (true) {
+                // all 32 loads are issued before any tag is examined
+                unsigned long long w[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) w[j] = ld_cell(cin + (c0col + j) * NS);
+                bool all = true;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    hv[j] = __uint_as_float((uint32_t)w[j]);
+                    all = all && ((uint32_t)(w[j] >> 32) == want);
+                }
+                if (all) break;
+                if (clock64() - w0 > kWaitCycles) {
+                    late = true;
+                    break;
+                }
+                __nanosleep(128);
+            }
+            if (late) {
+                atomicOr(p.err, 1);
+                s_bad = 1;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) hv[j] = 0.f;
+        }
+        uint32_t r[32];
+        tc::fence_after_sync();
+        tc::tmem_ld16(tmem + lane_base + COL_S + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tc::tmem_ld16(tmem + lane_base + COL_S + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tc::tmem_wait_ld();
+        const float eend = __expf(rho_end);
+        const uint32_t tag = (uint32_t)(c + 1);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j])), tag);
+    }
+    load_c();  // C again, for the Ct stack of Y_off (an L2 hit)
+
+    // H_c becomes the B operand of Y_off (rows p, K = n) in S3, which G has
+    // released.  The warp holds a 32 (n) x 32 (p) block, one n per lane; a
+    // butterfly of shuffles transposes it so each lane owns one p and writes
+    // 16-byte runs of four consecutive n.
+    {
+#pragma unroll
+        for (int sbit = 16; sbit >= 1; sbit >>= 1) {
+            const bool upper = (lane & sbit) != 0;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                if ((j & sbit) == 0) {
+                    const float send = upper ? hv[j] : hv[j | sbit];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, sbit);
+                    if (upper) hv[j] = recv;
+                    else hv[j | sbit] = recv;
+                }
+            }
+        }
+        // now hv[j] = H_part[n0 + j][c0col + lane], n0 = first row of this warp
+        const int n0 = lrow - lane;
+        unsigned char* plane = sm3 + part * PLANE_BYTES;
+#pragma unroll
+        for (int k4 = 0; k4 < 8; ++k4)
+            *reinterpret_cast<float4*>(plane + koff(c0col + lane, n0 + 4 * k4, 64)) =
+                make_float4(tf32r(hv[4 * k4]), tf32r(hv[4 * k4 + 1]), tf32r(hv[4 * k4 + 2]), tf32r(hv[4 * k4 + 3]));
+    }
+
+    // ---- 6. Ct stack again into S1 once Y_diag has read M; Y_off' = Ct H_c
+    if (!tc::mbar_wait_bounded(&mbar[2], 0, kWaitCycles)) s_bad = 1;
+    store_ct();
+    tc::fence_proxy_async();
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        tc::fence_after_sync();
+        cgemm(tmem + COL_OFF, a1, a3);
         tc::commit(&mbar[3]);
     }
 
-    // ---- 6. y = Y_diag + e^{rho_l} Y_off' + D x
+    // ---- 7. y = Y_diag + e^{rho_l} Y_off' + D x
     {
-        const int q = warp & 3, chalf = warp >> 2;
-        const int L = q * 32 + lane;
-        const int part = L >> 6, l = L & 63;
-        const int p0 = chalf * 32;
         if (!tc::mbar_wait_bounded(&mbar[3], 0, kWaitCycles)) s_bad = 1;
         tc::fence_after_sync();
         uint32_t ry[32], ro[32];
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_Y + p0, *reinterpret_cast<uint32_t(*)[16]>(ry));
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_Y + p0 + 16,
-                      *reinterpret_cast<uint32_t(*)[16]>(ry + 16));
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_OFF + p0, *reinterpret_cast<uint32_t(*)[16]>(ro));
-        tc::tmem_ld16(tmem + ((uint32_t)(q * 32) << 16) + COL_OFF + p0 + 16,
-                      *reinterpret_cast<uint32_t(*)[16]>(ro + 16));
+        tc::tmem_ld16(tmem + lane_base + COL_Y + c0col, *reinterpret_cast<uint32_t(*)[16]>(ry));
+        tc::tmem_ld16(tmem + lane_base + COL_Y + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(ry + 16));
+        tc::tmem_ld16(tmem + lane_base + COL_OFF + c0col, *reinterpret_cast<uint32_t(*)[16]>(ro));
+        tc::tmem_ld16(tmem + lane_base + COL_OFF + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(ro + 16));
         tc::tmem_wait_ld();
-        const float el = __expf(s_rho[l]);
+        const float el = __expf(s_rho[lrow]);
         float* stage = reinterpret_cast<float*>(sm1);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            stage[l * STAGE_LD + 2 * (p0 + j) + part] = fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
+            stage[lrow * STAGE_LD + 2 * (c0col + j) + part] =
+                fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
     }
     __syncthreads();
     {
         const float Dh = p.D[h];
         const float* stage = reinterpret_cast<const float*>(sm1);
-        const float2* x2 = reinterpret_cast<const float2*>(p.x);
 #pragma unroll 4
         for (int i = tid; i < CH * PD; i += NT) {
             const int l = i >> 6, pp = i & 63;
             if (t0 + l < p.T) {
                 const size_t row = row0 + (size_t)l * rstride;
-                const float2 xv = __ldg(x2 + row * PD + pp);
+                // the skip term uses the exact fp32 input (an L2 hit), not the
+                // tf32-rounded X planes
+                const float2 xv = __ldg(reinterpret_cast<const float2*>(p.x) + row * PD + pp);
                 const float yr = stage[l * STAGE_LD + 2 * pp], yi = stage[l * STAGE_LD + 2 * pp + 1];
                 p.y[row * PD + pp] = make_float2(fmaf(Dh, xv.x, yr), fmaf(Dh, xv.y, yi));
             }
         }
     }
 
-    // ---- 7. final state of the sequence, rotated back
+    // ---- 8. final state of the sequence, H_final = e^{rho_end} H_c + S',
+    // rotated back to the original frame (staged through S3, free after Y_off).
     if (c == p.nc - 1 && p.h_final) {
+        uint32_t r[32];
+        tc::fence_after_sync();
+        tc::tmem_ld16(tmem + lane_base + COL_S + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tc::tmem_ld16(tmem + lane_base + COL_S + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tc::tmem_wait_ld();
+        const unsigned long long* cin =
+            p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
+        const float eend = __expf(rho_end);
+        float* hs = reinterpret_cast<float*>(sm3);  // [part][n][p] fp32, 32 KB
+        float hc[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) hc[j] = (c > 0) ? __uint_as_float((uint32_t)ld_cell(cin + (c0col + j) * NS)) : 0.f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) hs[(part * NS + lrow) * PD + c0col + j] = fmaf(eend, hc[j], __uint_as_float(r[j]));
+        __syncthreads();
         const float cs = s_rot_last.x, sn = s_rot_last.y;
         for (int i = tid; i < NS * PD; i += NT) {
-            const int n = i >> 6, pp = i & 63;
-            const float hr = __ldcg(slot_out + (size_t)pp * NS + n);
-            const float hi = __ldcg(slot_out + (size_t)PD * NS + (size_t)pp * NS + n);
+            const float hr = hs[i], hi = hs[NS * PD + i];
             p.h_final[(size_t)bh * NS * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
         }
     }
@@ -494,8 +582,8 @@ bool tc_forward_supported(int64_t N, int64_t P, int chunk) { return N == NS && P
 
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H) {
     const int64_t BH = Bz * H, nc = (T + CH - 1) / CH;
-    size_t off = (size_t)BH * RING * 2 * PD * NS * sizeof(float);  // ring
-    off += 256 + ((size_t)BH * sizeof(int) + 255) / 256 * 256;      // ticket+err, flags
+    size_t off = (size_t)BH * RING * 2 * PD * NS * sizeof(unsigned long long);  // hand-off cells
+    off += 256;                                                                  // ticket, err
     off += ((size_t)BH * nc * sizeof(float) + 255) / 256 * 256;     // phi
     return off;
 }
@@ -504,13 +592,11 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     TcParams p;
     const int64_t BH = a.Bz * a.H, nc = (a.T + CH - 1) / CH;
     unsigned char* w = static_cast<unsigned char*>(ws);
-    p.ring = reinterpret_cast<float*>(w);
-    w += (size_t)BH * RING * 2 * PD * NS * sizeof(float);
+    p.ring = reinterpret_cast<unsigned long long*>(w);
+    w += (size_t)BH * RING * 2 * PD * NS * sizeof(unsigned long long);
     p.ticket = reinterpret_cast<int*>(w);
     p.err = reinterpret_cast<int*>(w) + 1;
     w += 256;
-    p.flags = reinterpret_cast<int*>(w);
-    w += ((size_t)BH * sizeof(int) + 255) / 256 * 256;
     p.phi = reinterpret_cast<float*>(w);
     p.x = reinterpret_cast<const float4*>(a.x);
     p.dt = a.dt;
