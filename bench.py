@@ -267,9 +267,9 @@ def run_ours(args, rank, world, local):
     fwd_units = Bz * T * H
     alg_bytes = fwd_units * (8 * P + 16 * N + 4 + 8 * P)  # x, B, C, dt in; y out
     achieved = alg_bytes / (k_ms / 1e3) / 1e9
-    roof = {"bound": "hbm", "kernel": "chunk_output", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+    roof = {"bound": "hbm", "kernel": "fused_chunk_kernel", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
-            "traffic": recorded_traffic("chunk_output", fwd_units), "kernel_ms": round(k_ms, 5),
+            "traffic": recorded_traffic("fused_chunk_kernel", fwd_units), "kernel_ms": round(k_ms, 5),
             "alg_bytes_per_launch": alg_bytes}
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -331,9 +331,9 @@ def bench_decode(args, dev):
     gbs = alg / (us / 1e6) / 1e9
     return {"workload": f"decode Bz{w.batch} H{w.nheads} N{N} P{P}, one token per call",
             "value": round(units / (us / 1e6), 1), "unit": UNIT, "us_per_step": round(us, 3), "steps": n,
-            "roofline": {"bound": "hbm", "kernel": "step", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
+            "roofline": {"bound": "hbm", "kernel": "step_kernel", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbs / hbm, 4), "peak_kind": kind,
-                         "traffic": recorded_traffic("step", units), "alg_bytes_per_launch": alg}}
+                         "traffic": recorded_traffic("step_kernel", units), "alg_bytes_per_launch": alg}}
 
 
 # ---------------------------------------------------------------- CPU oracle
