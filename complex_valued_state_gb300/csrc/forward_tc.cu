@@ -68,10 +68,11 @@ __device__ __forceinline__ uint32_t koff(int row, int k, int rows) {
     return (uint32_t)((((k >> 2) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + ((k & 3) << 2));
 }
 
+// Round an fp32 value to the nearest TF32 value (10 explicit mantissa bits),
+// ties away from zero: add half a TF32 unit to the magnitude bits, then clear
+// the 13 low bits.  Two integer operations.
 __device__ __forceinline__ float tf32r(float v) {
-    uint32_t u;
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(u) : "f"(v));
-    return __uint_as_float(u);
+    return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
 }
 
 __device__ __forceinline__ void st_f32(unsigned char* base, uint32_t off, float v) {
@@ -134,6 +135,7 @@ __global__ void __launch_bounds__(256) phase_prep_kernel(TcParams p) {
     const float beta = p.A[h].y;
     __shared__ double wsum[8];
     __shared__ double carry;
+    __shared__ double sth[256];
     {
         ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring + (size_t)bh * RING * 2 * PD * NS);
         for (int i = threadIdx.x; i < RING * PD * NS; i += 256) cells[i] = make_ulonglong2(0ull, 0ull);
@@ -148,15 +150,38 @@ __global__ void __launch_bounds__(256) phase_prep_kernel(TcParams p) {
     __syncthreads();
     const double two_pi = 6.283185307179586476925286766559;
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    const float* dtb = p.dt + (size_t)b * p.T * p.H + h;  // token t at dtb[t * H]
     for (int c0 = 0; c0 < p.nc; c0 += 256) {
-        const int c = c0 + threadIdx.x;
-        double th = 0.0;
-        if (c < p.nc) {
-            float s = 0.f;
-            const int t0 = c * CH, t1 = min(t0 + CH, p.T);
-            for (int t = t0; t < t1; ++t) s += softplusf(p.dt[((size_t)b * p.T + t) * p.H + h]);
-            th = (double)(s * beta);
+        // Phase total of chunks c0 .. c0+255: warp w sums chunks c0 + w + 8k,
+        // two tokens per lane, eight chunks' loads in flight at a time.
+        for (int k = 0; k < 32; k += 4) {
+            float v[4][2];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + wid + 8 * (k + u);
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = c * CH + hh * 32 + lane;
+                    v[u][hh] = (c < p.nc && t < p.T) ? __ldg(dtb + (size_t)t * p.H) : 0.f;
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int c = c0 + wid + 8 * (k + u);
+                float sum = 0.f;
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {
+                    const int t = c * CH + hh * 32 + lane;
+                    if (c < p.nc && t < p.T) sum += softplusf(v[u][hh]);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
+                if (lane == 0) sth[wid + 8 * (k + u)] = (double)(sum * beta);
+            }
         }
+        __syncthreads();
+        const int c = c0 + threadIdx.x;
+        const double th = (c < p.nc) ? sth[threadIdx.x] : 0.0;
         // block-wide inclusive scan of th
         double v = th;
 #pragma unroll
@@ -388,8 +413,10 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         float m[32];
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
+            // causal mask as exp(-inf) = 0: a select, not a branch around exp
             const int sidx = c0col + j;
-            m[j] = (sidx <= lrow) ? tf32r(__expf(rl - s_rho[sidx]) * __uint_as_float(r[j])) : 0.f;
+            const float arg = (sidx <= lrow) ? rl - s_rho[sidx] : -INFINITY;
+            m[j] = tf32r(__expf(arg) * __uint_as_float(r[j]));
         }
         // 16-byte stores: four consecutive K of one row fill one core-matrix row
 #pragma unroll
