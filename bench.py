@@ -44,6 +44,7 @@ def parse():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-long", action="store_true", help="skip the long_seq forward measurement")
     return ap.parse_args()
 
 
@@ -257,6 +258,9 @@ def run_ours(args, rank, world, local):
     decode = None
     if not args.no_decode:
         decode = bench_decode(args, dev)
+    long_seq = None
+    if not args.no_long:
+        long_seq = bench_long_seq(args, dev)
 
     if rank != 0:
         if pg:
@@ -287,6 +291,8 @@ def run_ours(args, rank, world, local):
     }
     if decode:
         out["decode"] = decode
+    if long_seq:
+        out["long_seq"] = long_seq
     if world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(host, tok)
     print(json.dumps(out), flush=True)
@@ -334,6 +340,56 @@ def bench_decode(args, dev):
             "roofline": {"bound": "hbm", "kernel": "step_kernel", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbs / hbm, 4), "peak_kind": kind,
                          "traffic": recorded_traffic("step_kernel", units), "alg_bytes_per_launch": alg}}
+
+
+def bench_long_seq(args, dev):
+    """Forward on the long_seq workload (batch 1, T 65536, 32 heads, N 128, P 64, chunk 128)."""
+    import torch
+
+    from complex_valued_state_gb300 import cssd
+    from complex_valued_state_gb300 import workloads as wl
+
+    w = wl.LONG_SEQ
+    host = wl.make_inputs(w)
+    g = {k: torch.from_numpy(host[k]).to(dev) for k in ("x", "dt", "A", "B", "C", "D")}
+    del host
+    Bz, T, H, N, P, ch = w.batch, w.seqlen, w.nheads, w.dstate, w.headdim, w.chunk
+    y = torch.empty((Bz, T, H, P), dtype=torch.complex64, device=dev)
+    h = torch.empty((Bz, H, N, P), dtype=torch.complex64, device=dev)
+    ws = torch.empty(cssd.workspace_bytes(Bz, T, H, N, P, ch), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        cssd.chunked_forward(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk=ch, y=y, h_final=h, workspace=ws)
+
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize(dev)
+    n = 5
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in kb + ke:
+        e.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(n):
+        cssd.profile_events(kb[i], ke[i])
+        fwd()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    cssd.profile_events(None, None)
+    ms = e0.elapsed_time(e1) / n
+    k_ms = sum(kb[i].elapsed_time(ke[i]) for i in range(n)) / n
+    units = Bz * T * H
+    alg = units * (8 * P + 16 * N + 4 + 8 * P)
+    hbm, kind = peaks()
+    gbs = alg / (k_ms / 1e3) / 1e9
+    return {"workload": f"long_seq Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch}, forward only",
+            "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4), "steps": n,
+            "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel", "achieved": round(gbs, 1), "peak": hbm,
+                         "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind, "kernel_ms": round(k_ms, 4),
+                         "alg_bytes_per_launch": alg}}
 
 
 # ---------------------------------------------------------------- CPU oracle

@@ -41,7 +41,7 @@ extern thread_local cudaEvent_t g_prof_begin;
 extern thread_local cudaEvent_t g_prof_end;
 
 // The chunked forward: the fused tensor-core kernel where its shape applies
-// (chunk = dstate = headdim = 64), else the CUDA-core chunk kernels.
+// (headdim 64, dstate 64 or 128), else the CUDA-core chunk kernels.
 size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
 int forward_launches(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
 cudaError_t launch_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
@@ -52,7 +52,7 @@ cudaError_t launch_seq_forward(const FwdArgs& a, void* workspace, cudaStream_t s
 
 // Fused tensor-core kernel (forward_tc.cu).
 bool tc_forward_supported(int64_t N, int64_t P, int chunk);
-size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H);
+size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N);
 cudaError_t launch_tc_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
 
 // Decode step (step.cu).

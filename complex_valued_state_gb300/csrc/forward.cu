@@ -1,5 +1,5 @@
 // Chooses the kernels of the chunked forward by shape: the fused tensor-core
-// kernel for chunk = dstate = headdim = 64, the CUDA-core chunk kernels for
+// kernel for headdim 64 with dstate 64 or 128, the CUDA-core chunk kernels for
 // every other supported shape.  Both compute the same chunkwise decomposition.
 
 #include "cssd_internal.h"
@@ -7,7 +7,7 @@
 namespace cssd {
 
 size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
-    if (tc_forward_supported(N, P, chunk)) return tc_forward_workspace_bytes(Bz, T, H);
+    if (tc_forward_supported(N, P, chunk)) return tc_forward_workspace_bytes(Bz, T, H, N);
     return seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);
 }
 

@@ -95,7 +95,7 @@ struct TcParams {
     int* ticket;       // [1]
     float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
     int* err;          // [1] error bits
-    int T, H, BH, nc;
+    int T, H, BH, nc, NH;
 };
 
 // ------------------------------------------------------------------ helpers
@@ -137,8 +137,8 @@ __global__ void __launch_bounds__(256) phase_prep_kernel(TcParams p) {
     __shared__ double carry;
     __shared__ double sth[256];
     {
-        ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring + (size_t)bh * RING * 2 * PD * NS);
-        for (int i = threadIdx.x; i < RING * PD * NS; i += 256) cells[i] = make_ulonglong2(0ull, 0ull);
+        ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring + (size_t)bh * p.NH * RING * 2 * PD * NS);
+        for (int i = threadIdx.x; i < p.NH * RING * PD * NS; i += 256) cells[i] = make_ulonglong2(0ull, 0ull);
     }
     if (threadIdx.x == 0) {
         carry = 0.0;
@@ -207,7 +207,13 @@ __global__ void __launch_bounds__(256) phase_prep_kernel(TcParams p) {
 }
 
 // ------------------------------------------------------------------ main
+// One 64-token tile of one sequence per CTA.  The state rows are processed in
+// NH halves of 64 (dstate = 64 NH): the state GEMM, the hand-off and the
+// carried-in readout run once per half, the score GEMM accumulates over the
+// halves, and the masked scores and Y_diag run once.
+template <int NH>
 __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
+    constexpr int N = NS * NH;  // dstate
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ float s_rho[CH];
     __shared__ float2 s_rot[CH];  // (cos, sin) of Theta_l; first used as scan scratch
@@ -246,9 +252,29 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     const float phi_c = p.phi[(size_t)bh * p.nc + c];
     const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
 
-    // ---- 0. every input of the chunk in flight at once: dt first (the
-    // rotations depend on it), raw B and X rows by cp.async into S3 and S2,
-    // the C tile into registers.
+    // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
+    // mapped so that 16 consecutive items fill one 8-row core matrix.
+    auto item = [&](int i, int& l, int& n) {
+        const int e = tid + NT * i;
+        const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
+        l = g * 8 + r8;
+        n = kc * 4 + half * 2;
+    };
+    // 64 columns (half hf) of a token-major [.., N] complex tile, into registers.
+    auto load_half = [&](const float4* src, int hf, float4 (&v)[8]) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int l, n;
+            item(i, l, n);
+            const bool ok = t0 + l < p.T;
+            v[i] = ok ? __ldg(src + (row0 + (size_t)l * rstride) * (N / 2) + hf * 32 + (n >> 1))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+
+    // ---- 0. inputs in flight at once: dt first (the rotations depend on
+    // it), raw X rows (and, for one half, raw B rows) by cp.async into S2 / S3,
+    // the C half into registers.
     float dt_raw = 0.f;
     if (tid < CH && t0 + tid < p.T) dt_raw = __ldg(p.dt + row0 + (size_t)tid * rstride);
 #pragma unroll
@@ -257,40 +283,12 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         const int l = e >> 5, j = e & 31;
         const bool ok = t0 + l < p.T;
         const size_t row = row0 + (ok ? (size_t)l * rstride : 0);
-        cp_async16(a3 + raw_off(l, j), p.B + row * (NS / 2) + j, ok);
+        cp_async16(a3 + raw_off(l, j), p.B + row * (N / 2) + j, ok);
         cp_async16(a2 + raw_off(l, j), p.x + row * (PD / 2) + j, ok);
     }
     cp_async_commit();
-    // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
-    // mapped so that 16 consecutive items fill one 8-row core matrix.
     float4 cv[8];
-    auto load_c = [&]() {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + NT * i;
-            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-            const int l = g * 8 + r8, n = kc * 4 + half * 2;
-            const bool ok = t0 + l < p.T;
-            const size_t row = row0 + (size_t)l * rstride;
-            cv[i] = ok ? __ldg(p.C + row * (NS / 2) + (n >> 1)) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-    // Ct = e^{+i Theta} C as the stack [-Ct_i; Ct_r; Ct_i] in S1 (rows l, K = n).
-    auto store_ct = [&]() {
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + NT * i;
-            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-            const int l = g * 8 + r8, n = kc * 4 + half * 2;
-            const float cs = s_rot[l].x, sn = s_rot[l].y;
-            const float c0r = tf32r(cs * cv[i].x - sn * cv[i].y), c0i = tf32r(cs * cv[i].y + sn * cv[i].x);
-            const float c1r = tf32r(cs * cv[i].z - sn * cv[i].w), c1i = tf32r(cs * cv[i].w + sn * cv[i].z);
-            st_f32x2(sm1, koff(l, n, 192), -c0i, -c1i);
-            st_f32x2(sm1, koff(64 + l, n, 192), c0r, c1r);
-            st_f32x2(sm1, koff(128 + l, n, 192), c0i, c1i);
-        }
-    };
-    load_c();
+    load_half(p.C, 0, cv);
 
     // ---- 1. per-token log-steps, their inclusive cumsums, and the rotations
     if (tid < CH) {
@@ -321,76 +319,31 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     cp_async_wait_all();
     __syncthreads();
     const float rho_end = s_rho[CH - 1];
+    const float eend = __expf(rho_end);
 
-    // ---- 2. B and X: Bt planes (S3, over raw B), F stack (S1), X planes (S2, over raw X)
-    {
-        float4 bv[8], xv[8];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + NT * i;
-            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-            const int l = g * 8 + r8, j = kc * 2 + half;
-            bv[i] = *reinterpret_cast<const float4*>(sm3 + raw_off(l, j));
-            xv[i] = *reinterpret_cast<const float4*>(sm2 + raw_off(l, j));
-        }
-        __syncthreads();  // raw tiles are overwritten below
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int e = tid + NT * i;
-            const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-            const int l = g * 8 + r8, n = kc * 4 + half * 2;
-            const float cs = s_rot[l].x, sn = s_rot[l].y;
-            // Bt = e^{-i Theta} B
-            const float b0r = cs * bv[i].x + sn * bv[i].y, b0i = cs * bv[i].y - sn * bv[i].x;
-            const float b1r = cs * bv[i].z + sn * bv[i].w, b1i = cs * bv[i].w - sn * bv[i].z;
-            st_f32x2(sm3, koff(l, n, 64), tf32r(b0r), tf32r(b1r));
-            st_f32x2(sm3 + PLANE_BYTES, koff(l, n, 64), tf32r(b0i), tf32r(b1i));
-            // F[n][l] = exp(rho_end - rho_l) Bt[l][n]
-            const float ds = __expf(rho_end - s_rho[l]);
-            const float f0r = tf32r(ds * b0r), f0i = tf32r(ds * b0i), f1r = tf32r(ds * b1r), f1i = tf32r(ds * b1i);
-            st_f32(sm1, koff(n, l, 192), -f0i);
-            st_f32(sm1, koff(n + 1, l, 192), -f1i);
-            st_f32(sm1, koff(64 + n, l, 192), f0r);
-            st_f32(sm1, koff(64 + n + 1, l, 192), f1r);
-            st_f32(sm1, koff(128 + n, l, 192), f0i);
-            st_f32(sm1, koff(128 + n + 1, l, 192), f1i);
-            // X planes, rows p (= n here), K = l
-            st_f32(sm2, koff(n, l, 64), tf32r(xv[i].x));
-            st_f32(sm2, koff(n + 1, l, 64), tf32r(xv[i].z));
-            st_f32(sm2 + PLANE_BYTES, koff(n, l, 64), tf32r(xv[i].y));
-            st_f32(sm2 + PLANE_BYTES, koff(n + 1, l, 64), tf32r(xv[i].w));
-        }
-    }
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
     const uint32_t ID = tc::idesc_tf32(128, 64);
     // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`.
-    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs) {
+    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs, bool accumulate) {
         for (int ks = 0; ks < 8; ++ks)
             tc::mma_tf32(d, tc::make_desc(as + ks * 2 * STACK_LBO + 8 * SBO, STACK_LBO, SBO),
-                         tc::make_desc(bs + ks * 2 * PLANE_LBO, PLANE_LBO, SBO), ID, ks > 0);
+                         tc::make_desc(bs + ks * 2 * PLANE_LBO, PLANE_LBO, SBO), ID, (accumulate || ks > 0) ? 1u : 0u);
         for (int ks = 0; ks < 8; ++ks)
             tc::mma_tf32(d, tc::make_desc(as + ks * 2 * STACK_LBO, STACK_LBO, SBO),
-                         tc::make_desc(bs + PLANE_BYTES + ks * 2 * PLANE_LBO, PLANE_LBO, SBO), ID, 1);
+                         tc::make_desc(bs + PLANE_BYTES + ks * 2 * PLANE_LBO, PLANE_LBO, SBO), ID, 1u);
     };
-    if (tid == 0) {
-        tc::fence_after_sync();
-        cgemm(tmem + COL_S, a1, a2);  // S' = F X
-        tc::commit(&mbar[0]);
-    }
-
-    // ---- 3. Ct stack into S1 once the state GEMM has read F; G = Ct Bt^T
-    if (!tc::mbar_wait_bounded(&mbar[0], 0, kWaitCycles)) s_bad = 1;
-    store_ct();
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        tc::fence_after_sync();
-        cgemm(tmem + COL_G, a1, a3);
-        tc::commit(&mbar[1]);
-    }
+    auto issue = [&](uint32_t d, uint32_t as, uint32_t bs, bool accumulate, uint64_t* bar) {
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            cgemm(d, as, bs, accumulate);
+            tc::commit(bar);
+        }
+    };
+    auto wait_bar = [&](uint64_t* bar, uint32_t parity) {
+        if (!tc::mbar_wait_bounded(bar, parity, kWaitCycles)) s_bad = 1;
+    };
 
     // Thread roles for the TMEM epilogues: lane quarter q, column half chalf;
     // accumulator row L = 32 q + lane is the real part (L < 64) or the
@@ -401,8 +354,177 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     const int c0col = chalf * 32;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
 
-    // ---- 4. masked scores M = L o G into S1 (G has read Ct); Y_diag = M X
-    if (!tc::mbar_wait_bounded(&mbar[1], 0, kWaitCycles)) s_bad = 1;
+    // ---- 2. X planes (S2, over raw X), once.
+    {
+        float4 xv[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int l, n;
+            item(i, l, n);
+            xv[i] = *reinterpret_cast<const float4*>(sm2 + raw_off(l, n >> 1));
+        }
+        __syncthreads();  // raw X is overwritten below
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int l, n;
+            item(i, l, n);
+            st_f32(sm2, koff(n, l, 64), tf32r(xv[i].x));
+            st_f32(sm2, koff(n + 1, l, 64), tf32r(xv[i].z));
+            st_f32(sm2 + PLANE_BYTES, koff(n, l, 64), tf32r(xv[i].y));
+            st_f32(sm2 + PLANE_BYTES, koff(n + 1, l, 64), tf32r(xv[i].w));
+        }
+    }
+
+#pragma unroll 1
+    for (int hf = 0; hf < NH; ++hf) {
+        const uint32_t ph = (uint32_t)(hf & 1);  // barrier parity of this half
+        // ---- 3. B half: Bt planes (S3) and F stack (S1); S'_hf = F X
+        {
+            float4 bv[8];
+            if (hf == 0) {
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    int l, n;
+                    item(i, l, n);
+                    bv[i] = *reinterpret_cast<const float4*>(sm3 + raw_off(l, n >> 1));
+                }
+            } else {
+                load_half(p.B, hf, bv);
+                wait_bar(&mbar[2], ph ^ 1);  // Y_off of the previous half has read Ct and H
+            }
+            __syncthreads();  // raw B (half 0) and last half's operands are overwritten below
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                int l, n;
+                item(i, l, n);
+                const float cs = s_rot[l].x, sn = s_rot[l].y;
+                // Bt = e^{-i Theta} B
+                const float b0r = cs * bv[i].x + sn * bv[i].y, b0i = cs * bv[i].y - sn * bv[i].x;
+                const float b1r = cs * bv[i].z + sn * bv[i].w, b1i = cs * bv[i].w - sn * bv[i].z;
+                st_f32x2(sm3, koff(l, n, 64), tf32r(b0r), tf32r(b1r));
+                st_f32x2(sm3 + PLANE_BYTES, koff(l, n, 64), tf32r(b0i), tf32r(b1i));
+                // F[n][l] = exp(rho_end - rho_l) Bt[l][n]
+                const float ds = __expf(rho_end - s_rho[l]);
+                const float f0r = tf32r(ds * b0r), f0i = tf32r(ds * b0i), f1r = tf32r(ds * b1r),
+                            f1i = tf32r(ds * b1i);
+                st_f32(sm1, koff(n, l, 192), -f0i);
+                st_f32(sm1, koff(n + 1, l, 192), -f1i);
+                st_f32(sm1, koff(64 + n, l, 192), f0r);
+                st_f32(sm1, koff(64 + n + 1, l, 192), f1r);
+                st_f32(sm1, koff(128 + n, l, 192), f0i);
+                st_f32(sm1, koff(128 + n + 1, l, 192), f1i);
+            }
+        }
+        issue(tmem + COL_S, a1, a2, false, &mbar[0]);
+
+        // ---- 4. Ct half stack into S1 once the state GEMM has read F; G += Ct Bt^T
+        if (hf > 0) load_half(p.C, hf, cv);
+        wait_bar(&mbar[0], ph);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            int l, n;
+            item(i, l, n);
+            const float cs = s_rot[l].x, sn = s_rot[l].y;
+            const float c0r = tf32r(cs * cv[i].x - sn * cv[i].y), c0i = tf32r(cs * cv[i].y + sn * cv[i].x);
+            const float c1r = tf32r(cs * cv[i].z - sn * cv[i].w), c1i = tf32r(cs * cv[i].w + sn * cv[i].z);
+            st_f32x2(sm1, koff(l, n, 192), -c0i, -c1i);
+            st_f32x2(sm1, koff(64 + l, n, 192), c0r, c1r);
+            st_f32x2(sm1, koff(128 + l, n, 192), c0i, c1i);
+        }
+        issue(tmem + COL_G, a1, a3, hf > 0, &mbar[1]);
+
+        // ---- 5. hand-off of this half: the thread owns state row lrow of part
+        // `part` and 32 columns; it takes H_c from the cells the same thread
+        // position of chunk c-1 wrote and writes H_{c+1} = e^{rho_end} H_c + S'.
+        float hv[32];
+        {
+            const size_t ring_hf = ((size_t)bh * NH + hf) * RING;
+            const unsigned long long* cin =
+                p.ring + (ring_hf + (c % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
+            unsigned long long* cout =
+                p.ring + (ring_hf + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
+            if (c > 0) {
+                const uint32_t want = (uint32_t)c;
+                const long long w0 = clock64();
+                // one lane per warp watches one cell, then every lane reads its own
+                if (lane == 0) {
+                    while ((uint32_t)(ld_cell(cin + c0col * NS) >> 32) != want) {
+                        if (clock64() - w0 > kWaitCycles) break;
+                        __nanosleep(128);
+                    }
+                }
+                __syncwarp();
+                bool late = false;
+                while (true) {
+                    // all 32 loads are issued before any tag is examined
+                    unsigned long long w[32];
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) w[j] = ld_cell(cin + (c0col + j) * NS);
+                    bool all = true;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        hv[j] = __uint_as_float((uint32_t)w[j]);
+                        all = all && ((uint32_t)(w[j] >> 32) == want);
+                    }
+                    if (all) break;
+                    if (clock64() - w0 > kWaitCycles) {
+                        late = true;
+                        break;
+                    }
+                    __nanosleep(128);
+                }
+                if (late) {
+                    atomicOr(p.err, 1);
+                    s_bad = 1;
+                }
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) hv[j] = 0.f;
+            }
+            uint32_t r[32];
+            tc::fence_after_sync();
+            tc::tmem_ld16(tmem + lane_base + COL_S + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+            tc::tmem_ld16(tmem + lane_base + COL_S + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+            tc::tmem_wait_ld();
+            const uint32_t tag = (uint32_t)(c + 1);
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j])), tag);
+        }
+
+        // ---- 6. H_c of this half as the B operand of Y_off (rows p, K = n) in
+        // S3 once G has read Bt.  The warp holds a 32 (n) x 32 (p) block, one n
+        // per lane; a butterfly of shuffles transposes it so that each lane
+        // owns one p and writes 16-byte runs of four consecutive n.
+        {
+#pragma unroll
+            for (int sbit = 16; sbit >= 1; sbit >>= 1) {
+                const bool upper = (lane & sbit) != 0;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                    if ((j & sbit) == 0) {
+                        const float send = upper ? hv[j] : hv[j | sbit];
+                        const float recv = __shfl_xor_sync(0xffffffffu, send, sbit);
+                        if (upper) hv[j] = recv;
+                        else hv[j | sbit] = recv;
+                    }
+                }
+            }
+            // now hv[j] = H_part[n0 + j][c0col + lane], n0 = first row of this warp
+            const int n0 = lrow - lane;
+            wait_bar(&mbar[1], ph);
+            unsigned char* plane = sm3 + part * PLANE_BYTES;
+#pragma unroll
+            for (int k4 = 0; k4 < 8; ++k4)
+                *reinterpret_cast<float4*>(plane + koff(c0col + lane, n0 + 4 * k4, 64)) = make_float4(
+                    tf32r(hv[4 * k4]), tf32r(hv[4 * k4 + 1]), tf32r(hv[4 * k4 + 2]), tf32r(hv[4 * k4 + 3]));
+        }
+        issue(tmem + COL_OFF, a1, a3, hf > 0, &mbar[2]);  // Y_off' += Ct H_c
+    }
+
+    // ---- 7. masked scores M = L o G into S1 once the last Y_off has read Ct;
+    // Y_diag = M X
+    wait_bar(&mbar[1], (NH - 1) & 1);
     {
         uint32_t r[32];
         tc::fence_after_sync();
@@ -418,6 +540,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
             const float arg = (sidx <= lrow) ? rl - s_rho[sidx] : -INFINITY;
             m[j] = tf32r(__expf(arg) * __uint_as_float(r[j]));
         }
+        wait_bar(&mbar[2], (NH - 1) & 1);
         // 16-byte stores: four consecutive K of one row fill one core-matrix row
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
@@ -426,120 +549,16 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                 *reinterpret_cast<float4*>(sm1 + koff(64 + lrow, c0col + 4 * k4, 192)) = v;
             } else {
                 *reinterpret_cast<float4*>(sm1 + koff(128 + lrow, c0col + 4 * k4, 192)) = v;
-                *reinterpret_cast<float4*>(sm1 + koff(lrow, c0col + 4 * k4, 192)) = make_float4(-v.x, -v.y, -v.z, -v.w);
+                *reinterpret_cast<float4*>(sm1 + koff(lrow, c0col + 4 * k4, 192)) =
+                    make_float4(-v.x, -v.y, -v.z, -v.w);
             }
         }
     }
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        tc::fence_after_sync();
-        cgemm(tmem + COL_Y, a1, a2);  // Y_diag = M X
-        tc::commit(&mbar[2]);
-    }
+    issue(tmem + COL_Y, a1, a2, false, &mbar[3]);
 
-    // ---- 5. inter-chunk hand-off.  This thread owns state row lrow of part
-    // `part` and 32 columns; it takes H_c from the cells the same thread
-    // position of chunk c-1 wrote and writes H_{c+1} = e^{rho_end} H_c + S'.
-    float hv[32];
+    // ---- 8. y = Y_diag + e^{rho_l} Y_off' + D x
     {
-        const unsigned long long* cin =
-            p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
-        unsigned long long* cout =
-            p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
-        if (c > 0) {
-            const uint32_t want = (uint32_t)c;
-            const long long w0 = clock64();
-            // one lane per warp watches one cell, then every lane reads its own
-            if (lane == 0) {
-                while ((uint32_t)(ld_cell(cin + c0col * NS) >> 32) != want) {
-                    if (clock64() - w0 > kWaitCycles) break;
-                    __nanosleep(128);
-                }
-            }
-            __syncwarp();
-            bool late = false;
-            while (true) {
-                // all 32 loads are issued before any tag is examined
-                unsigned long long w[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) w[j] = ld_cell(cin + (c0col + j) * NS);
-                bool all = true;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    hv[j] = __uint_as_float((uint32_t)w[j]);
-                    all = all && ((uint32_t)(w[j] >> 32) == want);
-                }
-                if (all) break;
-                if (clock64() - w0 > kWaitCycles) {
-                    late = true;
-                    break;
-                }
-                __nanosleep(128);
-            }
-            if (late) {
-                atomicOr(p.err, 1);
-                s_bad = 1;
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) hv[j] = 0.f;
-        }
-        uint32_t r[32];
-        tc::fence_after_sync();
-        tc::tmem_ld16(tmem + lane_base + COL_S + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tc::tmem_ld16(tmem + lane_base + COL_S + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-        tc::tmem_wait_ld();
-        const float eend = __expf(rho_end);
-        const uint32_t tag = (uint32_t)(c + 1);
-#pragma unroll
-        for (int j = 0; j < 32; ++j) st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j])), tag);
-    }
-    load_c();  // C again, for the Ct stack of Y_off (an L2 hit)
-
-    // H_c becomes the B operand of Y_off (rows p, K = n) in S3, which G has
-    // released.  The warp holds a 32 (n) x 32 (p) block, one n per lane; a
-    // butterfly of shuffles transposes it so each lane owns one p and writes
-    // 16-byte runs of four consecutive n.
-    {
-#pragma unroll
-        for (int sbit = 16; sbit >= 1; sbit >>= 1) {
-            const bool upper = (lane & sbit) != 0;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                if ((j & sbit) == 0) {
-                    const float send = upper ? hv[j] : hv[j | sbit];
-                    const float recv = __shfl_xor_sync(0xffffffffu, send, sbit);
-                    if (upper) hv[j] = recv;
-                    else hv[j | sbit] = recv;
-                }
-            }
-        }
-        // now hv[j] = H_part[n0 + j][c0col + lane], n0 = first row of this warp
-        const int n0 = lrow - lane;
-        unsigned char* plane = sm3 + part * PLANE_BYTES;
-#pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4)
-            *reinterpret_cast<float4*>(plane + koff(c0col + lane, n0 + 4 * k4, 64)) =
-                make_float4(tf32r(hv[4 * k4]), tf32r(hv[4 * k4 + 1]), tf32r(hv[4 * k4 + 2]), tf32r(hv[4 * k4 + 3]));
-    }
-
-    // ---- 6. Ct stack again into S1 once Y_diag has read M; Y_off' = Ct H_c
-    if (!tc::mbar_wait_bounded(&mbar[2], 0, kWaitCycles)) s_bad = 1;
-    store_ct();
-    tc::fence_proxy_async();
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        tc::fence_after_sync();
-        cgemm(tmem + COL_OFF, a1, a3);
-        tc::commit(&mbar[3]);
-    }
-
-    // ---- 7. y = Y_diag + e^{rho_l} Y_off' + D x
-    {
-        if (!tc::mbar_wait_bounded(&mbar[3], 0, kWaitCycles)) s_bad = 1;
+        wait_bar(&mbar[3], 0);
         tc::fence_after_sync();
         uint32_t ry[32], ro[32];
         tc::tmem_ld16(tmem + lane_base + COL_Y + c0col, *reinterpret_cast<uint32_t(*)[16]>(ry));
@@ -551,8 +570,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         float* stage = reinterpret_cast<float*>(sm1);
 #pragma unroll
         for (int j = 0; j < 32; ++j)
-            stage[lrow * STAGE_LD + 2 * (c0col + j) + part] =
-                fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
+            stage[lrow * STAGE_LD + 2 * (c0col + j) + part] = fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
     }
     __syncthreads();
     {
@@ -572,28 +590,18 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         }
     }
 
-    // ---- 8. final state of the sequence, H_final = e^{rho_end} H_c + S',
-    // rotated back to the original frame (staged through S3, free after Y_off).
+    // ---- 9. final state of the sequence: the H_final cells this CTA just
+    // published (read back after the barrier above), rotated back to the
+    // original frame.
     if (c == p.nc - 1 && p.h_final) {
-        uint32_t r[32];
-        tc::fence_after_sync();
-        tc::tmem_ld16(tmem + lane_base + COL_S + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tc::tmem_ld16(tmem + lane_base + COL_S + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-        tc::tmem_wait_ld();
-        const unsigned long long* cin =
-            p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
-        const float eend = __expf(rho_end);
-        float* hs = reinterpret_cast<float*>(sm3);  // [part][n][p] fp32, 32 KB
-        float hc[32];
-#pragma unroll
-        for (int j = 0; j < 32; ++j) hc[j] = (c > 0) ? __uint_as_float((uint32_t)ld_cell(cin + (c0col + j) * NS)) : 0.f;
-#pragma unroll
-        for (int j = 0; j < 32; ++j) hs[(part * NS + lrow) * PD + c0col + j] = fmaf(eend, hc[j], __uint_as_float(r[j]));
-        __syncthreads();
         const float cs = s_rot_last.x, sn = s_rot_last.y;
-        for (int i = tid; i < NS * PD; i += NT) {
-            const float hr = hs[i], hi = hs[NS * PD + i];
-            p.h_final[(size_t)bh * NS * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
+        for (int i = tid; i < N * PD; i += NT) {
+            const int n = i >> 6, pp = i & 63, hf = n >> 6, nn = n & 63;
+            const unsigned long long* cell =
+                p.ring + (((size_t)bh * NH + hf) * RING + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)pp * NS + nn;
+            const float hr = __uint_as_float((uint32_t)ld_cell(cell));
+            const float hi = __uint_as_float((uint32_t)ld_cell(cell + PD * NS));
+            p.h_final[(size_t)bh * N * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
         }
     }
 
@@ -605,22 +613,45 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
 
 }  // namespace
 
-bool tc_forward_supported(int64_t N, int64_t P, int chunk) { return N == NS && P == PD && chunk == CH; }
+// The tensor-core kernel runs 64-token tiles with headdim 64 and dstate 64 or
+// 128; a requested chunk of 128 is computed as two consecutive 64-token tiles
+// with the state handed over between them, which is the same decomposition.
+bool tc_forward_supported(int64_t N, int64_t P, int chunk) {
+    return P == PD && (N == NS || N == 2 * NS) && (chunk == CH || chunk == 2 * CH);
+}
 
-size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H) {
-    const int64_t BH = Bz * H, nc = (T + CH - 1) / CH;
-    size_t off = (size_t)BH * RING * 2 * PD * NS * sizeof(unsigned long long);  // hand-off cells
-    off += 256;                                                                  // ticket, err
-    off += ((size_t)BH * nc * sizeof(float) + 255) / 256 * 256;     // phi
+size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N) {
+    const int64_t BH = Bz * H, nc = (T + CH - 1) / CH, NH = N / NS;
+    size_t off = (size_t)BH * NH * RING * 2 * PD * NS * sizeof(unsigned long long);  // hand-off cells
+    off += 256;                                                                       // ticket, err
+    off += ((size_t)BH * nc * sizeof(float) + 255) / 256 * 256;                       // phi
     return off;
+}
+
+template <int NH>
+static cudaError_t launch_fused(const TcParams& p, int64_t tiles, cudaStream_t st) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static bool attr_set[128] = {};
+    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(fused_chunk_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        if (dev >= 0 && dev < 128) attr_set[dev] = true;
+    }
+    if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
+    fused_chunk_kernel<NH><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (g_prof_end) cudaEventRecord(g_prof_end, st);
+    return e;
 }
 
 cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     TcParams p;
-    const int64_t BH = a.Bz * a.H, nc = (a.T + CH - 1) / CH;
+    const int64_t BH = a.Bz * a.H, nc = (a.T + CH - 1) / CH, NH = a.N / NS;
     unsigned char* w = static_cast<unsigned char*>(ws);
     p.ring = reinterpret_cast<unsigned long long*>(w);
-    w += (size_t)BH * RING * 2 * PD * NS * sizeof(unsigned long long);
+    w += (size_t)BH * NH * RING * 2 * PD * NS * sizeof(unsigned long long);
     p.ticket = reinterpret_cast<int*>(w);
     p.err = reinterpret_cast<int*>(w) + 1;
     w += 256;
@@ -637,22 +668,11 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.H = (int)a.H;
     p.BH = (int)BH;
     p.nc = (int)nc;
+    p.NH = (int)NH;
     phase_prep_kernel<<<(unsigned)BH, 256, 0, st>>>(p);
-    cudaError_t e = cudaGetLastError();
+    const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    static bool attr_set[128] = {};
-    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-        e = cudaFuncSetAttribute(fused_chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 128) attr_set[dev] = true;
-    }
-    if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
-    fused_chunk_kernel<<<(unsigned)(BH * nc), NT, SMEM_BYTES, st>>>(p);
-    e = cudaGetLastError();
-    if (g_prof_end) cudaEventRecord(g_prof_end, st);
-    return e;
+    return NH == 1 ? launch_fused<1>(p, BH * nc, st) : launch_fused<2>(p, BH * nc, st);
 }
 
 }  // namespace cssd

@@ -42,14 +42,17 @@ def test_status_strings(lib):
 
 
 def test_workspace_bytes(lib):
-    # fused tensor-core path: a two-slot state ring per sequence plus per-chunk phases
+    # tensor-core path (headdim 64, dstate 64 or 128): two slots of tagged
+    # 8-byte hand-off words per sequence and 64-row state half, plus per-chunk phases
     got = cssd.workspace_bytes(4, 2048, 24, 64, 64, 64)
-    assert got >= 4 * 24 * 2 * 64 * 64 * 8 + 4 * 24 * 32 * 4
+    assert got >= 4 * 24 * 2 * 2 * 64 * 64 * 8 + 4 * 24 * 32 * 4
+    assert cssd.workspace_bytes(1, 65536, 32, 128, 64, 128) >= 32 * 2 * 2 * 2 * 64 * 64 * 8 + 32 * 1024 * 4
     # CUDA-core path: every chunk's end state plus per-chunk decay totals
-    got = cssd.workspace_bytes(1, 65536, 32, 128, 64, 128)
-    assert got >= 32 * 512 * 128 * 64 * 8
+    got = cssd.workspace_bytes(1, 4096, 8, 32, 32, 128)
+    assert got >= 8 * 32 * 32 * 32 * 8
     assert cssd.forward_launches(4, 2048, 24, 64, 64, 64) == 2
-    assert cssd.forward_launches(1, 65536, 32, 128, 64, 128) == 3
+    assert cssd.forward_launches(1, 65536, 32, 128, 64, 128) == 2
+    assert cssd.forward_launches(1, 4096, 8, 32, 32, 128) == 3
     assert cssd.workspace_bytes(1, 65, 1, 16, 16, 64) > cssd.workspace_bytes(1, 64, 1, 16, 16, 64)
     assert cssd.workspace_bytes(1, 64, 1, 16, 16, 96) == 0  # unsupported chunk
     assert cssd.workspace_bytes(1, 0, 1, 16, 16, 64) == 0  # empty sequence
