@@ -41,7 +41,9 @@ namespace {
 constexpr int CH = 64;    // chunk length
 constexpr int NS = 64;    // dstate
 constexpr int PD = 64;    // headdim
-constexpr int NT = 256;   // threads per CTA
+constexpr int NT = 512;   // threads per CTA
+constexpr int IT = 2048 / NT;       // tile items (float4) per thread
+constexpr int CPT = 64 / (NT / 128);  // accumulator columns per thread
 constexpr int RING = 2;   // state slots per sequence
 
 // Shared memory regions (bytes).
@@ -123,6 +125,12 @@ __device__ __forceinline__ unsigned long long ld_cell(const unsigned long long* 
 __device__ __forceinline__ void st_cell(unsigned long long* q, float v, uint32_t tag) {
     const unsigned long long w = ((unsigned long long)tag << 32) | __float_as_uint(v);
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(q), "l"(w) : "memory");
+}
+
+// CPT consecutive TMEM columns of this warp's lane quarter into registers.
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CPT]) {
+#pragma unroll
+    for (int k = 0; k < CPT / 16; ++k) tc::tmem_ld16(taddr + 16 * k, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * k));
 }
 
 // ------------------------------------------------------------------ prep
@@ -261,9 +269,9 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         n = kc * 4 + half * 2;
     };
     // 64 columns (half hf) of a token-major [.., N] complex tile, into registers.
-    auto load_half = [&](const float4* src, int hf, float4 (&v)[8]) {
+    auto load_half = [&](const float4* src, int hf, float4 (&v)[IT]) {
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < IT; ++i) {
             int l, n;
             item(i, l, n);
             const bool ok = t0 + l < p.T;
@@ -278,7 +286,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     float dt_raw = 0.f;
     if (tid < CH && t0 + tid < p.T) dt_raw = __ldg(p.dt + row0 + (size_t)tid * rstride);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
+    for (int i = 0; i < IT; ++i) {
         const int e = tid + NT * i;  // row l = e / 32, 16-byte chunk j = e % 32
         const int l = e >> 5, j = e & 31;
         const bool ok = t0 + l < p.T;
@@ -287,7 +295,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         cp_async16(a2 + raw_off(l, j), p.x + row * (PD / 2) + j, ok);
     }
     cp_async_commit();
-    float4 cv[8];
+    float4 cv[IT];
     load_half(p.C, 0, cv);
 
     // ---- 1. per-token log-steps, their inclusive cumsums, and the rotations
@@ -345,27 +353,27 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         if (!tc::mbar_wait_bounded(bar, parity, kWaitCycles)) s_bad = 1;
     };
 
-    // Thread roles for the TMEM epilogues: lane quarter q, column half chalf;
-    // accumulator row L = 32 q + lane is the real part (L < 64) or the
-    // imaginary part (L >= 64) of row lrow = L mod 64.
-    const int q = warp & 3, chalf = warp >> 2;
+    // Thread roles for the TMEM epilogues: lane quarter q, column block of
+    // CPT columns; accumulator row L = 32 q + lane is the real part (L < 64)
+    // or the imaginary part (L >= 64) of row lrow = L mod 64.
+    const int q = warp & 3, cblk = warp >> 2;
     const int L = q * 32 + lane;
     const int part = L >> 6, lrow = L & 63;
-    const int c0col = chalf * 32;
+    const int c0col = cblk * CPT;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
 
     // ---- 2. X planes (S2, over raw X), once.
     {
-        float4 xv[8];
+        float4 xv[IT];
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < IT; ++i) {
             int l, n;
             item(i, l, n);
             xv[i] = *reinterpret_cast<const float4*>(sm2 + raw_off(l, n >> 1));
         }
         __syncthreads();  // raw X is overwritten below
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < IT; ++i) {
             int l, n;
             item(i, l, n);
             st_f32(sm2, koff(n, l, 64), tf32r(xv[i].x));
@@ -380,10 +388,10 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         const uint32_t ph = (uint32_t)(hf & 1);  // barrier parity of this half
         // ---- 3. B half: Bt planes (S3) and F stack (S1); S'_hf = F X
         {
-            float4 bv[8];
+            float4 bv[IT];
             if (hf == 0) {
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
+                for (int i = 0; i < IT; ++i) {
                     int l, n;
                     item(i, l, n);
                     bv[i] = *reinterpret_cast<const float4*>(sm3 + raw_off(l, n >> 1));
@@ -394,7 +402,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
             }
             __syncthreads();  // raw B (half 0) and last half's operands are overwritten below
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
+            for (int i = 0; i < IT; ++i) {
                 int l, n;
                 item(i, l, n);
                 const float cs = s_rot[l].x, sn = s_rot[l].y;
@@ -421,7 +429,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         if (hf > 0) load_half(p.C, hf, cv);
         wait_bar(&mbar[0], ph);
 #pragma unroll
-        for (int i = 0; i < 8; ++i) {
+        for (int i = 0; i < IT; ++i) {
             int l, n;
             item(i, l, n);
             const float cs = s_rot[l].x, sn = s_rot[l].y;
@@ -436,7 +444,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         // ---- 5. hand-off of this half: the thread owns state row lrow of part
         // `part` and 32 columns; it takes H_c from the cells the same thread
         // position of chunk c-1 wrote and writes H_{c+1} = e^{rho_end} H_c + S'.
-        float hv[32];
+        float hv[CPT];
         {
             const size_t ring_hf = ((size_t)bh * NH + hf) * RING;
             const unsigned long long* cin =
@@ -457,12 +465,12 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                 bool late = false;
                 while (true) {
                     // all 32 loads are issued before any tag is examined
-                    unsigned long long w[32];
+                    unsigned long long w[CPT];
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) w[j] = ld_cell(cin + (c0col + j) * NS);
+                    for (int j = 0; j < CPT; ++j) w[j] = ld_cell(cin + (c0col + j) * NS);
                     bool all = true;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
+                    for (int j = 0; j < CPT; ++j) {
                         hv[j] = __uint_as_float((uint32_t)w[j]);
                         all = all && ((uint32_t)(w[j] >> 32) == want);
                     }
@@ -479,29 +487,28 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                 }
             } else {
 #pragma unroll
-                for (int j = 0; j < 32; ++j) hv[j] = 0.f;
+                for (int j = 0; j < CPT; ++j) hv[j] = 0.f;
             }
-            uint32_t r[32];
+            uint32_t r[CPT];
             tc::fence_after_sync();
-            tc::tmem_ld16(tmem + lane_base + COL_S + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
-            tc::tmem_ld16(tmem + lane_base + COL_S + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+            tmem_ld_cols(tmem + lane_base + COL_S + c0col, r);
             tc::tmem_wait_ld();
             const uint32_t tag = (uint32_t)(c + 1);
 #pragma unroll
-            for (int j = 0; j < 32; ++j)
+            for (int j = 0; j < CPT; ++j)
                 st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j])), tag);
         }
 
         // ---- 6. H_c of this half as the B operand of Y_off (rows p, K = n) in
-        // S3 once G has read Bt.  The warp holds a 32 (n) x 32 (p) block, one n
-        // per lane; a butterfly of shuffles transposes it so that each lane
-        // owns one p and writes 16-byte runs of four consecutive n.
+        // S3 once G has read Bt.  Each group of CPT lanes holds a CPT (n) x CPT
+        // (p) block, one n per lane; a butterfly of shuffles transposes it so
+        // that each lane owns one p and writes 16-byte runs of four consecutive n.
         {
 #pragma unroll
-            for (int sbit = 16; sbit >= 1; sbit >>= 1) {
+            for (int sbit = CPT / 2; sbit >= 1; sbit >>= 1) {
                 const bool upper = (lane & sbit) != 0;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
+                for (int j = 0; j < CPT; ++j) {
                     if ((j & sbit) == 0) {
                         const float send = upper ? hv[j] : hv[j | sbit];
                         const float recv = __shfl_xor_sync(0xffffffffu, send, sbit);
@@ -510,13 +517,14 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                     }
                 }
             }
-            // now hv[j] = H_part[n0 + j][c0col + lane], n0 = first row of this warp
-            const int n0 = lrow - lane;
+            // now hv[j] = H_part[n0 + j][c0col + (lane mod CPT)], n0 = first row of the lane group
+            const int n0 = lrow - (lane & (CPT - 1));
+            const int pcol = c0col + (lane & (CPT - 1));
             wait_bar(&mbar[1], ph);
             unsigned char* plane = sm3 + part * PLANE_BYTES;
 #pragma unroll
-            for (int k4 = 0; k4 < 8; ++k4)
-                *reinterpret_cast<float4*>(plane + koff(c0col + lane, n0 + 4 * k4, 64)) = make_float4(
+            for (int k4 = 0; k4 < CPT / 4; ++k4)
+                *reinterpret_cast<float4*>(plane + koff(pcol, n0 + 4 * k4, 64)) = make_float4(
                     tf32r(hv[4 * k4]), tf32r(hv[4 * k4 + 1]), tf32r(hv[4 * k4 + 2]), tf32r(hv[4 * k4 + 3]));
         }
         issue(tmem + COL_OFF, a1, a3, hf > 0, &mbar[2]);  // Y_off' += Ct H_c
@@ -526,15 +534,14 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     // Y_diag = M X
     wait_bar(&mbar[1], (NH - 1) & 1);
     {
-        uint32_t r[32];
+        uint32_t r[CPT];
         tc::fence_after_sync();
-        tc::tmem_ld16(tmem + lane_base + COL_G + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tc::tmem_ld16(tmem + lane_base + COL_G + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tmem_ld_cols(tmem + lane_base + COL_G + c0col, r);
         tc::tmem_wait_ld();
         const float rl = s_rho[lrow];
-        float m[32];
+        float m[CPT];
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < CPT; ++j) {
             // causal mask as exp(-inf) = 0: a select, not a branch around exp
             const int sidx = c0col + j;
             const float arg = (sidx <= lrow) ? rl - s_rho[sidx] : -INFINITY;
@@ -543,7 +550,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         wait_bar(&mbar[2], (NH - 1) & 1);
         // 16-byte stores: four consecutive K of one row fill one core-matrix row
 #pragma unroll
-        for (int k4 = 0; k4 < 8; ++k4) {
+        for (int k4 = 0; k4 < CPT / 4; ++k4) {
             const float4 v = make_float4(m[4 * k4], m[4 * k4 + 1], m[4 * k4 + 2], m[4 * k4 + 3]);
             if (part == 0) {
                 *reinterpret_cast<float4*>(sm1 + koff(64 + lrow, c0col + 4 * k4, 192)) = v;
@@ -560,16 +567,14 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     {
         wait_bar(&mbar[3], 0);
         tc::fence_after_sync();
-        uint32_t ry[32], ro[32];
-        tc::tmem_ld16(tmem + lane_base + COL_Y + c0col, *reinterpret_cast<uint32_t(*)[16]>(ry));
-        tc::tmem_ld16(tmem + lane_base + COL_Y + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(ry + 16));
-        tc::tmem_ld16(tmem + lane_base + COL_OFF + c0col, *reinterpret_cast<uint32_t(*)[16]>(ro));
-        tc::tmem_ld16(tmem + lane_base + COL_OFF + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(ro + 16));
+        uint32_t ry[CPT], ro[CPT];
+        tmem_ld_cols(tmem + lane_base + COL_Y + c0col, ry);
+        tmem_ld_cols(tmem + lane_base + COL_OFF + c0col, ro);
         tc::tmem_wait_ld();
         const float el = __expf(s_rho[lrow]);
         float* stage = reinterpret_cast<float*>(sm1);
 #pragma unroll
-        for (int j = 0; j < 32; ++j)
+        for (int j = 0; j < CPT; ++j)
             stage[lrow * STAGE_LD + 2 * (c0col + j) + part] = fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
     }
     __syncthreads();
