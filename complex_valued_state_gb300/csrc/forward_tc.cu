@@ -331,13 +331,19 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
 
     const uint32_t ID = tc::idesc_tf32(128, 64);
     // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`.
+    // Descriptors are built once; stepping K by 8 advances the start-address
+    // field (bytes / 16) by 2 * LBO / 16.
     auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs, bool accumulate) {
+        const uint64_t a_hi = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
+        const uint64_t a_lo = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
+        const uint64_t b_re = tc::make_desc(bs, PLANE_LBO, SBO);
+        const uint64_t b_im = tc::make_desc(bs + PLANE_BYTES, PLANE_LBO, SBO);
+        constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4, B_STEP = (2 * PLANE_LBO) >> 4;
+#pragma unroll
         for (int ks = 0; ks < 8; ++ks)
-            tc::mma_tf32(d, tc::make_desc(as + ks * 2 * STACK_LBO + 8 * SBO, STACK_LBO, SBO),
-                         tc::make_desc(bs + ks * 2 * PLANE_LBO, PLANE_LBO, SBO), ID, (accumulate || ks > 0) ? 1u : 0u);
-        for (int ks = 0; ks < 8; ++ks)
-            tc::mma_tf32(d, tc::make_desc(as + ks * 2 * STACK_LBO, STACK_LBO, SBO),
-                         tc::make_desc(bs + PLANE_BYTES + ks * 2 * PLANE_LBO, PLANE_LBO, SBO), ID, 1u);
+            tc::mma_tf32(d, a_hi + ks * A_STEP, b_re + ks * B_STEP, ID, (accumulate || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) tc::mma_tf32(d, a_lo + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
     };
     auto issue = [&](uint32_t d, uint32_t as, uint32_t bs, bool accumulate, uint64_t* bar) {
         tc::fence_proxy_async();
@@ -563,7 +569,17 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     }
     issue(tmem + COL_Y, a1, a2, false, &mbar[3]);
 
-    // ---- 8. y = Y_diag + e^{rho_l} Y_off' + D x
+    // ---- 8. y = Y_diag + e^{rho_l} Y_off' + D x.  The skip term uses the
+    // exact fp32 input (an L2 hit, fetched while Y_diag runs), not the
+    // tf32-rounded X planes.
+    constexpr int YI = CH * PD / NT;  // output elements per thread
+    float2 xs[YI];
+#pragma unroll
+    for (int k = 0; k < YI; ++k) {
+        const int i = tid + NT * k, l = i >> 6, pp = i & 63;
+        xs[k] = (t0 + l < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + (row0 + (size_t)l * rstride) * PD + pp)
+                               : make_float2(0.f, 0.f);
+    }
     {
         wait_bar(&mbar[3], 0);
         tc::fence_after_sync();
@@ -581,16 +597,13 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     {
         const float Dh = p.D[h];
         const float* stage = reinterpret_cast<const float*>(sm1);
-#pragma unroll 4
-        for (int i = tid; i < CH * PD; i += NT) {
-            const int l = i >> 6, pp = i & 63;
+#pragma unroll
+        for (int k = 0; k < YI; ++k) {
+            const int i = tid + NT * k, l = i >> 6, pp = i & 63;
             if (t0 + l < p.T) {
                 const size_t row = row0 + (size_t)l * rstride;
-                // the skip term uses the exact fp32 input (an L2 hit), not the
-                // tf32-rounded X planes
-                const float2 xv = __ldg(reinterpret_cast<const float2*>(p.x) + row * PD + pp);
                 const float yr = stage[l * STAGE_LD + 2 * pp], yi = stage[l * STAGE_LD + 2 * pp + 1];
-                p.y[row * PD + pp] = make_float2(fmaf(Dh, xv.x, yr), fmaf(Dh, xv.y, yi));
+                p.y[row * PD + pp] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
             }
         }
     }
