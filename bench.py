@@ -64,6 +64,23 @@ def peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+# ---------------------------------------------------------------- multi-rank helpers
+def reduce_max(pg, value: float, device) -> float:
+    """Max of `value` over all ranks (the slowest rank sets the step time)."""
+    if pg is None:
+        return float(value)
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(world: int, units_per_rank: int, ms_per_step: float) -> float:
+    """Units processed by all ranks per second, each rank doing its own replica."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 # ---------------------------------------------------------------- clocks
 class ClockSampler:
     """nvidia-smi samples of SM clock and throttle reasons while running."""
@@ -214,11 +231,8 @@ def run_ours(args, rank, world, local):
             pg.barrier()
     ms = t0.elapsed_time(t1) / args.steps
     k_ms = sum(kb[i].elapsed_time(ke[i]) for i in range(args.steps)) / args.steps
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * units / (ms / 1e3)
+    ms = reduce_max(pg, ms, dev)
+    value = whole_job_rate(world, units, ms)
 
     # end to end: pinned host inputs in, results out, every step
     pin = {k: torch.from_numpy(host[k]).pin_memory() for k in ("x", "dt", "B", "C")}
@@ -250,10 +264,7 @@ def run_ours(args, rank, world, local):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     e_ms = e0.elapsed_time(e1) / e_steps
-    if pg:
-        t = torch.tensor([e_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        e_ms = float(t.item())
+    e_ms = reduce_max(pg, e_ms, dev)
 
     decode = None
     if not args.no_decode:
@@ -284,7 +295,7 @@ def run_ours(args, rank, world, local):
                    "units_per_step": units, "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (%.2f GB read+written per step)" % (alg_bytes / 1e9)},
         "roofline": roof,
-        "e2e": {"value": round(world * units / (e_ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(whole_job_rate(world, units, e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 5)},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),

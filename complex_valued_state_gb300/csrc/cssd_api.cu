@@ -75,6 +75,18 @@ int cssd_profile_events(void* ev_begin, void* ev_end) {
     return CSSD_OK;
 }
 
+int cssd_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cssd_stream_t stream) {
+    if (!err_bits) return CSSD_ERR_NULL;
+    if (wait_cycles <= 0) return CSSD_ERR_DIMS;
+    const cudaError_t e =
+        cssd::tc_selftest_handoff_timeout(wait_cycles, err_bits, reinterpret_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CSSD_ERR_CUDA;
+    }
+    return CSSD_OK;
+}
+
 const char* cssd_status_string(int status) {
     switch (status) {
         case CSSD_OK: return "ok";

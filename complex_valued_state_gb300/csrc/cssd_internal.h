@@ -54,6 +54,7 @@ cudaError_t launch_seq_forward(const FwdArgs& a, void* workspace, cudaStream_t s
 bool tc_forward_supported(int64_t N, int64_t P, int chunk);
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N);
 cudaError_t launch_tc_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
+cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cudaStream_t stream);
 
 // Decode step (step.cu).
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);

@@ -98,6 +98,8 @@ struct TcParams {
     float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
     int* err;          // [1] error bits
     int T, H, BH, nc, NH;
+    int first_ticket;       // tickets start here (0 in normal use)
+    long long wait_cycles;  // limit of the hand-off wait (SM clocks)
 };
 
 // ------------------------------------------------------------------ helpers
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(256) phase_prep_kernel(TcParams p) {
     if (threadIdx.x == 0) {
         carry = 0.0;
         if (bh == 0) {
-            *p.ticket = 0;
+            *p.ticket = p.first_ticket;
             *p.err = 0;
         }
     }
@@ -251,6 +253,12 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     tc::fence_after_sync();
     const uint32_t tmem = s_tmem;
     const int ticket = s_ticket;
+    if (ticket >= p.BH * p.nc) {  // nothing left to do (only when tickets start past 0)
+        tc::fence_before_sync();
+        __syncthreads();
+        if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+        return;
+    }
     const int c = ticket / p.BH, bh = ticket - c * p.BH;
     const int b = bh / p.H, h = bh - b * p.H;
     const float2 Ah = p.A[h];
@@ -463,7 +471,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                 // one lane per warp watches one cell, then every lane reads its own
                 if (lane == 0) {
                     while ((uint32_t)(ld_cell(cin + c0col * NS) >> 32) != want) {
-                        if (clock64() - w0 > kWaitCycles) break;
+                        if (clock64() - w0 > p.wait_cycles) break;
                         __nanosleep(128);
                     }
                 }
@@ -481,7 +489,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                         all = all && ((uint32_t)(w[j] >> 32) == want);
                     }
                     if (all) break;
-                    if (clock64() - w0 > kWaitCycles) {
+                    if (clock64() - w0 > p.wait_cycles) {
                         late = true;
                         break;
                     }
@@ -687,10 +695,86 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.BH = (int)BH;
     p.nc = (int)nc;
     p.NH = (int)NH;
+    p.first_ticket = 0;
+    p.wait_cycles = kWaitCycles;
     phase_prep_kernel<<<(unsigned)BH, 256, 0, st>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     return NH == 1 ? launch_fused<1>(p, BH * nc, st) : launch_fused<2>(p, BH * nc, st);
+}
+
+// Failure-detection self-test: a two-sequence, two-chunk forward whose
+// tickets start at the second chunk, so no CTA ever publishes the first
+// chunk's state and the hand-off wait of the second chunk must give up after
+// `wait_cycles`.  Returns the kernel's error bits (bit 0: a hand-off wait
+// timed out) through *err_bits after synchronising the stream.
+cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cudaStream_t st) {
+    const int Bz = 1, T = 2 * CH, H = 2, N = NS, P = PD;
+    const size_t nx = (size_t)Bz * T * H * P, nb = (size_t)Bz * T * H * N, nt = (size_t)Bz * T * H;
+    const size_t ws_bytes = tc_forward_workspace_bytes(Bz, T, H, N);
+    const size_t total = (2 * nx + 2 * nb) * sizeof(float2) + nt * sizeof(float) + H * (sizeof(float2) + sizeof(float)) +
+                         (size_t)Bz * H * N * P * sizeof(float2) + ws_bytes + 8 * 256;
+    unsigned char* buf = nullptr;
+    cudaError_t e = cudaMallocAsync(reinterpret_cast<void**>(&buf), total, st);
+    if (e != cudaSuccess) return e;
+    e = cudaMemsetAsync(buf, 0, total, st);  // zero inputs: any values would do
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        unsigned char* q = buf + off;
+        off += (bytes + 255) / 256 * 256;
+        return q;
+    };
+    FwdArgs a;
+    a.Bz = Bz;
+    a.T = T;
+    a.H = H;
+    a.N = N;
+    a.P = P;
+    a.chunk = CH;
+    a.x = reinterpret_cast<const float2*>(take(nx * sizeof(float2)));
+    a.dt = reinterpret_cast<const float*>(take(nt * sizeof(float)));
+    a.A = reinterpret_cast<const float2*>(take(H * sizeof(float2)));
+    a.B = reinterpret_cast<const float2*>(take(nb * sizeof(float2)));
+    a.C = reinterpret_cast<const float2*>(take(nb * sizeof(float2)));
+    a.D = reinterpret_cast<const float*>(take(H * sizeof(float)));
+    a.y = reinterpret_cast<float2*>(take(nx * sizeof(float2)));
+    a.h_final = reinterpret_cast<float2*>(take((size_t)Bz * H * N * P * sizeof(float2)));
+    unsigned char* ws = take(ws_bytes);
+    TcParams p;
+    const int64_t BH = Bz * H, nc = 2;
+    unsigned char* w = ws;
+    p.ring = reinterpret_cast<unsigned long long*>(w);
+    w += (size_t)BH * 1 * RING * 2 * PD * NS * sizeof(unsigned long long);
+    p.ticket = reinterpret_cast<int*>(w);
+    p.err = reinterpret_cast<int*>(w) + 1;
+    w += 256;
+    p.phi = reinterpret_cast<float*>(w);
+    p.x = reinterpret_cast<const float4*>(a.x);
+    p.dt = a.dt;
+    p.A = a.A;
+    p.B = reinterpret_cast<const float4*>(a.B);
+    p.C = reinterpret_cast<const float4*>(a.C);
+    p.D = a.D;
+    p.y = a.y;
+    p.h_final = a.h_final;
+    p.T = T;
+    p.H = H;
+    p.BH = (int)BH;
+    p.nc = (int)nc;
+    p.NH = 1;
+    p.first_ticket = (int)BH;  // chunk 0 of every sequence is never taken
+    p.wait_cycles = wait_cycles;
+    if (e == cudaSuccess) {
+        phase_prep_kernel<<<(unsigned)BH, 256, 0, st>>>(p);
+        e = cudaGetLastError();
+    }
+    if (e == cudaSuccess) e = launch_fused<1>(p, BH * nc, st);
+    int bits = -1;
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
+    cudaFreeAsync(buf, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (err_bits) *err_bits = bits;
+    return e;
 }
 
 }  // namespace cssd

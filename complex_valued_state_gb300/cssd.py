@@ -32,7 +32,8 @@ STATUS = {
 
 # Every symbol include/cssd.h declares.
 EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward",
-           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_profile_events", "cssd_status_string")
+           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_profile_events", "cssd_selftest_handoff_timeout",
+           "cssd_status_string")
 
 # Scratch array size of cssd_chunked_forward_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -73,6 +74,8 @@ def load(path: str = LIB_PATH):
             lib.cssd_step.restype = ctypes.c_int
             lib.cssd_profile_events.argtypes = [vp, vp]
             lib.cssd_profile_events.restype = ctypes.c_int
+            lib.cssd_selftest_handoff_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int), vp]
+            lib.cssd_selftest_handoff_timeout.restype = ctypes.c_int
             lib.cssd_status_string.argtypes = [ctypes.c_int]
             lib.cssd_status_string.restype = ctypes.c_char_p
             _lib = lib
@@ -121,6 +124,19 @@ def profile_events(begin=None, end=None):
     st = load().cssd_profile_events(h(begin), h(end))
     if st != CSSD_OK:
         raise CssdError(st, "cssd_profile_events")
+
+
+def selftest_handoff_timeout(wait_cycles: int = 2_000_000, stream=None) -> int:
+    """Run the forward with a predecessor chunk that never publishes; return the
+    kernel's error bits (bit 0 set = the bounded hand-off wait gave up)."""
+    import torch as _t
+
+    bits = ctypes.c_int(-1)
+    st = load().cssd_selftest_handoff_timeout(int(wait_cycles), ctypes.byref(bits),
+                                              _stream_handle(stream, _t.device("cuda", _t.cuda.current_device())))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_selftest_handoff_timeout")
+    return int(bits.value)
 
 
 def workspace_bytes(batch: int, seqlen: int, nheads: int, dstate: int, headdim: int, chunk: int) -> int:

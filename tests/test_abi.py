@@ -95,6 +95,12 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert _step(lib, (1, 1, 1, 16, 16), {"y": 0x10004}) == -4
 
 
+def test_selftest_argument_errors(lib):
+    bits = ctypes.c_int(0)
+    assert lib.cssd_selftest_handoff_timeout(1000, None, None) == -1
+    assert lib.cssd_selftest_handoff_timeout(0, ctypes.byref(bits), None) == -2
+
+
 def test_binding_rejects_wrong_dtypes_and_shapes():
     import torch
 
