@@ -11,9 +11,9 @@ size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int6
     return seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);
 }
 
-int forward_launches(int64_t, int64_t, int64_t, int64_t N, int64_t P, int chunk) {
-    return tc_forward_supported(N, P, chunk) ? 2 : 3;
-}
+// Tensor-core path: two prep kernels and the chunk kernel; CUDA-core path:
+// chunk states, scan, readout.
+int forward_launches(int64_t, int64_t, int64_t, int64_t, int64_t, int) { return 3; }
 
 cudaError_t launch_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     if (tc_forward_supported(a.N, a.P, a.chunk)) return launch_tc_forward(a, ws, st);

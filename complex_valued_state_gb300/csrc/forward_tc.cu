@@ -96,6 +96,7 @@ struct TcParams {
     unsigned long long* ring;  // [BH][RING][2][P][N] tagged cells
     int* ticket;       // [1]
     float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
+    float2* tok;       // [BH][nc][CH] per token: (rho_l, theta_l) within the chunk
     int* err;          // [1] error bits
     int T, H, BH, nc, NH;
     int first_ticket;       // tickets start here (0 in normal use)
@@ -136,83 +137,82 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CPT])
 }
 
 // ------------------------------------------------------------------ prep
-// Per sequence: the phase accumulated before each chunk, Phi_c =
-// beta * sum_{t < c*CH} softplus(dt_t) (mod 2 pi, accumulated in double),
-// clearing of the sequence's hand-off cells, and reset of the ticket.
-__global__ void __launch_bounds__(256) phase_prep_kernel(TcParams p) {
-    const int bh = blockIdx.x;
-    const int b = bh / p.H, h = bh % p.H;
-    const float beta = p.A[h].y;
-    __shared__ double wsum[8];
-    __shared__ double carry;
-    __shared__ double sth[256];
+// Two small kernels before the chunk kernel.
+//
+// chunk_prep_kernel: one warp per (sequence, 64-token chunk).  Inclusive
+// cumsum of softplus(dt) over the chunk's tokens (padded tokens add nothing),
+// stored per token as rho_l = alpha cs_l and theta_l = beta cs_l, and the
+// chunk's phase total beta cs_63.  The same CTAs clear the hand-off words.
+__global__ void __launch_bounds__(256) chunk_prep_kernel(TcParams p) {
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);  // global warp = bh * nc + c
     {
-        ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring + (size_t)bh * p.NH * RING * 2 * PD * NS);
-        for (int i = threadIdx.x; i < p.NH * RING * PD * NS; i += 256) cells[i] = make_ulonglong2(0ull, 0ull);
+        // hand-off words: NH * RING * 2 * 64 * 64 per sequence, spread over all threads
+        const size_t words = (size_t)p.BH * p.NH * RING * 2 * PD * NS;
+        ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring);
+        const size_t nthreads = (size_t)gridDim.x * blockDim.x;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < words / 2; i += nthreads)
+            cells[i] = make_ulonglong2(0ull, 0ull);
     }
-    if (threadIdx.x == 0) {
-        carry = 0.0;
-        if (bh == 0) {
-            *p.ticket = p.first_ticket;
-            *p.err = 0;
-        }
-    }
-    __syncthreads();
-    const double two_pi = 6.283185307179586476925286766559;
-    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    if (gw >= p.BH * p.nc) return;
+    const int bh = gw / p.nc, c = gw - bh * p.nc;
+    const int b = bh / p.H, h = bh % p.H;
+    const float alpha = p.A[h].x, beta = p.A[h].y;
     const float* dtb = p.dt + (size_t)b * p.T * p.H + h;  // token t at dtb[t * H]
-    for (int c0 = 0; c0 < p.nc; c0 += 256) {
-        // Phase total of chunks c0 .. c0+255: warp w sums chunks c0 + w + 8k,
-        // two tokens per lane, eight chunks' loads in flight at a time.
-        for (int k = 0; k < 32; k += 4) {
-            float v[4][2];
+    float v[2];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + wid + 8 * (k + u);
+    for (int hh = 0; hh < 2; ++hh) {
+        const int t = c * CH + hh * 32 + lane;
+        v[hh] = (t < p.T) ? __ldg(dtb + (size_t)t * p.H) : 0.f;
+    }
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = c * CH + hh * 32 + lane;
-                    v[u][hh] = (c < p.nc && t < p.T) ? __ldg(dtb + (size_t)t * p.H) : 0.f;
-                }
-            }
+    for (int hh = 0; hh < 2; ++hh) {
+        const int t = c * CH + hh * 32 + lane;
+        v[hh] = (t < p.T) ? softplusf(v[hh]) : 0.f;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int c = c0 + wid + 8 * (k + u);
-                float sum = 0.f;
-#pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    const int t = c * CH + hh * 32 + lane;
-                    if (c < p.nc && t < p.T) sum += softplusf(v[u][hh]);
-                }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-                if (lane == 0) sth[wid + 8 * (k + u)] = (double)(sum * beta);
-            }
+        for (int o = 1; o < 32; o <<= 1) {
+            const float u = __shfl_up_sync(0xffffffffu, v[hh], o);
+            if (lane >= o) v[hh] += u;
         }
-        __syncthreads();
-        const int c = c0 + threadIdx.x;
-        const double th = (c < p.nc) ? sth[threadIdx.x] : 0.0;
-        // block-wide inclusive scan of th
+    }
+    v[1] += __shfl_sync(0xffffffffu, v[0], 31);
+    float2* out = p.tok + (size_t)gw * CH;
+    out[lane] = make_float2(v[0] * alpha, v[0] * beta);
+    out[32 + lane] = make_float2(v[1] * alpha, v[1] * beta);
+    if (lane == 31) p.phi[gw] = v[1] * beta;  // phase total, turned into Phi_c below
+}
+
+// phase_scan_kernel: one warp per sequence.  Phi_c = sum of the phase totals of
+// the chunks before c, accumulated in double and reduced mod 2 pi, written over
+// the totals; resets the ticket and the error word.
+__global__ void __launch_bounds__(256) phase_scan_kernel(TcParams p) {
+    const int lane = threadIdx.x & 31;
+    const int bh = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        *p.ticket = p.first_ticket;
+        *p.err = 0;
+    }
+    if (bh >= p.BH) return;
+    const double two_pi = 6.283185307179586476925286766559;
+    float* ph = p.phi + (size_t)bh * p.nc;
+    double carry = 0.0;
+    for (int c0 = 0; c0 < p.nc; c0 += 32) {
+        const int c = c0 + lane;
+        const double th = (c < p.nc) ? (double)ph[c] : 0.0;
         double v = th;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const double u = __shfl_up_sync(0xffffffffu, v, o);
             if (lane >= o) v += u;
         }
-        if (lane == 31) wsum[wid] = v;
-        __syncthreads();
-        double before = carry;
-        for (int w = 0; w < wid; ++w) before += wsum[w];
-        const double excl = before + v - th;
+        const double excl = carry + v - th;
         if (c < p.nc) {
             double r = fmod(excl, two_pi);
             if (r > 3.141592653589793) r -= two_pi;
             if (r < -3.141592653589793) r += two_pi;
-            p.phi[(size_t)bh * p.nc + c] = (float)r;
+            ph[c] = (float)r;
         }
-        __syncthreads();
-        if (threadIdx.x == 255) carry = fmod(excl + th, two_pi);
-        __syncthreads();
+        carry = fmod(carry + __shfl_sync(0xffffffffu, v, 31), two_pi);
     }
 }
 
@@ -265,7 +265,6 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     const int t0 = c * CH;
     const size_t row0 = ((size_t)b * p.T + t0) * p.H + h;  // token row of l = 0
     const size_t rstride = (size_t)p.H;                    // rows between tokens
-    const float phi_c = p.phi[(size_t)bh * p.nc + c];
     const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
 
     // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
@@ -291,8 +290,12 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     // ---- 0. inputs in flight at once: dt first (the rotations depend on
     // it), raw X rows (and, for one half, raw B rows) by cp.async into S2 / S3,
     // the C half into registers.
-    float dt_raw = 0.f;
-    if (tid < CH && t0 + tid < p.T) dt_raw = __ldg(p.dt + row0 + (size_t)tid * rstride);
+    float2 tk = make_float2(0.f, 0.f);  // (rho_l, theta_l) of this thread's token
+    float phi_c = 0.f;                  // phase accumulated before the chunk
+    if (tid < CH) {
+        tk = __ldcg(p.tok + ((size_t)bh * p.nc + c) * CH + tid);
+        phi_c = __ldcg(p.phi + (size_t)bh * p.nc + c);
+    }
 #pragma unroll
     for (int i = 0; i < IT; ++i) {
         const int e = tid + NT * i;  // row l = e / 32, 16-byte chunk j = e % 32
@@ -306,29 +309,11 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     float4 cv[IT];
     load_half(p.C, 0, cv);
 
-    // ---- 1. per-token log-steps, their inclusive cumsums, and the rotations
-    if (tid < CH) {
-        const float sp = (t0 + tid < p.T) ? softplusf(dt_raw) : 0.f;
-        float v = sp;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += u;
-        }
-        reinterpret_cast<float*>(s_rot)[tid] = v;  // per-warp partial sums
-    }
-    __syncthreads();
-    float th_mine = 0.f;
-    if (tid < CH) {
-        float v = reinterpret_cast<float*>(s_rot)[tid];
-        if (tid >= 32) v += reinterpret_cast<float*>(s_rot)[31];
-        s_rho[tid] = v * Ah.x;
-        th_mine = v * Ah.y;
-    }
-    __syncthreads();
+    // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
     if (tid < CH) {
         float sn, cs;
-        sincosf(phi_c + th_mine, &sn, &cs);  // Theta_l = Phi_c + theta_l
+        sincosf(phi_c + tk.y, &sn, &cs);
+        s_rho[tid] = tk.x;
         s_rot[tid] = make_float2(cs, sn);
         if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
     }
@@ -651,7 +636,17 @@ size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N) {
     size_t off = (size_t)BH * NH * RING * 2 * PD * NS * sizeof(unsigned long long);  // hand-off cells
     off += 256;                                                                       // ticket, err
     off += ((size_t)BH * nc * sizeof(float) + 255) / 256 * 256;                       // phi
+    off += (size_t)BH * nc * CH * sizeof(float2);                                     // per-token table
     return off;
+}
+
+static cudaError_t launch_prep(const TcParams& p, cudaStream_t st) {
+    const int64_t warps = (int64_t)p.BH * p.nc;
+    chunk_prep_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    phase_scan_kernel<<<(unsigned)((p.BH + 7) / 8), 256, 0, st>>>(p);
+    return cudaGetLastError();
 }
 
 template <int NH>
@@ -682,6 +677,8 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.err = reinterpret_cast<int*>(w) + 1;
     w += 256;
     p.phi = reinterpret_cast<float*>(w);
+    w += ((size_t)BH * nc * sizeof(float) + 255) / 256 * 256;
+    p.tok = reinterpret_cast<float2*>(w);
     p.x = reinterpret_cast<const float4*>(a.x);
     p.dt = a.dt;
     p.A = a.A;
@@ -697,8 +694,7 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.NH = (int)NH;
     p.first_ticket = 0;
     p.wait_cycles = kWaitCycles;
-    phase_prep_kernel<<<(unsigned)BH, 256, 0, st>>>(p);
-    const cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_prep(p, st);
     if (e != cudaSuccess) return e;
     return NH == 1 ? launch_fused<1>(p, BH * nc, st) : launch_fused<2>(p, BH * nc, st);
 }
@@ -749,6 +745,8 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.err = reinterpret_cast<int*>(w) + 1;
     w += 256;
     p.phi = reinterpret_cast<float*>(w);
+    w += ((size_t)BH * nc * sizeof(float) + 255) / 256 * 256;
+    p.tok = reinterpret_cast<float2*>(w);
     p.x = reinterpret_cast<const float4*>(a.x);
     p.dt = a.dt;
     p.A = a.A;
@@ -764,10 +762,7 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.NH = 1;
     p.first_ticket = (int)BH;  // chunk 0 of every sequence is never taken
     p.wait_cycles = wait_cycles;
-    if (e == cudaSuccess) {
-        phase_prep_kernel<<<(unsigned)BH, 256, 0, st>>>(p);
-        e = cudaGetLastError();
-    }
+    if (e == cudaSuccess) e = launch_prep(p, st);
     if (e == cudaSuccess) e = launch_fused<1>(p, BH * nc, st);
     int bits = -1;
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
