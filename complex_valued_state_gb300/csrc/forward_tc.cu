@@ -71,10 +71,11 @@ __device__ __forceinline__ uint32_t koff(int row, int k, int rows) {
 }
 
 // Round an fp32 value to the nearest TF32 value (10 explicit mantissa bits),
-// ties away from zero: add half a TF32 unit to the magnitude bits, then clear
-// the 13 low bits.  Two integer operations.
+// ties away from zero; the result keeps the fp32 format with 13 zero low bits.
 __device__ __forceinline__ float tf32r(float v) {
-    return __uint_as_float((__float_as_uint(v) + 0x1000u) & 0xFFFFE000u);
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
 }
 
 __device__ __forceinline__ void st_f32(unsigned char* base, uint32_t off, float v) {
@@ -267,24 +268,26 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     const size_t rstride = (size_t)p.H;                    // rows between tokens
     const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
 
-    // Item e in [0, 2048): float4 (two complex) of a 64 x 64 complex tile,
-    // mapped so that 16 consecutive items fill one 8-row core matrix.
-    auto item = [&](int i, int& l, int& n) {
-        const int e = tid + NT * i;
-        const int half = e & 1, r8 = (e >> 1) & 7, kc = (e >> 4) & 15, g = e >> 8;
-        l = g * 8 + r8;
-        n = kc * 4 + half * 2;
-    };
+    // This thread's items of a 64 x 64 complex tile: the column pair
+    // (n0, n0 + 1) of rows l0 + 16 i, i < IT, so that 16 consecutive threads
+    // fill one 8-row core matrix.  Every offset below is a per-thread base plus
+    // a constant step in i.
+    static_assert(NT == 512 && IT == 4, "item mapping is laid out for 512 threads");
+    const int l0 = (tid >> 8) * 8 + ((tid >> 1) & 7);
+    const int n0 = ((tid >> 4) & 15) * 4 + (tid & 1) * 2;
+    const uint32_t o_raw = raw_off(l0, n0 >> 1);  // raw tile, + 8192 i
+    const uint32_t o_kl64 = koff(n0, l0, 64);     // plane with rows n, K = l: + 4096 i
+    const uint32_t o_lk64 = koff(l0, n0, 64);     // plane with rows l, K = n: + 256 i
+    const uint32_t o_kl192 = koff(n0, l0, 192);   // stack with rows n, K = l: + 12288 i
+    const uint32_t o_lk192 = koff(l0, n0, 192);   // stack with rows l, K = n: + 256 i
+    constexpr uint32_t BLK = 1024;                // 64 rows further down a stack
     // 64 columns (half hf) of a token-major [.., N] complex tile, into registers.
     auto load_half = [&](const float4* src, int hf, float4 (&v)[IT]) {
+        const float4* g = src + (row0 + (size_t)l0 * rstride) * (N / 2) + hf * 32 + (n0 >> 1);
+        const size_t step = 16 * rstride * (N / 2);
 #pragma unroll
-        for (int i = 0; i < IT; ++i) {
-            int l, n;
-            item(i, l, n);
-            const bool ok = t0 + l < p.T;
-            v[i] = ok ? __ldg(src + (row0 + (size_t)l * rstride) * (N / 2) + hf * 32 + (n >> 1))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+        for (int i = 0; i < IT; ++i)
+            v[i] = (t0 + l0 + 16 * i < p.T) ? __ldg(g + i * step) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
 
     // ---- 0. inputs in flight at once: dt first (the rotations depend on
@@ -296,14 +299,20 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         tk = __ldcg(p.tok + ((size_t)bh * p.nc + c) * CH + tid);
         phi_c = __ldcg(p.phi + (size_t)bh * p.nc + c);
     }
+    {
+        // warp w copies rows w + 16 i, one 16-byte chunk per lane
+        const int lr = tid >> 5, j = tid & 31;
+        const uint32_t o = raw_off(lr, j);
+        const float4* gb = p.B + row0 * (N / 2) + j;
+        const float4* gx = p.x + row0 * (PD / 2) + j;
+        const size_t sb = 16 * rstride * (N / 2), sx = 16 * rstride * (PD / 2);
+        const size_t rb = (size_t)lr * rstride * (N / 2), rx = (size_t)lr * rstride * (PD / 2);
 #pragma unroll
-    for (int i = 0; i < IT; ++i) {
-        const int e = tid + NT * i;  // row l = e / 32, 16-byte chunk j = e % 32
-        const int l = e >> 5, j = e & 31;
-        const bool ok = t0 + l < p.T;
-        const size_t row = row0 + (ok ? (size_t)l * rstride : 0);
-        cp_async16(a3 + raw_off(l, j), p.B + row * (N / 2) + j, ok);
-        cp_async16(a2 + raw_off(l, j), p.x + row * (PD / 2) + j, ok);
+        for (int i = 0; i < IT; ++i) {
+            const bool ok = t0 + lr + 16 * i < p.T;
+            cp_async16(a3 + o + 8192 * i, ok ? gb + rb + i * sb : gb, ok);
+            cp_async16(a2 + o + 8192 * i, ok ? gx + rx + i * sx : gx, ok);
+        }
     }
     cp_async_commit();
     float4 cv[IT];
@@ -365,20 +374,15 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     {
         float4 xv[IT];
 #pragma unroll
-        for (int i = 0; i < IT; ++i) {
-            int l, n;
-            item(i, l, n);
-            xv[i] = *reinterpret_cast<const float4*>(sm2 + raw_off(l, n >> 1));
-        }
+        for (int i = 0; i < IT; ++i) xv[i] = *reinterpret_cast<const float4*>(sm2 + o_raw + 8192 * i);
         __syncthreads();  // raw X is overwritten below
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
-            int l, n;
-            item(i, l, n);
-            st_f32(sm2, koff(n, l, 64), tf32r(xv[i].x));
-            st_f32(sm2, koff(n + 1, l, 64), tf32r(xv[i].z));
-            st_f32(sm2 + PLANE_BYTES, koff(n, l, 64), tf32r(xv[i].y));
-            st_f32(sm2 + PLANE_BYTES, koff(n + 1, l, 64), tf32r(xv[i].w));
+            const uint32_t o = o_kl64 + 4096 * i;  // rows p = n0, n0 + 1; K = l
+            st_f32(sm2, o, tf32r(xv[i].x));
+            st_f32(sm2, o + 16, tf32r(xv[i].z));
+            st_f32(sm2 + PLANE_BYTES, o, tf32r(xv[i].y));
+            st_f32(sm2 + PLANE_BYTES, o + 16, tf32r(xv[i].w));
         }
     }
 
@@ -390,11 +394,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
             float4 bv[IT];
             if (hf == 0) {
 #pragma unroll
-                for (int i = 0; i < IT; ++i) {
-                    int l, n;
-                    item(i, l, n);
-                    bv[i] = *reinterpret_cast<const float4*>(sm3 + raw_off(l, n >> 1));
-                }
+                for (int i = 0; i < IT; ++i) bv[i] = *reinterpret_cast<const float4*>(sm3 + o_raw + 8192 * i);
             } else {
                 load_half(p.B, hf, bv);
                 wait_bar(&mbar[2], ph ^ 1);  // Y_off of the previous half has read Ct and H
@@ -402,24 +402,25 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
             __syncthreads();  // raw B (half 0) and last half's operands are overwritten below
 #pragma unroll
             for (int i = 0; i < IT; ++i) {
-                int l, n;
-                item(i, l, n);
+                const int l = l0 + 16 * i;
                 const float cs = s_rot[l].x, sn = s_rot[l].y;
                 // Bt = e^{-i Theta} B
                 const float b0r = cs * bv[i].x + sn * bv[i].y, b0i = cs * bv[i].y - sn * bv[i].x;
                 const float b1r = cs * bv[i].z + sn * bv[i].w, b1i = cs * bv[i].w - sn * bv[i].z;
-                st_f32x2(sm3, koff(l, n, 64), tf32r(b0r), tf32r(b1r));
-                st_f32x2(sm3 + PLANE_BYTES, koff(l, n, 64), tf32r(b0i), tf32r(b1i));
+                const uint32_t ob = o_lk64 + 256 * i;
+                st_f32x2(sm3, ob, tf32r(b0r), tf32r(b1r));
+                st_f32x2(sm3 + PLANE_BYTES, ob, tf32r(b0i), tf32r(b1i));
                 // F[n][l] = exp(rho_end - rho_l) Bt[l][n]
                 const float ds = __expf(rho_end - s_rho[l]);
                 const float f0r = tf32r(ds * b0r), f0i = tf32r(ds * b0i), f1r = tf32r(ds * b1r),
                             f1i = tf32r(ds * b1i);
-                st_f32(sm1, koff(n, l, 192), -f0i);
-                st_f32(sm1, koff(n + 1, l, 192), -f1i);
-                st_f32(sm1, koff(64 + n, l, 192), f0r);
-                st_f32(sm1, koff(64 + n + 1, l, 192), f1r);
-                st_f32(sm1, koff(128 + n, l, 192), f0i);
-                st_f32(sm1, koff(128 + n + 1, l, 192), f1i);
+                const uint32_t of = o_kl192 + 12288 * i;
+                st_f32(sm1, of, -f0i);
+                st_f32(sm1, of + 16, -f1i);
+                st_f32(sm1, of + BLK, f0r);
+                st_f32(sm1, of + BLK + 16, f1r);
+                st_f32(sm1, of + 2 * BLK, f0i);
+                st_f32(sm1, of + 2 * BLK + 16, f1i);
             }
         }
         issue(tmem + COL_S, a1, a2, false, &mbar[0]);
@@ -429,14 +430,14 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         wait_bar(&mbar[0], ph);
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
-            int l, n;
-            item(i, l, n);
+            const int l = l0 + 16 * i;
             const float cs = s_rot[l].x, sn = s_rot[l].y;
             const float c0r = tf32r(cs * cv[i].x - sn * cv[i].y), c0i = tf32r(cs * cv[i].y + sn * cv[i].x);
             const float c1r = tf32r(cs * cv[i].z - sn * cv[i].w), c1i = tf32r(cs * cv[i].w + sn * cv[i].z);
-            st_f32x2(sm1, koff(l, n, 192), -c0i, -c1i);
-            st_f32x2(sm1, koff(64 + l, n, 192), c0r, c1r);
-            st_f32x2(sm1, koff(128 + l, n, 192), c0i, c1i);
+            const uint32_t oc = o_lk192 + 256 * i;
+            st_f32x2(sm1, oc, -c0i, -c1i);
+            st_f32x2(sm1, oc + BLK, c0r, c1r);
+            st_f32x2(sm1, oc + 2 * BLK, c0i, c1i);
         }
         issue(tmem + COL_G, a1, a3, hf > 0, &mbar[1]);
 
@@ -516,14 +517,14 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                     }
                 }
             }
-            // now hv[j] = H_part[n0 + j][c0col + (lane mod CPT)], n0 = first row of the lane group
-            const int n0 = lrow - (lane & (CPT - 1));
+            // now hv[j] = H_part[nb + j][c0col + (lane mod CPT)], nb = first row of the lane group
+            const int nb = lrow - (lane & (CPT - 1));
             const int pcol = c0col + (lane & (CPT - 1));
             wait_bar(&mbar[1], ph);
-            unsigned char* plane = sm3 + part * PLANE_BYTES;
+            unsigned char* plane = sm3 + part * PLANE_BYTES + koff(pcol, nb, 64);
 #pragma unroll
-            for (int k4 = 0; k4 < CPT / 4; ++k4)
-                *reinterpret_cast<float4*>(plane + koff(pcol, n0 + 4 * k4, 64)) = make_float4(
+            for (int k4 = 0; k4 < CPT / 4; ++k4)  // K = nb + 4 k4: one core matrix further per step
+                *reinterpret_cast<float4*>(plane + 1024 * k4) = make_float4(
                     tf32r(hv[4 * k4]), tf32r(hv[4 * k4 + 1]), tf32r(hv[4 * k4 + 2]), tf32r(hv[4 * k4 + 3]));
         }
         issue(tmem + COL_OFF, a1, a3, hf > 0, &mbar[2]);  // Y_off' += Ct H_c
@@ -547,16 +548,17 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
             m[j] = tf32r(__expf(arg) * __uint_as_float(r[j]));
         }
         wait_bar(&mbar[2], (NH - 1) & 1);
-        // 16-byte stores: four consecutive K of one row fill one core-matrix row
+        // 16-byte stores: four consecutive K of one row fill one core-matrix
+        // row; K + 4 is one core matrix (24 row groups) further
+        unsigned char* mrow = sm1 + koff(lrow, c0col, 192);
 #pragma unroll
         for (int k4 = 0; k4 < CPT / 4; ++k4) {
             const float4 v = make_float4(m[4 * k4], m[4 * k4 + 1], m[4 * k4 + 2], m[4 * k4 + 3]);
             if (part == 0) {
-                *reinterpret_cast<float4*>(sm1 + koff(64 + lrow, c0col + 4 * k4, 192)) = v;
+                *reinterpret_cast<float4*>(mrow + BLK + 3072 * k4) = v;
             } else {
-                *reinterpret_cast<float4*>(sm1 + koff(128 + lrow, c0col + 4 * k4, 192)) = v;
-                *reinterpret_cast<float4*>(sm1 + koff(lrow, c0col + 4 * k4, 192)) =
-                    make_float4(-v.x, -v.y, -v.z, -v.w);
+                *reinterpret_cast<float4*>(mrow + 2 * BLK + 3072 * k4) = v;
+                *reinterpret_cast<float4*>(mrow + 3072 * k4) = make_float4(-v.x, -v.y, -v.z, -v.w);
             }
         }
     }
@@ -565,14 +567,15 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     // ---- 8. y = Y_diag + e^{rho_l} Y_off' + D x.  The skip term uses the
     // exact fp32 input (an L2 hit, fetched while Y_diag runs), not the
     // tf32-rounded X planes.
-    constexpr int YI = CH * PD / NT;  // output elements per thread
+    constexpr int YI = CH * PD / NT;  // output elements per thread: rows ly + 8 k, column py
+    const int ly = tid >> 6, py = tid & 63;
+    const size_t ystep = 8 * rstride * PD;
+    const size_t yoff = (row0 + (size_t)ly * rstride) * PD + py;
     float2 xs[YI];
 #pragma unroll
-    for (int k = 0; k < YI; ++k) {
-        const int i = tid + NT * k, l = i >> 6, pp = i & 63;
-        xs[k] = (t0 + l < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + (row0 + (size_t)l * rstride) * PD + pp)
-                               : make_float2(0.f, 0.f);
-    }
+    for (int k = 0; k < YI; ++k)
+        xs[k] = (t0 + ly + 8 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
+                                        : make_float2(0.f, 0.f);
     {
         wait_bar(&mbar[3], 0);
         tc::fence_after_sync();
@@ -589,14 +592,12 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     __syncthreads();
     {
         const float Dh = p.D[h];
-        const float* stage = reinterpret_cast<const float*>(sm1);
+        const float* stage = reinterpret_cast<const float*>(sm1) + ly * STAGE_LD + 2 * py;
 #pragma unroll
         for (int k = 0; k < YI; ++k) {
-            const int i = tid + NT * k, l = i >> 6, pp = i & 63;
-            if (t0 + l < p.T) {
-                const size_t row = row0 + (size_t)l * rstride;
-                const float yr = stage[l * STAGE_LD + 2 * pp], yi = stage[l * STAGE_LD + 2 * pp + 1];
-                p.y[row * PD + pp] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
+            if (t0 + ly + 8 * k < p.T) {
+                const float yr = stage[8 * k * STAGE_LD], yi = stage[8 * k * STAGE_LD + 1];
+                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
             }
         }
     }
