@@ -266,9 +266,10 @@ def run_ours(args, rank, world, local):
     e_ms = e0.elapsed_time(e1) / e_steps
     e_ms = reduce_max(pg, e_ms, dev)
 
-    decode = None
+    decode = const_input = None
     if not args.no_decode:
         decode = bench_decode(args, dev)
+        const_input = bench_const_input(args, dev)
     long_seq = None
     if not args.no_long:
         long_seq = bench_long_seq(args, dev)
@@ -302,6 +303,8 @@ def run_ours(args, rank, world, local):
     }
     if decode:
         out["decode"] = decode
+    if const_input:
+        out["const_input"] = const_input
     if long_seq:
         out["long_seq"] = long_seq
     if world == 1 and not args.no_cpu_baseline:
@@ -351,6 +354,57 @@ def bench_decode(args, dev):
             "roofline": {"bound": "hbm", "kernel": "step_kernel", "achieved": round(gbs, 1), "peak": hbm, "unit": "GB/s",
                          "frac": round(gbs / hbm, 4), "peak_kind": kind,
                          "traffic": recorded_traffic("step_kernel", units), "alg_bytes_per_launch": alg}}
+
+
+def bench_const_input(args, dev):
+    """Constant-input shortcuts on the decode shapes: cssd_step_n with the
+    4096-step run of the decode workload (one call), and cssd_step_infinite."""
+    import torch
+
+    from complex_valued_state_gb300 import cssd
+    from complex_valued_state_gb300 import workloads as wl
+
+    w = wl.DECODE
+    nsteps = 4096
+    fx = wl.decode_fixed(w)
+    h = torch.from_numpy(fx["h"]).to(dev)
+    A, D = torch.from_numpy(fx["A"]).to(dev), torch.from_numpy(fx["D"]).to(dev)
+    t = {k: torch.from_numpy(v).to(dev) for k, v in wl.decode_token(w, 0).items()}
+    y = torch.empty((w.batch, w.nheads, w.headdim), dtype=torch.complex64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def timed(fn, n):
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) * 1e3 / n
+
+    n = max(20, 5 * args.steps)
+    us_n = timed(lambda: cssd.step_n(h, t["x"], t["dt"], A, t["B"], t["C"], D, nsteps, y=y), n)
+    us_inf = timed(lambda: cssd.step_infinite(t["x"], t["dt"], A, t["B"], t["C"], D, y=y), n)
+    units = w.batch * w.nheads
+    N, P = w.dstate, w.headdim
+    alg_n = units * (2 * 8 * N * P + 8 * P + 16 * N + 4 + 8 * P)  # state read+write, x, B, C, dt, y
+    alg_inf = units * (8 * P + 16 * N + 4 + 8 * P)  # x, B, C, dt, y: no state
+    hbm, kind = peaks()
+    gbs_n, gbs_inf = alg_n / (us_n / 1e6) / 1e9, alg_inf / (us_inf / 1e6) / 1e9
+    return {"workload": f"decode Bz{w.batch} H{w.nheads} N{N} P{P}, one token held for {nsteps} steps",
+            "metric": "token-heads/s folded into the state (nsteps x heads per call)",
+            "value": round(units * nsteps / (us_n / 1e6), 1), "us_per_call": round(us_n, 3), "calls": n,
+            "roofline": {"bound": "hbm", "kernel": "step_kernel (closed form)", "achieved": round(gbs_n, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(gbs_n / hbm, 4), "peak_kind": kind,
+                         "alg_bytes_per_launch": alg_n},
+            "infinite": {"us_per_call": round(us_inf, 3), "kernel": "step_infinite_kernel",
+                         "achieved": round(gbs_inf, 1), "unit": "GB/s", "frac": round(gbs_inf / hbm, 4),
+                         "alg_bytes_per_launch": alg_inf,
+                         "note": "back-to-back calls, each with its host argument and pointer checks; the "
+                                 "inputs (%.1f MB) fit in L2" % (alg_inf / 1e6)}}
 
 
 def bench_long_seq(args, dev):

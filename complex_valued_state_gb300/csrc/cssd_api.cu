@@ -66,6 +66,42 @@ thread_local cudaEvent_t g_prof_begin = nullptr;
 thread_local cudaEvent_t g_prof_end = nullptr;
 }  // namespace cssd
 
+namespace {
+// Shared argument checks and launch of cssd_step (nsteps < 0), cssd_step_n
+// (nsteps >= 0) and cssd_step_infinite (no state: with_h = false).
+int step_common(const cssd_dims* d, void* h, const void* x, const float* dt, const void* A, const void* B,
+                       const void* C, const float* D, void* y, int64_t nsteps, bool with_h, cssd_stream_t stream_) {
+    int s = check_dims(d, false);
+    if (s != CSSD_OK) return s;
+    if ((with_h && !h) || !x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
+    if ((with_h && !aligned(h, 16)) || !aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+        !aligned(A, 8) || !aligned(dt, 4) || !aligned(D, 4))
+        return CSSD_ERR_ALIGN;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    if ((s = stream_device(stream, &dev)) != CSSD_OK) return s;
+    if ((s = check_all_device(dev, (const void*)h, x, (const void*)dt, A, B, C, (const void*)D, (const void*)y)) !=
+        CSSD_OK)
+        return s;
+    cssd::StepArgs a;
+    a.Bz = d->batch;
+    a.H = d->nheads;
+    a.N = d->dstate;
+    a.P = d->headdim;
+    a.nsteps = nsteps;
+    a.h = static_cast<float2*>(h);
+    a.x = static_cast<const float2*>(x);
+    a.dt = dt;
+    a.A = static_cast<const float2*>(A);
+    a.B = static_cast<const float2*>(B);
+    a.C = static_cast<const float2*>(C);
+    a.D = D;
+    a.y = static_cast<float2*>(y);
+    const cudaError_t e = with_h ? cssd::launch_step(a, stream) : cssd::launch_step_infinite(a, stream);
+    return e == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+}
+}  // namespace
+
 extern "C" {
 
 int cssd_profile_events(void* ev_begin, void* ev_end) {
@@ -160,32 +196,18 @@ int cssd_chunked_forward(const cssd_dims* d, const void* x, const float* dt, con
 
 int cssd_step(const cssd_dims* d, void* h, const void* x, const float* dt, const void* A, const void* B,
               const void* C, const float* D, void* y, cssd_stream_t stream_) {
-    int s = check_dims(d, false);
-    if (s != CSSD_OK) return s;
-    if (!h || !x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
-    if (!aligned(h, 16) || !aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
-        !aligned(A, 8) || !aligned(dt, 4) || !aligned(D, 4))
-        return CSSD_ERR_ALIGN;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    int dev = 0;
-    if ((s = stream_device(stream, &dev)) != CSSD_OK) return s;
-    if ((s = check_all_device(dev, (const void*)h, x, (const void*)dt, A, B, C, (const void*)D, (const void*)y)) !=
-        CSSD_OK)
-        return s;
-    cssd::StepArgs a;
-    a.Bz = d->batch;
-    a.H = d->nheads;
-    a.N = d->dstate;
-    a.P = d->headdim;
-    a.h = static_cast<float2*>(h);
-    a.x = static_cast<const float2*>(x);
-    a.dt = dt;
-    a.A = static_cast<const float2*>(A);
-    a.B = static_cast<const float2*>(B);
-    a.C = static_cast<const float2*>(C);
-    a.D = D;
-    a.y = static_cast<float2*>(y);
-    return cssd::launch_step(a, stream) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+    return step_common(d, h, x, dt, A, B, C, D, y, -1, true, stream_);
+}
+
+int cssd_step_n(const cssd_dims* d, void* h, const void* x, const float* dt, const void* A, const void* B,
+                const void* C, const float* D, int64_t nsteps, void* y, cssd_stream_t stream_) {
+    if (nsteps < 0) return CSSD_ERR_DIMS;
+    return step_common(d, h, x, dt, A, B, C, D, y, nsteps, true, stream_);
+}
+
+int cssd_step_infinite(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B,
+                       const void* C, const float* D, void* y, cssd_stream_t stream_) {
+    return step_common(d, nullptr, x, dt, A, B, C, D, y, 0, false, stream_);
 }
 
 }  // extern "C"

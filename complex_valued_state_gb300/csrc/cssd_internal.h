@@ -25,6 +25,7 @@ struct FwdArgs {
 
 struct StepArgs {
     int64_t Bz, H, N, P;
+    int64_t nsteps = -1;  // < 0: one ordinary step; >= 0: that many steps of a constant input, in closed form
     float2* h;
     const float2* x;
     const float* dt;
@@ -58,5 +59,7 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
 
 // Decode step (step.cu).
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
+// Output of a constant input held forever (h is not used).
+cudaError_t launch_step_infinite(const StepArgs& a, cudaStream_t stream);
 
 }  // namespace cssd

@@ -32,8 +32,8 @@ STATUS = {
 
 # Every symbol include/cssd.h declares.
 EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward",
-           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_profile_events", "cssd_selftest_handoff_timeout",
-           "cssd_status_string")
+           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_profile_events",
+           "cssd_selftest_handoff_timeout", "cssd_status_string")
 
 # Scratch array size of cssd_chunked_forward_noalloc (bytes).
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -72,6 +72,10 @@ def load(path: str = LIB_PATH):
             lib.cssd_chunked_forward_noalloc.restype = ctypes.c_int
             lib.cssd_step.argtypes = [dims_p] + [vp] * 8 + [vp]
             lib.cssd_step.restype = ctypes.c_int
+            lib.cssd_step_n.argtypes = [dims_p] + [vp] * 7 + [ctypes.c_int64, vp, vp]
+            lib.cssd_step_n.restype = ctypes.c_int
+            lib.cssd_step_infinite.argtypes = [dims_p] + [vp] * 7 + [vp]
+            lib.cssd_step_infinite.restype = ctypes.c_int
             lib.cssd_profile_events.argtypes = [vp, vp]
             lib.cssd_profile_events.restype = ctypes.c_int
             lib.cssd_selftest_handoff_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int), vp]
@@ -223,17 +227,8 @@ def chunked_forward_noalloc(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_fin
     return y, h_final
 
 
-def step(h, x, dt, A, B, C, D, *, y=None, stream=None):
-    """cssd_step on device tensors: h updated in place; returns y.
-
-    h complex64 [Bz,H,N,P]; x complex64 [Bz,H,P]; dt float32 [Bz,H];
-    A complex64 [H]; B, C complex64 [Bz,H,N]; D float32 [H].
-    """
-    lib = load()
-    dev = h.device
-    Bz, H, N, P = h.shape
+def _check_step_inputs(dev, Bz, H, N, P, x, dt, A, B, C, D, y):
     c64, f32 = torch.complex64, torch.float32
-    _check(h, "h", c64, (Bz, H, N, P), dev)
     _check(x, "x", c64, (Bz, H, P), dev)
     _check(dt, "dt", f32, (Bz, H), dev)
     _check(A, "A", c64, (H,), dev)
@@ -243,9 +238,55 @@ def step(h, x, dt, A, B, C, D, *, y=None, stream=None):
     if y is None:
         y = torch.empty((Bz, H, P), dtype=c64, device=dev)
     _check(y, "y", c64, (Bz, H, P), dev)
+    return y
+
+
+def step(h, x, dt, A, B, C, D, *, y=None, stream=None):
+    """cssd_step on device tensors: h updated in place; returns y.
+
+    h complex64 [Bz,H,N,P]; x complex64 [Bz,H,P]; dt float32 [Bz,H];
+    A complex64 [H]; B, C complex64 [Bz,H,N]; D float32 [H].
+    """
+    lib = load()
+    dev = h.device
+    Bz, H, N, P = h.shape
+    _check(h, "h", torch.complex64, (Bz, H, N, P), dev)
+    y = _check_step_inputs(dev, Bz, H, N, P, x, dt, A, B, C, D, y)
     d = Dims(Bz, 1, H, N, P)
     st = lib.cssd_step(ctypes.byref(d), _ptr(h), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y),
                        _stream_handle(stream, dev))
     if st != CSSD_OK:
         raise CssdError(st, "cssd_step")
+    return y
+
+
+def step_n(h, x, dt, A, B, C, D, nsteps, *, y=None, stream=None):
+    """cssd_step_n: `nsteps` steps of the same token in closed form; h updated
+    in place; returns the n-th step's y.  Shapes as in step()."""
+    lib = load()
+    dev = h.device
+    Bz, H, N, P = h.shape
+    _check(h, "h", torch.complex64, (Bz, H, N, P), dev)
+    y = _check_step_inputs(dev, Bz, H, N, P, x, dt, A, B, C, D, y)
+    d = Dims(Bz, 1, H, N, P)
+    st = lib.cssd_step_n(ctypes.byref(d), _ptr(h), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                         ctypes.c_int64(int(nsteps)), _ptr(y), _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_step_n")
+    return y
+
+
+def step_infinite(x, dt, A, B, C, D, *, y=None, stream=None):
+    """cssd_step_infinite: the output of the same token held forever (no
+    state); returns y [Bz,H,P].  Shapes as in step()."""
+    lib = load()
+    dev = x.device
+    Bz, H, P = x.shape
+    N = B.shape[-1]
+    y = _check_step_inputs(dev, Bz, H, N, P, x, dt, A, B, C, D, y)
+    d = Dims(Bz, 1, H, N, P)
+    st = lib.cssd_step_infinite(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y),
+                                _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_step_infinite")
     return y

@@ -134,6 +134,37 @@ int cssd_chunked_forward_noalloc(const cssd_dims* dims, const void* x, const flo
 int cssd_step(const cssd_dims* dims, void* h, const void* x, const float* dt, const void* A,
               const void* B, const void* C, const float* D, void* y, cssd_stream_t stream);
 
+/* `nsteps` decode steps that all feed the same token (x, dt, B, C), in
+ * closed form: the result equals nsteps calls of cssd_step with these inputs
+ * (up to rounding), at the cost of one.  This is the constant-input shortcut
+ * of "Constant-input stepping shortcuts - step_n_approx / step_infinite"
+ * (burn-mamba docs, module step_constant), which there is stated for a block
+ * whose input rotates each step; in this recurrence the rotation is part of
+ * the complex per-step factor a = exp(softplus(dt) A), so the n steps are the
+ * scalar geometric series
+ *     h <- a^n h + g_n B x^T,   g_n = 1 + a + ... + a^(n-1),
+ *     y  = C^T h + D x          (the output of the n-th step).
+ * a^n and g_n are formed per (batch, head) in double, with the angle reduced
+ * mod 2 pi, so n may be large (up to 2^53 keeps n exact).
+ *   Arguments and layouts are those of cssd_step; nsteps >= 0 (0 leaves h
+ *   unchanged and returns C^T h + D x).  nsteps < 0 returns CSSD_ERR_DIMS.
+ *   When |a| > 1 the state grows like |a|^n and overflows to inf for large n,
+ *   as the step-by-step loop would.
+ * Returns a cssd_status. */
+int cssd_step_n(const cssd_dims* dims, void* h, const void* x, const float* dt, const void* A,
+                const void* B, const void* C, const float* D, int64_t nsteps, void* y, cssd_stream_t stream);
+
+/* Output of the same token held forever (the step_infinite shortcut of the
+ * passage above): for |a| < 1 the state's dependence on its start decays like
+ * |a|^n and y tends to
+ *     y_inf = (C^T B) x / (1 - a) + D x,
+ * which needs no state.  Arguments and layouts are those of cssd_step without
+ * h.  The formula is evaluated as written for every a; it is a limit of the
+ * recurrence only when |a| < 1 (Re A < 0), and a = 1 (A = 0) divides by zero.
+ * Returns a cssd_status. */
+int cssd_step_infinite(const cssd_dims* dims, const void* x, const float* dt, const void* A, const void* B,
+                       const void* C, const float* D, void* y, cssd_stream_t stream);
+
 /* Measurement hook.  ev_begin / ev_end are cudaEvent_t handles created by
  * the caller on the device in use; every later cssd_chunked_forward call made
  * from the same host thread records ev_begin on its stream just before the

@@ -95,6 +95,20 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert _step(lib, (1, 1, 1, 16, 16), {"y": 0x10004}) == -4
 
 
+def test_constant_input_argument_errors(lib):
+    ok = cssd.Dims(1, 1, 1, 16, 16)
+    args = [ctypes.c_void_p(0x10000 + 0x100 * i) for i in range(8)]  # h, x, dt, A, B, C, D, y
+    h, x, dt, A, B, C, D, y = args
+    assert lib.cssd_step_n(ctypes.byref(ok), h, x, dt, A, B, C, D, -1, y, None) == -2
+    assert lib.cssd_step_n(None, h, x, dt, A, B, C, D, 5, y, None) == -1
+    assert lib.cssd_step_n(ctypes.byref(ok), None, x, dt, A, B, C, D, 5, y, None) == -1
+    assert lib.cssd_step_n(ctypes.byref(ok), ctypes.c_void_p(0x10008), x, dt, A, B, C, D, 5, y, None) == -4
+    assert lib.cssd_step_n(ctypes.byref(cssd.Dims(1, 1, 1, 24, 16)), h, x, dt, A, B, C, D, 5, y, None) == -3
+    assert lib.cssd_step_infinite(ctypes.byref(ok), x, dt, A, B, C, D, None, None) == -1
+    assert lib.cssd_step_infinite(ctypes.byref(ok), x, dt, A, ctypes.c_void_p(0x10404), C, D, y, None) == -4
+    assert lib.cssd_step_infinite(ctypes.byref(cssd.Dims(0, 1, 1, 16, 16)), x, dt, A, B, C, D, y, None) == -2
+
+
 def test_selftest_argument_errors(lib):
     bits = ctypes.c_int(0)
     assert lib.cssd_selftest_handoff_timeout(1000, None, None) == -1
