@@ -62,8 +62,12 @@ MAMBA2_LAYER = Workload("mamba2_layer", 4, 2048, 24, 64, 64, 64, seed=1)
 LONG_SEQ = Workload("long_seq", 1, 65536, 32, 128, 64, 128, seed=2, kind="slow_decay")
 PAM = Workload("pam", 8, 1024, 12, 64, 64, 64, seed=3, kind="pam")
 DECODE = Workload("decode", 256, 1, 32, 128, 64, 64, seed=4, kind="decode", steps=1000)
+# Per-coordinate Cayley-phase scan at the H-Mamba shapes (16 heads of 16 complex
+# coordinates, 1024-token sequences, chunk 64) and its per-accelerator training
+# batch of 256 sequences; headdim is unused by this recurrence.
+HMAMBA_SCAN = Workload("hmamba_scan", 256, 1024, 16, 16, 16, 64, seed=5, kind="cayley")
 
-WORKLOADS = {w.name: w for w in (TINY, MAMBA2_LAYER, LONG_SEQ, PAM, DECODE)}
+WORKLOADS = {w.name: w for w in (TINY, MAMBA2_LAYER, LONG_SEQ, PAM, DECODE, HMAMBA_SCAN)}
 
 
 def _cgauss(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndarray:
@@ -180,3 +184,37 @@ def random_case(seed: int, Bz: int, T: int, H: int, N: int, P: int, *, dt_mean: 
     A = (_rate_A(rng, H) * np.complex64(a_scale)).astype(np.complex64)
     D = rng.standard_normal(H).astype(np.float32)
     return dict(x=x, dt=dt, A=A, B=B, C=C, D=D)
+
+
+def make_cayley_inputs(w: Workload = HMAMBA_SCAN, seed: int | None = None, *, gate_mean: float = 0.0) -> dict:
+    """Inputs of the per-coordinate Cayley-phase scan (workload `w`'s shapes).
+
+        phi  [Bz,T,H,N] float32    phase parameter, phi = dt/2 (delta + omega)
+        u    [Bz,T,H,N] float32    gate logits
+        b    [Bz,T,H,N] complex64  input projection
+        C    [Bz,T,H,N] complex64  readout projection
+        psi0 [Bz,H,N]   complex64  initial state
+
+    Recipe (the H-Mamba substrate's parameterisation and initialisation): step
+    sizes dt ~ U[0.1, 0.6] per (batch, token, head) (the range of a softplus
+    step floored at 0.1); shifts delta ~ N(0, 0.1^2); base frequencies omega_k
+    on a geometric grid over two decades, [0.05, 5], with alternating sign;
+    gate logits u ~ N(gate_mean, 1) (near zero at initialisation, so gates
+    near 1/2); b, C complex Gaussian with re, im ~ N(0, 1/2); psi0 a complex
+    Gaussian prior per head normalised to unit norm, shared by the batch.
+    Draw order: dt, delta, u, b, C, prior.
+    """
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    Bz, T, H, N = w.batch, w.seqlen, w.nheads, w.dstate
+    dt = rng.uniform(0.1, 0.6, size=(Bz, T, H, 1)).astype(np.float32)
+    delta = (rng.standard_normal((Bz, T, H, N), dtype=np.float32) * np.float32(0.1)).astype(np.float32)
+    omega = np.geomspace(0.05, 5.0, N).astype(np.float32) * np.where(np.arange(N) % 2 == 0, 1, -1).astype(np.float32)
+    phi = (np.float32(0.5) * dt * (delta + omega)).astype(np.float32)
+    del delta
+    u = (rng.standard_normal((Bz, T, H, N), dtype=np.float32) + np.float32(gate_mean)).astype(np.float32)
+    b = _cgauss(rng, (Bz, T, H, N))
+    C = _cgauss(rng, (Bz, T, H, N))
+    prior = _cgauss(rng, (H, N)).astype(np.complex128)
+    prior /= np.linalg.norm(prior, axis=1, keepdims=True)
+    psi0 = np.ascontiguousarray(np.broadcast_to(prior.astype(np.complex64), (Bz, H, N)))
+    return dict(phi=phi, u=u, b=b, C=C, psi0=psi0)

@@ -22,7 +22,7 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRC = os.path.join(_HERE, "cssd_oracle.c")
+_SRCS = [os.path.join(_HERE, "cssd_oracle.c"), os.path.join(_HERE, "cayley_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -30,10 +30,10 @@ _lib = None
 
 def build(force: bool = False) -> str:
     """Compile the oracle with gcc (OpenMP over independent (batch, head) pairs)."""
-    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < max(os.path.getmtime(f) for f in _SRCS):
         tmp = _LIB + f".tmp{os.getpid()}"
         cmd = ["gcc", "-O2", "-std=c11", "-fcx-limited-range", "-fPIC", "-shared", "-fopenmp",
-               _SRC, "-o", tmp, "-lm"]
+               *_SRCS, "-o", tmp, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(tmp, _LIB)
     return _LIB
@@ -51,8 +51,12 @@ def _load():
             lib.oracle_cssd_step.argtypes = [i64] * 4 + [dp] * 8
             lib.oracle_cssd_chunked.argtypes = [i64] * 6 + [dp] * 8
             lib.oracle_geom_closed_form.argtypes = [i64] * 5 + [dp] * 10
+            lib.oracle_cayley_coefficients.argtypes = [i64] + [dp] * 3
+            lib.oracle_cayley_recurrence.argtypes = [i64] * 4 + [dp] * 7
+            lib.oracle_cayley_chunked.argtypes = [i64] * 5 + [ctypes.c_double] + [dp] * 7
             for f in (lib.oracle_cssd_naive, lib.oracle_cssd_step, lib.oracle_cssd_chunked,
-                      lib.oracle_geom_closed_form):
+                      lib.oracle_geom_closed_form, lib.oracle_cayley_coefficients, lib.oracle_cayley_recurrence,
+                      lib.oracle_cayley_chunked):
                 f.restype = None
             _lib = lib
     return _lib
@@ -127,3 +131,43 @@ def geom_closed_form(h0, x, dt, A, B, C, D, nsteps: int):
     lib.oracle_geom_closed_form(Bz, H, N, P, int(nsteps), _p(h0), _p(x), _p(dt), _p(A), _p(B), _p(C),
                                 _p(D), _p(hn), _p(yn), _p(yinf))
     return hn, yn, yinf
+
+
+# ---- per-coordinate Cayley-phase recurrence ("Complex Phase-State Dynamics
+# Reduce the Optimization Steps of Sequence Models", sections 5.2-5.5 and
+# Appendix A, Algorithms 1-2)
+
+def cayley_coefficients(phi, u):
+    """Algorithm 1: a = sigmoid(u) (1 + i phi) / (1 - i phi), elementwise."""
+    lib = _load()
+    phi, u = _r(phi), _r(u)
+    a = np.empty(phi.shape, np.complex128)
+    lib.oracle_cayley_coefficients(phi.size, _p(phi), _p(u), _p(a))
+    return a
+
+
+def cayley_recurrence(phi, u, b, C, psi0=None):
+    """Equation (2) step by step; returns (y [Bz,T,H,N], psi_final [Bz,H,N])."""
+    lib = _load()
+    phi, u, b, C = _r(phi), _r(u), _c(b), _c(C)
+    Bz, T, H, N = phi.shape
+    p0 = None if psi0 is None else _c(psi0)
+    y = np.empty((Bz, T, H, N), np.complex128)
+    pf = np.empty((Bz, H, N), np.complex128)
+    lib.oracle_cayley_recurrence(Bz, T, H, N, _p(phi), _p(u), _p(b), _p(C), None if p0 is None else _p(p0),
+                                 _p(y), _p(pf))
+    return y, pf
+
+
+def cayley_chunked(phi, u, b, C, chunk: int, log_clamp: float = -30.0, psi0=None):
+    """Algorithm 2 (chunked polar scan, cumulative log-gate clamped to
+    [log_clamp, 0]); returns (y, psi_final)."""
+    lib = _load()
+    phi, u, b, C = _r(phi), _r(u), _c(b), _c(C)
+    Bz, T, H, N = phi.shape
+    p0 = None if psi0 is None else _c(psi0)
+    y = np.empty((Bz, T, H, N), np.complex128)
+    pf = np.empty((Bz, H, N), np.complex128)
+    lib.oracle_cayley_chunked(Bz, T, H, N, int(chunk), float(log_clamp), _p(phi), _p(u), _p(b), _p(C),
+                              None if p0 is None else _p(p0), _p(y), _p(pf))
+    return y, pf
