@@ -2,6 +2,7 @@
 // handling, and the launches.  See include/cssd.h for the contract.
 
 #include <cuda_runtime.h>
+#include <math.h>
 #include <stdint.h>
 
 #include "../../include/cssd.h"
@@ -208,6 +209,42 @@ int cssd_step_n(const cssd_dims* d, void* h, const void* x, const float* dt, con
 int cssd_step_infinite(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B,
                        const void* C, const float* D, void* y, cssd_stream_t stream_) {
     return step_common(d, nullptr, x, dt, A, B, C, D, y, 0, false, stream_);
+}
+
+int cssd_cayley_scan(const cssd_dims* d, const float* phi, const float* u, const void* b, const void* C,
+                     const void* psi0, void* y, void* psi_final, int chunk, float log_clamp, cssd_stream_t stream_) {
+    if (!d) return CSSD_ERR_NULL;
+    if (d->batch <= 0 || d->seqlen <= 0 || d->nheads <= 0 || d->dstate <= 0) return CSSD_ERR_DIMS;
+    if (d->seqlen > kMaxInt || d->nheads * d->dstate > kMaxInt || d->batch * d->nheads * d->dstate > kMaxInt)
+        return CSSD_ERR_DIMS;
+    if (chunk < 1) return CSSD_ERR_DIMS;
+    if (!(log_clamp == -INFINITY || (log_clamp >= -80.f && log_clamp <= 0.f))) return CSSD_ERR_DIMS;
+    if (!phi || !u || !b || !C || !y) return CSSD_ERR_NULL;
+    if (!aligned(phi, 4) || !aligned(u, 4) || !aligned(b, 8) || !aligned(C, 8) || !aligned(y, 8) ||
+        (psi0 && !aligned(psi0, 8)) || (psi_final && !aligned(psi_final, 8)))
+        return CSSD_ERR_ALIGN;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    int s = stream_device(stream, &dev);
+    if (s != CSSD_OK) return s;
+    if ((s = check_all_device(dev, (const void*)phi, (const void*)u, b, C, psi0, (const void*)y,
+                              (const void*)psi_final)) != CSSD_OK)
+        return s;
+    cssd::CayleyArgs a;
+    a.Bz = d->batch;
+    a.T = d->seqlen;
+    a.H = d->nheads;
+    a.N = d->dstate;
+    a.phi = phi;
+    a.u = u;
+    a.b = static_cast<const float2*>(b);
+    a.C = static_cast<const float2*>(C);
+    a.psi0 = static_cast<const float2*>(psi0);
+    a.y = static_cast<float2*>(y);
+    a.psi_final = static_cast<float2*>(psi_final);
+    a.chunk = chunk;
+    a.log_clamp = log_clamp;
+    return cssd::launch_cayley_scan(a, stream) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
 }
 
 }  // extern "C"

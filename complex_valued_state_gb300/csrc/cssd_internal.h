@@ -58,7 +58,21 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* workspace, cudaStream_t st
 cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cudaStream_t stream);
 
 // Decode step (step.cu).
+struct CayleyArgs {
+    int64_t Bz, T, H, N;
+    const float* phi;
+    const float* u;
+    const float2* b;
+    const float2* C;
+    const float2* psi0;  // may be null (zero state)
+    float2* y;
+    float2* psi_final;   // may be null
+    int chunk;
+    float log_clamp;     // -inf: the recurrence step by step; finite: the clamped chunked scan
+};
+
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
+cudaError_t launch_cayley_scan(const CayleyArgs& a, cudaStream_t stream);
 // Output of a constant input held forever (h is not used).
 cudaError_t launch_step_infinite(const StepArgs& a, cudaStream_t stream);
 

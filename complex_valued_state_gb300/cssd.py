@@ -32,7 +32,8 @@ STATUS = {
 
 # Every symbol include/cssd.h declares.
 EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward",
-           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_profile_events",
+           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_cayley_scan",
+           "cssd_profile_events",
            "cssd_selftest_handoff_timeout", "cssd_status_string")
 
 # Scratch array size of cssd_chunked_forward_noalloc (bytes).
@@ -76,6 +77,8 @@ def load(path: str = LIB_PATH):
             lib.cssd_step_n.restype = ctypes.c_int
             lib.cssd_step_infinite.argtypes = [dims_p] + [vp] * 7 + [vp]
             lib.cssd_step_infinite.restype = ctypes.c_int
+            lib.cssd_cayley_scan.argtypes = [dims_p] + [vp] * 7 + [ctypes.c_int, ctypes.c_float, vp]
+            lib.cssd_cayley_scan.restype = ctypes.c_int
             lib.cssd_profile_events.argtypes = [vp, vp]
             lib.cssd_profile_events.restype = ctypes.c_int
             lib.cssd_selftest_handoff_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int), vp]
@@ -290,3 +293,35 @@ def step_infinite(x, dt, A, B, C, D, *, y=None, stream=None):
     if st != CSSD_OK:
         raise CssdError(st, "cssd_step_infinite")
     return y
+
+
+def cayley_scan(phi, u, b, C, *, psi0=None, chunk=64, log_clamp=-30.0, y=None, psi_final=None, stream=None):
+    """cssd_cayley_scan on device tensors; returns (y, psi_final).
+
+    phi, u float32 [Bz,T,H,N]; b, C complex64 [Bz,T,H,N]; psi0 complex64
+    [Bz,H,N] or None.  log_clamp=-inf evaluates the recurrence exactly; a
+    finite value (the paper's -30) runs the paper's clamped chunked scan.
+    """
+    lib = load()
+    dev = phi.device
+    Bz, T, H, N = phi.shape
+    c64, f32 = torch.complex64, torch.float32
+    _check(phi, "phi", f32, (Bz, T, H, N), dev)
+    _check(u, "u", f32, (Bz, T, H, N), dev)
+    _check(b, "b", c64, (Bz, T, H, N), dev)
+    _check(C, "C", c64, (Bz, T, H, N), dev)
+    if psi0 is not None:
+        _check(psi0, "psi0", c64, (Bz, H, N), dev)
+    if y is None:
+        y = torch.empty((Bz, T, H, N), dtype=c64, device=dev)
+    _check(y, "y", c64, (Bz, T, H, N), dev)
+    if psi_final is None:
+        psi_final = torch.empty((Bz, H, N), dtype=c64, device=dev)
+    _check(psi_final, "psi_final", c64, (Bz, H, N), dev)
+    d = Dims(Bz, T, H, N, 0)
+    st = lib.cssd_cayley_scan(ctypes.byref(d), _ptr(phi), _ptr(u), _ptr(b), _ptr(C), _ptr(psi0), _ptr(y),
+                              _ptr(psi_final), int(chunk), ctypes.c_float(float(log_clamp)),
+                              _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_cayley_scan")
+    return y, psi_final

@@ -216,5 +216,5 @@ def make_cayley_inputs(w: Workload = HMAMBA_SCAN, seed: int | None = None, *, ga
     C = _cgauss(rng, (Bz, T, H, N))
     prior = _cgauss(rng, (H, N)).astype(np.complex128)
     prior /= np.linalg.norm(prior, axis=1, keepdims=True)
-    psi0 = np.ascontiguousarray(np.broadcast_to(prior.astype(np.complex64), (Bz, H, N)))
+    psi0 = np.broadcast_to(prior.astype(np.complex64), (Bz, H, N)).copy()
     return dict(phi=phi, u=u, b=b, C=C, psi0=psi0)

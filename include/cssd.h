@@ -165,6 +165,35 @@ int cssd_step_n(const cssd_dims* dims, void* h, const void* x, const float* dt, 
 int cssd_step_infinite(const cssd_dims* dims, const void* x, const float* dt, const void* A, const void* B,
                        const void* C, const float* D, void* y, cssd_stream_t stream);
 
+/* Per-coordinate Cayley-phase recurrence ("Complex Phase-State Dynamics Reduce
+ * the Optimization Steps of Sequence Models", section 5.2 equations (2)-(3),
+ * section 5.5, Appendix A Algorithms 1-2).  Per (batch, head) a state psi in
+ * C^N evolves coordinatewise:
+ *     a_t   = sigmoid(u_t) (1 + i phi_t) / (1 - i phi_t)   (gate times unit Cayley phase)
+ *     psi_t = a_t psi_{t-1} + b_t,    y_t = conj(C_t) psi_t  (readout after the update)
+ * from psi0 (zero when NULL).
+ *   dims     batch, seqlen, nheads, dstate = N (any N >= 1); headdim is ignored
+ *   phi      float32   [batch, seqlen, nheads, N]  phase parameters
+ *   u        float32   [batch, seqlen, nheads, N]  gate logits
+ *   b        complex64 [batch, seqlen, nheads, N]  input projection
+ *   C        complex64 [batch, seqlen, nheads, N]  readout projection
+ *   psi0     complex64 [batch, nheads, N]          initial state, may be NULL
+ *   y        complex64 [batch, seqlen, nheads, N]  output (written)
+ *   psi_final complex64 [batch, nheads, N]         last state (written), may be NULL
+ *   chunk    >= 1, the chunk length of the scan (the paper uses 64)
+ *   log_clamp  -INFINITY evaluates the recurrence exactly (chunk then has no
+ *            effect).  A finite value in [-80, 0] evaluates the paper's
+ *            Algorithm 2 as published: per chunk, the cumulative log-gate is
+ *            clamped to [log_clamp, 0] (the paper: -30) before the polar
+ *            reassembly.  That equals the recurrence while no chunk's
+ *            cumulative log-gate falls below log_clamp, and departs from it
+ *            (inputs stop decaying) once one does.
+ * Alignment: phi, u 4 bytes; b, C, y, psi0, psi_final 8 bytes.  Other
+ * log_clamp values, chunk < 1 or non-positive sizes return CSSD_ERR_DIMS.
+ * Returns a cssd_status. */
+int cssd_cayley_scan(const cssd_dims* dims, const float* phi, const float* u, const void* b, const void* C,
+                     const void* psi0, void* y, void* psi_final, int chunk, float log_clamp, cssd_stream_t stream);
+
 /* Measurement hook.  ev_begin / ev_end are cudaEvent_t handles created by
  * the caller on the device in use; every later cssd_chunked_forward call made
  * from the same host thread records ev_begin on its stream just before the

@@ -109,6 +109,24 @@ def test_constant_input_argument_errors(lib):
     assert lib.cssd_step_infinite(ctypes.byref(cssd.Dims(0, 1, 1, 16, 16)), x, dt, A, B, C, D, y, None) == -2
 
 
+def test_cayley_scan_argument_errors(lib):
+    ok = cssd.Dims(1, 8, 2, 16, 0)
+    p = [ctypes.c_void_p(0x10000 + 0x100 * i) for i in range(7)]  # phi, u, b, C, psi0, y, psi_final
+    f = lib.cssd_cayley_scan
+    assert f(None, *p, 64, ctypes.c_float(-30.0), None) == -1
+    assert f(ctypes.byref(cssd.Dims(1, 0, 2, 16, 0)), *p, 64, ctypes.c_float(-30.0), None) == -2
+    assert f(ctypes.byref(ok), *p, 0, ctypes.c_float(-30.0), None) == -2  # chunk
+    assert f(ctypes.byref(ok), *p, 64, ctypes.c_float(1.0), None) == -2  # clamp above 0
+    assert f(ctypes.byref(ok), *p, 64, ctypes.c_float(-100.0), None) == -2  # e^100 would overflow
+    assert f(ctypes.byref(ok), *p, 64, ctypes.c_float(float("nan")), None) == -2
+    q = list(p)
+    q[0] = None
+    assert f(ctypes.byref(ok), *q, 64, ctypes.c_float(-30.0), None) == -1
+    q = list(p)
+    q[2] = ctypes.c_void_p(0x10204)  # complex64 wants 8-byte alignment
+    assert f(ctypes.byref(ok), *q, 64, ctypes.c_float(float("-inf")), None) == -4
+
+
 def test_selftest_argument_errors(lib):
     bits = ctypes.c_int(0)
     assert lib.cssd_selftest_handoff_timeout(1000, None, None) == -1
