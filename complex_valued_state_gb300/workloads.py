@@ -66,8 +66,12 @@ DECODE = Workload("decode", 256, 1, 32, 128, 64, 64, seed=4, kind="decode", step
 # coordinates, 1024-token sequences, chunk 64) and its per-accelerator training
 # batch of 256 sequences; headdim is unused by this recurrence.
 HMAMBA_SCAN = Workload("hmamba_scan", 256, 1024, 16, 16, 16, 64, seed=5, kind="cayley")
+# Causal Born attention at the H-Transformer shapes (16 heads of width D = N = 16,
+# 1024-token sequences) and the same per-accelerator batch of 256 sequences;
+# dstate holds the head width D, headdim and chunk are unused.
+HTRANSFORMER_ATTN = Workload("htransformer_attn", 256, 1024, 16, 16, 16, 64, seed=6, kind="born")
 
-WORKLOADS = {w.name: w for w in (TINY, MAMBA2_LAYER, LONG_SEQ, PAM, DECODE, HMAMBA_SCAN)}
+WORKLOADS = {w.name: w for w in (TINY, MAMBA2_LAYER, LONG_SEQ, PAM, DECODE, HMAMBA_SCAN, HTRANSFORMER_ATTN)}
 
 
 def _cgauss(rng: np.random.Generator, shape, scale: float = 1.0) -> np.ndarray:
@@ -218,3 +222,30 @@ def make_cayley_inputs(w: Workload = HMAMBA_SCAN, seed: int | None = None, *, ga
     prior /= np.linalg.norm(prior, axis=1, keepdims=True)
     psi0 = np.broadcast_to(prior.astype(np.complex64), (Bz, H, N)).copy()
     return dict(phi=phi, u=u, b=b, C=C, psi0=psi0)
+
+
+def make_born_inputs(w: Workload = HTRANSFORMER_ATTN, seed: int | None = None) -> dict:
+    """Inputs of causal Born attention (workload `w`'s shapes, D = w.dstate).
+
+        q, k, v [Bz,T,H,D] complex64   queries, keys, values
+        tau     [Bz,T,H]   float32     positive temperatures
+
+    Recipe: q, k, v complex Gaussian with re, im ~ N(0, 1/2); queries and keys
+    then carry the H-Transformer's per-position phase, component a of position
+    t multiplied by e^{i t omega_a} with the base frequencies omega on a
+    geometric grid over two decades, [0.05, 5], with alternating sign (the
+    initialisation the phase-state paper describes); tau ~ U[0.5, 2].  Draw
+    order: q, k, v, tau.
+    """
+    rng = np.random.default_rng(w.seed if seed is None else seed)
+    Bz, T, H, D = w.batch, w.seqlen, w.nheads, w.dstate
+    q = _cgauss(rng, (Bz, T, H, D))
+    k = _cgauss(rng, (Bz, T, H, D))
+    v = _cgauss(rng, (Bz, T, H, D))
+    tau = rng.uniform(0.5, 2.0, size=(Bz, T, H)).astype(np.float32)
+    omega = np.geomspace(0.05, 5.0, D) * np.where(np.arange(D) % 2 == 0, 1.0, -1.0)
+    ang = np.arange(T, dtype=np.float64)[:, None] * omega[None, :]  # [T, D]
+    rot = np.exp(1j * ang).astype(np.complex64)[None, :, None, :]
+    q = (q * rot).astype(np.complex64)
+    k = (k * rot).astype(np.complex64)
+    return dict(q=q, k=k, v=v, tau=tau)

@@ -22,7 +22,8 @@ import threading
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_SRCS = [os.path.join(_HERE, "cssd_oracle.c"), os.path.join(_HERE, "cayley_oracle.c")]
+_SRCS = [os.path.join(_HERE, "cssd_oracle.c"), os.path.join(_HERE, "cayley_oracle.c"),
+         os.path.join(_HERE, "born_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -54,9 +55,11 @@ def _load():
             lib.oracle_cayley_coefficients.argtypes = [i64] + [dp] * 3
             lib.oracle_cayley_recurrence.argtypes = [i64] * 4 + [dp] * 7
             lib.oracle_cayley_chunked.argtypes = [i64] * 5 + [ctypes.c_double] + [dp] * 7
+            lib.oracle_born_attention.argtypes = [i64] * 4 + [dp] * 5
+            lib.oracle_born_attention_feature_map.argtypes = [i64] * 4 + [dp] * 4
             for f in (lib.oracle_cssd_naive, lib.oracle_cssd_step, lib.oracle_cssd_chunked,
                       lib.oracle_geom_closed_form, lib.oracle_cayley_coefficients, lib.oracle_cayley_recurrence,
-                      lib.oracle_cayley_chunked):
+                      lib.oracle_cayley_chunked, lib.oracle_born_attention, lib.oracle_born_attention_feature_map):
                 f.restype = None
             _lib = lib
     return _lib
@@ -171,3 +174,27 @@ def cayley_chunked(phi, u, b, C, chunk: int, log_clamp: float = -30.0, psi0=None
     lib.oracle_cayley_chunked(Bz, T, H, N, int(chunk), float(log_clamp), _p(phi), _p(u), _p(b), _p(C),
                               None if p0 is None else _p(p0), _p(y), _p(pf))
     return y, pf
+
+
+def born_attention(q, k, v, tau):
+    """Causal Born attention, Algorithm 3 step by step: q, k, v [Bz,T,H,D]
+    complex, tau [Bz,T,H] real; returns psi [Bz,T,H,D] (0 where a row's
+    scores are all zero)."""
+    lib = _load()
+    q, k, v, tau = _c(q), _c(k), _c(v), _r(tau)
+    Bz, T, H, D = q.shape
+    psi = np.empty((Bz, T, H, D), np.complex128)
+    lib.oracle_born_attention(Bz, T, H, D, _p(q), _p(k), _p(v), _p(tau), _p(psi))
+    return psi
+
+
+def born_attention_feature_map(q, k, v):
+    """The same quantity through the recurrent feature-map form
+    (|<q|k>|^2 = q^H k k^H q, carried as D x D matrices); used only to pin
+    born_attention.  O(T D^4) per head: small cases only."""
+    lib = _load()
+    q, k, v = _c(q), _c(k), _c(v)
+    Bz, T, H, D = q.shape
+    psi = np.empty((Bz, T, H, D), np.complex128)
+    lib.oracle_born_attention_feature_map(Bz, T, H, D, _p(q), _p(k), _p(v), _p(psi))
+    return psi
