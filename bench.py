@@ -46,6 +46,7 @@ def parse():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-long", action="store_true", help="skip the long_seq forward measurement")
     ap.add_argument("--no-cayley", action="store_true", help="skip the per-coordinate Cayley scan measurement")
+    ap.add_argument("--no-born", action="store_true", help="skip the causal Born attention measurement")
     return ap.parse_args()
 
 
@@ -267,12 +268,14 @@ def run_ours(args, rank, world, local):
     e_ms = e0.elapsed_time(e1) / e_steps
     e_ms = reduce_max(pg, e_ms, dev)
 
-    decode = const_input = cayley = None
+    decode = const_input = cayley = born = None
     if not args.no_decode:
         decode = bench_decode(args, dev)
         const_input = bench_const_input(args, dev)
     if not args.no_cayley:
         cayley = bench_cayley(args, dev)
+    if not args.no_born:
+        born = bench_born(args, dev)
     long_seq = None
     if not args.no_long:
         long_seq = bench_long_seq(args, dev)
@@ -310,6 +313,8 @@ def run_ours(args, rank, world, local):
         out["const_input"] = const_input
     if cayley:
         out["cayley_scan"] = cayley
+    if born:
+        out["born_attention"] = born
     if long_seq:
         out["long_seq"] = long_seq
     if world == 1 and not args.no_cpu_baseline:
@@ -456,6 +461,63 @@ def bench_cayley(args, dev):
                                   "alg_bytes_per_launch": alg}}
     out["context"] = "the paper's ~48,000 tokens/s is a whole 253M-parameter model training on an A100, not this scan"
     return out
+
+
+def tf32_peak():
+    """Dense TF32 tensor peak: the measured bf16 burst figure times the nominal
+    TF32 / bf16 ratio (1.1 / 2.25 PFLOP/s), else the fallback bf16 figure times it."""
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    ratio = 1.1 / 2.25
+    if os.path.exists(p):
+        with open(p) as f:
+            return float(json.load(f)["bf16_tflops"]) * ratio, "measured bf16 burst x nominal tf32/bf16 (1.1/2.25)"
+    return 1900.0 * ratio, "fallback bf16 x nominal tf32/bf16 (1.1/2.25)"
+
+
+def bench_born(args, dev):
+    """Causal Born attention at the H-Transformer shapes (batch 256, T 1024,
+    16 heads of width 16).  Tensor-bound: the roofline counts the MMA flops the
+    kernel executes (full 64 x 64 blocks up to the diagonal: G = 2 (D/8)
+    instructions of 128x64x8, the value GEMM 8 of 128x(2D+16)x8); the minimal
+    flop count of the causal pairs is reported beside it."""
+    import torch
+
+    from complex_valued_state_gb300 import cssd
+    from complex_valued_state_gb300 import workloads as wl
+
+    w = wl.HTRANSFORMER_ATTN
+    host = wl.make_born_inputs(w)
+    g = {k: torch.from_numpy(host[k]).to(dev) for k in ("q", "k", "v")}
+    del host
+    Bz, T, H, D = w.batch, w.seqlen, w.nheads, w.dstate
+    psi = torch.empty_like(g["q"])
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        cssd.born_attention(g["q"], g["k"], g["v"], psi=psi)
+    torch.cuda.synchronize(dev)
+    n = max(10, args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        cssd.born_attention(g["q"], g["k"], g["v"], psi=psi)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / n
+    nqb = (T + 63) // 64
+    blocks = Bz * H * nqb * (nqb + 1) // 2  # key blocks of 64 visited, summed over query blocks
+    dense = blocks * (2 * (D // 8) * 2 * 128 * 64 * 8 + (64 // 8) * 2 * 128 * (2 * D + 16) * 8)
+    pairs = Bz * H * T * (T + 1) // 2
+    minimal = pairs * (8 * D + 3 + 4 * D + 1)  # <q|k>, |.|^2, s v and the score sum
+    peak, kind = tf32_peak()
+    tf = dense / (ms / 1e3) / 1e12
+    return {"workload": f"htransformer_attn Bz{Bz} T{T} H{H} D{D}", "ms_per_call": round(ms, 4), "calls": n,
+            "value": round(Bz * T * H / (ms / 1e3), 1), "unit": "token-heads/s",
+            "roofline": {"bound": "tensor", "kernel": "born_kernel<16>", "achieved": round(tf, 1), "peak": round(peak, 1),
+                         "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_kind": kind,
+                         "flops_per_launch": dense, "minimal_flops_per_launch": minimal,
+                         "minimal_tflops": round(minimal / (ms / 1e3) / 1e12, 1)},
+            "hbm_bytes_per_launch": 4 * Bz * T * H * D * 8,
+            "context": "the paper's ~80,000 tokens/s is a whole 253M-parameter H-Transformer training on A100s, not this kernel"}
 
 
 def bench_long_seq(args, dev):

@@ -1,0 +1,306 @@
+// Causal Born attention on the tcgen05 tensor cores ("Complex Phase-State
+// Dynamics Reduce the Optimization Steps of Sequence Models", section 5.5,
+// equation (5), Appendix A Algorithm 3).  Per (batch, head):
+//     s_ij  = |<q_i|k_j>|^2 / (D tau_i),  <q|k> = sum_a conj(q_a) k_a,  j <= i
+//     psi_i = sum_{j<=i} s_ij v_j / sum_{j<=i} s_ij
+// The factor 1/(D tau_i) is common to a row's numerator and denominator and is
+// left out (psi does not depend on it).
+//
+// One CTA (128 threads, one per tensor-memory lane) owns 64 queries of one
+// head and walks the key blocks of 64 up to the diagonal:
+//   G = conj(Q) K^T     stacked real form: A = [-Ai; Ar; Ai] of A = conj(Q),
+//                       B = planes Kr, Ki, so lanes 0-63 hold Re G and lanes
+//                       64-127 Im G (the chunk kernels' complex GEMM)
+//   S = G o G           squared in place in tensor memory by the thread that
+//                       owns the lane (Re^2 on lanes 0-63, Im^2 on 64-127),
+//                       causal mask on the diagonal block
+//   ACC += S [Vr; Vi; 1]^T   A = S read from tensor memory; the row of ones
+//                       makes the last column the running sum of scores
+// and at the end sums the two lane halves (|g|^2 = Re^2 + Im^2) and divides.
+// Scores need no rescaling between key blocks: they are non-negative and the
+// normalisation is a plain sum, so numerator and denominator accumulate in
+// fp32 in tensor memory across all blocks.
+
+#include "cssd_common.cuh"
+#include "cssd_internal.h"
+#include "tcgen05.cuh"
+
+namespace cssd {
+namespace {
+
+constexpr int BQ = 64;   // queries per CTA
+constexpr int BT = 128;  // threads: one per tensor-memory lane
+constexpr long long kBornWait = 4000000000LL;  // ~2 s at 2 GHz
+
+__device__ int g_born_err;  // bit 0: an MMA completion wait gave up
+
+__device__ __forceinline__ uint32_t kofs(int row, int k, int rows) {
+    return (uint32_t)((((k >> 2) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + ((k & 3) << 2));
+}
+__device__ __forceinline__ float rna_tf32(float v) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+    return __uint_as_float(r);
+}
+__device__ __forceinline__ void sts(unsigned char* base, uint32_t off, float v) {
+    *reinterpret_cast<float*>(base + off) = v;
+}
+__device__ __forceinline__ void sts2(unsigned char* base, uint32_t off, float a, float b) {
+    *reinterpret_cast<float2*>(base + off) = make_float2(a, b);
+}
+
+template <int D>
+struct BornCfg {
+    static constexpr int BK = 64;                     // keys per block
+    static constexpr int NB = 2 * D + 16;             // value operand rows: Vr, Vi, ones, zeros
+    static constexpr int Q_BYTES = 3 * BQ * D * 4;    // conj(Q) stack, 192 rows x D
+    static constexpr int KP_BYTES = BK * D * 4;       // one key plane, BK rows x D
+    static constexpr int V_BYTES = NB * BK * 4;       // value operand, NB rows x BK keys
+    static constexpr int KV_BYTES = 2 * KP_BYTES + V_BYTES;  // one key block's operands
+    static constexpr int SMEM = Q_BYTES + 2 * KV_BYTES;        // two key blocks in flight
+    static constexpr int ITEMS = BK * D / 2 / BT;     // float4 (two complex) per thread per key block
+    static constexpr int STAGE_LD = 2 * D + 1;        // staged floats per query row
+    // One score buffer and the sums: 128 columns at width 16 (four CTAs per SM).
+    static constexpr uint32_t COL_G = 0, COL_ACC = BK;
+    static constexpr uint32_t TMEM_COLS = COL_ACC + NB <= 128 ? 128 : 256;
+    static_assert(COL_ACC + NB <= TMEM_COLS, "tensor-memory budget");
+    static_assert(BQ * STAGE_LD * 4 <= SMEM, "staging fits in shared memory");
+    static_assert(ITEMS * BT * 2 == BK * D, "item mapping covers a key block");
+};
+
+template <int D>
+__global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, const float4* __restrict__ k,
+                                                  const float4* __restrict__ v, float2* __restrict__ psi, int T,
+                                                  int H, int BH, int nqb) {
+    using Cfg = BornCfg<D>;
+    constexpr int NB = Cfg::NB, IT = Cfg::ITEMS, BK = Cfg::BK;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ __align__(8) uint64_t mbar[3];  // G done, (unused), ACC update done
+    __shared__ uint32_t s_tmem;
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    unsigned char* sq = smem;
+    // key block kb's operands live in buffer kb & 1: planes Kr, Ki, then the value operand
+    auto skb = [&](int buf) { return smem + Cfg::Q_BYTES + buf * Cfg::KV_BYTES; };
+    auto svb = [&](int buf) { return skb(buf) + 2 * Cfg::KP_BYTES; };
+    const int qb = nqb - 1 - (int)(blockIdx.x / BH);  // latest (longest) query blocks first
+    const int bh = (int)(blockIdx.x % BH);
+    const int b = bh / H, h = bh - b * H;
+    const int i0 = qb * BQ;
+    // float4 pointer to token t of this head (D / 2 float4 per token)
+    auto tok = [&](const float4* base, int t) { return base + ((size_t)((size_t)b * T + t) * H + h) * (D / 2); };
+
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, Cfg::TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        for (int i = 0; i < 3; ++i) tc::mbar_init(&mbar[i], 1);
+        tc::mbar_fence_init();
+    }
+    // Rows 2D.. of both value operands: ones (the score sum), then zeros.
+    for (int e = tid; e < 2 * (NB - 2 * D) * BK; e += BT) {
+        const int buf = e / ((NB - 2 * D) * BK), f = e % ((NB - 2 * D) * BK);
+        const int r = 2 * D + f / BK, j = f % BK;
+        sts(svb(buf), kofs(r, j, NB), r == 2 * D ? 1.f : 0.f);
+    }
+    // conj(Q) as the stack [-Ai; Ar; Ai] with Ar = Re q, Ai = -Im q.
+    for (int e = tid; e < BQ * D / 2; e += BT) {
+        const int i = e / (D / 2), c = e % (D / 2);
+        const float4 x = (i0 + i < T) ? __ldg(tok(q, i0 + i) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float r0 = rna_tf32(x.x), m0 = rna_tf32(x.y), r1 = rna_tf32(x.z), m1 = rna_tf32(x.w);
+        sts2(sq, kofs(i, 2 * c, 3 * BQ), m0, m1);
+        sts2(sq, kofs(BQ + i, 2 * c, 3 * BQ), r0, r1);
+        sts2(sq, kofs(2 * BQ + i, 2 * c, 3 * BQ), -m0, -m1);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+
+    // Tensor-memory lane of this thread: L = 32 warp + lane, part 0 (lanes 0-63)
+    // or 1 (64-127) of query row lrow.
+    const int L = warp * 32 + lane;
+    const int part = L >> 6, lrow = L & 63;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+
+    // Key and value rows of a block: item e = tid + BT i is float4 c of key j.
+    float4 kr[IT], vr[IT];
+    auto load_kv = [&](int kb) {
+#pragma unroll
+        for (int i = 0; i < IT; ++i) {
+            const int e = tid + BT * i, j = e / (D / 2), c = e % (D / 2);
+            const int t = kb * BK + j;
+            kr[i] = t < T ? __ldg(tok(k, t) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            vr[i] = t < T ? __ldg(tok(v, t) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    };
+
+    const uint32_t ID_G = tc::idesc_tf32(128, BK), ID_V = tc::idesc_tf32(128, NB);
+    constexpr uint32_t Q_LBO = (3 * BQ / 8) * 128, K_LBO = (BK / 8) * 128, V_LBO = (NB / 8) * 128, SBO = 128;
+    const uint64_t a_hi = tc::make_desc(tc::smem_u32(sq) + 8 * SBO, Q_LBO, SBO);  // [Ar; Ai]
+    const uint64_t a_lo = tc::make_desc(tc::smem_u32(sq), Q_LBO, SBO);            // [-Ai; Ar]
+    bool ok = true;
+
+    // Key planes (rows j, K = a) and value operand (rows m, K = j) of the
+    // block held in registers, into buffer buf.
+    auto write_kv = [&](int buf) {
+        unsigned char* sk = skb(buf);
+        unsigned char* sv = svb(buf);
+#pragma unroll
+        for (int i = 0; i < IT; ++i) {
+            const int e = tid + BT * i, j = e / (D / 2), c = e % (D / 2);
+            sts2(sk, kofs(j, 2 * c, BK), rna_tf32(kr[i].x), rna_tf32(kr[i].z));
+            sts2(sk + Cfg::KP_BYTES, kofs(j, 2 * c, BK), rna_tf32(kr[i].y), rna_tf32(kr[i].w));
+            sts(sv, kofs(2 * c, j, NB), rna_tf32(vr[i].x));
+            sts(sv, kofs(2 * c + 1, j, NB), rna_tf32(vr[i].z));
+            sts(sv, kofs(D + 2 * c, j, NB), rna_tf32(vr[i].y));
+            sts(sv, kofs(D + 2 * c + 1, j, NB), rna_tf32(vr[i].w));
+        }
+        tc::fence_proxy_async();
+    };
+    // G of block kb (operands in buffer kb & 1) into the score columns.
+    auto issue_g = [&](int kb) {
+        const uint32_t kbase = tc::smem_u32(skb(kb & 1));
+        const uint64_t b_re = tc::make_desc(kbase, K_LBO, SBO);
+        const uint64_t b_im = tc::make_desc(kbase + Cfg::KP_BYTES, K_LBO, SBO);
+        const uint32_t d = tmem + Cfg::COL_G;
+        constexpr uint64_t A_STEP = (2 * Q_LBO) >> 4, B_STEP = (2 * K_LBO) >> 4;
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks) tc::mma_tf32(d, a_hi + ks * A_STEP, b_re + ks * B_STEP, ID_G, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < D / 8; ++ks) tc::mma_tf32(d, a_lo + ks * A_STEP, b_im + ks * B_STEP, ID_G, 1u);
+        tc::commit(&mbar[0]);
+    };
+
+    // Per key block kb: G (tensor cores) -> S = G o G in place (threads) ->
+    // ACC += S V (tensor cores), and while the ACC update runs the threads
+    // write block kb + 1's operands into the other buffer and fetch block
+    // kb + 2's rows.  mbar[0] completes once per G, mbar[2] once per ACC
+    // update, in block order, and every wait comes before the next commit to
+    // the same barrier.  Key blocks 0 .. last cover every key up to the query
+    // block's last position.
+    const int last = (i0 + BQ) / BK - 1;
+    load_kv(0);
+    write_kv(0);
+    if (last > 0) load_kv(1);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (tid == 0) {
+        tc::fence_after_sync();
+        issue_g(0);
+    }
+#pragma unroll 1
+    for (int kb = 0; kb <= last; ++kb) {
+        const int buf = kb & 1;
+        ok = tc::mbar_wait_bounded(&mbar[0], (uint32_t)(kb & 1), kBornWait) && ok;
+        tc::fence_after_sync();
+        // S = G o G in place; keys after the query are masked (only the last
+        // block reaches past a query).
+        const int kq = i0 + lrow - kb * BK;  // last key of this block the row may see
+        const uint32_t gcol = tmem + lane_base + Cfg::COL_G;
+        uint32_t r[BK];
+#pragma unroll
+        for (int cb = 0; cb < BK / 16; ++cb) tc::tmem_ld16(gcol + 16 * cb, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * cb));
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < BK; ++j) {
+            const float g = __uint_as_float(r[j]);
+            r[j] = __float_as_uint(j <= kq ? g * g : 0.f);
+        }
+#pragma unroll
+        for (int cb = 0; cb < BK / 16; ++cb) tc::tmem_st16(gcol + 16 * cb, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * cb));
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            const uint64_t b_v = tc::make_desc(tc::smem_u32(svb(buf)), V_LBO, SBO);
+            constexpr uint64_t V_STEP = (2 * V_LBO) >> 4;
+#pragma unroll
+            for (int ks = 0; ks < BK / 8; ++ks)
+                tc::mma_tf32_ts(tmem + Cfg::COL_ACC, tmem + Cfg::COL_G + 8 * ks, b_v + ks * V_STEP, ID_V,
+                                (kb > 0 || ks > 0) ? 1u : 0u);
+            tc::commit(&mbar[2]);
+        }
+        if (kb < last) {
+            // The other buffer was last read by G and the ACC update of block
+            // kb - 1, both complete.
+            write_kv(buf ^ 1);
+            if (kb + 1 < last) load_kv(kb + 2);
+            // The score columns are free once this block's ACC update is done.
+            ok = tc::mbar_wait_bounded(&mbar[2], (uint32_t)(kb & 1), kBornWait) && ok;
+            tc::fence_before_sync();
+            __syncthreads();
+            if (tid == 0) {
+                tc::fence_after_sync();
+                issue_g(kb + 1);
+            }
+        }
+    }
+    ok = tc::mbar_wait_bounded(&mbar[2], (uint32_t)(last & 1), kBornWait) && ok;
+    tc::fence_after_sync();
+
+    // Epilogue: lanes 0-63 hold the Re^2-weighted sums, lanes 64-127 the
+    // Im^2-weighted ones; columns [0, D) real parts, [D, 2D) imaginary parts,
+    // 2D the score sum.  Part 0 stages its row, part 1 adds and divides.
+    float* stage = reinterpret_cast<float*>(smem) + lrow * Cfg::STAGE_LD;
+    uint32_t acc[(2 * D + 16) / 16 * 16];
+#pragma unroll
+    for (int cb = 0; cb < (2 * D + 16) / 16; ++cb) {
+        uint32_t r[16];
+        tc::tmem_ld16(tmem + lane_base + Cfg::COL_ACC + 16 * cb, r);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) acc[16 * cb + j] = r[j];
+    }
+    tc::tmem_wait_ld();
+    __syncthreads();  // every MMA has read the conj(Q) stack: the staging may overwrite it
+    if (part == 0) {
+#pragma unroll
+        for (int m = 0; m <= 2 * D; ++m) stage[m] = __uint_as_float(acc[m]);
+    }
+    __syncthreads();
+    if (part == 1 && i0 + lrow < T) {
+        const float den = stage[2 * D] + __uint_as_float(acc[2 * D]);
+        const float inv = den != 0.f ? 1.f / den : 0.f;
+        float2* out = psi + ((size_t)((size_t)b * T + i0 + lrow) * H + h) * D;
+#pragma unroll
+        for (int m = 0; m < D; ++m)
+            out[m] = make_float2((stage[m] + __uint_as_float(acc[m])) * inv,
+                                 (stage[D + m] + __uint_as_float(acc[D + m])) * inv);
+    }
+    if (!ok && tid == 0) atomicOr(&g_born_err, 1);
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
+}
+
+template <int D>
+cudaError_t launch_born_d(const BornArgs& a, cudaStream_t st) {
+    using Cfg = BornCfg<D>;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    static bool attr_set[128] = {};
+    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
+    if (!attr_set[dev]) {
+        e = cudaFuncSetAttribute(born_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const int64_t BH = a.Bz * a.H, nqb = (a.T + BQ - 1) / BQ;
+    born_kernel<D><<<(unsigned)(BH * nqb), BT, Cfg::SMEM, st>>>(
+        reinterpret_cast<const float4*>(a.q), reinterpret_cast<const float4*>(a.k), reinterpret_cast<const float4*>(a.v),
+        a.psi, (int)a.T, (int)a.H, (int)BH, (int)nqb);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool born_supported(int64_t D) { return D == 16 || D == 32; }
+
+cudaError_t launch_born(const BornArgs& a, cudaStream_t st) {
+    return a.D == 16 ? launch_born_d<16>(a, st) : launch_born_d<32>(a, st);
+}
+
+}  // namespace cssd

@@ -247,4 +247,31 @@ int cssd_cayley_scan(const cssd_dims* d, const float* phi, const float* u, const
     return cssd::launch_cayley_scan(a, stream) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
 }
 
+int cssd_born_attention(const cssd_dims* d, const void* q, const void* k, const void* v, void* psi,
+                        cssd_stream_t stream_) {
+    if (!d) return CSSD_ERR_NULL;
+    if (d->batch <= 0 || d->seqlen <= 0 || d->nheads <= 0 || d->dstate <= 0) return CSSD_ERR_DIMS;
+    if (d->seqlen > kMaxInt || d->batch * d->nheads > kMaxInt ||
+        d->batch * d->nheads * ((d->seqlen + 63) / 64) > kMaxInt)
+        return CSSD_ERR_DIMS;
+    if (!cssd::born_supported(d->dstate)) return CSSD_ERR_UNSUPPORTED;
+    if (!q || !k || !v || !psi) return CSSD_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(psi, 16)) return CSSD_ERR_ALIGN;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    int s = stream_device(stream, &dev);
+    if (s != CSSD_OK) return s;
+    if ((s = check_all_device(dev, q, k, v, (const void*)psi)) != CSSD_OK) return s;
+    cssd::BornArgs a;
+    a.Bz = d->batch;
+    a.T = d->seqlen;
+    a.H = d->nheads;
+    a.D = d->dstate;
+    a.q = static_cast<const float2*>(q);
+    a.k = static_cast<const float2*>(k);
+    a.v = static_cast<const float2*>(v);
+    a.psi = static_cast<float2*>(psi);
+    return cssd::launch_born(a, stream) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+}
+
 }  // extern "C"

@@ -71,8 +71,19 @@ struct CayleyArgs {
     float log_clamp;     // -inf: the recurrence step by step; finite: the clamped chunked scan
 };
 
+struct BornArgs {
+    int64_t Bz, T, H, D;
+    const float2* q;
+    const float2* k;
+    const float2* v;
+    float2* psi;
+};
+
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_cayley_scan(const CayleyArgs& a, cudaStream_t stream);
+// Causal Born attention (born.cu).
+bool born_supported(int64_t D);
+cudaError_t launch_born(const BornArgs& a, cudaStream_t stream);
 // Output of a constant input held forever (h is not used).
 cudaError_t launch_step_infinite(const StepArgs& a, cudaStream_t stream);
 

@@ -32,7 +32,7 @@ STATUS = {
 
 # Every symbol include/cssd.h declares.
 EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward",
-           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_cayley_scan",
+           "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_cayley_scan", "cssd_born_attention",
            "cssd_profile_events",
            "cssd_selftest_handoff_timeout", "cssd_status_string")
 
@@ -79,6 +79,8 @@ def load(path: str = LIB_PATH):
             lib.cssd_step_infinite.restype = ctypes.c_int
             lib.cssd_cayley_scan.argtypes = [dims_p] + [vp] * 7 + [ctypes.c_int, ctypes.c_float, vp]
             lib.cssd_cayley_scan.restype = ctypes.c_int
+            lib.cssd_born_attention.argtypes = [dims_p] + [vp] * 4 + [vp]
+            lib.cssd_born_attention.restype = ctypes.c_int
             lib.cssd_profile_events.argtypes = [vp, vp]
             lib.cssd_profile_events.restype = ctypes.c_int
             lib.cssd_selftest_handoff_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int), vp]
@@ -325,3 +327,25 @@ def cayley_scan(phi, u, b, C, *, psi0=None, chunk=64, log_clamp=-30.0, y=None, p
     if st != CSSD_OK:
         raise CssdError(st, "cssd_cayley_scan")
     return y, psi_final
+
+
+def born_attention(q, k, v, *, psi=None, stream=None):
+    """cssd_born_attention on device tensors; returns psi.
+
+    q, k, v complex64 [Bz,T,H,D] (D = 16 or 32).  The temperature of the
+    scores cancels in the normalisation and is not an argument.
+    """
+    lib = load()
+    dev = q.device
+    Bz, T, H, D = q.shape
+    c64 = torch.complex64
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check(t, n, c64, (Bz, T, H, D), dev)
+    if psi is None:
+        psi = torch.empty((Bz, T, H, D), dtype=c64, device=dev)
+    _check(psi, "psi", c64, (Bz, T, H, D), dev)
+    d = Dims(Bz, T, H, D, 0)
+    st = lib.cssd_born_attention(ctypes.byref(d), _ptr(q), _ptr(k), _ptr(v), _ptr(psi), _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_born_attention")
+    return psi

@@ -194,6 +194,25 @@ int cssd_step_infinite(const cssd_dims* dims, const void* x, const float* dt, co
 int cssd_cayley_scan(const cssd_dims* dims, const float* phi, const float* u, const void* b, const void* C,
                      const void* psi0, void* y, void* psi_final, int chunk, float log_clamp, cssd_stream_t stream);
 
+/* Causal Born attention ("Complex Phase-State Dynamics Reduce the
+ * Optimization Steps of Sequence Models", section 5.5 equation (5), Appendix A
+ * Algorithm 3).  Per (batch, head), for every query position i:
+ *     s_ij  = |<q_i|k_j>|^2 / (D tau_i)   for j <= i,   <q|k> = sum_a conj(q_a) k_a
+ *     psi_i = sum_{j<=i} s_ij v_j / sum_{j<=i} s_ij
+ * The factor 1/(D tau_i) is common to numerator and denominator, so psi does
+ * not depend on the temperature and it is not an argument.  A row whose scores
+ * are all zero (q_i orthogonal to every k_j, j <= i) returns psi_i = 0.
+ *   dims  batch, seqlen, nheads, dstate = D (head width: 16 or 32); headdim
+ *         is ignored
+ *   q, k, v  complex64 [batch, seqlen, nheads, D]  queries, keys, values
+ *            (any phase rotation of q and k is applied by the caller)
+ *   psi      complex64 [batch, seqlen, nheads, D]  output (written)
+ * Scores and values enter the tensor cores as TF32 (round to nearest),
+ * accumulation is fp32.  All four pointers are device pointers, 16-byte
+ * aligned.  Other D return CSSD_ERR_UNSUPPORTED.  Returns a cssd_status. */
+int cssd_born_attention(const cssd_dims* dims, const void* q, const void* k, const void* v, void* psi,
+                        cssd_stream_t stream);
+
 /* Measurement hook.  ev_begin / ev_end are cudaEvent_t handles created by
  * the caller on the device in use; every later cssd_chunked_forward call made
  * from the same host thread records ev_begin on its stream just before the

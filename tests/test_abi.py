@@ -127,6 +127,21 @@ def test_cayley_scan_argument_errors(lib):
     assert f(ctypes.byref(ok), *q, 64, ctypes.c_float(float("-inf")), None) == -4
 
 
+def test_born_attention_argument_errors(lib):
+    ok = cssd.Dims(1, 8, 2, 16, 0)
+    p = [ctypes.c_void_p(0x10000 + 0x100 * i) for i in range(4)]  # q, k, v, psi
+    f = lib.cssd_born_attention
+    assert f(None, *p, None) == -1
+    assert f(ctypes.byref(cssd.Dims(1, 0, 2, 16, 0)), *p, None) == -2
+    assert f(ctypes.byref(cssd.Dims(1, 8, 2, 24, 0)), *p, None) == -3  # width not 16 or 32
+    q = list(p)
+    q[3] = None
+    assert f(ctypes.byref(ok), *q, None) == -1
+    q = list(p)
+    q[1] = ctypes.c_void_p(0x10108)  # 8-byte aligned only
+    assert f(ctypes.byref(ok), *q, None) == -4
+
+
 def test_selftest_argument_errors(lib):
     bits = ctypes.c_int(0)
     assert lib.cssd_selftest_handoff_timeout(1000, None, None) == -1
