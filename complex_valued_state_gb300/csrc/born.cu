@@ -7,7 +7,8 @@
 // left out (psi does not depend on it).
 //
 // One CTA (128 threads, one per tensor-memory lane) owns 64 queries of one
-// head and walks the key blocks of 64 up to the diagonal:
+// head and walks the key blocks of 64 up to the diagonal (a head's CTAs are
+// launched together, so its keys and values are read from DRAM about once):
 //   G = conj(Q) K^T     stacked real form: A = [-Ai; Ar; Ai] of A = conj(Q),
 //                       B = planes Kr, Ki, so lanes 0-63 hold Re G and lanes
 //                       64-127 Im G (the chunk kernels' complex GEMM)
@@ -83,8 +84,11 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
     // key block kb's operands live in buffer kb & 1: planes Kr, Ki, then the value operand
     auto skb = [&](int buf) { return smem + Cfg::Q_BYTES + buf * Cfg::KV_BYTES; };
     auto svb = [&](int buf) { return skb(buf) + 2 * Cfg::KP_BYTES; };
-    const int qb = nqb - 1 - (int)(blockIdx.x / BH);  // latest (longest) query blocks first
-    const int bh = (int)(blockIdx.x % BH);
+    // The query blocks of one head are consecutive CTAs (its latest, longest
+    // block first), so they run close together and read the head's keys and
+    // values from L2 rather than each from DRAM.
+    const int bh = (int)(blockIdx.x / nqb);
+    const int qb = nqb - 1 - (int)(blockIdx.x % nqb);
     const int b = bh / H, h = bh - b * H;
     const int i0 = qb * BQ;
     // float4 pointer to token t of this head (D / 2 float4 per token)
