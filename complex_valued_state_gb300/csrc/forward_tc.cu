@@ -53,8 +53,11 @@ constexpr int S1 = 0;                          // F, then Ct, then M, then y sta
 constexpr int S2 = S1 + STACK_BYTES;           // X planes (Xr, Xi)
 constexpr int S3 = S2 + 2 * PLANE_BYTES;       // Bt planes, then H planes
 constexpr int SMEM_BYTES = S3 + 2 * PLANE_BYTES;  // 112 KB
-constexpr int STAGE_LD = 2 * PD + 1;           // y staging row stride (floats)
-static_assert(CH * STAGE_LD * 4 <= STACK_BYTES, "y staging fits in S1");
+// y staging: a real and an imaginary 64 x 64 plane with an odd row stride, so
+// that both the column-wise writes from tensor-memory lanes and the row-wise
+// reads of the output pass fall on 32 distinct banks.
+constexpr int STAGE_LD = PD + 1;
+static_assert(2 * CH * STAGE_LD * 4 <= STACK_BYTES, "y staging fits in S1");
 
 // TMEM columns of the four accumulators (each 128 lanes x 64 columns).
 constexpr uint32_t COL_S = 0, COL_G = 64, COL_OFF = 128, COL_Y = 192, TMEM_COLS = 256;
@@ -106,9 +109,11 @@ struct TcParams {
 
 // ------------------------------------------------------------------ helpers
 // Raw 64 x 64 complex tiles land in shared memory row by row (512 bytes per
-// token); 16-byte chunk j of row l is stored at chunk j ^ (l & 7) so that the
-// transform's reads spread over the banks.
-__device__ __forceinline__ uint32_t raw_off(int l, int j) { return (uint32_t)(l * 512 + ((j ^ (l & 7)) << 4)); }
+// token); 16-byte chunk j of row l is stored at chunk j ^ 2 (l mod 4).  Each
+// 8-lane phase of the transform's 16-byte reads touches rows l..l+3 and two
+// neighbouring chunks, which this places on eight distinct bank groups; the
+// row-wise copies stay conflict-free under any per-row XOR.
+__device__ __forceinline__ uint32_t raw_off(int l, int j) { return (uint32_t)(l * 512 + ((j ^ ((l & 3) << 1)) << 4)); }
 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gptr), "r"(valid ? 16 : 0)
@@ -281,6 +286,11 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     const uint32_t o_kl192 = koff(n0, l0, 192);   // stack with rows n, K = l: + 12288 i
     const uint32_t o_lk192 = koff(l0, n0, 192);   // stack with rows l, K = n: + 256 i
     constexpr uint32_t BLK = 1024;                // 64 rows further down a stack
+    // Stores into K-major operands with rows n0, n0 + 1 and K = l: lanes with
+    // l0 & 4 write row n0 + 1 first, so that each store instruction covers all
+    // eight rows of a core matrix and the 32 lanes hit 32 distinct banks.
+    const bool swap_rows = ((l0 >> 2) & 1) != 0;
+    const uint32_t sx = swap_rows ? 16u : 0u;
     // 64 columns (half hf) of a token-major [.., N] complex tile, into registers.
     auto load_half = [&](const float4* src, int hf, float4 (&v)[IT]) {
         const float4* g = src + (row0 + (size_t)l0 * rstride) * (N / 2) + hf * 32 + (n0 >> 1);
@@ -379,10 +389,11 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
             const uint32_t o = o_kl64 + 4096 * i;  // rows p = n0, n0 + 1; K = l
-            st_f32(sm2, o, tf32r(xv[i].x));
-            st_f32(sm2, o + 16, tf32r(xv[i].z));
-            st_f32(sm2 + PLANE_BYTES, o, tf32r(xv[i].y));
-            st_f32(sm2 + PLANE_BYTES, o + 16, tf32r(xv[i].w));
+            const float r0 = tf32r(xv[i].x), r1 = tf32r(xv[i].z), m0 = tf32r(xv[i].y), m1 = tf32r(xv[i].w);
+            st_f32(sm2, o + sx, swap_rows ? r1 : r0);
+            st_f32(sm2, o + (sx ^ 16), swap_rows ? r0 : r1);
+            st_f32(sm2 + PLANE_BYTES, o + sx, swap_rows ? m1 : m0);
+            st_f32(sm2 + PLANE_BYTES, o + (sx ^ 16), swap_rows ? m0 : m1);
         }
     }
 
@@ -415,12 +426,14 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                 const float f0r = tf32r(ds * b0r), f0i = tf32r(ds * b0i), f1r = tf32r(ds * b1r),
                             f1i = tf32r(ds * b1i);
                 const uint32_t of = o_kl192 + 12288 * i;
-                st_f32(sm1, of, -f0i);
-                st_f32(sm1, of + 16, -f1i);
-                st_f32(sm1, of + BLK, f0r);
-                st_f32(sm1, of + BLK + 16, f1r);
-                st_f32(sm1, of + 2 * BLK, f0i);
-                st_f32(sm1, of + 2 * BLK + 16, f1i);
+                const float fAr = swap_rows ? f1r : f0r, fAi = swap_rows ? f1i : f0i;  // row written first
+                const float fBr = swap_rows ? f0r : f1r, fBi = swap_rows ? f0i : f1i;
+                st_f32(sm1, of + sx, -fAi);
+                st_f32(sm1, of + (sx ^ 16), -fBi);
+                st_f32(sm1, of + BLK + sx, fAr);
+                st_f32(sm1, of + BLK + (sx ^ 16), fBr);
+                st_f32(sm1, of + 2 * BLK + sx, fAi);
+                st_f32(sm1, of + 2 * BLK + (sx ^ 16), fBi);
             }
         }
         issue(tmem + COL_S, a1, a2, false, &mbar[0]);
@@ -584,19 +597,18 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         tmem_ld_cols(tmem + lane_base + COL_OFF + c0col, ro);
         tc::tmem_wait_ld();
         const float el = __expf(s_rho[lrow]);
-        float* stage = reinterpret_cast<float*>(sm1);
+        float* stage = reinterpret_cast<float*>(sm1) + part * CH * STAGE_LD + lrow * STAGE_LD + c0col;
 #pragma unroll
-        for (int j = 0; j < CPT; ++j)
-            stage[lrow * STAGE_LD + 2 * (c0col + j) + part] = fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
+        for (int j = 0; j < CPT; ++j) stage[j] = fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
     }
     __syncthreads();
     {
         const float Dh = p.D[h];
-        const float* stage = reinterpret_cast<const float*>(sm1) + ly * STAGE_LD + 2 * py;
+        const float* stage = reinterpret_cast<const float*>(sm1) + ly * STAGE_LD + py;
 #pragma unroll
         for (int k = 0; k < YI; ++k) {
             if (t0 + ly + 8 * k < p.T) {
-                const float yr = stage[8 * k * STAGE_LD], yi = stage[8 * k * STAGE_LD + 1];
+                const float yr = stage[8 * k * STAGE_LD], yi = stage[CH * STAGE_LD + 8 * k * STAGE_LD];
                 p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
             }
         }
