@@ -108,9 +108,14 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
         const int r = 2 * D + f / BK, j = f % BK;
         sts(svb(buf), kofs(r, j, NB), r == 2 * D ? 1.f : 0.f);
     }
+    // Key and value rows of a block: item e = tid + BT i is float4 c (two
+    // complex) of key j, so that consecutive lanes read consecutive 16-byte
+    // pieces of a row.
+    auto item_j = [&](int e) { return e / (D / 2); };
+    auto item_c = [&](int e) { return e % (D / 2); };
     // conj(Q) as the stack [-Ai; Ar; Ai] with Ar = Re q, Ai = -Im q.
     for (int e = tid; e < BQ * D / 2; e += BT) {
-        const int i = e / (D / 2), c = e % (D / 2);
+        const int i = item_j(e), c = item_c(e);
         const float4 x = (i0 + i < T) ? __ldg(tok(q, i0 + i) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
         const float r0 = rna_tf32(x.x), m0 = rna_tf32(x.y), r1 = rna_tf32(x.z), m1 = rna_tf32(x.w);
         sts2(sq, kofs(i, 2 * c, 3 * BQ), m0, m1);
@@ -128,12 +133,11 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
     const int part = L >> 6, lrow = L & 63;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 
-    // Key and value rows of a block: item e = tid + BT i is float4 c of key j.
     float4 kr[IT], vr[IT];
     auto load_kv = [&](int kb) {
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
-            const int e = tid + BT * i, j = e / (D / 2), c = e % (D / 2);
+            const int e = tid + BT * i, j = item_j(e), c = item_c(e);
             const int t = kb * BK + j;
             kr[i] = t < T ? __ldg(tok(k, t) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
             vr[i] = t < T ? __ldg(tok(v, t) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
@@ -153,13 +157,18 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
         unsigned char* sv = svb(buf);
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
-            const int e = tid + BT * i, j = e / (D / 2), c = e % (D / 2);
+            const int e = tid + BT * i, j = item_j(e), c = item_c(e);
             sts2(sk, kofs(j, 2 * c, BK), rna_tf32(kr[i].x), rna_tf32(kr[i].z));
             sts2(sk + Cfg::KP_BYTES, kofs(j, 2 * c, BK), rna_tf32(kr[i].y), rna_tf32(kr[i].w));
-            sts(sv, kofs(2 * c, j, NB), rna_tf32(vr[i].x));
-            sts(sv, kofs(2 * c + 1, j, NB), rna_tf32(vr[i].z));
-            sts(sv, kofs(D + 2 * c, j, NB), rna_tf32(vr[i].y));
-            sts(sv, kofs(D + 2 * c + 1, j, NB), rna_tf32(vr[i].w));
+            // Rows 2c and 2c + 1 of the value operand: lanes with c & 4 write
+            // row 2c + 1 first, so each store covers all eight rows of a core
+            // matrix and the 32 lanes hit 32 distinct banks.
+            const bool sw = (c & 4) != 0;
+            const float r0 = rna_tf32(vr[i].x), r1 = rna_tf32(vr[i].z), m0 = rna_tf32(vr[i].y), m1 = rna_tf32(vr[i].w);
+            sts(sv, kofs(2 * c + (sw ? 1 : 0), j, NB), sw ? r1 : r0);
+            sts(sv, kofs(2 * c + (sw ? 0 : 1), j, NB), sw ? r0 : r1);
+            sts(sv, kofs(D + 2 * c + (sw ? 1 : 0), j, NB), sw ? m1 : m0);
+            sts(sv, kofs(D + 2 * c + (sw ? 0 : 1), j, NB), sw ? m0 : m1);
         }
         tc::fence_proxy_async();
     };
@@ -199,18 +208,25 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
         const int buf = kb & 1;
         ok = tc::mbar_wait_bounded(&mbar[0], (uint32_t)(kb & 1), kBornWait) && ok;
         tc::fence_after_sync();
-        // S = G o G in place; keys after the query are masked (only the last
-        // block reaches past a query).
+        // S = G o G in place.
         const int kq = i0 + lrow - kb * BK;  // last key of this block the row may see
         const uint32_t gcol = tmem + lane_base + Cfg::COL_G;
         uint32_t r[BK];
 #pragma unroll
         for (int cb = 0; cb < BK / 16; ++cb) tc::tmem_ld16(gcol + 16 * cb, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * cb));
         tc::tmem_wait_ld();
+        if (kb == last) {  // the diagonal block: keys after the query are masked
 #pragma unroll
-        for (int j = 0; j < BK; ++j) {
-            const float g = __uint_as_float(r[j]);
-            r[j] = __float_as_uint(j <= kq ? g * g : 0.f);
+            for (int j = 0; j < BK; ++j) {
+                const float g = __uint_as_float(r[j]);
+                r[j] = __float_as_uint(j <= kq ? g * g : 0.f);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < BK; ++j) {
+                const float g = __uint_as_float(r[j]);
+                r[j] = __float_as_uint(g * g);
+            }
         }
 #pragma unroll
         for (int cb = 0; cb < BK / 16; ++cb) tc::tmem_st16(gcol + 16 * cb, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * cb));
