@@ -326,7 +326,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     }
     cp_async_commit();
     float4 cv[IT];
-    if constexpr (NH == 1) load_half(p.C, 0, cv);  // with two halves, C is fetched per half (registers)
+    load_half(p.C, 0, cv);  // C (its first half when dstate is 128) in registers, in flight with the rest
 
     // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
     if (tid < CH) {
@@ -439,7 +439,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         issue(tmem + COL_S, a1, a2, false, &mbar[0]);
 
         // ---- 4. Ct half stack into S1 once the state GEMM has read F; G += Ct Bt^T
-        if (NH > 1) load_half(p.C, hf, cv);
+        if (NH > 1 && hf > 0) load_half(p.C, hf, cv);
         wait_bar(&mbar[0], ph);
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
