@@ -133,14 +133,22 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
     const int part = L >> 6, lrow = L & 63;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
 
+    // This thread's items: float4 c of keys j0 + JS i (c and the key step are
+    // the same for every item), so each address below is a per-thread base
+    // plus a constant step in i, computed once.
+    constexpr int JS = BT / (D / 2);
+    const int j0 = item_j(tid), c0 = item_c(tid);
+    const size_t tok_stride = (size_t)H * (D / 2);  // float4 between consecutive tokens of the head
+    const float4* kbase = tok(k, 0) + (size_t)j0 * tok_stride + c0;
+    const float4* vbase = tok(v, 0) + (size_t)j0 * tok_stride + c0;
     float4 kr[IT], vr[IT];
     auto load_kv = [&](int kb) {
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
-            const int e = tid + BT * i, j = item_j(e), c = item_c(e);
-            const int t = kb * BK + j;
-            kr[i] = t < T ? __ldg(tok(k, t) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-            vr[i] = t < T ? __ldg(tok(v, t) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            const int t = kb * BK + j0 + JS * i;
+            const size_t o = (size_t)(kb * BK + JS * i) * tok_stride;
+            kr[i] = t < T ? __ldg(kbase + o) : make_float4(0.f, 0.f, 0.f, 0.f);
+            vr[i] = t < T ? __ldg(vbase + o) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
     };
 
@@ -151,24 +159,30 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
     bool ok = true;
 
     // Key planes (rows j, K = a) and value operand (rows m, K = j) of the
-    // block held in registers, into buffer buf.
+    // block held in registers, into buffer buf.  Rows 2c and 2c + 1 of the
+    // value operand: lanes with c & 4 write row 2c + 1 first, so each store
+    // covers all eight rows of a core matrix and the 32 lanes hit 32 distinct
+    // banks.
+    const bool sw = (c0 & 4) != 0;
+    const uint32_t k_off = kofs(j0, 2 * c0, BK);
+    const uint32_t v_off0 = kofs(2 * c0 + (sw ? 1 : 0), j0, NB), v_off1 = kofs(2 * c0 + (sw ? 0 : 1), j0, NB);
+    constexpr uint32_t K_ISTEP = (JS / 8) * 128;                // JS keys further: JS / 8 row groups
+    constexpr uint32_t V_ISTEP = (JS / 4) * (NB / 8) * 128;     // JS keys further: JS / 4 K groups
+    constexpr uint32_t V_IM = (D / 8) * 128;                    // rows D.. (imaginary parts)
+    static_assert(JS % 8 == 0, "key step keeps the row within its core matrix");
     auto write_kv = [&](int buf) {
         unsigned char* sk = skb(buf);
         unsigned char* sv = svb(buf);
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
-            const int e = tid + BT * i, j = item_j(e), c = item_c(e);
-            sts2(sk, kofs(j, 2 * c, BK), rna_tf32(kr[i].x), rna_tf32(kr[i].z));
-            sts2(sk + Cfg::KP_BYTES, kofs(j, 2 * c, BK), rna_tf32(kr[i].y), rna_tf32(kr[i].w));
-            // Rows 2c and 2c + 1 of the value operand: lanes with c & 4 write
-            // row 2c + 1 first, so each store covers all eight rows of a core
-            // matrix and the 32 lanes hit 32 distinct banks.
-            const bool sw = (c & 4) != 0;
+            const uint32_t ko = k_off + K_ISTEP * i;
+            sts2(sk, ko, rna_tf32(kr[i].x), rna_tf32(kr[i].z));
+            sts2(sk + Cfg::KP_BYTES, ko, rna_tf32(kr[i].y), rna_tf32(kr[i].w));
             const float r0 = rna_tf32(vr[i].x), r1 = rna_tf32(vr[i].z), m0 = rna_tf32(vr[i].y), m1 = rna_tf32(vr[i].w);
-            sts(sv, kofs(2 * c + (sw ? 1 : 0), j, NB), sw ? r1 : r0);
-            sts(sv, kofs(2 * c + (sw ? 0 : 1), j, NB), sw ? r0 : r1);
-            sts(sv, kofs(D + 2 * c + (sw ? 1 : 0), j, NB), sw ? m1 : m0);
-            sts(sv, kofs(D + 2 * c + (sw ? 0 : 1), j, NB), sw ? m0 : m1);
+            sts(sv, v_off0 + V_ISTEP * i, sw ? r1 : r0);
+            sts(sv, v_off1 + V_ISTEP * i, sw ? r0 : r1);
+            sts(sv, v_off0 + V_IM + V_ISTEP * i, sw ? m1 : m0);
+            sts(sv, v_off1 + V_IM + V_ISTEP * i, sw ? m0 : m1);
         }
         tc::fence_proxy_async();
     };
