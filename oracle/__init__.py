@@ -23,7 +23,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRCS = [os.path.join(_HERE, "cssd_oracle.c"), os.path.join(_HERE, "cayley_oracle.c"),
-         os.path.join(_HERE, "born_oracle.c")]
+         os.path.join(_HERE, "born_oracle.c"), os.path.join(_HERE, "backward_oracle.c")]
 _LIB = os.path.join(_HERE, "liboracle.so")
 _lock = threading.Lock()
 _lib = None
@@ -56,10 +56,12 @@ def _load():
             lib.oracle_cayley_recurrence.argtypes = [i64] * 4 + [dp] * 7
             lib.oracle_cayley_chunked.argtypes = [i64] * 5 + [ctypes.c_double] + [dp] * 7
             lib.oracle_born_attention.argtypes = [i64] * 4 + [dp] * 5
+            lib.oracle_cssd_backward.argtypes = [i64] * 5 + [dp] * 13
             lib.oracle_born_attention_feature_map.argtypes = [i64] * 4 + [dp] * 4
             for f in (lib.oracle_cssd_naive, lib.oracle_cssd_step, lib.oracle_cssd_chunked,
                       lib.oracle_geom_closed_form, lib.oracle_cayley_coefficients, lib.oracle_cayley_recurrence,
-                      lib.oracle_cayley_chunked, lib.oracle_born_attention, lib.oracle_born_attention_feature_map):
+                      lib.oracle_cayley_chunked, lib.oracle_born_attention, lib.oracle_born_attention_feature_map,
+                      lib.oracle_cssd_backward):
                 f.restype = None
             _lib = lib
     return _lib
@@ -198,3 +200,19 @@ def born_attention_feature_map(q, k, v):
     psi = np.empty((Bz, T, H, D), np.complex128)
     lib.oracle_born_attention_feature_map(Bz, T, H, D, _p(q), _p(k), _p(v), _p(psi))
     return psi
+
+
+def cssd_backward(x, dt, A, B, C, D, dy):
+    """Gradients of the forward with respect to every input, given the
+    upstream gradient dy [Bz,T,H,P] (complex): returns a dict gx, gdt, gA, gB,
+    gC, gD (complex inputs get dL/dRe + i dL/dIm, real ones dL/dw).  Keeps
+    every forward state: small cases only."""
+    lib = _load()
+    x, dt, A, B, C, D, dy = _c(x), _r(dt), _c(A), _c(B), _c(C), _r(D), _c(dy)
+    Bz, T, H, P = x.shape
+    N = B.shape[-1]
+    g = dict(gx=np.empty_like(x), gdt=np.empty_like(dt), gA=np.empty_like(A), gB=np.empty_like(B),
+             gC=np.empty_like(C), gD=np.empty_like(D))
+    lib.oracle_cssd_backward(Bz, T, H, N, P, _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(dy),
+                             _p(g["gx"]), _p(g["gdt"]), _p(g["gA"]), _p(g["gB"]), _p(g["gC"]), _p(g["gD"]))
+    return g
