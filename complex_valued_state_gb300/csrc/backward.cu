@@ -1,0 +1,319 @@
+// Gradients of the chunked forward with respect to every input.
+//
+// Forward (per batch row and head): a_t = exp(z_t), z_t = softplus(dt_t) A,
+// h_t = a_t h_{t-1} + B_t x_t^T, y_t = C_t^T h_t + D x_t.  Given the upstream
+// gradient dy, with the convention dL = Re sum conj(g_w) dw, the adjoint state
+// G_t = dL/dh_t obeys G_t = conj(a_{t+1}) G_{t+1} + conj(C_t) dy_t^T, and
+//     gx_t = sum_n conj(B_t[n]) G_t[n,:] + D dy_t
+//     gB_t = sum_p G_t[:,p] conj(x_t[p])
+//     gC_t = sum_p conj(h_t[:,p]) dy_t[p]
+// Each of these is itself a run of the forward recurrence, so the library's
+// own forward kernels compute it:
+//   gx: time reversed, input dy, input coupling conj(C), readout conj(B),
+//       rate conj(A) (conj(a) = exp(softplus(dt) conj(A))), the step of token
+//       t + 1 at reversed position T - 1 - t, skip D;
+//   gB: the same reversed run with the state transposed (input conj(C) of
+//       width N, coupling dy of width P, readout conj(x)), no skip;
+//   gC: the forward run with the state transposed (input B, coupling x,
+//       readout conj(dy)), no skip; gC = conj(output).
+// The step and rate gradients need G_t and h_{t-1} together; since y is linear
+// in x, with r_t = sum_p (conj(dy_t[p]) y_t[p] - x_t[p] conj(gx_t[p])) and
+// R_t = sum_{u >= t} r_u one has dL/dz_t = conj(R_t), so
+//     gdt_t = Re(R_t A) sigmoid(dt_t),   gA = sum_{b,t} softplus(dt_t) conj(R_t),
+// and gD = sum_{b,t,p} Re(conj(dy) x).  The total of r vanishes (R_0 = 0: the
+// first step multiplies the zero initial state), so R_t = -sum_{u < t} r_u too.
+// r_t is a small difference of two sums of P products, so y and gx, which it
+// is formed from, are computed by the fp32 CUDA-core chunk kernels (with the
+// TF32 tensor-core forward its error reached 1e-2 of the largest gdt); gB and
+// gC, read directly, take the tensor-core kernel where it applies.
+// The derivation differentiates the sequential recurrence ("Complex-Valued
+// State Spaces", "The discretization"; "SSD Theory" section 2), which the
+// chunked form computes exactly up to rounding.
+
+#include "cssd_common.cuh"
+#include "cssd_internal.h"
+
+namespace cssd {
+namespace {
+
+constexpr int EB = 256;  // threads per block of the element kernels
+
+// dst[b, tau, :] = (conj?) src[b, T - 1 - tau, :], rows of `row` complex numbers.
+__global__ void reverse_rows_kernel(const float2* __restrict__ src, float2* __restrict__ dst, int64_t Bz, int64_t T,
+                                    int64_t row, bool conj_) {
+    const int64_t total = Bz * T * row;
+    for (int64_t i = (int64_t)blockIdx.x * EB + threadIdx.x; i < total; i += (int64_t)gridDim.x * EB) {
+        const int64_t b = i / (T * row), r = i - b * T * row;
+        const int64_t tau = r / row, e = r - tau * row;
+        float2 v = src[(b * T + (T - 1 - tau)) * row + e];
+        if (conj_) v.y = -v.y;
+        dst[i] = v;
+    }
+}
+
+// dst = conj(src), n complex numbers.
+__global__ void conj_kernel(const float2* __restrict__ src, float2* __restrict__ dst, int64_t n) {
+    for (int64_t i = (int64_t)blockIdx.x * EB + threadIdx.x; i < n; i += (int64_t)gridDim.x * EB) {
+        const float2 v = src[i];
+        dst[i] = make_float2(v.x, -v.y);
+    }
+}
+
+// Step of the reversed runs: position tau takes the step of token T - tau
+// (the decay between tokens T - 1 - tau and T - tau); position 0 has no
+// predecessor and takes 0.  Also conj(A) and a zero skip per head.
+__global__ void reverse_steps_kernel(const float* __restrict__ dt, float* __restrict__ dts, int64_t Bz, int64_t T,
+                                     int64_t H, const float2* __restrict__ A, float2* __restrict__ Ac,
+                                     float* __restrict__ zero) {
+    const int64_t total = Bz * T * H;
+    for (int64_t i = (int64_t)blockIdx.x * EB + threadIdx.x; i < total; i += (int64_t)gridDim.x * EB) {
+        const int64_t b = i / (T * H), r = i - b * T * H;
+        const int64_t tau = r / H, h = r - tau * H;
+        dts[i] = tau == 0 ? 0.f : dt[(b * T + (T - tau)) * H + h];
+        if (i < H) {
+            Ac[i] = make_float2(A[i].x, -A[i].y);
+            zero[i] = 0.f;
+        }
+    }
+}
+
+// One warp per token-head: r = sum_p (conj(dy) y - x conj(gx)) and
+// d = sum_p Re(conj(dy) x).
+__global__ void token_terms_kernel(const float2* __restrict__ x, const float2* __restrict__ y,
+                                   const float2* __restrict__ dy, const float2* __restrict__ gx, float2* __restrict__ r,
+                                   float* __restrict__ d, int64_t units, int P) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warps = (int64_t)gridDim.x * (EB / 32);
+    for (int64_t u = ((int64_t)blockIdx.x * EB + threadIdx.x) >> 5; u < units; u += warps) {
+        float rr = 0.f, ri = 0.f, dd = 0.f;
+        for (int p = lane; p < P; p += 32) {
+            const int64_t i = u * P + p;
+            const float2 a = dy[i], yy = y[i], xx = x[i], g = gx[i];
+            // conj(dy) y - x conj(g)
+            rr += a.x * yy.x + a.y * yy.y - (xx.x * g.x + xx.y * g.y);
+            ri += a.x * yy.y - a.y * yy.x - (xx.y * g.x - xx.x * g.y);
+            dd += a.x * xx.x + a.y * xx.y;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            rr += __shfl_xor_sync(0xffffffffu, rr, o);
+            ri += __shfl_xor_sync(0xffffffffu, ri, o);
+            dd += __shfl_xor_sync(0xffffffffu, dd, o);
+        }
+        if (lane == 0) {
+            r[u] = make_float2(rr, ri);
+            d[u] = dd;
+        }
+    }
+}
+
+// One warp per (batch, head): R_t, gdt_t = Re(R_t A) sigmoid(dt_t), and the
+// (batch, head) partial sums of softplus(dt_t) conj(R_t) and of d_t.  Since
+// the total of r vanishes, R_t = sum_{u >= t} r_u = -sum_{u < t} r_u; the
+// shorter side is summed (in double), so R_0 = 0 exactly and rounding grows
+// with min(t, T - t) rather than with T.
+__global__ void reverse_scan_kernel(const float2* __restrict__ r, const float* __restrict__ d,
+                                    const float* __restrict__ dt, const float2* __restrict__ A, float* __restrict__ gdt,
+                                    double2* __restrict__ gA_part, double* __restrict__ gD_part, int64_t Bz, int64_t T,
+                                    int64_t H) {
+    const int lane = threadIdx.x & 31;
+    const int64_t bh = ((int64_t)blockIdx.x * EB + threadIdx.x) >> 5;
+    if (bh >= Bz * H) return;  // uniform across the warp
+    const int64_t b = bh / H, h = bh - b * H;
+    const float2 Ah = A[h];
+    const int64_t half = (T + 1) / 2;  // token 0 is always on the prefix side: R_0 = 0
+    double ga_r = 0.0, ga_i = 0.0, gd = 0.0;
+    auto emit = [&](int64_t i, double Rr, double Ri) {
+        const float v = dt[i];
+        const float sig = v >= 0.f ? 1.f / (1.f + __expf(-v)) : __expf(v) / (1.f + __expf(v));
+        gdt[i] = (float)(Rr * Ah.x - Ri * Ah.y) * sig;
+        const double sp = softplusf(v);
+        ga_r += sp * Rr;
+        ga_i -= sp * Ri;
+        gd += d[i];
+    };
+    // Tokens t < half, oldest first: R_t = -(r_0 + ... + r_{t-1}).
+    double carry_r = 0.0, carry_i = 0.0;
+    for (int64_t t0 = 0; t0 < half; t0 += 32) {
+        const int64_t t = t0 + lane;
+        const bool ok = t < half;
+        const int64_t i = (b * T + (ok ? t : 0)) * H + h;
+        const float2 rv = ok ? r[i] : make_float2(0.f, 0.f);
+        double sr = rv.x, si = rv.y;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double ur = __shfl_up_sync(0xffffffffu, sr, o), ui = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) {
+                sr += ur;
+                si += ui;
+            }
+        }
+        if (ok) emit(i, -(carry_r + sr - rv.x), -(carry_i + si - rv.y));
+        carry_r += __shfl_sync(0xffffffffu, sr, 31);
+        carry_i += __shfl_sync(0xffffffffu, si, 31);
+    }
+    // Tokens t >= half, newest first: R_t = r_t + ... + r_{T-1}.
+    carry_r = carry_i = 0.0;
+    for (int64_t t1 = T - 1; t1 >= half; t1 -= 32) {
+        const int64_t t = t1 - lane;  // lane 0 holds the newest token of this group
+        const bool ok = t >= half;
+        const int64_t i = (b * T + (ok ? t : 0)) * H + h;
+        const float2 rv = ok ? r[i] : make_float2(0.f, 0.f);
+        double sr = rv.x, si = rv.y;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double ur = __shfl_up_sync(0xffffffffu, sr, o), ui = __shfl_up_sync(0xffffffffu, si, o);
+            if (lane >= o) {
+                sr += ur;
+                si += ui;
+            }
+        }
+        if (ok) emit(i, carry_r + sr, carry_i + si);
+        carry_r += __shfl_sync(0xffffffffu, sr, 31);
+        carry_i += __shfl_sync(0xffffffffu, si, 31);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ga_r += __shfl_xor_sync(0xffffffffu, ga_r, o);
+        ga_i += __shfl_xor_sync(0xffffffffu, ga_i, o);
+        gd += __shfl_xor_sync(0xffffffffu, gd, o);
+    }
+    if (lane == 0) {
+        gA_part[bh] = make_double2(ga_r, ga_i);
+        gD_part[bh] = gd;
+    }
+}
+
+// gA[h], gD[h]: the batch rows' partial sums, added in order (deterministic).
+__global__ void head_sums_kernel(const double2* __restrict__ gA_part, const double* __restrict__ gD_part,
+                                 float2* __restrict__ gA, float* __restrict__ gD, int64_t Bz, int64_t H) {
+    const int64_t h = (int64_t)blockIdx.x * EB + threadIdx.x;
+    if (h >= H) return;
+    double ar = 0.0, ai = 0.0, dd = 0.0;
+    for (int64_t b = 0; b < Bz; ++b) {
+        ar += gA_part[b * H + h].x;
+        ai += gA_part[b * H + h].y;
+        dd += gD_part[b * H + h];
+    }
+    gA[h] = make_float2((float)ar, (float)ai);
+    gD[h] = (float)dd;
+}
+
+unsigned grid_for(int64_t n) {
+    const int64_t blocks = (n + EB - 1) / EB;
+    return (unsigned)(blocks < 65535 * 8 ? (blocks < 1 ? 1 : blocks) : 65535 * 8);
+}
+
+size_t align256(size_t v) { return (v + 255) / 256 * 256; }
+
+// Workspace regions of the backward, in order.
+struct BwdLayout {
+    size_t y, dyR, dts, ccR, bcR, xcR, dyc, tmp, Ac, zero, r, d, gAp, gDp, fwd, total;
+};
+
+BwdLayout bwd_layout(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
+    const size_t TP = (size_t)(Bz * T * H * P) * sizeof(float2), TN = (size_t)(Bz * T * H * N) * sizeof(float2);
+    const size_t TH = (size_t)(Bz * T * H);
+    BwdLayout L;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t o = off;
+        off += align256(bytes);
+        return o;
+    };
+    L.y = take(TP);
+    L.dyR = take(TP);
+    L.dts = take(TH * sizeof(float));
+    L.ccR = take(TN);
+    L.bcR = take(TN);
+    L.xcR = take(TP);
+    L.dyc = take(TP);
+    L.tmp = take(TP > TN ? TP : TN);
+    L.Ac = take((size_t)H * sizeof(float2));
+    L.zero = take((size_t)H * sizeof(float));
+    L.r = take(TH * sizeof(float2));
+    L.d = take(TH * sizeof(float));
+    L.gAp = take((size_t)(Bz * H) * sizeof(double2));
+    L.gDp = take((size_t)(Bz * H) * sizeof(double));
+    const size_t f1 = seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);  // y and gx runs (fp32 kernels)
+    const size_t f2 = forward_workspace_bytes(Bz, T, H, P, N, chunk);      // transposed-state runs
+    L.fwd = take(f1 > f2 ? f1 : f2);
+    L.total = off;
+    return L;
+}
+
+}  // namespace
+
+bool backward_supported(int64_t N, int64_t P) {
+    auto ok = [](int64_t v) { return v == 16 || v == 32 || v == 64; };
+    return ok(N) && ok(P);
+}
+
+size_t backward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
+    return bwd_layout(Bz, T, H, N, P, chunk).total;
+}
+
+cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t st) {
+    const int64_t Bz = a.Bz, T = a.T, H = a.H, N = a.N, P = a.P;
+    const BwdLayout L = bwd_layout(Bz, T, H, N, P, a.chunk);
+    unsigned char* w = static_cast<unsigned char*>(workspace);
+    auto f2p = [&](size_t o) { return reinterpret_cast<float2*>(w + o); };
+    auto fp = [&](size_t o) { return reinterpret_cast<float*>(w + o); };
+    void* fws = w + L.fwd;
+    cudaError_t e = cudaSuccess;
+    auto check = [&]() { return (e = cudaGetLastError()) == cudaSuccess; };
+
+    // Forward output, in fp32.
+    const float2* y = f2p(L.y);
+    {
+        FwdArgs f{Bz, T, H, N, P, a.chunk, a.x, a.dt, a.A, a.B, a.C, a.D, f2p(L.y), nullptr};
+        if ((e = launch_seq_forward(f, fws, st)) != cudaSuccess) return e;
+    }
+
+    // Reversed and conjugated inputs.
+    float2 *dyR = f2p(L.dyR), *ccR = f2p(L.ccR), *bcR = f2p(L.bcR), *xcR = f2p(L.xcR), *dyc = f2p(L.dyc);
+    float2* Ac = f2p(L.Ac);
+    float *dts = fp(L.dts), *zero = fp(L.zero);
+    reverse_rows_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(a.dy, dyR, Bz, T, H * P, false);
+    reverse_rows_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(a.C, ccR, Bz, T, H * N, true);
+    reverse_rows_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(a.B, bcR, Bz, T, H * N, true);
+    reverse_rows_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(a.x, xcR, Bz, T, H * P, true);
+    conj_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(a.dy, dyc, Bz * T * H * P);
+    reverse_steps_kernel<<<grid_for(Bz * T * H), EB, 0, st>>>(a.dt, dts, Bz, T, H, a.A, Ac, zero);
+    if (!check()) return e;
+
+    float2* tmp = f2p(L.tmp);
+    // gx: reversed run (fp32), then back to token order.
+    {
+        FwdArgs f{Bz, T, H, N, P, a.chunk, dyR, dts, Ac, ccR, bcR, a.D, tmp, nullptr};
+        if ((e = launch_seq_forward(f, fws, st)) != cudaSuccess) return e;
+        reverse_rows_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(tmp, a.gx, Bz, T, H * P, false);
+        if (!check()) return e;
+    }
+    // gB: reversed run with the state transposed (dstate P, headdim N).
+    {
+        FwdArgs f{Bz, T, H, P, N, a.chunk, ccR, dts, Ac, dyR, xcR, zero, tmp, nullptr};
+        if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
+        reverse_rows_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(tmp, a.gB, Bz, T, H * N, false);
+        if (!check()) return e;
+    }
+    // gC: forward run with the state transposed; gC = conj(output).
+    {
+        FwdArgs f{Bz, T, H, P, N, a.chunk, a.B, a.dt, a.A, a.x, dyc, zero, tmp, nullptr};
+        if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
+        conj_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(tmp, a.gC, Bz * T * H * N);
+        if (!check()) return e;
+    }
+    // Step, rate and skip gradients.
+    float2* r = f2p(L.r);
+    float* d = fp(L.d);
+    double2* gAp = reinterpret_cast<double2*>(w + L.gAp);
+    double* gDp = reinterpret_cast<double*>(w + L.gDp);
+    token_terms_kernel<<<grid_for(Bz * T * H * 32), EB, 0, st>>>(a.x, y, a.dy, a.gx, r, d, Bz * T * H, (int)P);
+    reverse_scan_kernel<<<grid_for(Bz * H * 32), EB, 0, st>>>(r, d, a.dt, a.A, a.gdt, gAp, gDp, Bz, T, H);
+    head_sums_kernel<<<grid_for(H), EB, 0, st>>>(gAp, gDp, a.gA, a.gD, Bz, H);
+    check();
+    return e;
+}
+
+}  // namespace cssd

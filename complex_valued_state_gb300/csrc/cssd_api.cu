@@ -247,6 +247,65 @@ int cssd_cayley_scan(const cssd_dims* d, const float* phi, const float* u, const
     return cssd::launch_cayley_scan(a, stream) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
 }
 
+size_t cssd_backward_workspace_bytes(const cssd_dims* d, int chunk) {
+    if (check_dims(d, true) != CSSD_OK || !supported_chunk(chunk) || !cssd::backward_supported(d->dstate, d->headdim))
+        return 0;
+    return cssd::backward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
+}
+
+int cssd_chunked_backward(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B,
+                          const void* C, const float* D, const void* dy, void* gx, float* gdt, void* gA, void* gB,
+                          void* gC, float* gD, int chunk, void* workspace, size_t workspace_bytes,
+                          cssd_stream_t stream_) {
+    int s = check_dims(d, true);
+    if (s != CSSD_OK) return s;
+    if (!supported_chunk(chunk) || !cssd::backward_supported(d->dstate, d->headdim)) return CSSD_ERR_UNSUPPORTED;
+    if (!x || !dt || !A || !B || !C || !D || !dy || !gx || !gdt || !gA || !gB || !gC || !gD) return CSSD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(dy, 16) || !aligned(gx, 16) ||
+        !aligned(gB, 16) || !aligned(gC, 16) || (workspace && !aligned(workspace, 16)) ||
+        !aligned(A, 8) || !aligned(gA, 8) || !aligned(dt, 4) || !aligned(gdt, 4) || !aligned(D, 4) ||
+        !aligned(gD, 4))
+        return CSSD_ERR_ALIGN;
+    const size_t need = cssd::backward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
+    if (workspace && workspace_bytes < need) return CSSD_ERR_WORKSPACE;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    if ((s = stream_device(stream, &dev)) != CSSD_OK) return s;
+    if ((s = check_all_device(dev, x, (const void*)dt, A, B, C, (const void*)D, dy, gx, (const void*)gdt, gA, gB,
+                              gC, (const void*)gD, (const void*)workspace)) != CSSD_OK)
+        return s;
+    void* ws = workspace;
+    if (!ws) {
+        if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return CSSD_ERR_WORKSPACE;
+        }
+    }
+    cssd::BwdArgs a;
+    a.Bz = d->batch;
+    a.T = d->seqlen;
+    a.H = d->nheads;
+    a.N = d->dstate;
+    a.P = d->headdim;
+    a.chunk = chunk;
+    a.x = static_cast<const float2*>(x);
+    a.dt = dt;
+    a.A = static_cast<const float2*>(A);
+    a.B = static_cast<const float2*>(B);
+    a.C = static_cast<const float2*>(C);
+    a.D = D;
+    a.dy = static_cast<const float2*>(dy);
+    a.gx = static_cast<float2*>(gx);
+    a.gdt = gdt;
+    a.gA = static_cast<float2*>(gA);
+    a.gB = static_cast<float2*>(gB);
+    a.gC = static_cast<float2*>(gC);
+    a.gD = gD;
+    const cudaError_t e = cssd::launch_backward(a, ws, stream);
+    if (!workspace) cudaFreeAsync(ws, stream);
+    return e == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+}
+
 int cssd_born_attention(const cssd_dims* d, const void* q, const void* k, const void* v, void* psi,
                         cssd_stream_t stream_) {
     if (!d) return CSSD_ERR_NULL;

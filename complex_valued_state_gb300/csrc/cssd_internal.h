@@ -81,6 +81,27 @@ struct BornArgs {
 
 cudaError_t launch_step(const StepArgs& a, cudaStream_t stream);
 cudaError_t launch_cayley_scan(const CayleyArgs& a, cudaStream_t stream);
+// Gradients of the forward (backward.cu).
+struct BwdArgs {
+    int64_t Bz, T, H, N, P;
+    int chunk;
+    const float2* x;
+    const float* dt;
+    const float2* A;
+    const float2* B;
+    const float2* C;
+    const float* D;
+    const float2* dy;
+    float2* gx;
+    float* gdt;
+    float2* gA;
+    float2* gB;
+    float2* gC;
+    float* gD;
+};
+bool backward_supported(int64_t N, int64_t P);
+size_t backward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
+cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t stream);
 // Causal Born attention (born.cu).
 bool born_supported(int64_t D);
 cudaError_t launch_born(const BornArgs& a, cudaStream_t stream);

@@ -32,6 +32,7 @@ STATUS = {
 
 # Every symbol include/cssd.h declares.
 EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward",
+           "cssd_backward_workspace_bytes", "cssd_chunked_backward",
            "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_cayley_scan", "cssd_born_attention",
            "cssd_profile_events",
            "cssd_selftest_handoff_timeout", "cssd_status_string")
@@ -79,6 +80,10 @@ def load(path: str = LIB_PATH):
             lib.cssd_step_infinite.restype = ctypes.c_int
             lib.cssd_cayley_scan.argtypes = [dims_p] + [vp] * 7 + [ctypes.c_int, ctypes.c_float, vp]
             lib.cssd_cayley_scan.restype = ctypes.c_int
+            lib.cssd_backward_workspace_bytes.argtypes = [dims_p, ctypes.c_int]
+            lib.cssd_backward_workspace_bytes.restype = ctypes.c_size_t
+            lib.cssd_chunked_backward.argtypes = [dims_p] + [vp] * 13 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
+            lib.cssd_chunked_backward.restype = ctypes.c_int
             lib.cssd_born_attention.argtypes = [dims_p] + [vp] * 4 + [vp]
             lib.cssd_born_attention.restype = ctypes.c_int
             lib.cssd_profile_events.argtypes = [vp, vp]
@@ -196,6 +201,52 @@ def chunked_forward(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None,
     if st != CSSD_OK:
         raise CssdError(st, "cssd_chunked_forward")
     return y, h_final
+
+
+def backward_workspace_bytes(batch: int, seqlen: int, nheads: int, dstate: int, headdim: int, chunk: int) -> int:
+    d = Dims(batch, seqlen, nheads, dstate, headdim)
+    return int(load().cssd_backward_workspace_bytes(ctypes.byref(d), int(chunk)))
+
+
+def chunked_backward(x, dt, A, B, C, D, dy, *, chunk: int = 64, grads=None, workspace=None, stream=None):
+    """cssd_chunked_backward on device tensors; returns a dict gx, gdt, gA, gB,
+    gC, gD (complex inputs: dL/dRe + i dL/dIm; real ones: dL/dw).
+
+    Inputs as chunked_forward; dy complex64 [Bz,T,H,P] is the upstream
+    gradient.  `grads` may hold preallocated outputs under the same keys.
+    """
+    lib = load()
+    dev = x.device
+    Bz, T, H, P = x.shape
+    N = B.shape[-1]
+    c64, f32 = torch.complex64, torch.float32
+    _check(x, "x", c64, (Bz, T, H, P), dev)
+    _check(dt, "dt", f32, (Bz, T, H), dev)
+    _check(A, "A", c64, (H,), dev)
+    _check(B, "B", c64, (Bz, T, H, N), dev)
+    _check(C, "C", c64, (Bz, T, H, N), dev)
+    _check(D, "D", f32, (H,), dev)
+    _check(dy, "dy", c64, (Bz, T, H, P), dev)
+    g = dict(grads or {})
+    shapes = {"gx": ((Bz, T, H, P), c64), "gdt": ((Bz, T, H), f32), "gA": ((H,), c64), "gB": ((Bz, T, H, N), c64),
+              "gC": ((Bz, T, H, N), c64), "gD": ((H,), f32)}
+    for k, (shp, dtp) in shapes.items():
+        if k not in g:
+            g[k] = torch.empty(shp, dtype=dtp, device=dev)
+        _check(g[k], k, dtp, shp, dev)
+    ws_bytes = 0
+    if workspace is not None:
+        if workspace.device != dev or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous tensor on the inputs' device")
+        ws_bytes = workspace.numel() * workspace.element_size()
+    d = Dims(Bz, T, H, N, P)
+    st = lib.cssd_chunked_backward(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(dy),
+                                   _ptr(g["gx"]), _ptr(g["gdt"]), _ptr(g["gA"]), _ptr(g["gB"]), _ptr(g["gC"]),
+                                   _ptr(g["gD"]), int(chunk), _ptr(workspace), ctypes.c_size_t(ws_bytes),
+                                   _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_chunked_backward")
+    return g
 
 
 def chunked_forward_noalloc(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None, want_state: bool = True,

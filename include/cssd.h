@@ -194,6 +194,39 @@ int cssd_step_infinite(const cssd_dims* dims, const void* x, const float* dt, co
 int cssd_cayley_scan(const cssd_dims* dims, const float* phi, const float* u, const void* b, const void* C,
                      const void* psi0, void* y, void* psi_final, int chunk, float log_clamp, cssd_stream_t stream);
 
+/* Gradients of cssd_chunked_forward with respect to every input ("The
+ * Chunkwise Complex SSD Algorithm", its backward section; the gradients are
+ * those of the sequential recurrence of "Complex-Valued State Spaces", "The
+ * discretization", which the chunked forward computes up to rounding).
+ * Given the upstream gradient dy of a real loss L, with the convention
+ *     dL = Re sum conj(g_w) dw      (complex w: g_w = dL/dRe w + i dL/dIm w;
+ *                                    real w: g_w = dL/dw)
+ * the call writes gx, gdt, gA, gB, gC, gD.  The adjoint state
+ * G_t = conj(a_{t+1}) G_{t+1} + conj(C_t) dy_t^T is itself a run of the forward
+ * recurrence (time reversed, rate conj(A)), so the gradients of x, B and C are
+ * three runs of the forward kernels on reversed and conjugated inputs; those of
+ * dt and A follow from R_t = sum_{u >= t} sum_p (conj(dy_u) y_u - x_u conj(gx_u)),
+ * since dL/dz_t = conj(R_t) for z_t = softplus(dt_t) A; gD = sum Re(conj(dy) x).
+ * The forward output y is recomputed, and it and gx come from the fp32
+ * CUDA-core chunk kernels: R_t is a small difference of large sums, which TF32
+ * operands would spoil; gB and gC use the tensor-core kernel where it applies.
+ *   dims, x, dt, A, B, C, D, chunk   as cssd_chunked_forward; dstate and
+ *            headdim in {16, 32, 64} (else CSSD_ERR_UNSUPPORTED)
+ *   dy       complex64 [batch, seqlen, nheads, headdim]  upstream gradient
+ *   gx       complex64 like x;  gdt float32 like dt;  gA complex64 [nheads];
+ *   gB, gC   complex64 like B, C;  gD float32 [nheads]     (all written)
+ *   workspace  device memory of at least cssd_backward_workspace_bytes(dims,
+ *            chunk) bytes, 16-byte aligned, or NULL (the library allocates and
+ *            frees it stream-ordered)
+ * Complex arrays 16-byte aligned, A and gA 8-byte, real ones 4-byte.  gA and gD
+ * sum over batch and tokens in a fixed order (deterministic).  Errors as
+ * cssd_chunked_forward.  Returns a cssd_status. */
+size_t cssd_backward_workspace_bytes(const cssd_dims* dims, int chunk);
+int cssd_chunked_backward(const cssd_dims* dims, const void* x, const float* dt, const void* A, const void* B,
+                          const void* C, const float* D, const void* dy, void* gx, float* gdt, void* gA, void* gB,
+                          void* gC, float* gD, int chunk, void* workspace, size_t workspace_bytes,
+                          cssd_stream_t stream);
+
 /* Causal Born attention ("Complex Phase-State Dynamics Reduce the
  * Optimization Steps of Sequence Models", section 5.5 equation (5), Appendix A
  * Algorithm 3).  Per (batch, head), for every query position i:
