@@ -38,16 +38,20 @@ namespace {
 
 constexpr int EB = 256;  // threads per block of the element kernels
 
-// dst[b, tau, :] = (conj?) src[b, T - 1 - tau, :], rows of `row` complex numbers.
+// dst[b, tau, :] = (conj?) src[b, T - 1 - tau, :], rows of `row` complex
+// numbers; one block per output row (grid-stride over rows), so each block
+// copies one contiguous row to another.
 __global__ void reverse_rows_kernel(const float2* __restrict__ src, float2* __restrict__ dst, int64_t Bz, int64_t T,
                                     int64_t row, bool conj_) {
-    const int64_t total = Bz * T * row;
-    for (int64_t i = (int64_t)blockIdx.x * EB + threadIdx.x; i < total; i += (int64_t)gridDim.x * EB) {
-        const int64_t b = i / (T * row), r = i - b * T * row;
-        const int64_t tau = r / row, e = r - tau * row;
-        float2 v = src[(b * T + (T - 1 - tau)) * row + e];
-        if (conj_) v.y = -v.y;
-        dst[i] = v;
+    for (int64_t o = blockIdx.x; o < Bz * T; o += gridDim.x) {
+        const int64_t b = o / T, tau = o - b * T;
+        const float2* s = src + (b * T + (T - 1 - tau)) * row;
+        float2* d = dst + o * row;
+        for (int64_t e = threadIdx.x; e < row; e += EB) {
+            float2 v = s[e];
+            if (conj_) v.y = -v.y;
+            d[e] = v;
+        }
     }
 }
 
@@ -107,23 +111,51 @@ __global__ void token_terms_kernel(const float2* __restrict__ x, const float2* _
     }
 }
 
-// One warp per (batch, head): R_t, gdt_t = Re(R_t A) sigmoid(dt_t), and the
-// (batch, head) partial sums of softplus(dt_t) conj(R_t) and of d_t.  Since
-// the total of r vanishes, R_t = sum_{u >= t} r_u = -sum_{u < t} r_u; the
-// shorter side is summed (in double), so R_0 = 0 exactly and rounding grows
-// with min(t, T - t) rather than with T.
-__global__ void reverse_scan_kernel(const float2* __restrict__ r, const float* __restrict__ d,
-                                    const float* __restrict__ dt, const float2* __restrict__ A, float* __restrict__ gdt,
-                                    double2* __restrict__ gA_part, double* __restrict__ gD_part, int64_t Bz, int64_t T,
-                                    int64_t H) {
-    const int lane = threadIdx.x & 31;
-    const int64_t bh = ((int64_t)blockIdx.x * EB + threadIdx.x) >> 5;
-    if (bh >= Bz * H) return;  // uniform across the warp
+// Inclusive scan of one double2 per thread across the block (EB threads),
+// in thread order; scratch holds EB / 32 double2.
+__device__ __forceinline__ double2 block_scan(double2 v, double2* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double ux = __shfl_up_sync(0xffffffffu, v.x, o), uy = __shfl_up_sync(0xffffffffu, v.y, o);
+        if (lane >= o) {
+            v.x += ux;
+            v.y += uy;
+        }
+    }
+    if (lane == 31) scratch[warp] = v;
+    __syncthreads();
+    double2 off = make_double2(0.0, 0.0);
+    for (int w = 0; w < warp; ++w) {
+        off.x += scratch[w].x;
+        off.y += scratch[w].y;
+    }
+    __syncthreads();
+    return make_double2(v.x + off.x, v.y + off.y);
+}
+
+// One CTA per (batch, head): R_t, gdt_t = Re(R_t A) sigmoid(dt_t), and the
+// (batch, head) sums of softplus(dt_t) conj(R_t) and of d_t.  Since the total
+// of r vanishes, R_t = sum_{u >= t} r_u = -sum_{u < t} r_u; the shorter side is
+// summed (in double), so R_0 = 0 exactly and rounding grows with
+// min(t, T - t) rather than with T.  Thread k holds the tokens
+// [k L, (k + 1) L) of the sequence.
+constexpr int SCAN_L = 16;  // tokens per thread and pass
+__global__ void __launch_bounds__(EB) reverse_scan_kernel(const float2* __restrict__ r, const float* __restrict__ d,
+                                                          const float* __restrict__ dt, const float2* __restrict__ A,
+                                                          float* __restrict__ gdt, double2* __restrict__ gA_part,
+                                                          double* __restrict__ gD_part, int64_t T, int64_t H) {
+    __shared__ double2 scratch[EB / 32];
+    __shared__ double2 red[EB / 32];
+    __shared__ double redd[EB / 32];
+    const int64_t bh = blockIdx.x;
     const int64_t b = bh / H, h = bh - b * H;
     const float2 Ah = A[h];
     const int64_t half = (T + 1) / 2;  // token 0 is always on the prefix side: R_0 = 0
+    const int tid = threadIdx.x;
     double ga_r = 0.0, ga_i = 0.0, gd = 0.0;
-    auto emit = [&](int64_t i, double Rr, double Ri) {
+    auto emit = [&](int64_t t, double Rr, double Ri) {
+        const int64_t i = (b * T + t) * H + h;
         const float v = dt[i];
         const float sig = v >= 0.f ? 1.f / (1.f + __expf(-v)) : __expf(v) / (1.f + __expf(v));
         gdt[i] = (float)(Rr * Ah.x - Ri * Ah.y) * sig;
@@ -132,55 +164,82 @@ __global__ void reverse_scan_kernel(const float2* __restrict__ r, const float* _
         ga_i -= sp * Ri;
         gd += d[i];
     };
-    // Tokens t < half, oldest first: R_t = -(r_0 + ... + r_{t-1}).
-    double carry_r = 0.0, carry_i = 0.0;
-    for (int64_t t0 = 0; t0 < half; t0 += 32) {
-        const int64_t t = t0 + lane;
-        const bool ok = t < half;
-        const int64_t i = (b * T + (ok ? t : 0)) * H + h;
-        const float2 rv = ok ? r[i] : make_float2(0.f, 0.f);
-        double sr = rv.x, si = rv.y;
+    // Prefix side, tokens [0, half) in passes of EB * SCAN_L: R_t = -(r_0 + ... + r_{t-1}).
+    double2 carry = make_double2(0.0, 0.0);
+    for (int64_t base = 0; base < half; base += (int64_t)EB * SCAN_L) {
+        const int64_t t0 = base + (int64_t)tid * SCAN_L;
+        double2 loc[SCAN_L];
+        double2 sum = make_double2(0.0, 0.0);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double ur = __shfl_up_sync(0xffffffffu, sr, o), ui = __shfl_up_sync(0xffffffffu, si, o);
-            if (lane >= o) {
-                sr += ur;
-                si += ui;
-            }
+        for (int k = 0; k < SCAN_L; ++k) {
+            const int64_t t = t0 + k;
+            const float2 v = t < half ? r[(b * T + t) * H + h] : make_float2(0.f, 0.f);
+            loc[k] = sum;  // exclusive within the thread
+            sum.x += v.x;
+            sum.y += v.y;
         }
-        if (ok) emit(i, -(carry_r + sr - rv.x), -(carry_i + si - rv.y));
-        carry_r += __shfl_sync(0xffffffffu, sr, 31);
-        carry_i += __shfl_sync(0xffffffffu, si, 31);
-    }
-    // Tokens t >= half, newest first: R_t = r_t + ... + r_{T-1}.
-    carry_r = carry_i = 0.0;
-    for (int64_t t1 = T - 1; t1 >= half; t1 -= 32) {
-        const int64_t t = t1 - lane;  // lane 0 holds the newest token of this group
-        const bool ok = t >= half;
-        const int64_t i = (b * T + (ok ? t : 0)) * H + h;
-        const float2 rv = ok ? r[i] : make_float2(0.f, 0.f);
-        double sr = rv.x, si = rv.y;
+        const double2 incl = block_scan(sum, scratch);
+        const double2 excl = make_double2(carry.x + incl.x - sum.x, carry.y + incl.y - sum.y);
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double ur = __shfl_up_sync(0xffffffffu, sr, o), ui = __shfl_up_sync(0xffffffffu, si, o);
-            if (lane >= o) {
-                sr += ur;
-                si += ui;
-            }
+        for (int k = 0; k < SCAN_L; ++k) {
+            const int64_t t = t0 + k;
+            if (t < half) emit(t, -(excl.x + loc[k].x), -(excl.y + loc[k].y));
         }
-        if (ok) emit(i, carry_r + sr, carry_i + si);
-        carry_r += __shfl_sync(0xffffffffu, sr, 31);
-        carry_i += __shfl_sync(0xffffffffu, si, 31);
+        if (tid == EB - 1) scratch[0] = incl;  // the pass total
+        __syncthreads();
+        carry.x += scratch[0].x;
+        carry.y += scratch[0].y;
+        __syncthreads();
     }
+    // Suffix side, tokens [half, T) newest first: R_t = r_t + ... + r_{T-1}.
+    carry = make_double2(0.0, 0.0);
+    for (int64_t base = T - 1; base >= half; base -= (int64_t)EB * SCAN_L) {
+        const int64_t t0 = base - (int64_t)tid * SCAN_L;  // this thread's newest token
+        double2 loc[SCAN_L];
+        double2 sum = make_double2(0.0, 0.0);
+#pragma unroll
+        for (int k = 0; k < SCAN_L; ++k) {
+            const int64_t t = t0 - k;
+            const float2 v = t >= half ? r[(b * T + t) * H + h] : make_float2(0.f, 0.f);
+            sum.x += v.x;
+            sum.y += v.y;
+            loc[k] = sum;  // inclusive within the thread
+        }
+        const double2 incl = block_scan(sum, scratch);
+        const double2 excl = make_double2(carry.x + incl.x - sum.x, carry.y + incl.y - sum.y);
+#pragma unroll
+        for (int k = 0; k < SCAN_L; ++k) {
+            const int64_t t = t0 - k;
+            if (t >= half) emit(t, excl.x + loc[k].x, excl.y + loc[k].y);
+        }
+        if (tid == EB - 1) scratch[0] = incl;
+        __syncthreads();
+        carry.x += scratch[0].x;
+        carry.y += scratch[0].y;
+        __syncthreads();
+    }
+    // Block sums of the rate and skip gradients.
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         ga_r += __shfl_xor_sync(0xffffffffu, ga_r, o);
         ga_i += __shfl_xor_sync(0xffffffffu, ga_i, o);
         gd += __shfl_xor_sync(0xffffffffu, gd, o);
     }
-    if (lane == 0) {
-        gA_part[bh] = make_double2(ga_r, ga_i);
-        gD_part[bh] = gd;
+    if ((tid & 31) == 0) {
+        red[tid >> 5] = make_double2(ga_r, ga_i);
+        redd[tid >> 5] = gd;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        double2 s2 = make_double2(0.0, 0.0);
+        double sd = 0.0;
+        for (int w = 0; w < EB / 32; ++w) {
+            s2.x += red[w].x;
+            s2.y += red[w].y;
+            sd += redd[w];
+        }
+        gA_part[bh] = s2;
+        gD_part[bh] = sd;
     }
 }
 
@@ -203,6 +262,8 @@ unsigned grid_for(int64_t n) {
     const int64_t blocks = (n + EB - 1) / EB;
     return (unsigned)(blocks < 65535 * 8 ? (blocks < 1 ? 1 : blocks) : 65535 * 8);
 }
+
+unsigned grid_rows(int64_t rows) { return (unsigned)(rows < 65535 * 8 ? rows : 65535 * 8); }
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
@@ -274,10 +335,10 @@ cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t st) 
     float2 *dyR = f2p(L.dyR), *ccR = f2p(L.ccR), *bcR = f2p(L.bcR), *xcR = f2p(L.xcR), *dyc = f2p(L.dyc);
     float2* Ac = f2p(L.Ac);
     float *dts = fp(L.dts), *zero = fp(L.zero);
-    reverse_rows_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(a.dy, dyR, Bz, T, H * P, false);
-    reverse_rows_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(a.C, ccR, Bz, T, H * N, true);
-    reverse_rows_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(a.B, bcR, Bz, T, H * N, true);
-    reverse_rows_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(a.x, xcR, Bz, T, H * P, true);
+    reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.dy, dyR, Bz, T, H * P, false);
+    reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.C, ccR, Bz, T, H * N, true);
+    reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.B, bcR, Bz, T, H * N, true);
+    reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.x, xcR, Bz, T, H * P, true);
     conj_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(a.dy, dyc, Bz * T * H * P);
     reverse_steps_kernel<<<grid_for(Bz * T * H), EB, 0, st>>>(a.dt, dts, Bz, T, H, a.A, Ac, zero);
     if (!check()) return e;
@@ -287,14 +348,14 @@ cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t st) 
     {
         FwdArgs f{Bz, T, H, N, P, a.chunk, dyR, dts, Ac, ccR, bcR, a.D, tmp, nullptr};
         if ((e = launch_seq_forward(f, fws, st)) != cudaSuccess) return e;
-        reverse_rows_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(tmp, a.gx, Bz, T, H * P, false);
+        reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(tmp, a.gx, Bz, T, H * P, false);
         if (!check()) return e;
     }
     // gB: reversed run with the state transposed (dstate P, headdim N).
     {
         FwdArgs f{Bz, T, H, P, N, a.chunk, ccR, dts, Ac, dyR, xcR, zero, tmp, nullptr};
         if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
-        reverse_rows_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(tmp, a.gB, Bz, T, H * N, false);
+        reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(tmp, a.gB, Bz, T, H * N, false);
         if (!check()) return e;
     }
     // gC: forward run with the state transposed; gC = conj(output).
@@ -310,7 +371,7 @@ cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t st) 
     double2* gAp = reinterpret_cast<double2*>(w + L.gAp);
     double* gDp = reinterpret_cast<double*>(w + L.gDp);
     token_terms_kernel<<<grid_for(Bz * T * H * 32), EB, 0, st>>>(a.x, y, a.dy, a.gx, r, d, Bz * T * H, (int)P);
-    reverse_scan_kernel<<<grid_for(Bz * H * 32), EB, 0, st>>>(r, d, a.dt, a.A, a.gdt, gAp, gDp, Bz, T, H);
+    reverse_scan_kernel<<<(unsigned)(Bz * H), EB, 0, st>>>(r, d, a.dt, a.A, a.gdt, gAp, gDp, T, H);
     head_sums_kernel<<<grid_for(H), EB, 0, st>>>(gAp, gDp, a.gA, a.gD, Bz, H);
     check();
     return e;
