@@ -47,6 +47,7 @@ def parse():
     ap.add_argument("--no-long", action="store_true", help="skip the long_seq forward measurement")
     ap.add_argument("--no-cayley", action="store_true", help="skip the per-coordinate Cayley scan measurement")
     ap.add_argument("--no-born", action="store_true", help="skip the causal Born attention measurement")
+    ap.add_argument("--no-backward", action="store_true", help="skip the gradient (backward) measurement")
     return ap.parse_args()
 
 
@@ -277,7 +278,7 @@ def run_ours(args, rank, world, local):
     e_ms = e0.elapsed_time(e1) / e_steps
     e_ms = reduce_max(pg, e_ms, dev)
 
-    decode = const_input = cayley = born = None
+    decode = const_input = cayley = born = backward = None
     if not args.no_decode:
         decode = bench_decode(args, dev)
         const_input = bench_const_input(args, dev)
@@ -285,6 +286,8 @@ def run_ours(args, rank, world, local):
         cayley = bench_cayley(args, dev)
     if not args.no_born:
         born = bench_born(args, dev)
+    if not args.no_backward:
+        backward = bench_backward(args, dev)
     long_seq = None
     if not args.no_long:
         long_seq = bench_long_seq(args, dev)
@@ -324,6 +327,8 @@ def run_ours(args, rank, world, local):
         out["cayley_scan"] = cayley
     if born:
         out["born_attention"] = born
+    if backward:
+        out["backward"] = backward
     if long_seq:
         out["long_seq"] = long_seq
     if world == 1 and not args.no_cpu_baseline:
@@ -529,6 +534,51 @@ def bench_born(args, dev):
             "hbm_bytes_per_launch": 4 * Bz * T * H * D * 8,
             "traffic": recorded_traffic("born_kernel", Bz * T * H),
             "context": "the paper's ~80,000 tokens/s is a whole 253M-parameter H-Transformer training on A100s, not this kernel"}
+
+
+def bench_backward(args, dev):
+    """Gradients of the mamba2_layer forward (cssd_chunked_backward: y and the
+    x-gradient run on the fp32 CUDA-core chunk kernels, the B and C gradients
+    on the tensor-core kernel).  HBM roofline on the algorithmic bytes: x, dt,
+    B, C, dy in and gx, gdt, gB, gC out."""
+    import numpy as np
+    import torch
+
+    from complex_valued_state_gb300 import cssd
+    from complex_valued_state_gb300 import workloads as wl
+
+    w = wl.MAMBA2_LAYER
+    host = wl.make_inputs(w)
+    g = {k: torch.from_numpy(host[k]).to(dev) for k in ("x", "dt", "A", "B", "C", "D")}
+    rng = np.random.default_rng(w.seed + 1000)
+    shape = (w.batch, w.seqlen, w.nheads, w.headdim)
+    dy = torch.from_numpy(((rng.standard_normal(shape) + 1j * rng.standard_normal(shape)) / np.sqrt(2))
+                          .astype(np.complex64)).to(dev)
+    ws = torch.empty(cssd.backward_workspace_bytes(w.batch, w.seqlen, w.nheads, w.dstate, w.headdim, w.chunk),
+                     dtype=torch.uint8, device=dev)
+    out = cssd.chunked_backward(**g, dy=dy, chunk=w.chunk, workspace=ws)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(3, args.warmup)):
+        cssd.chunked_backward(**g, dy=dy, chunk=w.chunk, workspace=ws, grads=out)
+    torch.cuda.synchronize(dev)
+    n = max(10, args.steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(n):
+        cssd.chunked_backward(**g, dy=dy, chunk=w.chunk, workspace=ws, grads=out)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / n
+    N, P = w.dstate, w.headdim
+    alg = w.units * (8 * P + 4 + 16 * N + 8 * P + 8 * P + 4 + 16 * N)
+    hbm, kind = peaks()
+    gbs = alg / (ms / 1e3) / 1e9
+    return {"workload": f"mamba2_layer backward Bz{w.batch} T{w.seqlen} H{w.nheads} N{N} P{P} chunk{w.chunk}",
+            "ms_per_call": round(ms, 4), "calls": n, "value": round(w.units / (ms / 1e3), 1), "unit": "token-heads/s",
+            "roofline": {"bound": "hbm", "kernel": "whole backward (24 launches)", "achieved": round(gbs, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
+                         "alg_bytes_per_call": alg},
+            "workspace_bytes": int(ws.numel())}
 
 
 def bench_long_seq(args, dev):
