@@ -101,6 +101,56 @@ int step_common(const cssd_dims* d, void* h, const void* x, const float* dt, con
     const cudaError_t e = with_h ? cssd::launch_step(a, stream) : cssd::launch_step_infinite(a, stream);
     return e == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
 }
+// Shared checks and launch of cssd_chunked_forward (h0 == NULL) and
+// cssd_chunked_forward_h0.
+int forward_common(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B, const void* C,
+                   const float* D, const void* h0, void* y, void* h_final, int chunk, void* workspace,
+                   size_t workspace_bytes, cssd_stream_t stream_) {
+    int s = check_dims(d, true);
+    if (s != CSSD_OK) return s;
+    if (!supported_chunk(chunk)) return CSSD_ERR_UNSUPPORTED;
+    if (!x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
+    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
+        (h_final && !aligned(h_final, 16)) || (h0 && !aligned(h0, 16)) || (workspace && !aligned(workspace, 16)) ||
+        !aligned(A, 8) || !aligned(dt, 4) || !aligned(D, 4))
+        return CSSD_ERR_ALIGN;
+    const size_t need = cssd::forward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
+    if (workspace && workspace_bytes < need) return CSSD_ERR_WORKSPACE;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    if ((s = stream_device(stream, &dev)) != CSSD_OK) return s;
+    if ((s = check_all_device(dev, x, (const void*)dt, A, B, C, (const void*)D, h0, (const void*)y,
+                              (const void*)h_final, (const void*)workspace)) != CSSD_OK)
+        return s;
+
+    void* ws = workspace;
+    if (!ws) {
+        if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return CSSD_ERR_WORKSPACE;
+        }
+    }
+    cssd::FwdArgs a;
+    a.Bz = d->batch;
+    a.T = d->seqlen;
+    a.H = d->nheads;
+    a.N = d->dstate;
+    a.P = d->headdim;
+    a.chunk = chunk;
+    a.x = static_cast<const float2*>(x);
+    a.dt = dt;
+    a.A = static_cast<const float2*>(A);
+    a.B = static_cast<const float2*>(B);
+    a.C = static_cast<const float2*>(C);
+    a.D = D;
+    a.y = static_cast<float2*>(y);
+    a.h_final = static_cast<float2*>(h_final);
+    a.h0 = static_cast<const float2*>(h0);
+    const cudaError_t e = cssd::launch_forward(a, ws, stream);
+    if (!workspace) cudaFreeAsync(ws, stream);
+    return e == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+}
+
 }  // namespace
 
 extern "C" {
@@ -151,48 +201,13 @@ int cssd_forward_launches(const cssd_dims* d, int chunk) {
 int cssd_chunked_forward(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B,
                          const void* C, const float* D, void* y, void* h_final, int chunk, void* workspace,
                          size_t workspace_bytes, cssd_stream_t stream_) {
-    int s = check_dims(d, true);
-    if (s != CSSD_OK) return s;
-    if (!supported_chunk(chunk)) return CSSD_ERR_UNSUPPORTED;
-    if (!x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
-    if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
-        (h_final && !aligned(h_final, 16)) || (workspace && !aligned(workspace, 16)) || !aligned(A, 8) ||
-        !aligned(dt, 4) || !aligned(D, 4))
-        return CSSD_ERR_ALIGN;
-    const size_t need = cssd::forward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
-    if (workspace && workspace_bytes < need) return CSSD_ERR_WORKSPACE;
-    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
-    int dev = 0;
-    if ((s = stream_device(stream, &dev)) != CSSD_OK) return s;
-    if ((s = check_all_device(dev, x, (const void*)dt, A, B, C, (const void*)D, (const void*)y, (const void*)h_final,
-                              (const void*)workspace)) != CSSD_OK)
-        return s;
+    return forward_common(d, x, dt, A, B, C, D, nullptr, y, h_final, chunk, workspace, workspace_bytes, stream_);
+}
 
-    void* ws = workspace;
-    if (!ws) {
-        if (cudaMallocAsync(&ws, need, stream) != cudaSuccess) {
-            cudaGetLastError();
-            return CSSD_ERR_WORKSPACE;
-        }
-    }
-    cssd::FwdArgs a;
-    a.Bz = d->batch;
-    a.T = d->seqlen;
-    a.H = d->nheads;
-    a.N = d->dstate;
-    a.P = d->headdim;
-    a.chunk = chunk;
-    a.x = static_cast<const float2*>(x);
-    a.dt = dt;
-    a.A = static_cast<const float2*>(A);
-    a.B = static_cast<const float2*>(B);
-    a.C = static_cast<const float2*>(C);
-    a.D = D;
-    a.y = static_cast<float2*>(y);
-    a.h_final = static_cast<float2*>(h_final);
-    const cudaError_t e = cssd::launch_forward(a, ws, stream);
-    if (!workspace) cudaFreeAsync(ws, stream);
-    return e == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+int cssd_chunked_forward_h0(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B,
+                            const void* C, const float* D, const void* h0, void* y, void* h_final, int chunk,
+                            void* workspace, size_t workspace_bytes, cssd_stream_t stream_) {
+    return forward_common(d, x, dt, A, B, C, D, h0, y, h_final, chunk, workspace, workspace_bytes, stream_);
 }
 
 int cssd_step(const cssd_dims* d, void* h, const void* x, const float* dt, const void* A, const void* B,

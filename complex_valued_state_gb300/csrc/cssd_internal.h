@@ -20,7 +20,8 @@ struct FwdArgs {
     const float2* C;
     const float* D;
     float2* y;
-    float2* h_final;  // may be null
+    float2* h_final;             // may be null
+    const float2* h0 = nullptr;  // state before the first token [Bz,H,N,P]; null = zero
 };
 
 struct StepArgs {

@@ -5,8 +5,8 @@
 //      the chunk's tokens from a zero state and stores the chunk's end state
 //      S_c (N x P) and its total decay E_c = exp(sum of the chunk's log-steps);
 //   2. state_scan    (grid state-slices x heads*batch): the inter-chunk scan
-//      H_{c+1} = E_c H_c + S_c, H_0 = 0, written over S_c in place, plus the
-//      final state;
+//      H_{c+1} = E_c H_c + S_c, H_0 = the initial state (zero unless given),
+//      written over S_c in place, plus the final state;
 //   3. chunk_output  (grid chunks x heads x batch): the recurrence over the
 //      chunk again, started from H_c, with the readout y = C^T h + D x.
 // The split into per-chunk end states, a short scan over chunks and a
@@ -117,14 +117,19 @@ __global__ void __launch_bounds__(SeqShape<N, P>::NT)
 // state through all chunks.  S_c is replaced by H_c (the state entering c).
 // Grid: x = batch * head, y = 256-wide slices of the state.
 __global__ void __launch_bounds__(256)
-    state_scan_kernel(float4* __restrict__ Sbuf, const float2* __restrict__ Ebuf, float4* __restrict__ h_final,
-                      int np2, int nc) {
+    state_scan_kernel(float4* __restrict__ Sbuf, const float2* __restrict__ Ebuf, const float4* __restrict__ h0,
+                      float4* __restrict__ h_final, int np2, int nc) {
     const int idx = blockIdx.y * blockDim.x + threadIdx.x;
     if (idx >= np2) return;
     const size_t bh = blockIdx.x;
     float4* Sp = Sbuf + bh * (size_t)nc * np2 + idx;
     const float2* E = Ebuf + bh * nc;
     float2 c0 = make_float2(0.f, 0.f), c1 = c0;
+    if (h0) {  // the caller's state before the first token
+        const float4 v = h0[bh * np2 + idx];
+        c0 = make_float2(v.x, v.y);
+        c1 = make_float2(v.z, v.w);
+    }
     constexpr int U = 8;
     for (int cb = 0; cb < nc; cb += U) {
         float4 v[U];
@@ -159,7 +164,8 @@ cudaError_t launch_np(const FwdArgs& a, float2* Sbuf, float2* Ebuf, cudaStream_t
     if (e != cudaSuccess) return e;
     const int np2 = (int)(a.N * a.P / 2);
     state_scan_kernel<<<dim3((unsigned)(a.Bz * a.H), (np2 + 255) / 256), 256, 0, st>>>(
-        reinterpret_cast<float4*>(Sbuf), Ebuf, reinterpret_cast<float4*>(a.h_final), np2, nc);
+        reinterpret_cast<float4*>(Sbuf), Ebuf, reinterpret_cast<const float4*>(a.h0),
+        reinterpret_cast<float4*>(a.h_final), np2, nc);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);

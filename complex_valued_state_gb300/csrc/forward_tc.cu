@@ -17,7 +17,8 @@
 //     H_{c+1}      = exp(rho_end) H_c + S_c               (inter-chunk)
 //     Y_off        = exp(rho_l) Ct_l H_c                  (carried-in state)
 //     y            = Y_diag + Y_off + D x,   h_final = e^{i Theta_last} H_final
-// so the epilogues scale real and imaginary parts independently.
+// so the epilogues scale real and imaginary parts independently.  H_0 is the
+// caller's initial state (zero when none is given).
 //
 // One CTA per (chunk, batch*head), dispatched in chunk-major order through an
 // atomic ticket so that the CTA owning chunk c-1 of a sequence has always
@@ -97,6 +98,7 @@ struct TcParams {
     const float* D;    // [H]
     float2* y;         // [Bz,T,H,P]
     float2* h_final;   // [Bz,H,N,P] or null
+    const float2* h0;  // [Bz,H,N,P] state before the first token, or null (zero)
     unsigned long long* ring;  // [BH][RING][2][P][N] tagged cells
     int* ticket;       // [1]
     float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
@@ -104,6 +106,7 @@ struct TcParams {
     int* err;          // [1] error bits
     int T, H, BH, nc, NH;
     int first_ticket;       // tickets start here (0 in normal use)
+    int pf_dist;            // L2 prefetch distance in tickets (0: none)
     long long wait_cycles;  // limit of the hand-off wait (SM clocks)
 };
 
@@ -118,6 +121,10 @@ __device__ __forceinline__ uint32_t raw_off(int l, int j) { return (uint32_t)(l 
 __device__ __forceinline__ void cp_async16(uint32_t saddr, const void* gptr, bool valid) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(saddr), "l"(gptr), "r"(valid ? 16 : 0)
                  : "memory");
+}
+// Hint: bring `bytes` (a multiple of 16, 16-byte aligned) at `g` into L2.
+__device__ __forceinline__ void prefetch_l2(const void* g, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(g), "r"(bytes) : "memory");
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
@@ -299,6 +306,23 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         for (int i = 0; i < IT; ++i)
             v[i] = (t0 + l0 + 16 * i < p.T) ? __ldg(g + i * step) : make_float4(0.f, 0.f, 0.f, 0.f);
     };
+
+    // Rows of x, B and C of the tile one wave of resident CTAs ahead are
+    // pulled into L2 now, so that the CTA that takes that ticket finds its
+    // inputs there and the DRAM reads run in the background of this tile.
+    if (p.pf_dist > 0 && tid < 3 * CH) {
+        const int pt = ticket + p.pf_dist;
+        if (pt < p.BH * p.nc) {
+            const int pc = pt / p.BH, pbh = pt - pc * p.BH;
+            const int tok = pc * CH + (tid & (CH - 1));
+            if (tok < p.T) {
+                const size_t prow = ((size_t)(pbh / p.H) * p.T + tok) * p.H + pbh % p.H;
+                const int which = tid / CH;  // 0: x, 1: B, 2: C
+                if (which == 0) prefetch_l2(p.x + prow * (PD / 2), PD * 8);
+                else prefetch_l2((which == 1 ? p.B : p.C) + prow * (N / 2), N * 8);
+            }
+        }
+    }
 
     // ---- 0. inputs in flight at once: dt first (the rotations depend on
     // it), raw X rows (and, for one half, raw B rows) by cp.async into S2 / S3,
@@ -498,6 +522,13 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                     atomicOr(p.err, 1);
                     s_bad = 1;
                 }
+            } else if (p.h0) {
+                // H_0 is the given initial state: the rotated frame coincides
+                // with the original one before the first token (Theta = 0).
+                const float* src =
+                    reinterpret_cast<const float*>(p.h0 + ((size_t)bh * N + hf * NS + lrow) * PD + c0col) + part;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) hv[j] = __ldg(src + 2 * j);
             } else {
 #pragma unroll
                 for (int j = 0; j < CPT; ++j) hv[j] = 0.f;
@@ -662,17 +693,34 @@ static cudaError_t launch_prep(const TcParams& p, cudaStream_t st) {
     return cudaGetLastError();
 }
 
+// Prefetch distance in tickets: half the CTAs that fit on the device at once
+// (measured against 0, 1/2, 1 and 2 waves: half a wave shortened the long
+// sequence forward by ~4 %, the others gained nothing).
+
+// `prefetch`: whether CTAs prefetch the inputs of the tile one wave ahead.
 template <int NH>
-static cudaError_t launch_fused(const TcParams& p, int64_t tiles, cudaStream_t st) {
+static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefetch, cudaStream_t st) {
     int dev = 0;
     cudaGetDevice(&dev);
     static bool attr_set[128] = {};
-    if (dev < 0 || dev >= 128 || !attr_set[dev]) {
-        const cudaError_t e =
+    static int resident[128] = {};  // CTAs of this kernel resident on the whole device
+    const bool cached = dev >= 0 && dev < 128;
+    if (!cached || !attr_set[dev]) {
+        cudaError_t e =
             cudaFuncSetAttribute(fused_chunk_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        if (dev >= 0 && dev < 128) attr_set[dev] = true;
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel<NH>, NT, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        if (cached) {
+            resident[dev] = per_sm * sms;
+            attr_set[dev] = true;
+        }
     }
+    TcParams p = p_in;
+    p.pf_dist = (prefetch && cached) ? resident[dev] / 2 : 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
     fused_chunk_kernel<NH><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
@@ -700,16 +748,18 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.D = a.D;
     p.y = a.y;
     p.h_final = a.h_final;
+    p.h0 = a.h0;
     p.T = (int)a.T;
     p.H = (int)a.H;
     p.BH = (int)BH;
     p.nc = (int)nc;
     p.NH = (int)NH;
     p.first_ticket = 0;
+    p.pf_dist = 0;
     p.wait_cycles = kWaitCycles;
     cudaError_t e = launch_prep(p, st);
     if (e != cudaSuccess) return e;
-    return NH == 1 ? launch_fused<1>(p, BH * nc, st) : launch_fused<2>(p, BH * nc, st);
+    return NH == 1 ? launch_fused<1>(p, BH * nc, true, st) : launch_fused<2>(p, BH * nc, true, st);
 }
 
 // Failure-detection self-test: a two-sequence, two-chunk forward whose
@@ -768,15 +818,17 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.D = a.D;
     p.y = a.y;
     p.h_final = a.h_final;
+    p.h0 = nullptr;
     p.T = T;
     p.H = H;
     p.BH = (int)BH;
     p.nc = (int)nc;
     p.NH = 1;
     p.first_ticket = (int)BH;  // chunk 0 of every sequence is never taken
+    p.pf_dist = 0;
     p.wait_cycles = wait_cycles;
     if (e == cudaSuccess) e = launch_prep(p, st);
-    if (e == cudaSuccess) e = launch_fused<1>(p, BH * nc, st);
+    if (e == cudaSuccess) e = launch_fused<1>(p, BH * nc, false, st);
     int bits = -1;
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
     cudaFreeAsync(buf, st);

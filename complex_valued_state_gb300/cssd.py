@@ -31,7 +31,8 @@ STATUS = {
 }
 
 # Every symbol include/cssd.h declares.
-EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward",
+EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward", "cssd_chunked_forward_h0",
+           "cssd_host_forward_device_bytes", "cssd_chunked_forward_host",
            "cssd_backward_workspace_bytes", "cssd_chunked_backward",
            "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_cayley_scan", "cssd_born_attention",
            "cssd_profile_events",
@@ -70,6 +71,13 @@ def load(path: str = LIB_PATH):
             lib.cssd_forward_launches.restype = ctypes.c_int
             lib.cssd_chunked_forward.argtypes = [dims_p] + [vp] * 8 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
             lib.cssd_chunked_forward.restype = ctypes.c_int
+            lib.cssd_chunked_forward_h0.argtypes = [dims_p] + [vp] * 9 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
+            lib.cssd_chunked_forward_h0.restype = ctypes.c_int
+            lib.cssd_host_forward_device_bytes.argtypes = [dims_p, ctypes.c_int, ctypes.c_int64]
+            lib.cssd_host_forward_device_bytes.restype = ctypes.c_size_t
+            lib.cssd_chunked_forward_host.argtypes = [dims_p] + [vp] * 9 + [ctypes.c_int, ctypes.c_int64, vp,
+                                                                           ctypes.c_size_t, vp]
+            lib.cssd_chunked_forward_host.restype = ctypes.c_int
             lib.cssd_chunked_forward_noalloc.argtypes = [dims_p] + [vp] * 8 + [ctypes.c_int, vp]
             lib.cssd_chunked_forward_noalloc.restype = ctypes.c_int
             lib.cssd_step.argtypes = [dims_p] + [vp] * 8 + [vp]
@@ -164,11 +172,13 @@ def forward_launches(batch: int, seqlen: int, nheads: int, dstate: int, headdim:
 
 
 def chunked_forward(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None, want_state: bool = True,
-                    workspace=None, stream=None):
-    """cssd_chunked_forward on device tensors; returns (y, h_final or None).
+                    workspace=None, stream=None, h0=None):
+    """cssd_chunked_forward (cssd_chunked_forward_h0 when `h0` is given) on
+    device tensors; returns (y, h_final or None).
 
     x complex64 [Bz,T,H,P]; dt float32 [Bz,T,H]; A complex64 [H];
-    B, C complex64 [Bz,T,H,N]; D float32 [H].  `workspace` is an optional
+    B, C complex64 [Bz,T,H,N]; D float32 [H]; h0 complex64 [Bz,H,N,P], the
+    state before the first token (zero when None).  `workspace` is an optional
     uint8 device tensor of at least workspace_bytes(...) bytes.
     """
     lib = load()
@@ -195,11 +205,79 @@ def chunked_forward(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None,
             raise ValueError("workspace must be a contiguous tensor on the inputs' device")
         ws_bytes = workspace.numel() * workspace.element_size()
     d = Dims(Bz, T, H, N, P)
-    st = lib.cssd_chunked_forward(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(y),
-                                  _ptr(h_final), int(chunk), _ptr(workspace), ctypes.c_size_t(ws_bytes),
-                                  _stream_handle(stream, dev))
+    if h0 is None:
+        st = lib.cssd_chunked_forward(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                      _ptr(y), _ptr(h_final), int(chunk), _ptr(workspace),
+                                      ctypes.c_size_t(ws_bytes), _stream_handle(stream, dev))
+        if st != CSSD_OK:
+            raise CssdError(st, "cssd_chunked_forward")
+        return y, h_final
+    _check(h0, "h0", c64, (Bz, H, N, P), dev)
+    st = lib.cssd_chunked_forward_h0(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                     _ptr(h0), _ptr(y), _ptr(h_final), int(chunk), _ptr(workspace),
+                                     ctypes.c_size_t(ws_bytes), _stream_handle(stream, dev))
     if st != CSSD_OK:
-        raise CssdError(st, "cssd_chunked_forward")
+        raise CssdError(st, "cssd_chunked_forward_h0")
+    return y, h_final
+
+
+def host_forward_device_bytes(batch: int, seqlen: int, nheads: int, dstate: int, headdim: int, chunk: int,
+                              piece_len: int = 0) -> int:
+    d = Dims(batch, seqlen, nheads, dstate, headdim)
+    return int(load().cssd_host_forward_device_bytes(ctypes.byref(d), int(chunk), int(piece_len)))
+
+
+def chunked_forward_host(x, dt, A, B, C, D, *, chunk: int = 64, piece_len: int = 0, y=None, h_final=None, h0=None,
+                         want_state: bool = True, device_buffer=None, device=None, stream=None):
+    """cssd_chunked_forward_host: the forward over host tensors (pin them for
+    copies that overlap the compute), streamed through `device` (default: the
+    current CUDA device) in pieces of `piece_len` tokens (0: library's choice).
+
+    Shapes as chunked_forward.  y and h_final are host tensors (pinned when
+    created here) unless passed in; h_final may also be a device tensor, h0
+    a host or device tensor.  Returns (y, h_final); they are complete once
+    `stream` (default: the device's current stream) has run past the call.
+    """
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    Bz, T, H, P = x.shape
+    N = B.shape[-1]
+    c64, f32 = torch.complex64, torch.float32
+
+    def chk(t, name, dtype, shape):
+        if not isinstance(t, torch.Tensor):
+            raise TypeError(f"{name} must be a torch.Tensor")
+        if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+            raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)}")
+        if t.device.type == "cuda" and t.device != dev:
+            raise ValueError(f"{name} must be on the host or on {dev}")
+
+    chk(x, "x", c64, (Bz, T, H, P))
+    chk(dt, "dt", f32, (Bz, T, H))
+    chk(A, "A", c64, (H,))
+    chk(B, "B", c64, (Bz, T, H, N))
+    chk(C, "C", c64, (Bz, T, H, N))
+    chk(D, "D", f32, (H,))
+    if y is None:
+        y = torch.empty((Bz, T, H, P), dtype=c64, pin_memory=True)
+    chk(y, "y", c64, (Bz, T, H, P))
+    if h_final is None and want_state:
+        h_final = torch.empty((Bz, H, N, P), dtype=c64, pin_memory=True)
+    if h_final is not None:
+        chk(h_final, "h_final", c64, (Bz, H, N, P))
+    if h0 is not None:
+        chk(h0, "h0", c64, (Bz, H, N, P))
+    nbytes = 0
+    if device_buffer is not None:
+        if device_buffer.device != dev or not device_buffer.is_contiguous():
+            raise ValueError("device_buffer must be a contiguous tensor on the device")
+        nbytes = device_buffer.numel() * device_buffer.element_size()
+    d = Dims(Bz, T, H, N, P)
+    st = lib.cssd_chunked_forward_host(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+                                       _ptr(h0), _ptr(y), _ptr(h_final), int(chunk), int(piece_len),
+                                       _ptr(device_buffer), ctypes.c_size_t(nbytes), _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_chunked_forward_host")
     return y, h_final
 
 

@@ -190,6 +190,12 @@ def random_case(seed: int, Bz: int, T: int, H: int, N: int, P: int, *, dt_mean: 
     return dict(x=x, dt=dt, A=A, B=B, C=C, D=D)
 
 
+def random_state(seed: int, Bz: int, H: int, N: int, P: int) -> np.ndarray:
+    """An initial state h0 [Bz,H,N,P] complex64: complex Gaussian, as the decode
+    workload's state."""
+    return _cgauss(np.random.default_rng(seed), (Bz, H, N, P))
+
+
 def make_cayley_inputs(w: Workload = HMAMBA_SCAN, seed: int | None = None, *, gate_mean: float = 0.0) -> dict:
     """Inputs of the per-coordinate Cayley-phase scan (workload `w`'s shapes).
 

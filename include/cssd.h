@@ -21,7 +21,8 @@
  *   - Complex numbers are complex64: interleaved [re, im] float32 pairs.
  *   - Arrays are dense and row-major with the shapes given per argument.
  *   - Every array pointer is a DEVICE pointer on the device that `stream`
- *     belongs to (the current device when stream is NULL).  The caller owns
+ *     belongs to (the current device when stream is NULL), except in
+ *     cssd_chunked_forward_host, which takes host memory.  The caller owns
  *     all memory; apart from the measurement hook cssd_profile_events the
  *     library keeps no state between calls.
  *   - Execution is asynchronous on `stream`.  Argument errors are detected on
@@ -120,6 +121,56 @@ int cssd_forward_launches(const cssd_dims* dims, int chunk);
 int cssd_chunked_forward_noalloc(const cssd_dims* dims, const void* x, const float* dt, const void* A,
                                  const void* B, const void* C, const float* D, void* y, void* h_final,
                                  int chunk, cssd_stream_t stream);
+
+/* cssd_chunked_forward started from a given state instead of zero: h_{-1} =
+ * h0 in the recurrence above.  "The Chunkwise Complex SSD Algorithm" gives its
+ * inter-chunk scan an initial-states input, which the chunked form takes as the
+ * state entering the first chunk; the result equals the sequential recurrence
+ * started from h0.  Continuing a sequence in pieces is exact: the forward over
+ * tokens [0, T) equals the forward over [0, T1) followed by this call over
+ * [T1, T) with h0 = the first call's h_final.
+ *   h0  complex64 [batch, nheads, dstate, headdim], device, 16-byte aligned;
+ *       NULL means zero (the call is then cssd_chunked_forward).  h0 and
+ *       h_final may be the same buffer (continuation in place: every state
+ *       element is read before it is overwritten) but must not otherwise
+ *       overlap.
+ * Every other argument, the workspace size and the status are those of
+ * cssd_chunked_forward. */
+int cssd_chunked_forward_h0(const cssd_dims* dims, const void* x, const float* dt, const void* A,
+                            const void* B, const void* C, const float* D, const void* h0, void* y,
+                            void* h_final, int chunk, void* workspace, size_t workspace_bytes,
+                            cssd_stream_t stream);
+
+/* Forward over tensors that live in HOST memory, streamed through the device
+ * in pieces of `piece_len` tokens: while one piece computes, the next one's
+ * inputs are copied in and the previous one's output copied out, and each
+ * piece continues from the state the previous piece left on the device (the
+ * initial-state identity of cssd_chunked_forward_h0), so the result equals one
+ * cssd_chunked_forward over the whole sequence up to rounding.  The pages have
+ * no counterpart: it serves callers whose sequences are produced and consumed
+ * on the host.
+ *   x, dt, A, B, C, D, y, h0, h_final: shapes and meaning as in
+ *       cssd_chunked_forward_h0, but any memory cudaMemcpyAsync can address:
+ *       page-locked host memory (cudaHostAlloc / cudaHostRegister) for copies
+ *       that overlap the compute, pageable host memory (correct, but the
+ *       driver stages those copies), or device memory.  h0 and h_final may be
+ *       NULL.  Inputs must stay unchanged, and outputs are not complete, until
+ *       `stream` has run past this call.
+ *   piece_len  tokens per piece (>= 1); 0 lets the library choose (~48 MB of
+ *       inputs per piece, a multiple of chunk).
+ *   device_buffer, device_bytes: device scratch of at least
+ *       cssd_host_forward_device_bytes(dims, chunk, piece_len) bytes on the
+ *       stream's device, 256-byte aligned; NULL makes the library allocate and
+ *       free it stream-ordered on `stream`.
+ * The copies run on two library-owned streams of the device that are ordered
+ * after the work already on `stream`, and `stream` waits for all of them
+ * before its next work, so the call behaves as one operation on `stream`.
+ * Host pointers are not checked for page-locking.  Returns a cssd_status. */
+size_t cssd_host_forward_device_bytes(const cssd_dims* dims, int chunk, int64_t piece_len);
+int cssd_chunked_forward_host(const cssd_dims* dims, const void* x, const float* dt, const void* A,
+                              const void* B, const void* C, const float* D, const void* h0, void* y,
+                              void* h_final, int chunk, int64_t piece_len, void* device_buffer,
+                              size_t device_bytes, cssd_stream_t stream);
 
 /* One decode token for every (batch, head): the same recurrence, one step.
  *   h   complex64 [batch, nheads, dstate, headdim]  state, read then updated in place

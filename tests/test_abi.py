@@ -160,6 +160,46 @@ def test_born_attention_argument_errors(lib):
     assert f(ctypes.byref(ok), *q, None) == -4
 
 
+def test_initial_state_and_host_forward_argument_errors(lib):
+    ok = cssd.Dims(1, 64, 1, 16, 16)
+    p = [ctypes.c_void_p(0x10000 + 0x100 * i) for i in range(9)]  # x dt A B C D h0 y h_final
+    f = lib.cssd_chunked_forward_h0
+    assert f(None, *p, 64, None, 0, None) == -1
+    assert f(ctypes.byref(cssd.Dims(1, 64, 1, 24, 16)), *p, 64, None, 0, None) == -3
+    q = list(p)
+    q[6] = ctypes.c_void_p(0x10608)  # h0 is complex64 state: 16-byte alignment
+    assert f(ctypes.byref(ok), *q, 64, None, 0, None) == -4
+    q = list(p)
+    q[7] = None  # y
+    assert f(ctypes.byref(ok), *q, 64, None, 0, None) == -1
+    assert f(ctypes.byref(ok), *p, 64, ctypes.c_void_p(0x900000), 16, None) == -5
+
+    g = lib.cssd_chunked_forward_host
+    assert g(None, *p, 64, 0, None, 0, None) == -1
+    assert g(ctypes.byref(cssd.Dims(1, 0, 1, 16, 16)), *p, 64, 0, None, 0, None) == -2
+    assert g(ctypes.byref(ok), *p, 64, -1, None, 0, None) == -2  # piece length
+    assert g(ctypes.byref(ok), *p, 96, 0, None, 0, None) == -3  # chunk
+    assert g(ctypes.byref(cssd.Dims(1, 64, 1, 16, 8)), *p, 64, 0, None, 0, None) == -3
+    q = list(p)
+    q[0] = None
+    assert g(ctypes.byref(ok), *q, 64, 0, None, 0, None) == -1
+    assert g(ctypes.byref(ok), *p, 64, 0, ctypes.c_void_p(0x900010), 1 << 30, None) == -4  # buffer alignment
+    assert g(ctypes.byref(ok), *p, 64, 0, ctypes.c_void_p(0x900000), 16, None) == -5  # buffer size
+
+    # device bytes: two slots of one piece's x, dt, B, C, y plus two states and the piece's workspace
+    m = cssd.Dims(4, 2048, 24, 64, 64)
+    in_per_token = 4 * 24 * (8 * 64 + 4 + 16 * 64)  # x, dt, B, C
+    piece = (48 << 20) // in_per_token // 64 * 64  # default: ~48 MB of inputs, whole chunks (320 tokens)
+    auto = lib.cssd_host_forward_device_bytes(ctypes.byref(m), 64, 0)
+    assert auto >= 2 * piece * (in_per_token + 4 * 24 * 8 * 64) + 2 * 4 * 24 * 64 * 64 * 8
+    assert lib.cssd_host_forward_device_bytes(ctypes.byref(m), 64, piece) == auto
+    assert lib.cssd_host_forward_device_bytes(ctypes.byref(m), 64, 128) < auto
+    assert lib.cssd_host_forward_device_bytes(ctypes.byref(m), 64, 1 << 20) == \
+        lib.cssd_host_forward_device_bytes(ctypes.byref(m), 64, 2048)  # a piece never exceeds the sequence
+    assert lib.cssd_host_forward_device_bytes(ctypes.byref(m), 64, -1) == 0
+    assert lib.cssd_host_forward_device_bytes(ctypes.byref(m), 96, 0) == 0
+
+
 def test_selftest_argument_errors(lib):
     bits = ctypes.c_int(0)
     assert lib.cssd_selftest_handoff_timeout(1000, None, None) == -1
