@@ -48,6 +48,7 @@ def parse():
     ap.add_argument("--no-cayley", action="store_true", help="skip the per-coordinate Cayley scan measurement")
     ap.add_argument("--no-born", action="store_true", help="skip the causal Born attention measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the gradient (backward) measurement")
+    ap.add_argument("--no-precise", action="store_true", help="skip the split-precision forward measurement")
     return ap.parse_args()
 
 
@@ -146,11 +147,13 @@ class ClockSampler:
 # ---------------------------------------------------------------- traffic record
 # Sources that define each kernel with recorded DRAM traffic: the counters in
 # profiles/dram_traffic.json hold only while these files are unchanged.
+# Files that hold each kernel's device code (its .cu and the device headers it
+# includes; cssd_internal.h only declares host launchers).
 KERNEL_SOURCES = {
-    "fused_chunk_kernel": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh", "cssd_internal.h"),
-    "step_kernel": ("step.cu", "cssd_common.cuh", "cssd_internal.h"),
-    "cayley_scan_kernel": ("cayley.cu", "cssd_common.cuh", "cssd_internal.h"),
-    "born_kernel": ("born.cu", "tcgen05.cuh", "cssd_common.cuh", "cssd_internal.h"),
+    "fused_chunk_kernel": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
+    "step_kernel": ("step.cu", "cssd_common.cuh"),
+    "cayley_scan_kernel": ("cayley.cu", "cssd_common.cuh"),
+    "born_kernel": ("born.cu", "tcgen05.cuh", "cssd_common.cuh"),
 }
 
 
@@ -291,6 +294,7 @@ def run_ours(args, rank, world, local):
         born = bench_born(args, dev)
     if not args.no_backward:
         backward = bench_backward(args, dev)
+    precise = None if args.no_precise else bench_precise(args, dev)
     long_seq = None
     if not args.no_long:
         long_seq = bench_long_seq(args, dev)
@@ -333,6 +337,8 @@ def run_ours(args, rank, world, local):
         out["born_attention"] = born
     if backward:
         out["backward"] = backward
+    if precise:
+        out["precise_forward"] = precise
     if long_seq:
         out["long_seq"] = long_seq
     if world == 1 and not args.no_cpu_baseline:
@@ -633,6 +639,64 @@ def bench_long_seq(args, dev):
             "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel", "achieved": round(gbs, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind, "kernel_ms": round(k_ms, 4),
                          "alg_bytes_per_launch": alg}}
+
+
+def bench_precise(args, dev):
+    """Split-precision forward (cssd_chunked_forward_precise) on the mamba2_layer workload."""
+    import torch
+
+    from complex_valued_state_gb300 import cssd
+    from complex_valued_state_gb300 import workloads as wl
+
+    w = wl.MAMBA2_LAYER
+    host = wl.make_inputs(w)
+    g = {k: torch.from_numpy(host[k]).to(dev) for k in ("x", "dt", "A", "B", "C", "D")}
+    del host
+    Bz, T, H, N, P, ch = w.batch, w.seqlen, w.nheads, w.dstate, w.headdim, w.chunk
+    y = torch.empty((Bz, T, H, P), dtype=torch.complex64, device=dev)
+    h = torch.empty((Bz, H, N, P), dtype=torch.complex64, device=dev)
+    ws = torch.empty(cssd.workspace_bytes(Bz, T, H, N, P, ch), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def fwd():
+        cssd.chunked_forward(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk=ch, y=y, h_final=h, workspace=ws,
+                             precise=True)
+
+    for _ in range(3):
+        fwd()
+    torch.cuda.synchronize(dev)
+    n = 20
+    kb = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    ke = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in kb + ke:
+        e.record(stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    e0.record(stream)
+    for i in range(n):
+        cssd.profile_events(kb[i], ke[i])
+        fwd()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    cssd.profile_events(None, None)
+    ms = e0.elapsed_time(e1) / n
+    k_ms = sum(kb[i].elapsed_time(ke[i]) for i in range(n)) / n
+    units = Bz * T * H
+    alg = units * (8 * P + 16 * N + 4 + 8 * P)
+    hbm, kind = peaks()
+    gbs = alg / (k_ms / 1e3) / 1e9
+    # executed tensor work: four complex 64x64x64 GEMMs per 64-token tile, each
+    # taken three times (hi.hi, hi.lo, lo.hi), 8 real flops per complex MAC
+    flops = 3 * units * 4 * 64 * 64 * 8
+    tf = flops / (k_ms / 1e3) / 1e12
+    tpk, tkind = tf32_peak()
+    return {"workload": f"mamba2_layer Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch}, split-precision forward",
+            "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_call": round(ms, 4), "calls": n,
+            "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel (split)", "achieved": round(gbs, 1),
+                         "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
+                         "kernel_ms": round(k_ms, 4), "alg_bytes_per_launch": alg},
+            "tensor": {"executed_tflops": round(tf, 1), "peak": round(tpk, 1), "peak_kind": tkind,
+                       "frac": round(tf / tpk, 4), "flops_per_launch": flops}}
 
 
 # ---------------------------------------------------------------- CPU oracle

@@ -23,9 +23,11 @@
 // and gD = sum_{b,t,p} Re(conj(dy) x).  The total of r vanishes (R_0 = 0: the
 // first step multiplies the zero initial state), so R_t = -sum_{u < t} r_u too.
 // r_t is a small difference of two sums of P products, so y and gx, which it
-// is formed from, are computed by the fp32 CUDA-core chunk kernels (with the
-// TF32 tensor-core forward its error reached 1e-2 of the largest gdt); gB and
-// gC, read directly, take the tensor-core kernel where it applies.
+// is formed from, are computed to about fp32 accuracy (with the plain TF32
+// tensor-core forward the error reached 1e-2 of the largest gdt): by the
+// split-precision tensor-core kernel where its shape applies, else by the
+// fp32 CUDA-core chunk kernels.  gB and gC, read directly, take the plain
+// tensor-core kernel where it applies.
 // The derivation differentiates the sequential recurrence ("Complex-Valued
 // State Spaces", "The discretization"; "SSD Theory" section 2), which the
 // chunked form computes exactly up to rounding.
@@ -267,6 +269,19 @@ unsigned grid_rows(int64_t rows) { return (unsigned)(rows < 65535 * 8 ? rows : 6
 
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
+// The forward to about fp32 accuracy: the split-precision tensor-core kernel
+// (three TF32 products per product) where its shape applies, else the fp32
+// CUDA-core chunk kernels.
+size_t precise_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
+    if (tc_forward_supported(N, P, chunk)) return tc_forward_workspace_bytes(Bz, T, H, N);
+    return seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);
+}
+cudaError_t launch_precise_forward(FwdArgs f, void* ws, cudaStream_t st) {
+    if (!tc_forward_supported(f.N, f.P, f.chunk)) return launch_seq_forward(f, ws, st);
+    f.split_tf32 = true;
+    return launch_tc_forward(f, ws, st);
+}
+
 // Workspace regions of the backward, in order.
 struct BwdLayout {
     size_t y, dyR, dts, ccR, bcR, xcR, dyc, tmp, Ac, zero, r, d, gAp, gDp, fwd, total;
@@ -296,7 +311,7 @@ BwdLayout bwd_layout(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int
     L.d = take(TH * sizeof(float));
     L.gAp = take((size_t)(Bz * H) * sizeof(double2));
     L.gDp = take((size_t)(Bz * H) * sizeof(double));
-    const size_t f1 = seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);  // y and gx runs (fp32 kernels)
+    const size_t f1 = precise_forward_workspace_bytes(Bz, T, H, N, P, chunk);  // y and gx runs
     const size_t f2 = forward_workspace_bytes(Bz, T, H, P, N, chunk);      // transposed-state runs
     L.fwd = take(f1 > f2 ? f1 : f2);
     L.total = off;
@@ -324,11 +339,11 @@ cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t st) 
     cudaError_t e = cudaSuccess;
     auto check = [&]() { return (e = cudaGetLastError()) == cudaSuccess; };
 
-    // Forward output, in fp32.
+    // Forward output, to about fp32 accuracy.
     const float2* y = f2p(L.y);
     {
         FwdArgs f{Bz, T, H, N, P, a.chunk, a.x, a.dt, a.A, a.B, a.C, a.D, f2p(L.y), nullptr};
-        if ((e = launch_seq_forward(f, fws, st)) != cudaSuccess) return e;
+        if ((e = launch_precise_forward(f, fws, st)) != cudaSuccess) return e;
     }
 
     // Reversed and conjugated inputs.
@@ -344,10 +359,10 @@ cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t st) 
     if (!check()) return e;
 
     float2* tmp = f2p(L.tmp);
-    // gx: reversed run (fp32), then back to token order.
+    // gx: reversed run (about fp32 accuracy), then back to token order.
     {
         FwdArgs f{Bz, T, H, N, P, a.chunk, dyR, dts, Ac, ccR, bcR, a.D, tmp, nullptr};
-        if ((e = launch_seq_forward(f, fws, st)) != cudaSuccess) return e;
+        if ((e = launch_precise_forward(f, fws, st)) != cudaSuccess) return e;
         reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(tmp, a.gx, Bz, T, H * P, false);
         if (!check()) return e;
     }

@@ -105,10 +105,11 @@ int step_common(const cssd_dims* d, void* h, const void* x, const float* dt, con
 // cssd_chunked_forward_h0.
 int forward_common(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B, const void* C,
                    const float* D, const void* h0, void* y, void* h_final, int chunk, void* workspace,
-                   size_t workspace_bytes, cssd_stream_t stream_) {
+                   size_t workspace_bytes, cssd_stream_t stream_, bool precise = false) {
     int s = check_dims(d, true);
     if (s != CSSD_OK) return s;
     if (!supported_chunk(chunk)) return CSSD_ERR_UNSUPPORTED;
+    if (precise && !cssd::precise_forward_supported(d->dstate, d->headdim, chunk)) return CSSD_ERR_UNSUPPORTED;
     if (!x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
     if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
         (h_final && !aligned(h_final, 16)) || (h0 && !aligned(h0, 16)) || (workspace && !aligned(workspace, 16)) ||
@@ -146,6 +147,7 @@ int forward_common(const cssd_dims* d, const void* x, const float* dt, const voi
     a.y = static_cast<float2*>(y);
     a.h_final = static_cast<float2*>(h_final);
     a.h0 = static_cast<const float2*>(h0);
+    a.split_tf32 = precise;
     const cudaError_t e = cssd::launch_forward(a, ws, stream);
     if (!workspace) cudaFreeAsync(ws, stream);
     return e == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
@@ -208,6 +210,12 @@ int cssd_chunked_forward_h0(const cssd_dims* d, const void* x, const float* dt, 
                             const void* C, const float* D, const void* h0, void* y, void* h_final, int chunk,
                             void* workspace, size_t workspace_bytes, cssd_stream_t stream_) {
     return forward_common(d, x, dt, A, B, C, D, h0, y, h_final, chunk, workspace, workspace_bytes, stream_);
+}
+
+int cssd_chunked_forward_precise(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B,
+                                 const void* C, const float* D, const void* h0, void* y, void* h_final, int chunk,
+                                 void* workspace, size_t workspace_bytes, cssd_stream_t stream_) {
+    return forward_common(d, x, dt, A, B, C, D, h0, y, h_final, chunk, workspace, workspace_bytes, stream_, true);
 }
 
 int cssd_step(const cssd_dims* d, void* h, const void* x, const float* dt, const void* A, const void* B,

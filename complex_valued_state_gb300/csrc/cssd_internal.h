@@ -22,6 +22,9 @@ struct FwdArgs {
     float2* y;
     float2* h_final;             // may be null
     const float2* h0 = nullptr;  // state before the first token [Bz,H,N,P]; null = zero
+    // Tensor-core path only: split-precision operands (three TF32 products per
+    // product, about fp32 accuracy, one CTA per SM) instead of plain TF32.
+    bool split_tf32 = false;
 };
 
 struct StepArgs {
@@ -43,7 +46,8 @@ extern thread_local cudaEvent_t g_prof_begin;
 extern thread_local cudaEvent_t g_prof_end;
 
 // The chunked forward: the fused tensor-core kernel where its shape applies
-// (headdim 64, dstate 64 or 128), else the CUDA-core chunk kernels.
+// (headdim 64, dstate 64 or 128; split-precision operands when
+// FwdArgs::split_tf32), else the CUDA-core chunk kernels.
 size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
 int forward_launches(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
 cudaError_t launch_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
@@ -54,6 +58,9 @@ cudaError_t launch_seq_forward(const FwdArgs& a, void* workspace, cudaStream_t s
 
 // Fused tensor-core kernel (forward_tc.cu).
 bool tc_forward_supported(int64_t N, int64_t P, int chunk);
+// Shapes the split-precision forward serves: the tensor-core shapes with
+// dstate 64, and every shape the CUDA-core kernels take (fp32 already).
+bool precise_forward_supported(int64_t N, int64_t P, int chunk);
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N);
 cudaError_t launch_tc_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
 cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cudaStream_t stream);

@@ -32,6 +32,8 @@
 // so one M = 128 accumulator holds the real part in TMEM lanes 0-63 and the
 // imaginary part in lanes 64-127.
 
+#include <type_traits>
+
 #include "cssd_common.cuh"
 #include "cssd_internal.h"
 #include "tcgen05.cuh"
@@ -47,13 +49,22 @@ constexpr int IT = 2048 / NT;       // tile items (float4) per thread
 constexpr int CPT = 64 / (NT / 128);  // accumulator columns per thread
 constexpr int RING = 2;   // state slots per sequence
 
-// Shared memory regions (bytes).
+// Shared memory regions (bytes).  With split precision every operand is held
+// twice, its TF32 value (hi) and the TF32 value of the remainder (lo), the lo
+// copy right after the hi one.
 constexpr int STACK_BYTES = 3 * 64 * 64 * 4;  // [-Ai; Ar; Ai], 192 rows x 64 K
 constexpr int PLANE_BYTES = 64 * 64 * 4;      // one 64 x 64 fp32 plane
-constexpr int S1 = 0;                          // F, then Ct, then M, then y staging
-constexpr int S2 = S1 + STACK_BYTES;           // X planes (Xr, Xi)
-constexpr int S3 = S2 + 2 * PLANE_BYTES;       // Bt planes, then H planes
-constexpr int SMEM_BYTES = S3 + 2 * PLANE_BYTES;  // 112 KB
+template <bool SPLIT>
+struct Smem {
+    static constexpr int K = SPLIT ? 2 : 1;
+    static constexpr int S1 = 0;                           // F, then Ct, then M, then y staging
+    static constexpr int S2 = S1 + K * STACK_BYTES;        // X planes (Xr, Xi)
+    static constexpr int S3 = S2 + K * 2 * PLANE_BYTES;    // Bt planes, then H planes
+    static constexpr int BYTES = S3 + K * 2 * PLANE_BYTES;  // 112 KB, or 224 KB split
+    static constexpr uint32_t LO1 = STACK_BYTES;           // lo copy of the S1 stack
+    static constexpr uint32_t LO23 = 2 * PLANE_BYTES;      // lo copy of an S2 / S3 plane pair
+};
+static_assert(Smem<true>::BYTES + 2048 <= 227 * 1024, "split operands fit in one CTA's shared memory");
 // y staging: a real and an imaginary 64 x 64 plane with an odd row stride, so
 // that both the column-wise writes from tensor-memory lanes and the row-wise
 // reads of the output pass fall on 32 distinct banks.
@@ -87,6 +98,46 @@ __device__ __forceinline__ void st_f32(unsigned char* base, uint32_t off, float 
 }
 __device__ __forceinline__ void st_f32x2(unsigned char* base, uint32_t off, float a, float b) {
     *reinterpret_cast<float2*>(base + off) = make_float2(a, b);
+}
+
+// An fp32 operand value as the TF32 pair hi + lo (hi = v rounded to TF32, lo =
+// the remainder rounded to TF32): the three products hi.hi + hi.lo + lo.hi of
+// two such pairs carry about 21 significant bits, the fp32 product up to
+// rounding.  Without SPLIT only hi is formed.
+template <bool SPLIT>
+struct Tf {
+    float hi, lo;
+    __device__ __forceinline__ explicit Tf(float v) {
+        hi = tf32r(v);
+        lo = SPLIT ? tf32r(v - hi) : 0.f;
+    }
+};
+// e^x for the decay factors: the fast exponential for plain TF32 (its error is
+// far below TF32 rounding), CUDA's accurate expf with split precision (the fast
+// one scales its argument in fp32 and loses ~1e-6 relative at |x| ~ 40).
+template <bool SPLIT>
+__device__ __forceinline__ float kexp(float x) {
+    return SPLIT ? expf(x) : __expf(x);
+}
+
+// Store one operand value (hi at `off`, lo `lo_delta` bytes further).
+template <bool SPLIT>
+__device__ __forceinline__ void st_op(unsigned char* base, uint32_t off, uint32_t lo_delta, float v) {
+    const Tf<SPLIT> t(v);
+    st_f32(base, off, t.hi);
+    if (SPLIT) st_f32(base, off + lo_delta, t.lo);
+}
+template <bool SPLIT>
+__device__ __forceinline__ void st_op2(unsigned char* base, uint32_t off, uint32_t lo_delta, float a, float b) {
+    const Tf<SPLIT> ta(a), tb(b);
+    st_f32x2(base, off, ta.hi, tb.hi);
+    if (SPLIT) st_f32x2(base, off + lo_delta, ta.lo, tb.lo);
+}
+template <bool SPLIT>
+__device__ __forceinline__ void st_op4(unsigned char* base, uint32_t off, uint32_t lo_delta, float4 v) {
+    const Tf<SPLIT> a(v.x), b(v.y), c(v.z), d(v.w);
+    *reinterpret_cast<float4*>(base + off) = make_float4(a.hi, b.hi, c.hi, d.hi);
+    if (SPLIT) *reinterpret_cast<float4*>(base + off + lo_delta) = make_float4(a.lo, b.lo, c.lo, d.lo);
 }
 
 struct TcParams {
@@ -155,8 +206,15 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CPT])
 // chunk_prep_kernel: one warp per (sequence, 64-token chunk).  Inclusive
 // cumsum of softplus(dt) over the chunk's tokens (padded tokens add nothing),
 // stored per token as rho_l = alpha cs_l and theta_l = beta cs_l, and the
-// chunk's phase total beta cs_63.  The same CTAs clear the hand-off words.
+// chunk's phase total (the same value as its last token's theta).  With
+// PRECISE (the split-precision forward) the cumsum runs in double and theta is
+// reduced to [-pi, pi], so that the angle Phi_c + theta_l the chunk kernel
+// rotates by stays within 2 pi and carries ~2e-7 of rounding instead of the
+// ~1e-5 a float cumsum to |theta| ~ 60 leaves; plain TF32 rounding is far
+// coarser than either.  The same CTAs clear the hand-off words.
+template <bool PRECISE>
 __global__ void __launch_bounds__(256) chunk_prep_kernel(TcParams p) {
+    using Real = typename std::conditional<PRECISE, double, float>::type;
     const int lane = threadIdx.x & 31;
     const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);  // global warp = bh * nc + c
     {
@@ -170,29 +228,34 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(TcParams p) {
     if (gw >= p.BH * p.nc) return;
     const int bh = gw / p.nc, c = gw - bh * p.nc;
     const int b = bh / p.H, h = bh % p.H;
-    const float alpha = p.A[h].x, beta = p.A[h].y;
+    const Real alpha = p.A[h].x, beta = p.A[h].y;
     const float* dtb = p.dt + (size_t)b * p.T * p.H + h;  // token t at dtb[t * H]
-    float v[2];
+    Real v[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         const int t = c * CH + hh * 32 + lane;
-        v[hh] = (t < p.T) ? __ldg(dtb + (size_t)t * p.H) : 0.f;
-    }
-#pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-        const int t = c * CH + hh * 32 + lane;
-        v[hh] = (t < p.T) ? softplusf(v[hh]) : 0.f;
+        v[hh] = (t < p.T) ? (Real)softplusf(__ldg(dtb + (size_t)t * p.H)) : (Real)0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const float u = __shfl_up_sync(0xffffffffu, v[hh], o);
+            const Real u = __shfl_up_sync(0xffffffffu, v[hh], o);
             if (lane >= o) v[hh] += u;
         }
     }
     v[1] += __shfl_sync(0xffffffffu, v[0], 31);
     float2* out = p.tok + (size_t)gw * CH;
-    out[lane] = make_float2(v[0] * alpha, v[0] * beta);
-    out[32 + lane] = make_float2(v[1] * alpha, v[1] * beta);
-    if (lane == 31) p.phi[gw] = v[1] * beta;  // phase total, turned into Phi_c below
+    float th[2];
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+        const Real a = beta * v[hh];
+        if (PRECISE) {
+            const double two_pi = 6.283185307179586476925286766559;
+            th[hh] = (float)fma(-rint((double)a * (1.0 / two_pi)), two_pi, (double)a);  // in [-pi, pi]
+        } else {
+            th[hh] = (float)a;
+        }
+        out[hh * 32 + lane] = make_float2((float)(alpha * v[hh]), th[hh]);
+    }
+    if (lane == 31) p.phi[gw] = th[1];  // phase total, turned into Phi_c below
 }
 
 // phase_scan_kernel: one warp per sequence.  Phi_c = sum of the phase totals of
@@ -234,9 +297,11 @@ __global__ void __launch_bounds__(256) phase_scan_kernel(TcParams p) {
 // NH halves of 64 (dstate = 64 NH): the state GEMM, the hand-off and the
 // carried-in readout run once per half, the score GEMM accumulates over the
 // halves, and the masked scores and Y_diag run once.
-template <int NH>
-__global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
+template <int NH, bool SPLIT>
+__global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams p) {
+    using SM = Smem<SPLIT>;
     constexpr int N = NS * NH;  // dstate
+    constexpr uint32_t LO1 = SM::LO1, LO23 = SM::LO23;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ float s_rho[CH];
     __shared__ float2 s_rot[CH];  // (cos, sin) of Theta_l; first used as scan scratch
@@ -247,9 +312,9 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     __shared__ int s_bad;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned char* sm1 = smem + S1;
-    unsigned char* sm2 = smem + S2;
-    unsigned char* sm3 = smem + S3;
+    unsigned char* sm1 = smem + SM::S1;
+    unsigned char* sm2 = smem + SM::S2;
+    unsigned char* sm3 = smem + SM::S3;
 
     if (warp == 0) {
         tc::tmem_alloc(&s_tmem, TMEM_COLS);
@@ -274,7 +339,6 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     }
     const int c = ticket / p.BH, bh = ticket - c * p.BH;
     const int b = bh / p.H, h = bh - b * p.H;
-    const float2 Ah = p.A[h];
     const int t0 = c * CH;
     const size_t row0 = ((size_t)b * p.T + t0) * p.H + h;  // token row of l = 0
     const size_t rstride = (size_t)p.H;                    // rows between tokens
@@ -363,23 +427,31 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     cp_async_wait_all();
     __syncthreads();
     const float rho_end = s_rho[CH - 1];
-    const float eend = __expf(rho_end);
+    const float eend = kexp<SPLIT>(rho_end);
 
     const uint32_t ID = tc::idesc_tf32(128, 64);
     // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`.
     // Descriptors are built once; stepping K by 8 advances the start-address
     // field (bytes / 16) by 2 * LBO / 16.
-    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs, bool accumulate) {
-        const uint64_t a_hi = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
-        const uint64_t a_lo = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
-        const uint64_t b_re = tc::make_desc(bs, PLANE_LBO, SBO);
-        const uint64_t b_im = tc::make_desc(bs + PLANE_BYTES, PLANE_LBO, SBO);
-        constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4, B_STEP = (2 * PLANE_LBO) >> 4;
+    // With SPLIT the product is taken three times: hi x hi, hi x lo, lo x hi
+    // (the operands' lo copies sit LO1 / LO23 bytes after the hi ones).
+    auto cgemm = [&](uint32_t d, uint32_t as0, uint32_t bs0, bool accumulate) {
+        constexpr int PASSES = SPLIT ? 3 : 1;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks)
-            tc::mma_tf32(d, a_hi + ks * A_STEP, b_re + ks * B_STEP, ID, (accumulate || ks > 0) ? 1u : 0u);
+        for (int pass = 0; pass < PASSES; ++pass) {
+            const uint32_t as = as0 + (pass == 2 ? LO1 : 0u), bs = bs0 + (pass == 1 ? LO23 : 0u);
+            const uint64_t a_up = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
+            const uint64_t a_dn = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
+            const uint64_t b_re = tc::make_desc(bs, PLANE_LBO, SBO);
+            const uint64_t b_im = tc::make_desc(bs + PLANE_BYTES, PLANE_LBO, SBO);
+            constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4, B_STEP = (2 * PLANE_LBO) >> 4;
 #pragma unroll
-        for (int ks = 0; ks < 8; ++ks) tc::mma_tf32(d, a_lo + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
+            for (int ks = 0; ks < 8; ++ks)
+                tc::mma_tf32(d, a_up + ks * A_STEP, b_re + ks * B_STEP, ID,
+                             (accumulate || pass > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 8; ++ks) tc::mma_tf32(d, a_dn + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
+        }
     };
     auto issue = [&](uint32_t d, uint32_t as, uint32_t bs, bool accumulate, uint64_t* bar) {
         tc::fence_proxy_async();
@@ -413,11 +485,11 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
             const uint32_t o = o_kl64 + 4096 * i;  // rows p = n0, n0 + 1; K = l
-            const float r0 = tf32r(xv[i].x), r1 = tf32r(xv[i].z), m0 = tf32r(xv[i].y), m1 = tf32r(xv[i].w);
-            st_f32(sm2, o + sx, swap_rows ? r1 : r0);
-            st_f32(sm2, o + (sx ^ 16), swap_rows ? r0 : r1);
-            st_f32(sm2 + PLANE_BYTES, o + sx, swap_rows ? m1 : m0);
-            st_f32(sm2 + PLANE_BYTES, o + (sx ^ 16), swap_rows ? m0 : m1);
+            const float r0 = xv[i].x, r1 = xv[i].z, m0 = xv[i].y, m1 = xv[i].w;
+            st_op<SPLIT>(sm2, o + sx, LO23, swap_rows ? r1 : r0);
+            st_op<SPLIT>(sm2, o + (sx ^ 16), LO23, swap_rows ? r0 : r1);
+            st_op<SPLIT>(sm2 + PLANE_BYTES, o + sx, LO23, swap_rows ? m1 : m0);
+            st_op<SPLIT>(sm2 + PLANE_BYTES, o + (sx ^ 16), LO23, swap_rows ? m0 : m1);
         }
     }
 
@@ -443,21 +515,20 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
                 const float b0r = cs * bv[i].x + sn * bv[i].y, b0i = cs * bv[i].y - sn * bv[i].x;
                 const float b1r = cs * bv[i].z + sn * bv[i].w, b1i = cs * bv[i].w - sn * bv[i].z;
                 const uint32_t ob = o_lk64 + 256 * i;
-                st_f32x2(sm3, ob, tf32r(b0r), tf32r(b1r));
-                st_f32x2(sm3 + PLANE_BYTES, ob, tf32r(b0i), tf32r(b1i));
+                st_op2<SPLIT>(sm3, ob, LO23, b0r, b1r);
+                st_op2<SPLIT>(sm3 + PLANE_BYTES, ob, LO23, b0i, b1i);
                 // F[n][l] = exp(rho_end - rho_l) Bt[l][n]
-                const float ds = __expf(rho_end - s_rho[l]);
-                const float f0r = tf32r(ds * b0r), f0i = tf32r(ds * b0i), f1r = tf32r(ds * b1r),
-                            f1i = tf32r(ds * b1i);
+                const float ds = kexp<SPLIT>(rho_end - s_rho[l]);
+                const float f0r = ds * b0r, f0i = ds * b0i, f1r = ds * b1r, f1i = ds * b1i;
                 const uint32_t of = o_kl192 + 12288 * i;
                 const float fAr = swap_rows ? f1r : f0r, fAi = swap_rows ? f1i : f0i;  // row written first
                 const float fBr = swap_rows ? f0r : f1r, fBi = swap_rows ? f0i : f1i;
-                st_f32(sm1, of + sx, -fAi);
-                st_f32(sm1, of + (sx ^ 16), -fBi);
-                st_f32(sm1, of + BLK + sx, fAr);
-                st_f32(sm1, of + BLK + (sx ^ 16), fBr);
-                st_f32(sm1, of + 2 * BLK + sx, fAi);
-                st_f32(sm1, of + 2 * BLK + (sx ^ 16), fBi);
+                st_op<SPLIT>(sm1, of + sx, LO1, -fAi);
+                st_op<SPLIT>(sm1, of + (sx ^ 16), LO1, -fBi);
+                st_op<SPLIT>(sm1, of + BLK + sx, LO1, fAr);
+                st_op<SPLIT>(sm1, of + BLK + (sx ^ 16), LO1, fBr);
+                st_op<SPLIT>(sm1, of + 2 * BLK + sx, LO1, fAi);
+                st_op<SPLIT>(sm1, of + 2 * BLK + (sx ^ 16), LO1, fBi);
             }
         }
         issue(tmem + COL_S, a1, a2, false, &mbar[0]);
@@ -469,12 +540,12 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         for (int i = 0; i < IT; ++i) {
             const int l = l0 + 16 * i;
             const float cs = s_rot[l].x, sn = s_rot[l].y;
-            const float c0r = tf32r(cs * cv[i].x - sn * cv[i].y), c0i = tf32r(cs * cv[i].y + sn * cv[i].x);
-            const float c1r = tf32r(cs * cv[i].z - sn * cv[i].w), c1i = tf32r(cs * cv[i].w + sn * cv[i].z);
+            const float c0r = cs * cv[i].x - sn * cv[i].y, c0i = cs * cv[i].y + sn * cv[i].x;
+            const float c1r = cs * cv[i].z - sn * cv[i].w, c1i = cs * cv[i].w + sn * cv[i].z;
             const uint32_t oc = o_lk192 + 256 * i;
-            st_f32x2(sm1, oc, -c0i, -c1i);
-            st_f32x2(sm1, oc + BLK, c0r, c1r);
-            st_f32x2(sm1, oc + 2 * BLK, c0i, c1i);
+            st_op2<SPLIT>(sm1, oc, LO1, -c0i, -c1i);
+            st_op2<SPLIT>(sm1, oc + BLK, LO1, c0r, c1r);
+            st_op2<SPLIT>(sm1, oc + 2 * BLK, LO1, c0i, c1i);
         }
         issue(tmem + COL_G, a1, a3, hf > 0, &mbar[1]);
 
@@ -568,8 +639,8 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
             unsigned char* plane = sm3 + part * PLANE_BYTES + koff(pcol, nb, 64);
 #pragma unroll
             for (int k4 = 0; k4 < CPT / 4; ++k4)  // K = nb + 4 k4: one core matrix further per step
-                *reinterpret_cast<float4*>(plane + 1024 * k4) = make_float4(
-                    tf32r(hv[4 * k4]), tf32r(hv[4 * k4 + 1]), tf32r(hv[4 * k4 + 2]), tf32r(hv[4 * k4 + 3]));
+                st_op4<SPLIT>(plane, 1024 * k4, LO23,
+                              make_float4(hv[4 * k4], hv[4 * k4 + 1], hv[4 * k4 + 2], hv[4 * k4 + 3]));
         }
         issue(tmem + COL_OFF, a1, a3, hf > 0, &mbar[2]);  // Y_off' += Ct H_c
     }
@@ -589,7 +660,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
             // causal mask as exp(-inf) = 0: a select, not a branch around exp
             const int sidx = c0col + j;
             const float arg = (sidx <= lrow) ? rl - s_rho[sidx] : -INFINITY;
-            m[j] = tf32r(__expf(arg) * __uint_as_float(r[j]));
+            m[j] = kexp<SPLIT>(arg) * __uint_as_float(r[j]);
         }
         wait_bar(&mbar[2], (NH - 1) & 1);
         // 16-byte stores: four consecutive K of one row fill one core-matrix
@@ -599,10 +670,10 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         for (int k4 = 0; k4 < CPT / 4; ++k4) {
             const float4 v = make_float4(m[4 * k4], m[4 * k4 + 1], m[4 * k4 + 2], m[4 * k4 + 3]);
             if (part == 0) {
-                *reinterpret_cast<float4*>(mrow + BLK + 3072 * k4) = v;
+                st_op4<SPLIT>(mrow, BLK + 3072 * k4, LO1, v);
             } else {
-                *reinterpret_cast<float4*>(mrow + 2 * BLK + 3072 * k4) = v;
-                *reinterpret_cast<float4*>(mrow + 3072 * k4) = make_float4(-v.x, -v.y, -v.z, -v.w);
+                st_op4<SPLIT>(mrow, 2 * BLK + 3072 * k4, LO1, v);
+                st_op4<SPLIT>(mrow, 3072 * k4, LO1, make_float4(-v.x, -v.y, -v.z, -v.w));
             }
         }
     }
@@ -627,7 +698,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
         tmem_ld_cols(tmem + lane_base + COL_Y + c0col, ry);
         tmem_ld_cols(tmem + lane_base + COL_OFF + c0col, ro);
         tc::tmem_wait_ld();
-        const float el = __expf(s_rho[lrow]);
+        const float el = kexp<SPLIT>(s_rho[lrow]);
         float* stage = reinterpret_cast<float*>(sm1) + part * CH * STAGE_LD + lrow * STAGE_LD + c0col;
 #pragma unroll
         for (int j = 0; j < CPT; ++j) stage[j] = fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
@@ -675,6 +746,8 @@ bool tc_forward_supported(int64_t N, int64_t P, int chunk) {
     return P == PD && (N == NS || N == 2 * NS) && (chunk == CH || chunk == 2 * CH);
 }
 
+bool precise_forward_supported(int64_t N, int64_t P, int chunk) { return !(tc_forward_supported(N, P, chunk) && N != NS); }
+
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N) {
     const int64_t BH = Bz * H, nc = (T + CH - 1) / CH, NH = N / NS;
     size_t off = (size_t)BH * NH * RING * 2 * PD * NS * sizeof(unsigned long long);  // hand-off cells
@@ -684,9 +757,12 @@ size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N) {
     return off;
 }
 
-static cudaError_t launch_prep(const TcParams& p, cudaStream_t st) {
+static cudaError_t launch_prep(const TcParams& p, bool precise, cudaStream_t st) {
     const int64_t warps = (int64_t)p.BH * p.nc;
-    chunk_prep_kernel<<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(p);
+    if (precise)
+        chunk_prep_kernel<true><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(p);
+    else
+        chunk_prep_kernel<false><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     phase_scan_kernel<<<(unsigned)((p.BH + 7) / 8), 256, 0, st>>>(p);
@@ -698,8 +774,9 @@ static cudaError_t launch_prep(const TcParams& p, cudaStream_t st) {
 // sequence forward by ~4 %, the others gained nothing).
 
 // `prefetch`: whether CTAs prefetch the inputs of the tile one wave ahead.
-template <int NH>
+template <int NH, bool SPLIT>
 static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefetch, cudaStream_t st) {
+    constexpr int SMEM_BYTES = Smem<SPLIT>::BYTES;
     int dev = 0;
     cudaGetDevice(&dev);
     static bool attr_set[128] = {};
@@ -707,10 +784,10 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     const bool cached = dev >= 0 && dev < 128;
     if (!cached || !attr_set[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(fused_chunk_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            cudaFuncSetAttribute(fused_chunk_kernel<NH, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         int per_sm = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel<NH>, NT, SMEM_BYTES);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel<NH, SPLIT>, NT, SMEM_BYTES);
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
@@ -722,7 +799,7 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     TcParams p = p_in;
     p.pf_dist = (prefetch && cached) ? resident[dev] / 2 : 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
-    fused_chunk_kernel<NH><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
+    fused_chunk_kernel<NH, SPLIT><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (g_prof_end) cudaEventRecord(g_prof_end, st);
     return e;
@@ -757,9 +834,13 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.first_ticket = 0;
     p.pf_dist = 0;
     p.wait_cycles = kWaitCycles;
-    cudaError_t e = launch_prep(p, st);
+    cudaError_t e = launch_prep(p, a.split_tf32, st);
     if (e != cudaSuccess) return e;
-    return NH == 1 ? launch_fused<1>(p, BH * nc, true, st) : launch_fused<2>(p, BH * nc, true, st);
+    // Split precision is built for dstate 64 only: the dstate-128 variant
+    // stalled in its first multi-chunk run and stays out until the cause is
+    // known (callers reject that shape first).
+    if (a.split_tf32) return NH == 1 ? launch_fused<1, true>(p, BH * nc, true, st) : cudaErrorNotSupported;
+    return NH == 1 ? launch_fused<1, false>(p, BH * nc, true, st) : launch_fused<2, false>(p, BH * nc, true, st);
 }
 
 // Failure-detection self-test: a two-sequence, two-chunk forward whose
@@ -827,8 +908,8 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.first_ticket = (int)BH;  // chunk 0 of every sequence is never taken
     p.pf_dist = 0;
     p.wait_cycles = wait_cycles;
-    if (e == cudaSuccess) e = launch_prep(p, st);
-    if (e == cudaSuccess) e = launch_fused<1>(p, BH * nc, false, st);
+    if (e == cudaSuccess) e = launch_prep(p, false, st);
+    if (e == cudaSuccess) e = launch_fused<1, false>(p, BH * nc, false, st);
     int bits = -1;
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
     cudaFreeAsync(buf, st);

@@ -141,6 +141,26 @@ int cssd_chunked_forward_h0(const cssd_dims* dims, const void* x, const float* d
                             void* h_final, int chunk, void* workspace, size_t workspace_bytes,
                             cssd_stream_t stream);
 
+/* cssd_chunked_forward_h0 to about fp32 accuracy.  The chunked form is exact
+ * up to rounding, and on the tensor-core path (headdim 64, dstate 64 or 128)
+ * the rounding of cssd_chunked_forward is that of TF32 operands (~1e-4 of the
+ * largest |y| on the pages' workloads).  Here every operand is held as two
+ * TF32 parts hi + lo (hi = the value rounded to TF32, lo = the remainder
+ * rounded to TF32) and every product is taken as hi.hi + hi.lo + lo.hi, which
+ * keeps ~21 significant bits per product; the decay exponentials use the
+ * accurate expf and the within-chunk cumulative log-steps are summed in double.
+ * Measured ~1e-6 of the largest |y|, at about 1.8x the time of
+ * cssd_chunked_forward (three times the tensor-core work and twice the shared
+ * memory, one CTA per SM).  Built for headdim 64 with dstate 64; dstate 128
+ * with headdim 64 returns CSSD_ERR_UNSUPPORTED.  Shapes the CUDA-core kernels
+ * take (headdim or dstate 16 / 32) run them, fp32 already, as in
+ * cssd_chunked_forward.  Arguments, workspace size (cssd_workspace_bytes) and
+ * status are otherwise those of cssd_chunked_forward_h0; h0 may be NULL. */
+int cssd_chunked_forward_precise(const cssd_dims* dims, const void* x, const float* dt, const void* A,
+                                 const void* B, const void* C, const float* D, const void* h0, void* y,
+                                 void* h_final, int chunk, void* workspace, size_t workspace_bytes,
+                                 cssd_stream_t stream);
+
 /* Forward over tensors that live in HOST memory, streamed through the device
  * in pieces of `piece_len` tokens: while one piece computes, the next one's
  * inputs are copied in and the previous one's output copied out, and each
@@ -258,9 +278,12 @@ int cssd_cayley_scan(const cssd_dims* dims, const float* phi, const float* u, co
  * three runs of the forward kernels on reversed and conjugated inputs; those of
  * dt and A follow from R_t = sum_{u >= t} sum_p (conj(dy_u) y_u - x_u conj(gx_u)),
  * since dL/dz_t = conj(R_t) for z_t = softplus(dt_t) A; gD = sum Re(conj(dy) x).
- * The forward output y is recomputed, and it and gx come from the fp32
- * CUDA-core chunk kernels: R_t is a small difference of large sums, which TF32
- * operands would spoil; gB and gC use the tensor-core kernel where it applies.
+ * The forward output y is recomputed, and it and gx are computed to about
+ * fp32 accuracy, because R_t is a small difference of large sums that plain
+ * TF32 operands would spoil: by the tensor-core kernel with split-precision
+ * operands (each value as two TF32 parts, three TF32 products per product)
+ * where headdim is 64 and dstate 64, else by the fp32 CUDA-core chunk kernels.
+ * gB and gC use the plain TF32 tensor-core kernel where it applies.
  *   dims, x, dt, A, B, C, D, chunk   as cssd_chunked_forward; dstate and
  *            headdim in {16, 32, 64} (else CSSD_ERR_UNSUPPORTED)
  *   dy       complex64 [batch, seqlen, nheads, headdim]  upstream gradient

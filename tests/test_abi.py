@@ -173,6 +173,14 @@ def test_initial_state_and_host_forward_argument_errors(lib):
     q[7] = None  # y
     assert f(ctypes.byref(ok), *q, 64, None, 0, None) == -1
     assert f(ctypes.byref(ok), *p, 64, ctypes.c_void_p(0x900000), 16, None) == -5
+    f = lib.cssd_chunked_forward_precise  # same arguments and checks
+    assert f(None, *p, 64, None, 0, None) == -1
+    assert f(ctypes.byref(ok), *p, 128 + 1, None, 0, None) == -3
+    assert f(ctypes.byref(cssd.Dims(1, 64, 1, 128, 64)), *p, 64, None, 0, None) == -3  # dstate 128, headdim 64
+    q = list(p)
+    q[6] = ctypes.c_void_p(0x10604)
+    assert f(ctypes.byref(ok), *q, 64, None, 0, None) == -4
+    assert f(ctypes.byref(ok), *p, 64, ctypes.c_void_p(0x900000), 16, None) == -5
 
     g = lib.cssd_chunked_forward_host
     assert g(None, *p, 64, 0, None, 0, None) == -1
