@@ -151,6 +151,7 @@ class ClockSampler:
 # includes; cssd_internal.h only declares host launchers).
 KERNEL_SOURCES = {
     "fused_chunk_kernel": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
+    "fused_chunk_kernel_split": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
     "step_kernel": ("step.cu", "cssd_common.cuh"),
     "cayley_scan_kernel": ("cayley.cu", "cssd_common.cuh"),
     "born_kernel": ("born.cu", "tcgen05.cuh", "cssd_common.cuh"),
@@ -694,6 +695,7 @@ def bench_precise(args, dev):
             "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_call": round(ms, 4), "calls": n,
             "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel (split)", "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
+                         "traffic": recorded_traffic("fused_chunk_kernel_split", units),
                          "kernel_ms": round(k_ms, 4), "alg_bytes_per_launch": alg},
             "tensor": {"executed_tflops": round(tf, 1), "peak": round(tpk, 1), "peak_kind": tkind,
                        "frac": round(tf / tpk, 4), "flops_per_launch": flops}}
