@@ -245,6 +245,141 @@ __global__ void __launch_bounds__(EB) reverse_scan_kernel(const float2* __restri
     }
 }
 
+// R at the chunk boundaries, from the states the two split-precision runs
+// published (T a multiple of 64): at t = 64 c, 0 < c < nc,
+//     R_t = a_t sum_{n,p} conj(G_t[n,p]) h_{t-1}[n,p]
+// (the product of the adjoint state after token t and the forward state before
+// it), an inner product of the forward run's state handed to chunk c (slot c)
+// and the reversed run's state handed on after original token t (slot nc - c),
+// each rotated back from its run's frame.  One block per (boundary, batch,
+// head); written to Rb[bh * (nc + 1) + c].
+__global__ void __launch_bounds__(EB) boundary_kernel(const float* __restrict__ Hd, const float2* __restrict__ Hrot,
+                                                      const float* __restrict__ Gd, const float2* __restrict__ Grot,
+                                                      const float* __restrict__ dt, const float2* __restrict__ A,
+                                                      double2* __restrict__ Rb, int64_t T, int64_t H, int nc) {
+    __shared__ double2 red[EB / 32];
+    constexpr int S = 64 * 64;  // state elements (dstate = headdim = 64)
+    const int64_t q = blockIdx.x;
+    const int c = (int)(q % (nc - 1)) + 1;
+    const int64_t bh = q / (nc - 1), b = bh / H, h = bh - b * H;
+    const float* hs = Hd + ((size_t)bh * (nc + 1) + c) * (2 * S);
+    const float* gs = Gd + ((size_t)bh * (nc + 1) + (nc - c)) * (2 * S);
+    // per-thread partial sums of 16 products in fp32 (the states themselves
+    // carry ~22 significant bits; FP64 arithmetic is slow on this part), the
+    // block reduction in double
+    float fr = 0.f, fi = 0.f;
+    for (int i = threadIdx.x; i < S; i += EB) {
+        const float hr = hs[i], hi = hs[S + i], gr = gs[i], gi = gs[S + i];
+        fr = fmaf(gr, hr, fmaf(gi, hi, fr));  // conj(g) h
+        fi = fmaf(gr, hi, fmaf(-gi, hr, fi));
+    }
+    double kr = fr, ki = fi;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        kr += __shfl_xor_sync(0xffffffffu, kr, o);
+        ki += __shfl_xor_sync(0xffffffffu, ki, o);
+    }
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = make_double2(kr, ki);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        kr = ki = 0.0;
+        for (int w = 0; w < EB / 32; ++w) {
+            kr += red[w].x;
+            ki += red[w].y;
+        }
+        // frames: h = e^{i thH} h~, G = e^{i thG} G~, so conj(G) h = e^{i (thH - thG)} conj(G~) h~
+        const float2 rh = Hrot[(size_t)bh * (nc + 1) + c], rg = Grot[(size_t)bh * (nc + 1) + (nc - c)];
+        const double er = (double)rh.x * rg.x + (double)rh.y * rg.y, ei = (double)rh.y * rg.x - (double)rh.x * rg.y;
+        const double pr = er * kr - ei * ki, pi = er * ki + ei * kr;
+        // a_t = exp(softplus(dt_t) A)
+        const double sp = softplusf(dt[((size_t)b * T + 64 * (size_t)c) * H + h]);
+        const double m = exp(sp * (double)A[h].x), ang = sp * (double)A[h].y;
+        const double ar = m * cos(ang), ai = m * sin(ang);
+        Rb[(size_t)bh * (nc + 1) + c] = make_double2(ar * pr - ai * pi, ar * pi + ai * pr);
+    }
+}
+
+// The step and rate gradients from chunk-local sums (T a multiple of 64): for
+// t in chunk c, R_t = r_t + ... + r_{64 c + 63} + R_{64 (c + 1)} with the
+// boundary value from boundary_kernel (0 after the last chunk), so no sum runs
+// across a chunk.  One CTA per (batch, head), four chunks per pass of 256
+// threads (one token each); outputs as reverse_scan_kernel.
+__global__ void __launch_bounds__(EB) chunk_scan_kernel(const float2* __restrict__ r, const float* __restrict__ d,
+                                                        const float* __restrict__ dt, const float2* __restrict__ A,
+                                                        const double2* __restrict__ Rb, float* __restrict__ gdt,
+                                                        double2* __restrict__ gA_part, double* __restrict__ gD_part,
+                                                        int64_t T, int64_t H, int nc) {
+    __shared__ double2 tot[EB / 32];
+    __shared__ double2 red[EB / 32];
+    __shared__ double redd[EB / 32];
+    const int64_t bh = blockIdx.x;
+    const int64_t b = bh / H, h = bh - b * H;
+    const float2 Ah = A[h];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    double ga_r = 0.0, ga_i = 0.0, gd = 0.0;
+    for (int c0 = 0; c0 < nc; c0 += EB / 64) {
+        const int c = c0 + (tid >> 6);
+        const int64_t t = 64 * (int64_t)c + (tid & 63);
+        const bool valid = c < nc && t < T;
+        const int64_t i = (b * T + t) * H + h;
+        double2 v = make_double2(0.0, 0.0);
+        if (valid) {
+            const float2 rv = r[i];
+            v = make_double2(rv.x, rv.y);
+        }
+        // suffix sums within the warp (32 tokens), then the upper warp's total
+        // added to the lower warp of the same chunk
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const double ux = __shfl_down_sync(0xffffffffu, v.x, o), uy = __shfl_down_sync(0xffffffffu, v.y, o);
+            if (lane + o < 32) {
+                v.x += ux;
+                v.y += uy;
+            }
+        }
+        if (lane == 0) tot[warp] = v;
+        __syncthreads();
+        if ((warp & 1) == 0) {
+            v.x += tot[warp + 1].x;
+            v.y += tot[warp + 1].y;
+        }
+        __syncthreads();
+        if (valid) {
+            const double2 Rn = (c + 1 < nc) ? Rb[(size_t)bh * (nc + 1) + c + 1] : make_double2(0.0, 0.0);
+            const double Rr = v.x + Rn.x, Ri = v.y + Rn.y;
+            const float dv = dt[i];
+            const float sig = dv >= 0.f ? 1.f / (1.f + __expf(-dv)) : __expf(dv) / (1.f + __expf(dv));
+            gdt[i] = (float)(Rr * Ah.x - Ri * Ah.y) * sig;
+            const double sp = softplusf(dv);
+            ga_r += sp * Rr;
+            ga_i -= sp * Ri;
+            gd += d[i];
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        ga_r += __shfl_xor_sync(0xffffffffu, ga_r, o);
+        ga_i += __shfl_xor_sync(0xffffffffu, ga_i, o);
+        gd += __shfl_xor_sync(0xffffffffu, gd, o);
+    }
+    if (lane == 0) {
+        red[warp] = make_double2(ga_r, ga_i);
+        redd[warp] = gd;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        double2 s2 = make_double2(0.0, 0.0);
+        double sd = 0.0;
+        for (int w = 0; w < EB / 32; ++w) {
+            s2.x += red[w].x;
+            s2.y += red[w].y;
+            sd += redd[w];
+        }
+        gA_part[bh] = s2;
+        gD_part[bh] = sd;
+    }
+}
+
 // gA[h], gD[h]: the batch rows' partial sums, added in order (deterministic).
 __global__ void head_sums_kernel(const double2* __restrict__ gA_part, const double* __restrict__ gD_part,
                                  float2* __restrict__ gA, float* __restrict__ gD, int64_t Bz, int64_t H) {
@@ -282,14 +417,30 @@ cudaError_t launch_precise_forward(FwdArgs f, void* ws, cudaStream_t st) {
     return launch_tc_forward(f, ws, st);
 }
 
-// Workspace regions of the backward, in order.
+// The adjoint runs take the tensor-core kernel's index and sign modes (time
+// reversal, conjugated operands and output, no skip) when both the state and
+// its transpose are tensor-core shapes; otherwise they run on reversed and
+// conjugated copies of the inputs.
+bool folded_runs(int64_t N, int64_t P, int chunk) {
+    return tc_forward_supported(N, P, chunk) && tc_forward_supported(P, N, chunk);
+}
+
+// With the folded runs and T a multiple of 64, R_t comes from chunk-local sums
+// and the boundary inner products of the two runs' published states.
+bool boundary_sums(int64_t T, int64_t N, int64_t P, int chunk) {
+    return folded_runs(N, P, chunk) && N == 64 && P == 64 && T % 64 == 0;
+}
+
+// Workspace regions of the backward, in order (the copies only without the
+// folded runs, the state dumps only with the boundary sums).
 struct BwdLayout {
-    size_t y, dyR, dts, ccR, bcR, xcR, dyc, tmp, Ac, zero, r, d, gAp, gDp, fwd, total;
+    size_t y, dyR, dts, ccR, bcR, xcR, dyc, tmp, Ac, zero, r, d, gAp, gDp, Hd, Gd, Hrot, Grot, Rb, fwd, total;
 };
 
 BwdLayout bwd_layout(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
     const size_t TP = (size_t)(Bz * T * H * P) * sizeof(float2), TN = (size_t)(Bz * T * H * N) * sizeof(float2);
     const size_t TH = (size_t)(Bz * T * H);
+    const bool folded = folded_runs(N, P, chunk);
     BwdLayout L;
     size_t off = 0;
     auto take = [&](size_t bytes) {
@@ -298,21 +449,31 @@ BwdLayout bwd_layout(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int
         return o;
     };
     L.y = take(TP);
-    L.dyR = take(TP);
-    L.dts = take(TH * sizeof(float));
-    L.ccR = take(TN);
-    L.bcR = take(TN);
-    L.xcR = take(TP);
-    L.dyc = take(TP);
-    L.tmp = take(TP > TN ? TP : TN);
-    L.Ac = take((size_t)H * sizeof(float2));
-    L.zero = take((size_t)H * sizeof(float));
+    if (!folded) {
+        L.dyR = take(TP);
+        L.dts = take(TH * sizeof(float));
+        L.ccR = take(TN);
+        L.bcR = take(TN);
+        L.xcR = take(TP);
+        L.dyc = take(TP);
+        L.tmp = take(TP > TN ? TP : TN);
+        L.Ac = take((size_t)H * sizeof(float2));
+        L.zero = take((size_t)H * sizeof(float));
+    }
     L.r = take(TH * sizeof(float2));
     L.d = take(TH * sizeof(float));
     L.gAp = take((size_t)(Bz * H) * sizeof(double2));
     L.gDp = take((size_t)(Bz * H) * sizeof(double));
+    if (boundary_sums(T, N, P, chunk)) {
+        const size_t slots = (size_t)(Bz * H) * (size_t)(T / 64 + 1);
+        L.Hd = take(slots * 2 * 64 * 64 * sizeof(float));
+        L.Gd = take(slots * 2 * 64 * 64 * sizeof(float));
+        L.Hrot = take(slots * sizeof(float2));
+        L.Grot = take(slots * sizeof(float2));
+        L.Rb = take(slots * sizeof(double2));
+    }
     const size_t f1 = precise_forward_workspace_bytes(Bz, T, H, N, P, chunk);  // y and gx runs
-    const size_t f2 = forward_workspace_bytes(Bz, T, H, P, N, chunk);      // transposed-state runs
+    const size_t f2 = forward_workspace_bytes(Bz, T, H, P, N, chunk);          // transposed-state runs
     L.fwd = take(f1 > f2 ? f1 : f2);
     L.total = off;
     return L;
@@ -339,46 +500,87 @@ cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t st) 
     cudaError_t e = cudaSuccess;
     auto check = [&]() { return (e = cudaGetLastError()) == cudaSuccess; };
 
-    // Forward output, to about fp32 accuracy.
+    const bool bsum = boundary_sums(T, N, P, a.chunk);
+    float* Hd = bsum ? fp(L.Hd) : nullptr;
+    float* Gd = bsum ? fp(L.Gd) : nullptr;
+    float2* Hrot = bsum ? f2p(L.Hrot) : nullptr;
+    float2* Grot = bsum ? f2p(L.Grot) : nullptr;
+
+    // Forward output, to about fp32 accuracy (and its chunk states).
     const float2* y = f2p(L.y);
     {
         FwdArgs f{Bz, T, H, N, P, a.chunk, a.x, a.dt, a.A, a.B, a.C, a.D, f2p(L.y), nullptr};
+        if (bsum) {
+            f.mode = kFwdDump;
+            f.dump = Hd;
+            f.rot_dump = Hrot;
+        }
         if ((e = launch_precise_forward(f, fws, st)) != cudaSuccess) return e;
     }
 
-    // Reversed and conjugated inputs.
-    float2 *dyR = f2p(L.dyR), *ccR = f2p(L.ccR), *bcR = f2p(L.bcR), *xcR = f2p(L.xcR), *dyc = f2p(L.dyc);
-    float2* Ac = f2p(L.Ac);
-    float *dts = fp(L.dts), *zero = fp(L.zero);
-    reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.dy, dyR, Bz, T, H * P, false);
-    reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.C, ccR, Bz, T, H * N, true);
-    reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.B, bcR, Bz, T, H * N, true);
-    reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.x, xcR, Bz, T, H * P, true);
-    conj_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(a.dy, dyc, Bz * T * H * P);
-    reverse_steps_kernel<<<grid_for(Bz * T * H), EB, 0, st>>>(a.dt, dts, Bz, T, H, a.A, Ac, zero);
-    if (!check()) return e;
+    if (folded_runs(N, P, a.chunk)) {
+        // gx: the adjoint run, time reversed (the step of token t + 1 at
+        // reversed position T - 1 - t), input dy, coupling conj(C), readout
+        // conj(B), rate conj(A), skip D; written in token order.
+        {
+            FwdArgs f{Bz, T, H, N, P, a.chunk, a.dy, a.dt, a.A, a.C, a.B, a.D, a.gx, nullptr};
+            f.mode = kFwdReverse | kFwdShiftDt | kFwdConjA | kFwdConjB | kFwdConjC;
+            if (bsum) {
+                f.mode |= kFwdDump;
+                f.dump = Gd;
+                f.rot_dump = Grot;
+            }
+            if ((e = launch_precise_forward(f, fws, st)) != cudaSuccess) return e;
+        }
+        // gB: the same reversed run with the state transposed: input conj(C),
+        // coupling dy, readout conj(x), no skip.
+        {
+            FwdArgs f{Bz, T, H, P, N, a.chunk, a.C, a.dt, a.A, a.dy, a.x, nullptr, a.gB, nullptr};
+            f.mode = kFwdReverse | kFwdShiftDt | kFwdConjA | kFwdConjX | kFwdConjC;
+            if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
+        }
+        // gC: the forward run with the state transposed (input B, coupling x,
+        // readout conj(dy)), output conjugated, no skip.
+        {
+            FwdArgs f{Bz, T, H, P, N, a.chunk, a.B, a.dt, a.A, a.x, a.dy, nullptr, a.gC, nullptr};
+            f.mode = kFwdConjC | kFwdConjY;
+            if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
+        }
+    } else {
+        // Reversed and conjugated inputs.
+        float2 *dyR = f2p(L.dyR), *ccR = f2p(L.ccR), *bcR = f2p(L.bcR), *xcR = f2p(L.xcR), *dyc = f2p(L.dyc);
+        float2* Ac = f2p(L.Ac);
+        float *dts = fp(L.dts), *zero = fp(L.zero);
+        reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.dy, dyR, Bz, T, H * P, false);
+        reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.C, ccR, Bz, T, H * N, true);
+        reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.B, bcR, Bz, T, H * N, true);
+        reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(a.x, xcR, Bz, T, H * P, true);
+        conj_kernel<<<grid_for(Bz * T * H * P), EB, 0, st>>>(a.dy, dyc, Bz * T * H * P);
+        reverse_steps_kernel<<<grid_for(Bz * T * H), EB, 0, st>>>(a.dt, dts, Bz, T, H, a.A, Ac, zero);
+        if (!check()) return e;
 
-    float2* tmp = f2p(L.tmp);
-    // gx: reversed run (about fp32 accuracy), then back to token order.
-    {
-        FwdArgs f{Bz, T, H, N, P, a.chunk, dyR, dts, Ac, ccR, bcR, a.D, tmp, nullptr};
-        if ((e = launch_precise_forward(f, fws, st)) != cudaSuccess) return e;
-        reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(tmp, a.gx, Bz, T, H * P, false);
-        if (!check()) return e;
-    }
-    // gB: reversed run with the state transposed (dstate P, headdim N).
-    {
-        FwdArgs f{Bz, T, H, P, N, a.chunk, ccR, dts, Ac, dyR, xcR, zero, tmp, nullptr};
-        if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
-        reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(tmp, a.gB, Bz, T, H * N, false);
-        if (!check()) return e;
-    }
-    // gC: forward run with the state transposed; gC = conj(output).
-    {
-        FwdArgs f{Bz, T, H, P, N, a.chunk, a.B, a.dt, a.A, a.x, dyc, zero, tmp, nullptr};
-        if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
-        conj_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(tmp, a.gC, Bz * T * H * N);
-        if (!check()) return e;
+        float2* tmp = f2p(L.tmp);
+        // gx: reversed run (about fp32 accuracy), then back to token order.
+        {
+            FwdArgs f{Bz, T, H, N, P, a.chunk, dyR, dts, Ac, ccR, bcR, a.D, tmp, nullptr};
+            if ((e = launch_precise_forward(f, fws, st)) != cudaSuccess) return e;
+            reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(tmp, a.gx, Bz, T, H * P, false);
+            if (!check()) return e;
+        }
+        // gB: reversed run with the state transposed (dstate P, headdim N).
+        {
+            FwdArgs f{Bz, T, H, P, N, a.chunk, ccR, dts, Ac, dyR, xcR, zero, tmp, nullptr};
+            if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
+            reverse_rows_kernel<<<grid_rows(Bz * T), EB, 0, st>>>(tmp, a.gB, Bz, T, H * N, false);
+            if (!check()) return e;
+        }
+        // gC: forward run with the state transposed; gC = conj(output).
+        {
+            FwdArgs f{Bz, T, H, P, N, a.chunk, a.B, a.dt, a.A, a.x, dyc, zero, tmp, nullptr};
+            if ((e = launch_forward(f, fws, st)) != cudaSuccess) return e;
+            conj_kernel<<<grid_for(Bz * T * H * N), EB, 0, st>>>(tmp, a.gC, Bz * T * H * N);
+            if (!check()) return e;
+        }
     }
     // Step, rate and skip gradients.
     float2* r = f2p(L.r);
@@ -386,7 +588,16 @@ cudaError_t launch_backward(const BwdArgs& a, void* workspace, cudaStream_t st) 
     double2* gAp = reinterpret_cast<double2*>(w + L.gAp);
     double* gDp = reinterpret_cast<double*>(w + L.gDp);
     token_terms_kernel<<<grid_for(Bz * T * H * 32), EB, 0, st>>>(a.x, y, a.dy, a.gx, r, d, Bz * T * H, (int)P);
-    reverse_scan_kernel<<<(unsigned)(Bz * H), EB, 0, st>>>(r, d, a.dt, a.A, a.gdt, gAp, gDp, T, H);
+    if (bsum) {
+        const int nc = (int)(T / 64);
+        double2* Rb = reinterpret_cast<double2*>(w + L.Rb);
+        if (nc > 1)
+            boundary_kernel<<<(unsigned)((int64_t)(nc - 1) * Bz * H), EB, 0, st>>>(Hd, Hrot, Gd, Grot, a.dt, a.A, Rb,
+                                                                                   T, H, nc);
+        chunk_scan_kernel<<<(unsigned)(Bz * H), EB, 0, st>>>(r, d, a.dt, a.A, Rb, a.gdt, gAp, gDp, T, H, nc);
+    } else {
+        reverse_scan_kernel<<<(unsigned)(Bz * H), EB, 0, st>>>(r, d, a.dt, a.A, a.gdt, gAp, gDp, T, H);
+    }
     head_sums_kernel<<<grid_for(H), EB, 0, st>>>(gAp, gDp, a.gA, a.gD, Bz, H);
     check();
     return e;

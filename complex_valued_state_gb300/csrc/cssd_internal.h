@@ -10,6 +10,19 @@
 
 namespace cssd {
 
+// Index and sign modes of a forward run, honoured by the tensor-core path only
+// (the backward runs its adjoint recurrences through them instead of copying
+// reversed or conjugated inputs).
+constexpr unsigned kFwdReverse = 1u;   // token tau of the run reads and writes original token T - 1 - tau
+constexpr unsigned kFwdShiftDt = 2u;   // with kFwdReverse: the step of token tau is that of original token
+                                       // T - tau (none at tau = 0)
+constexpr unsigned kFwdConjX = 4u;     // conj(x), also in the skip term
+constexpr unsigned kFwdConjB = 8u;     // conj(B)
+constexpr unsigned kFwdConjC = 16u;    // conj(C)
+constexpr unsigned kFwdConjY = 32u;    // the output is conjugated
+constexpr unsigned kFwdConjA = 64u;    // rate conj(A)
+constexpr unsigned kFwdDump = 128u;    // write every published chunk state and its rotation (dump, rot_dump)
+
 struct FwdArgs {
     int64_t Bz, T, H, N, P;
     int chunk;
@@ -25,6 +38,13 @@ struct FwdArgs {
     // Tensor-core path only: split-precision operands (three TF32 products per
     // product, about fp32 accuracy, one CTA per SM) instead of plain TF32.
     bool split_tf32 = false;
+    unsigned mode = 0;  // kFwd* bits (tensor-core path only); D may be null (no skip) when set
+    // kFwdDump: the state chunk c hands to chunk c + 1, in the rotated frame,
+    // at dump[((bh * NH + half) * (nc + 1) + c + 1) * 2 * 64 * 64 + part * 64 * 64 + p * 64 + n]
+    // (part 0 real, 1 imaginary; NH = dstate / 64, nc = 64-token chunks), and
+    // (cos, sin) of that frame's angle at rot_dump[bh * (nc + 1) + c + 1].
+    float* dump = nullptr;
+    float2* rot_dump = nullptr;
 };
 
 struct StepArgs {

@@ -17,6 +17,7 @@ int forward_launches(int64_t, int64_t, int64_t, int64_t, int64_t, int) { return 
 
 cudaError_t launch_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     if (tc_forward_supported(a.N, a.P, a.chunk)) return launch_tc_forward(a, ws, st);
+    if (a.mode != 0) return cudaErrorInvalidValue;  // index and sign modes: tensor-core path only
     return launch_seq_forward(a, ws, st);
 }
 

@@ -150,6 +150,9 @@ struct TcParams {
     float2* y;         // [Bz,T,H,P]
     float2* h_final;   // [Bz,H,N,P] or null
     const float2* h0;  // [Bz,H,N,P] state before the first token, or null (zero)
+    unsigned mode;     // kFwd* index and sign modes; D is null when there is no skip term
+    float* dump;       // kFwdDump: published chunk states (layout in FwdArgs)
+    float2* rot_dump;  // kFwdDump: (cos, sin) of each published state's frame
     unsigned long long* ring;  // [BH][RING][2][P][N] tagged cells
     int* ticket;       // [1]
     float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
@@ -228,13 +231,17 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(TcParams p) {
     if (gw >= p.BH * p.nc) return;
     const int bh = gw / p.nc, c = gw - bh * p.nc;
     const int b = bh / p.H, h = bh % p.H;
-    const Real alpha = p.A[h].x, beta = p.A[h].y;
+    const Real alpha = p.A[h].x, beta = (p.mode & kFwdConjA) ? -p.A[h].y : p.A[h].y;
     const float* dtb = p.dt + (size_t)b * p.T * p.H + h;  // token t at dtb[t * H]
     Real v[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
         const int t = c * CH + hh * 32 + lane;
-        v[hh] = (t < p.T) ? (Real)softplusf(__ldg(dtb + (size_t)t * p.H)) : (Real)0;
+        // original token whose step this position takes (-1: none)
+        int src = t;
+        if (p.mode & kFwdReverse) src = (p.mode & kFwdShiftDt) ? p.T - t : p.T - 1 - t;
+        if (src >= p.T) src = -1;
+        v[hh] = (t < p.T && src >= 0) ? (Real)softplusf(__ldg(dtb + (size_t)src * p.H)) : (Real)0;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const Real u = __shfl_up_sync(0xffffffffu, v[hh], o);
@@ -297,9 +304,10 @@ __global__ void __launch_bounds__(256) phase_scan_kernel(TcParams p) {
 // NH halves of 64 (dstate = 64 NH): the state GEMM, the hand-off and the
 // carried-in readout run once per half, the score GEMM accumulates over the
 // halves, and the masked scores and Y_diag run once.
-template <int NH, bool SPLIT>
+template <int NH, bool SPLIT, bool MODES>
 __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams p) {
     using SM = Smem<SPLIT>;
+    const unsigned mode = MODES ? p.mode : 0u;  // index and sign modes (compiled out for the plain forward)
     constexpr int N = NS * NH;  // dstate
     constexpr uint32_t LO1 = SM::LO1, LO23 = SM::LO23;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -340,8 +348,12 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     const int c = ticket / p.BH, bh = ticket - c * p.BH;
     const int b = bh / p.H, h = bh - b * p.H;
     const int t0 = c * CH;
-    const size_t row0 = ((size_t)b * p.T + t0) * p.H + h;  // token row of l = 0
-    const size_t rstride = (size_t)p.H;                    // rows between tokens
+    // Row of token l of the tile: row0 + l * rstride (time-reversed runs walk
+    // the original rows backwards).  Only rows of real tokens are formed.
+    const bool rev = (mode & kFwdReverse) != 0;
+    const long long row0 = ((long long)b * p.T + (rev ? p.T - 1 - t0 : t0)) * p.H + h;
+    const long long rstride = rev ? -(long long)p.H : (long long)p.H;
+    const bool cj_x = (mode & kFwdConjX) != 0, cj_b = (mode & kFwdConjB) != 0, cj_c = (mode & kFwdConjC) != 0;
     const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
 
     // This thread's items of a 64 x 64 complex tile: the column pair
@@ -363,12 +375,17 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     const bool swap_rows = ((l0 >> 2) & 1) != 0;
     const uint32_t sx = swap_rows ? 16u : 0u;
     // 64 columns (half hf) of a token-major [.., N] complex tile, into registers.
-    auto load_half = [&](const float4* src, int hf, float4 (&v)[IT]) {
-        const float4* g = src + (row0 + (size_t)l0 * rstride) * (N / 2) + hf * 32 + (n0 >> 1);
-        const size_t step = 16 * rstride * (N / 2);
+    auto load_half = [&](const float4* src, int hf, bool cj, float4 (&v)[IT]) {
+        const long long g = (row0 + (long long)l0 * rstride) * (N / 2) + hf * 32 + (n0 >> 1);
+        const long long step = 16 * rstride * (N / 2);
 #pragma unroll
-        for (int i = 0; i < IT; ++i)
-            v[i] = (t0 + l0 + 16 * i < p.T) ? __ldg(g + i * step) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < IT; ++i) {
+            v[i] = (t0 + l0 + 16 * i < p.T) ? __ldg(src + g + i * step) : make_float4(0.f, 0.f, 0.f, 0.f);
+            if (cj) {
+                v[i].y = -v[i].y;
+                v[i].w = -v[i].w;
+            }
+        }
     };
 
     // Rows of x, B and C of the tile one wave of resident CTAs ahead are
@@ -380,7 +397,8 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             const int pc = pt / p.BH, pbh = pt - pc * p.BH;
             const int tok = pc * CH + (tid & (CH - 1));
             if (tok < p.T) {
-                const size_t prow = ((size_t)(pbh / p.H) * p.T + tok) * p.H + pbh % p.H;
+                const int otok = (mode & kFwdReverse) ? p.T - 1 - tok : tok;  // original token
+                const size_t prow = ((size_t)(pbh / p.H) * p.T + otok) * p.H + pbh % p.H;
                 const int which = tid / CH;  // 0: x, 1: B, 2: C
                 if (which == 0) prefetch_l2(p.x + prow * (PD / 2), PD * 8);
                 else prefetch_l2((which == 1 ? p.B : p.C) + prow * (N / 2), N * 8);
@@ -403,8 +421,8 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
         const uint32_t o = raw_off(lr, j);
         const float4* gb = p.B + row0 * (N / 2) + j;
         const float4* gx = p.x + row0 * (PD / 2) + j;
-        const size_t sb = 16 * rstride * (N / 2), sx = 16 * rstride * (PD / 2);
-        const size_t rb = (size_t)lr * rstride * (N / 2), rx = (size_t)lr * rstride * (PD / 2);
+        const long long sb = 16 * rstride * (N / 2), sx = 16 * rstride * (PD / 2);
+        const long long rb = (long long)lr * rstride * (N / 2), rx = (long long)lr * rstride * (PD / 2);
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
             const bool ok = t0 + lr + 16 * i < p.T;
@@ -414,7 +432,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     }
     cp_async_commit();
     float4 cv[IT];
-    load_half(p.C, 0, cv);  // C (its first half when dstate is 128) in registers, in flight with the rest
+    load_half(p.C, 0, cj_c, cv);  // C (its first half when dstate is 128) in registers, in flight with the rest
 
     // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
     if (tid < CH) {
@@ -480,7 +498,13 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     {
         float4 xv[IT];
 #pragma unroll
-        for (int i = 0; i < IT; ++i) xv[i] = *reinterpret_cast<const float4*>(sm2 + o_raw + 8192 * i);
+        for (int i = 0; i < IT; ++i) {
+            xv[i] = *reinterpret_cast<const float4*>(sm2 + o_raw + 8192 * i);
+            if (cj_x) {
+                xv[i].y = -xv[i].y;
+                xv[i].w = -xv[i].w;
+            }
+        }
         __syncthreads();  // raw X is overwritten below
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
@@ -501,9 +525,15 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             float4 bv[IT];
             if (hf == 0) {
 #pragma unroll
-                for (int i = 0; i < IT; ++i) bv[i] = *reinterpret_cast<const float4*>(sm3 + o_raw + 8192 * i);
+                for (int i = 0; i < IT; ++i) {
+                    bv[i] = *reinterpret_cast<const float4*>(sm3 + o_raw + 8192 * i);
+                    if (cj_b) {
+                        bv[i].y = -bv[i].y;
+                        bv[i].w = -bv[i].w;
+                    }
+                }
             } else {
-                load_half(p.B, hf, bv);
+                load_half(p.B, hf, cj_b, bv);
                 wait_bar(&mbar[2], ph ^ 1);  // Y_off of the previous half has read Ct and H
             }
             __syncthreads();  // raw B (half 0) and last half's operands are overwritten below
@@ -534,7 +564,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
         issue(tmem + COL_S, a1, a2, false, &mbar[0]);
 
         // ---- 4. Ct half stack into S1 once the state GEMM has read F; G += Ct Bt^T
-        if (NH > 1 && hf > 0) load_half(p.C, hf, cv);
+        if (NH > 1 && hf > 0) load_half(p.C, hf, cj_c, cv);
         wait_bar(&mbar[0], ph);
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
@@ -609,9 +639,16 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             tmem_ld_cols(tmem + lane_base + COL_S + c0col, r);
             tc::tmem_wait_ld();
             const uint32_t tag = (uint32_t)(c + 1);
+            float* dmp = (mode & kFwdDump) ? p.dump + (((size_t)bh * NH + hf) * (p.nc + 1) + c + 1) * (2 * PD * NS) +
+                                                 (size_t)part * PD * NS + lrow
+                                           : nullptr;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j)
-                st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j])), tag);
+            for (int j = 0; j < CPT; ++j) {
+                const float v = fmaf(eend, hv[j], __uint_as_float(r[j]));
+                st_cell(cout + (c0col + j) * NS, v, tag);
+                if (dmp) dmp[(c0col + j) * NS] = v;
+            }
+            if ((mode & kFwdDump) && hf == 0 && tid == 0) p.rot_dump[(size_t)bh * (p.nc + 1) + c + 1] = s_rot_last;
         }
 
         // ---- 6. H_c of this half as the B operand of Y_off (rows p, K = n) in
@@ -684,13 +721,16 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     // tf32-rounded X planes.
     constexpr int YI = CH * PD / NT;  // output elements per thread: rows ly + 8 k, column py
     const int ly = tid >> 6, py = tid & 63;
-    const size_t ystep = 8 * rstride * PD;
-    const size_t yoff = (row0 + (size_t)ly * rstride) * PD + py;
+    const long long ystep = 8 * rstride * PD;
+    const long long yoff = (row0 + (long long)ly * rstride) * PD + py;
+    const bool skip = !MODES || p.D != nullptr;
     float2 xs[YI];
 #pragma unroll
-    for (int k = 0; k < YI; ++k)
-        xs[k] = (t0 + ly + 8 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
-                                        : make_float2(0.f, 0.f);
+    for (int k = 0; k < YI; ++k) {
+        xs[k] = (skip && t0 + ly + 8 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
+                                                : make_float2(0.f, 0.f);
+        if (cj_x) xs[k].y = -xs[k].y;
+    }
     {
         wait_bar(&mbar[3], 0);
         tc::fence_after_sync();
@@ -705,13 +745,14 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     }
     __syncthreads();
     {
-        const float Dh = p.D[h];
+        const float Dh = skip ? p.D[h] : 0.f;
+        const float ysign = (mode & kFwdConjY) ? -1.f : 1.f;
         const float* stage = reinterpret_cast<const float*>(sm1) + ly * STAGE_LD + py;
 #pragma unroll
         for (int k = 0; k < YI; ++k) {
             if (t0 + ly + 8 * k < p.T) {
                 const float yr = stage[8 * k * STAGE_LD], yi = stage[CH * STAGE_LD + 8 * k * STAGE_LD];
-                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
+                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), ysign * fmaf(Dh, xs[k].y, yi));
             }
         }
     }
@@ -774,7 +815,7 @@ static cudaError_t launch_prep(const TcParams& p, bool precise, cudaStream_t st)
 // sequence forward by ~4 %, the others gained nothing).
 
 // `prefetch`: whether CTAs prefetch the inputs of the tile one wave ahead.
-template <int NH, bool SPLIT>
+template <int NH, bool SPLIT, bool MODES>
 static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefetch, cudaStream_t st) {
     constexpr int SMEM_BYTES = Smem<SPLIT>::BYTES;
     int dev = 0;
@@ -784,10 +825,12 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     const bool cached = dev >= 0 && dev < 128;
     if (!cached || !attr_set[dev]) {
         cudaError_t e =
-            cudaFuncSetAttribute(fused_chunk_kernel<NH, SPLIT>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            cudaFuncSetAttribute(fused_chunk_kernel<NH, SPLIT, MODES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES);
         if (e != cudaSuccess) return e;
         int per_sm = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel<NH, SPLIT>, NT, SMEM_BYTES);
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel<NH, SPLIT, MODES>, NT,
+                                                          SMEM_BYTES);
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
@@ -799,7 +842,7 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     TcParams p = p_in;
     p.pf_dist = (prefetch && cached) ? resident[dev] / 2 : 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
-    fused_chunk_kernel<NH, SPLIT><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
+    fused_chunk_kernel<NH, SPLIT, MODES><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (g_prof_end) cudaEventRecord(g_prof_end, st);
     return e;
@@ -826,6 +869,9 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.y = a.y;
     p.h_final = a.h_final;
     p.h0 = a.h0;
+    p.mode = a.mode;
+    p.dump = a.dump;
+    p.rot_dump = a.rot_dump;
     p.T = (int)a.T;
     p.H = (int)a.H;
     p.BH = (int)BH;
@@ -839,8 +885,16 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     // Split precision is built for dstate 64 only: the dstate-128 variant
     // stalled in its first multi-chunk run and stays out until the cause is
     // known (callers reject that shape first).
-    if (a.split_tf32) return NH == 1 ? launch_fused<1, true>(p, BH * nc, true, st) : cudaErrorNotSupported;
-    return NH == 1 ? launch_fused<1, false>(p, BH * nc, true, st) : launch_fused<2, false>(p, BH * nc, true, st);
+    // The index and sign modes (the backward's runs) take their own dstate-64
+    // instances, so the plain forward is compiled without them.
+    if (a.mode != 0) {
+        if (NH != 1) return cudaErrorNotSupported;
+        return a.split_tf32 ? launch_fused<1, true, true>(p, BH * nc, true, st)
+                            : launch_fused<1, false, true>(p, BH * nc, true, st);
+    }
+    if (a.split_tf32) return NH == 1 ? launch_fused<1, true, false>(p, BH * nc, true, st) : cudaErrorNotSupported;
+    return NH == 1 ? launch_fused<1, false, false>(p, BH * nc, true, st)
+                   : launch_fused<2, false, false>(p, BH * nc, true, st);
 }
 
 // Failure-detection self-test: a two-sequence, two-chunk forward whose
@@ -900,6 +954,9 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.y = a.y;
     p.h_final = a.h_final;
     p.h0 = nullptr;
+    p.mode = 0;
+    p.dump = nullptr;
+    p.rot_dump = nullptr;
     p.T = T;
     p.H = H;
     p.BH = (int)BH;
@@ -909,7 +966,7 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.pf_dist = 0;
     p.wait_cycles = wait_cycles;
     if (e == cudaSuccess) e = launch_prep(p, false, st);
-    if (e == cudaSuccess) e = launch_fused<1, false>(p, BH * nc, false, st);
+    if (e == cudaSuccess) e = launch_fused<1, false, false>(p, BH * nc, false, st);
     int bits = -1;
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
     cudaFreeAsync(buf, st);

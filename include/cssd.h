@@ -275,9 +275,14 @@ int cssd_cayley_scan(const cssd_dims* dims, const float* phi, const float* u, co
  * the call writes gx, gdt, gA, gB, gC, gD.  The adjoint state
  * G_t = conj(a_{t+1}) G_{t+1} + conj(C_t) dy_t^T is itself a run of the forward
  * recurrence (time reversed, rate conj(A)), so the gradients of x, B and C are
- * three runs of the forward kernels on reversed and conjugated inputs; those of
- * dt and A follow from R_t = sum_{u >= t} sum_p (conj(dy_u) y_u - x_u conj(gx_u)),
- * since dL/dz_t = conj(R_t) for z_t = softplus(dt_t) A; gD = sum Re(conj(dy) x).
+ * three runs of the forward kernels on reversed and conjugated inputs (read in
+ * place through the kernels' indexing for headdim = dstate = 64, else copied);
+ * those of dt and A follow from R_t = sum_{u >= t} sum_p (conj(dy_u) y_u -
+ * x_u conj(gx_u)), since dL/dz_t = conj(R_t) for z_t = softplus(dt_t) A, and
+ * R_t = a_t sum conj(G_t) h_{t-1}: for headdim = dstate = 64 and seqlen a
+ * multiple of 64, R is taken at every 64-token boundary from that inner
+ * product of the two runs' states and summed only within chunks, otherwise
+ * summed over the sequence from its shorter end; gD = sum Re(conj(dy) x).
  * The forward output y is recomputed, and it and gx are computed to about
  * fp32 accuracy, because R_t is a small difference of large sums that plain
  * TF32 operands would spoil: by the tensor-core kernel with split-precision

@@ -63,6 +63,19 @@ def test_matches_oracle(cs, orc, N, P, T):
         assert rel_err(got[k], ref[k]) < TOL, k
 
 
+@pytest.mark.parametrize("T,chunk", [(64, 64), (128, 64), (640, 128), (1024, 64)])
+def test_chunk_boundary_sums(cs, orc, T, chunk):
+    """dstate = headdim = 64 with T a multiple of 64: the step and rate
+    gradients come from chunk-local sums plus the inner products of the
+    forward and adjoint states at the chunk boundaries."""
+    d = wl.random_case(4000 + T + chunk, 2, T, 3, 64, 64)
+    dy = upstream(4100 + T, (2, T, 3, 64))
+    got = run(cs, d, dy, chunk)
+    ref = orc.cssd_backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], dy)
+    for k in KEYS:
+        assert rel_err(got[k], ref[k]) < TOL, k
+
+
 def test_chunk_128(cs, orc):
     d = wl.random_case(5, 1, 300, 2, 64, 64)
     dy = upstream(6, (1, 300, 2, 64))
