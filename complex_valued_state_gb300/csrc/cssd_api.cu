@@ -26,6 +26,8 @@ int check_dims(const cssd_dims* d, bool need_seq) {
     if (d->batch > kMaxGridYZ || d->nheads > kMaxGridYZ) return CSSD_ERR_DIMS;
     if (d->batch * d->nheads > kMaxInt) return CSSD_ERR_DIMS;
     if (need_seq && d->seqlen > kMaxInt) return CSSD_ERR_DIMS;
+    // the chunk kernels index (batch, head, 64-token tile) in 32 bits
+    if (need_seq && (d->seqlen + 63) / 64 > kMaxInt / (d->batch * d->nheads)) return CSSD_ERR_DIMS;
     return CSSD_OK;
 }
 

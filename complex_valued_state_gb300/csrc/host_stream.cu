@@ -32,7 +32,8 @@ bool sizes_ok(const cssd_dims* d, int chunk) {
     if (!(d->headdim == 16 || d->headdim == 32 || d->headdim == 64)) return false;
     if (!(chunk == 64 || chunk == 128)) return false;
     return d->batch <= 65535 && d->nheads <= 65535 && d->seqlen <= 2147483647LL &&
-           d->batch * d->nheads <= 2147483647LL;
+           d->batch * d->nheads <= 2147483647LL &&
+           (d->seqlen + 63) / 64 <= 2147483647LL / (d->batch * d->nheads);  // 32-bit tile index
 }
 
 // Device memory of one call: A and D, two state buffers, the forward
@@ -152,7 +153,9 @@ int cssd_chunked_forward_host(const cssd_dims* d, const void* x, const float* dt
     if (d->batch <= 0 || d->seqlen <= 0 || d->nheads <= 0 || d->dstate <= 0 || d->headdim <= 0 || piece_len < 0)
         return CSSD_ERR_DIMS;
     if (!sizes_ok(d, chunk)) {
-        if (d->batch > 65535 || d->nheads > 65535 || d->seqlen > 2147483647LL) return CSSD_ERR_DIMS;
+        if (d->batch > 65535 || d->nheads > 65535 || d->seqlen > 2147483647LL ||
+            d->batch * d->nheads > 2147483647LL || (d->seqlen + 63) / 64 > 2147483647LL / (d->batch * d->nheads))
+            return CSSD_ERR_DIMS;
         return CSSD_ERR_UNSUPPORTED;
     }
     if (!x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;

@@ -91,7 +91,7 @@ extern "C" int cssd_chunked_forward_noalloc(const cssd_dims* d, const void* x, c
         !(chunk == 64 || chunk == 128))
         return CSSD_ERR_UNSUPPORTED;
     if (d->batch > 65535 || d->nheads > 65535 || d->seqlen > 2147483647LL ||
-        d->batch * d->nheads > 2147483647LL)
+        d->batch * d->nheads > 2147483647LL || (d->seqlen + 63) / 64 > 2147483647LL / (d->batch * d->nheads))
         return CSSD_ERR_DIMS;
     if (!x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
     if (!is_aligned(x, 16) || !is_aligned(B, 16) || !is_aligned(C, 16) || !is_aligned(y, 16) ||

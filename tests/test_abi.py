@@ -89,6 +89,7 @@ def test_argument_errors_are_caught_on_the_host(lib):
     assert _fwd(lib, ok, {"dt": 0x10102}) == -4
     assert _fwd(lib, ok, ws=0x900000, ws_bytes=16) == -5
     assert _fwd(lib, (70000, 64, 1, 16, 16)) == -2  # beyond the grid limit
+    assert _fwd(lib, (60000, 64 * 60000, 1, 16, 16)) == -2  # (batch, head, tile) count beyond 32 bits
     assert _step(lib, None) == -1
     assert _step(lib, (1, 1, 1, 16, 16), {"h": 0}) == -1
     assert _step(lib, (1, 1, 1, 16, 8)) == -3
