@@ -312,7 +312,7 @@ def run_ours(args, rank, world, local):
     roof = {"bound": "hbm", "kernel": "fused_chunk_kernel", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
             "frac": round(achieved / hbm, 4), "peak_kind": peak_kind,
             "traffic": recorded_traffic("fused_chunk_kernel", fwd_units), "kernel_ms": round(k_ms, 5),
-            "alg_bytes_per_launch": alg_bytes}
+            "alg_bytes_per_launch": alg_bytes, "tensor": fused_tensor(fwd_units, N, k_ms)}
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
@@ -639,7 +639,20 @@ def bench_long_seq(args, dev):
             "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4), "steps": n,
             "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel", "achieved": round(gbs, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind, "kernel_ms": round(k_ms, 4),
-                         "alg_bytes_per_launch": alg}}
+                         "alg_bytes_per_launch": alg, "tensor": fused_tensor(units, N, k_ms)}}
+
+
+def fused_tensor(units, dstate, k_ms, passes=1):
+    """Tensor pipe of the fused chunk kernel on its executed MMA work: per 64-token
+    tile, three complex 64x64x64 GEMMs per 64-row state half (chunk state, scores,
+    carried-in readout) and one for the masked scores times X, 8 real flops per
+    complex multiply-add; `passes` = 3 with split-precision operands."""
+    nh = dstate // 64
+    flops = passes * units * (3 * nh + 1) * 64 * 64 * 8
+    tf = flops / (k_ms / 1e3) / 1e12
+    peak, kind = tf32_peak()
+    return {"executed_tflops": round(tf, 1), "peak": round(peak, 1), "peak_kind": kind, "frac": round(tf / peak, 4),
+            "flops_per_launch": flops}
 
 
 def bench_precise(args, dev):
@@ -686,19 +699,14 @@ def bench_precise(args, dev):
     alg = units * (8 * P + 16 * N + 4 + 8 * P)
     hbm, kind = peaks()
     gbs = alg / (k_ms / 1e3) / 1e9
-    # executed tensor work: four complex 64x64x64 GEMMs per 64-token tile, each
-    # taken three times (hi.hi, hi.lo, lo.hi), 8 real flops per complex MAC
-    flops = 3 * units * 4 * 64 * 64 * 8
-    tf = flops / (k_ms / 1e3) / 1e12
-    tpk, tkind = tf32_peak()
+    tensor = fused_tensor(units, N, k_ms, passes=3)  # hi.hi, hi.lo, lo.hi
     return {"workload": f"mamba2_layer Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch}, split-precision forward",
             "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_call": round(ms, 4), "calls": n,
             "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel (split)", "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
                          "traffic": recorded_traffic("fused_chunk_kernel_split", units),
                          "kernel_ms": round(k_ms, 4), "alg_bytes_per_launch": alg},
-            "tensor": {"executed_tflops": round(tf, 1), "peak": round(tpk, 1), "peak_kind": tkind,
-                       "frac": round(tf / tpk, 4), "flops_per_launch": flops}}
+            "tensor": tensor}
 
 
 # ---------------------------------------------------------------- CPU oracle
