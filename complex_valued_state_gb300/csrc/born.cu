@@ -33,7 +33,6 @@ constexpr int BQ = 64;   // queries per CTA
 constexpr int BT = 128;  // threads: one per tensor-memory lane
 constexpr long long kBornWait = 4000000000LL;  // ~2 s at 2 GHz
 
-__device__ int g_born_err;  // bit 0: an MMA completion wait gave up
 
 __device__ __forceinline__ uint32_t kofs(int row, int k, int rows) {
     return (uint32_t)((((k >> 2) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + ((k & 3) << 2));
@@ -72,7 +71,7 @@ struct BornCfg {
 template <int D>
 __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, const float4* __restrict__ k,
                                                   const float4* __restrict__ v, float2* __restrict__ psi, int T,
-                                                  int H, int BH, int nqb) {
+                                                  int H, int BH, int nqb, unsigned* status) {
     using Cfg = BornCfg<D>;
     constexpr int NB = Cfg::NB, IT = Cfg::ITEMS, BK = Cfg::BK;
     extern __shared__ __align__(1024) unsigned char smem[];
@@ -303,7 +302,7 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
             out[m] = make_float2((stage[m] + __uint_as_float(acc[m])) * inv,
                                  (stage[D + m] + __uint_as_float(acc[D + m])) * inv);
     }
-    if (!ok && tid == 0) atomicOr(&g_born_err, 1);
+    if (!ok && tid == 0 && status) atomicOr(status, kStatusBornMma);  // a completion wait gave up
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
@@ -325,7 +324,7 @@ cudaError_t launch_born_d(const BornArgs& a, cudaStream_t st) {
     const int64_t BH = a.Bz * a.H, nqb = (a.T + BQ - 1) / BQ;
     born_kernel<D><<<(unsigned)(BH * nqb), BT, Cfg::SMEM, st>>>(
         reinterpret_cast<const float4*>(a.q), reinterpret_cast<const float4*>(a.k), reinterpret_cast<const float4*>(a.v),
-        a.psi, (int)a.T, (int)a.H, (int)BH, (int)nqb);
+        a.psi, (int)a.T, (int)a.H, (int)BH, (int)nqb, status_word());
     return cudaGetLastError();
 }
 

@@ -5,6 +5,8 @@
 #include <math.h>
 #include <stdint.h>
 
+#include <mutex>
+
 #include "../../include/cssd.h"
 #include "cssd_internal.h"
 
@@ -67,6 +69,33 @@ namespace cssd {
 // forward calls made from this host thread (both NULL = off).
 thread_local cudaEvent_t g_prof_begin = nullptr;
 thread_local cudaEvent_t g_prof_end = nullptr;
+}  // namespace cssd
+
+namespace {
+__device__ unsigned g_status_word;  // one per device that loads the library; starts at 0
+constexpr int kMaxStatusDevices = 128;
+unsigned* g_status_ptr[kMaxStatusDevices] = {};
+std::mutex g_status_mu;
+}  // namespace
+
+namespace cssd {
+unsigned* status_word() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStatusDevices) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lock(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void* q = nullptr;
+        if (cudaGetSymbolAddress(&q, g_status_word) != cudaSuccess) {
+            cudaGetLastError();
+            return nullptr;
+        }
+        g_status_ptr[dev] = static_cast<unsigned*>(q);
+    }
+    return g_status_ptr[dev];
+}
 }  // namespace cssd
 
 namespace {
@@ -175,6 +204,30 @@ int cssd_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cssd_str
         cudaGetLastError();
         return CSSD_ERR_CUDA;
     }
+    return CSSD_OK;
+}
+
+int cssd_device_status(unsigned* bits, int clear, cssd_stream_t stream_) {
+    if (!bits) return CSSD_ERR_NULL;
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    int dev = 0;
+    if (stream_device(stream, &dev) != CSSD_OK) return CSSD_ERR_CUDA;
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess || cur != dev) {
+        cudaGetLastError();
+        return CSSD_ERR_DEVICE;
+    }
+    unsigned* w = cssd::status_word();
+    if (!w) return CSSD_ERR_CUDA;
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, w, sizeof(unsigned), cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess && clear) e = cudaMemsetAsync(w, 0, sizeof(unsigned), stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return CSSD_ERR_CUDA;
+    }
+    *bits = v;
     return CSSD_OK;
 }
 

@@ -60,6 +60,14 @@ struct StepArgs {
     float2* y;
 };
 
+// The library's device status word on the current device (null if its address
+// cannot be had): kernels whose bounded waits give up OR a kStatus* bit into it,
+// and cssd_device_status reads and clears it.
+constexpr unsigned kStatusHandoff = 1u;   // chunk kernel: a state hand-off wait gave up
+constexpr unsigned kStatusChunkMma = 2u;  // chunk kernel: a tensor-core completion wait gave up
+constexpr unsigned kStatusBornMma = 4u;   // Born attention: a tensor-core completion wait gave up
+unsigned* status_word();
+
 // Events the forward records around its dominant kernel (null = off); set by
 // cssd_profile_events for the calling host thread.
 extern thread_local cudaEvent_t g_prof_begin;

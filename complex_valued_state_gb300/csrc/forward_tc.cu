@@ -157,7 +157,8 @@ struct TcParams {
     int* ticket;       // [1]
     float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
     float2* tok;       // [BH][nc][CH] per token: (rho_l, theta_l) within the chunk
-    int* err;          // [1] error bits
+    int* err;          // [1] error bits of this call (workspace)
+    unsigned* status;  // the library's status word (kStatus* bits), or null
     int T, H, BH, nc, NH;
     int first_ticket;       // tickets start here (0 in normal use)
     int pf_dist;            // L2 prefetch distance in tickets (0: none)
@@ -619,9 +620,9 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
                     }
                     __nanosleep(128);
                 }
-                if (late) {
+                if (late) {  // bit 1 / kStatusHandoff; s_bad is for completion waits only
                     atomicOr(p.err, 1);
-                    s_bad = 1;
+                    if (p.status) atomicOr(p.status, kStatusHandoff);
                 }
             } else if (p.h0) {
                 // H_0 is the given initial state: the rotated frame coincides
@@ -772,7 +773,10 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
         }
     }
 
-    if (s_bad && tid == 0) atomicOr(p.err, 2);
+    if (s_bad && tid == 0) {
+        atomicOr(p.err, 2);
+        if (p.status) atomicOr(p.status, kStatusChunkMma);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
@@ -878,6 +882,7 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.nc = (int)nc;
     p.NH = (int)NH;
     p.first_ticket = 0;
+    p.status = status_word();
     p.pf_dist = 0;
     p.wait_cycles = kWaitCycles;
     cudaError_t e = launch_prep(p, a.split_tf32, st);
@@ -963,6 +968,7 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.nc = (int)nc;
     p.NH = 1;
     p.first_ticket = (int)BH;  // chunk 0 of every sequence is never taken
+    p.status = status_word();
     p.pf_dist = 0;
     p.wait_cycles = wait_cycles;
     if (e == cudaSuccess) e = launch_prep(p, false, st);

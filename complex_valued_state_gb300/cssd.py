@@ -36,7 +36,7 @@ EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forwar
            "cssd_host_forward_device_bytes", "cssd_chunked_forward_host",
            "cssd_backward_workspace_bytes", "cssd_chunked_backward",
            "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_cayley_scan", "cssd_born_attention",
-           "cssd_profile_events",
+           "cssd_profile_events", "cssd_device_status",
            "cssd_selftest_handoff_timeout", "cssd_status_string")
 
 # Scratch array size of cssd_chunked_forward_noalloc (bytes).
@@ -97,6 +97,8 @@ def load(path: str = LIB_PATH):
             lib.cssd_chunked_backward.restype = ctypes.c_int
             lib.cssd_born_attention.argtypes = [dims_p] + [vp] * 4 + [vp]
             lib.cssd_born_attention.restype = ctypes.c_int
+            lib.cssd_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint), ctypes.c_int, vp]
+            lib.cssd_device_status.restype = ctypes.c_int
             lib.cssd_profile_events.argtypes = [vp, vp]
             lib.cssd_profile_events.restype = ctypes.c_int
             lib.cssd_selftest_handoff_timeout.argtypes = [ctypes.c_longlong, ctypes.POINTER(ctypes.c_int), vp]
@@ -132,6 +134,24 @@ def _stream_handle(stream, device):
     if stream is None:
         stream = torch.cuda.current_stream(device)
     return ctypes.c_void_p(stream.cuda_stream)
+
+
+# Bits of the device status word (cssd_device_status).
+STATUS_HANDOFF_TIMEOUT = 1
+STATUS_CHUNK_MMA_TIMEOUT = 2
+STATUS_BORN_MMA_TIMEOUT = 4
+
+
+def device_status(clear: bool = False, device=None, stream=None) -> int:
+    """The library's device status word (bits STATUS_*; 0 = no bounded wait has
+    given up), read after the work already on `stream`; cleared when `clear`."""
+    lib = load()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    bits = ctypes.c_uint(0)
+    st = lib.cssd_device_status(ctypes.byref(bits), 1 if clear else 0, _stream_handle(stream, dev))
+    if st != CSSD_OK:
+        raise CssdError(st, "cssd_device_status")
+    return int(bits.value)
 
 
 def profile_events(begin=None, end=None):

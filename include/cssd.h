@@ -23,8 +23,9 @@
  *   - Every array pointer is a DEVICE pointer on the device that `stream`
  *     belongs to (the current device when stream is NULL), except in
  *     cssd_chunked_forward_host, which takes host memory.  The caller owns
- *     all memory; apart from the measurement hook cssd_profile_events the
- *     library keeps no state between calls.
+ *     all memory; apart from the measurement hook cssd_profile_events and the
+ *     device status word (cssd_device_status) the library keeps no state
+ *     between calls.
  *   - Execution is asynchronous on `stream`.  Argument errors are detected on
  *     the host before anything is launched and leave every output untouched.
  *     A launch failure returns CSSD_ERR_CUDA.  Faults during execution surface
@@ -324,6 +325,22 @@ int cssd_chunked_backward(const cssd_dims* dims, const void* x, const float* dt,
  * aligned.  Other D return CSSD_ERR_UNSUPPORTED.  Returns a cssd_status. */
 int cssd_born_attention(const cssd_dims* dims, const void* q, const void* k, const void* v, void* psi,
                         cssd_stream_t stream);
+
+/* Device status word.  Every wait a kernel of this library makes on other
+ * threads or on the tensor cores is bounded; a wait that gives up lets the
+ * kernel finish (its results are then invalid) and ORs a bit into a status word
+ * the library keeps per device:
+ *   1  the chunked forward: a state hand-off from the previous chunk timed out
+ *   2  the chunked forward: a tensor-core completion wait timed out
+ *   4  Born attention: a tensor-core completion wait timed out
+ * The chunked forward's bits also cover cssd_chunked_backward, the precise
+ * and host-streamed forwards, which run the same kernel.  This call reads the
+ * word of the stream's device (which must be the current device) after the
+ * work already on `stream`, clears it when `clear` is nonzero, and waits for
+ * the stream.  The word starts at 0 and is never cleared by the library
+ * itself.  Returns a cssd_status (CSSD_ERR_DEVICE when the stream belongs to
+ * another device). */
+int cssd_device_status(unsigned* bits, int clear, cssd_stream_t stream);
 
 /* Measurement hook.  ev_begin / ev_end are cudaEvent_t handles created by
  * the caller on the device in use; every later cssd_chunked_forward call made

@@ -209,6 +209,10 @@ def test_initial_state_and_host_forward_argument_errors(lib):
     assert lib.cssd_host_forward_device_bytes(ctypes.byref(m), 96, 0) == 0
 
 
+def test_device_status_argument_errors(lib):
+    assert lib.cssd_device_status(None, 0, None) == -1
+
+
 def test_selftest_argument_errors(lib):
     bits = ctypes.c_int(0)
     assert lib.cssd_selftest_handoff_timeout(1000, None, None) == -1

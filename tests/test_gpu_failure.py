@@ -24,8 +24,13 @@ def cs():
 
 
 def test_handoff_wait_gives_up_and_device_stays_usable(cs, oracle_lib):
+    cs.device_status(clear=True)
     bits = cs.selftest_handoff_timeout(wait_cycles=2_000_000)  # about a millisecond
-    assert bits & 1, bits
+    assert bits == 1, bits  # the hand-off timed out; every tensor-core wait completed
+    # the library's status word reports it to any caller, and clears on request
+    assert cs.device_status() == cs.STATUS_HANDOFF_TIMEOUT
+    assert cs.device_status(clear=True) == cs.STATUS_HANDOFF_TIMEOUT
+    assert cs.device_status() == 0
     # the same context still computes correct results
     d = wl.random_case(3, 1, 200, 2, 64, 64)
     g = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "dt", "A", "B", "C", "D")}
@@ -34,3 +39,16 @@ def test_handoff_wait_gives_up_and_device_stays_usable(cs, oracle_lib):
     y_ref, h_ref = oracle_lib.cssd_naive(**d)
     err = np.max(np.abs(y.cpu().numpy() - y_ref)) / np.max(np.abs(y_ref))
     assert err < 2e-3
+
+
+def test_status_word_stays_clear_on_normal_work(cs):
+    cs.device_status(clear=True)
+    d = wl.random_case(4, 2, 300, 3, 64, 64)
+    g = {k: torch.from_numpy(d[k]).cuda() for k in ("x", "dt", "A", "B", "C", "D")}
+    cs.chunked_forward(**g, chunk=64)
+    cs.chunked_forward(**g, chunk=64, precise=True)
+    dy = torch.from_numpy(wl.random_case(5, 2, 300, 3, 64, 64)["x"]).cuda()
+    cs.chunked_backward(**g, dy=dy, chunk=64)
+    bi = wl.make_born_inputs(wl.HTRANSFORMER_ATTN.with_(batch=1, seqlen=200, nheads=2))
+    cs.born_attention(*(torch.from_numpy(bi[k]).cuda() for k in ("q", "k", "v")))
+    assert cs.device_status() == 0
