@@ -49,6 +49,8 @@ def parse():
     ap.add_argument("--no-born", action="store_true", help="skip the causal Born attention measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the gradient (backward) measurement")
     ap.add_argument("--no-precise", action="store_true", help="skip the split-precision forward measurement")
+    ap.add_argument("--long-seqlen", type=int, default=0,
+                    help="tokens of the long_seq forward (default: the workload's 65536; smaller for profiling)")
     return ap.parse_args()
 
 
@@ -152,6 +154,7 @@ class ClockSampler:
 KERNEL_SOURCES = {
     "fused_chunk_kernel": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
     "fused_chunk_kernel_split": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
+    "fused_chunk_kernel_dstate128": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
     "step_kernel": ("step.cu", "cssd_common.cuh"),
     "cayley_scan_kernel": ("cayley.cu", "cssd_common.cuh"),
     "born_kernel": ("born.cu", "tcgen05.cuh", "cssd_common.cuh"),
@@ -599,7 +602,7 @@ def bench_long_seq(args, dev):
     from complex_valued_state_gb300 import cssd
     from complex_valued_state_gb300 import workloads as wl
 
-    w = wl.LONG_SEQ
+    w = wl.LONG_SEQ if args.long_seqlen <= 0 else wl.LONG_SEQ.with_(seqlen=args.long_seqlen)
     host = wl.make_inputs(w)
     g = {k: torch.from_numpy(host[k]).to(dev) for k in ("x", "dt", "A", "B", "C", "D")}
     del host
@@ -639,6 +642,7 @@ def bench_long_seq(args, dev):
             "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4), "steps": n,
             "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel", "achieved": round(gbs, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind, "kernel_ms": round(k_ms, 4),
+                         "traffic": recorded_traffic("fused_chunk_kernel_dstate128", units),
                          "alg_bytes_per_launch": alg, "tensor": fused_tensor(units, N, k_ms)}}
 
 
