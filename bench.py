@@ -740,7 +740,7 @@ def cpu_baseline(host, tok, budget_s: float = 12.0):
         _oracle_step(oracle, arrays, tok_arrays)
         reps += 1
         el = time.perf_counter() - t0
-        if el >= budget_s or reps >= 50:
+        if el >= budget_s or reps >= 100:
             break
     return {"value": round(reps * units / el, 1), "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
             "sample": f"full mamba2_layer step (prefill + 1 decode token) x{reps}, {el:.1f} s"}
