@@ -22,6 +22,8 @@
 // normalisation is a plain sum, so numerator and denominator accumulate in
 // fp32 in tensor memory across all blocks.
 
+#include <atomic>
+
 #include "cssd_common.cuh"
 #include "cssd_internal.h"
 #include "tcgen05.cuh"
@@ -314,12 +316,12 @@ cudaError_t launch_born_d(const BornArgs& a, cudaStream_t st) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
-    static bool attr_set[128] = {};
+    static std::atomic<bool> attr_set[128];  // per device; setting the attribute twice is harmless
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-    if (!attr_set[dev]) {
+    if (!attr_set[dev].load(std::memory_order_relaxed)) {
         e = cudaFuncSetAttribute(born_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
         if (e != cudaSuccess) return e;
-        attr_set[dev] = true;
+        attr_set[dev].store(true, std::memory_order_relaxed);
     }
     const int64_t BH = a.Bz * a.H, nqb = (a.T + BQ - 1) / BQ;
     born_kernel<D><<<(unsigned)(BH * nqb), BT, Cfg::SMEM, st>>>(

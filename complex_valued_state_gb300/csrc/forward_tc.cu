@@ -32,6 +32,7 @@
 // so one M = 128 accumulator holds the real part in TMEM lanes 0-63 and the
 // imaginary part in lanes 64-127.
 
+#include <atomic>
 #include <type_traits>
 
 #include "cssd_common.cuh"
@@ -824,10 +825,13 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     constexpr int SMEM_BYTES = Smem<SPLIT>::BYTES;
     int dev = 0;
     cudaGetDevice(&dev);
-    static bool attr_set[128] = {};
-    static int resident[128] = {};  // CTAs of this kernel resident on the whole device
+    // CTAs of this kernel resident on the whole device, per device; nonzero
+    // once the shared-memory attribute is set (threads that race here both set
+    // the same attribute and store the same count)
+    static std::atomic<int> resident[128];
     const bool cached = dev >= 0 && dev < 128;
-    if (!cached || !attr_set[dev]) {
+    int res = cached ? resident[dev].load(std::memory_order_relaxed) : 0;
+    if (res == 0) {
         cudaError_t e =
             cudaFuncSetAttribute(fused_chunk_kernel<NH, SPLIT, MODES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES);
@@ -838,13 +842,11 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
-        if (cached) {
-            resident[dev] = per_sm * sms;
-            attr_set[dev] = true;
-        }
+        res = per_sm * sms;
+        if (cached) resident[dev].store(res, std::memory_order_relaxed);
     }
     TcParams p = p_in;
-    p.pf_dist = (prefetch && cached) ? resident[dev] / 2 : 0;
+    p.pf_dist = prefetch ? res / 2 : 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
     fused_chunk_kernel<NH, SPLIT, MODES><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
