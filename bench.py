@@ -426,6 +426,28 @@ def bench_const_input(args, dev):
     n = max(20, 5 * args.steps)
     us_n = timed(lambda: cssd.step_n(h, t["x"], t["dt"], A, t["B"], t["C"], D, nsteps, y=y), n)
     us_inf = timed(lambda: cssd.step_infinite(t["x"], t["dt"], A, t["B"], t["C"], D, y=y), n)
+    # the same call replayed from a CUDA graph of `reps` launches: the kernel's own
+    # time, without the per-call host checks (the inputs stay resident in L2)
+    reps = 50
+    side = torch.cuda.Stream(dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        cssd.step_infinite(t["x"], t["dt"], A, t["B"], t["C"], D, y=y)
+    torch.cuda.current_stream(dev).wait_stream(side)
+    torch.cuda.synchronize(dev)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(reps):
+            cssd.step_infinite(t["x"], t["dt"], A, t["B"], t["C"], D, y=y)
+    graph.replay()
+    torch.cuda.synchronize(dev)
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    g0.record(stream)
+    for _ in range(5):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize(dev)
+    us_inf_kernel = g0.elapsed_time(g1) * 1e3 / (5 * reps)
     units = w.batch * w.nheads
     N, P = w.dstate, w.headdim
     alg_n = units * (2 * 8 * N * P + 8 * P + 16 * N + 4 + 8 * P)  # state read+write, x, B, C, dt, y
@@ -439,10 +461,14 @@ def bench_const_input(args, dev):
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs_n / hbm, 4), "peak_kind": kind,
                          "alg_bytes_per_launch": alg_n},
             "infinite": {"us_per_call": round(us_inf, 3), "kernel": "step_infinite_kernel",
-                         "achieved": round(gbs_inf, 1), "unit": "GB/s", "frac": round(gbs_inf / hbm, 4),
+                         "us_per_launch_in_graph": round(us_inf_kernel, 3),
+                         "achieved": round(alg_inf / (us_inf_kernel / 1e6) / 1e9, 1), "unit": "GB/s",
                          "alg_bytes_per_launch": alg_inf,
-                         "note": "back-to-back calls, each with its host argument and pointer checks; the "
-                                 "inputs (%.1f MB) fit in L2" % (alg_inf / 1e6)}}
+                         "note": "us_per_call: back-to-back calls, each with the binding's and the library's "
+                                 "host argument and pointer checks, so the host sets the rate; "
+                                 "us_per_launch_in_graph: %d calls captured in one CUDA graph and replayed; the "
+                                 "inputs (%.1f MB) stay in L2, so achieved is an L2 rate, not an HBM fraction"
+                                 % (reps, alg_inf / 1e6)}}
 
 
 def bench_cayley(args, dev):

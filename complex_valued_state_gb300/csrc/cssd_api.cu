@@ -36,7 +36,7 @@ int check_dims(const cssd_dims* d, bool need_seq) {
 // Device of the stream (or the current device for the default stream).
 int stream_device(cudaStream_t s, int* dev) {
     if (s == nullptr) return cudaGetDevice(dev) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
-    return cudaStreamGetDevice(s, dev) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
+    return cssd::stream_device_of(s, dev) == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
 }
 
 // The pointer must be device (or managed) memory usable on `dev`.

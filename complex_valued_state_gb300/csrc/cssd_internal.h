@@ -10,6 +10,18 @@
 
 namespace cssd {
 
+// Device a stream belongs to, also while the stream is being captured into a
+// CUDA graph: cudaStreamGetDevice is not permitted then, and work captured on
+// a stream runs on the current device, which is what is returned.
+inline cudaError_t stream_device_of(cudaStream_t s, int* dev) {
+    if (s == nullptr) return cudaGetDevice(dev);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &cap);
+    if (e != cudaSuccess) return e;
+    if (cap != cudaStreamCaptureStatusNone) return cudaGetDevice(dev);
+    return cudaStreamGetDevice(s, dev);
+}
+
 // Index and sign modes of a forward run, honoured by the tensor-core path only
 // (the backward runs its adjoint recurrences through them instead of copying
 // reversed or conjugated inputs).

@@ -165,7 +165,7 @@ int cssd_chunked_forward_host(const cssd_dims* d, const void* x, const float* dt
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int dev = 0;
-    if ((stream ? cudaStreamGetDevice(stream, &dev) : cudaGetDevice(&dev)) != cudaSuccess || dev < 0 ||
+    if (cssd::stream_device_of(stream, &dev) != cudaSuccess || dev < 0 ||
         dev >= kMaxDevices) {
         cudaGetLastError();
         return CSSD_ERR_CUDA;

@@ -102,7 +102,7 @@ extern "C" int cssd_chunked_forward_noalloc(const cssd_dims* d, const void* x, c
 
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int dev = 0;
-    if ((stream ? cudaStreamGetDevice(stream, &dev) : cudaGetDevice(&dev)) != cudaSuccess) {
+    if (cssd::stream_device_of(stream, &dev) != cudaSuccess) {
         cudaGetLastError();
         return CSSD_ERR_CUDA;
     }

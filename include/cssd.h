@@ -30,6 +30,13 @@
  *     the host before anything is launched and leave every output untouched.
  *     A launch failure returns CSSD_ERR_CUDA.  Faults during execution surface
  *     at the caller's next synchronisation.  Nothing aborts or traps.
+ *   - CUDA graphs: every device-pointer entry point may be called while
+ *     `stream` is being captured, and the graph's replays then redo the call's
+ *     work on the captured buffers.  Make one call of the same entry point on
+ *     the device before the capture (it fills per-device caches of kernel
+ *     attributes and occupancy), and pass a workspace where the call takes
+ *     one.  cssd_chunked_forward_host, cssd_device_status and
+ *     cssd_selftest_handoff_timeout wait on the host and cannot be captured.
  *   - Alignment: x, B, C, y, h, h_final and the workspace must be 16-byte
  *     aligned; A 8-byte; dt and D 4-byte.
  *   - Supported sizes: dstate N in {16, 32, 64, 128}; headdim P in {16, 32, 64};
