@@ -32,6 +32,8 @@
 // so one M = 128 accumulator holds the real part in TMEM lanes 0-63 and the
 // imaginary part in lanes 64-127.
 
+#include <cuda_fp16.h>
+
 #include <atomic>
 #include <type_traits>
 
@@ -783,6 +785,564 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+// ------------------------------------------------------------------ fp16 operands
+// fused_chunk_kernel_h16: the same tile computation for dstate = headdim = 64
+// (plain forward), with the GEMM operands in IEEE half precision (kind::f16,
+// fp32 accumulation in tensor memory).
+//
+// Precision and range.  A half value has the same 11-bit significand as a
+// TF32 value, so rounding an operand to either costs the same relative error.
+// Its exponent range is narrow, so every operand tile gets a power-of-two scale
+// taken from its largest component: x, B and C of the tile, and the carried-in
+// state H_c, each scaled so that its largest component lies in [1, 2).  The
+// masked scores inherit the scales of C and B (|L o G| <= 64 * 8 = 512).
+// Accumulators hold scaled sums and the epilogues multiply the scales back
+// out, which is exact.  The hand-off cells keep fp32 values in the true scale.
+//
+// Footprint.  Half operands need half the bytes.  A CTA of 256 threads uses
+// 64 KB of shared memory (raw x and B rows staged first, the operands written
+// over them) and 128 tensor-memory columns (two accumulators, each reused:
+// S' then Y_off, G then Y_diag), so three CTAs share an SM.  The TF32 kernel
+// fits two CTAs of 512 threads.
+namespace h16 {
+constexpr int NT = 256;              // threads per CTA
+constexpr int CPT = 32;              // accumulator columns per thread
+constexpr uint32_t RAW_B = 32768;    // raw B rows (raw x rows at 0), 512 bytes per token each
+constexpr uint32_t XP = 0;           // X planes: rows p, K = l (re plane, then im plane)
+constexpr uint32_t STK = 16384;      // F, then Ct, then M: [-Ai; Ar; Ai], 192 rows x K 64
+constexpr uint32_t PL = 40960;       // Bt planes (rows l, K = n), then H planes (rows p, K = n)
+constexpr uint32_t PLANE = 64 * 64 * 2;
+constexpr uint32_t BLK = 1024;       // 64 rows further down a stack
+constexpr int BYTES = 65536;
+constexpr uint32_t COL_A = 0, COL_B = 64, TMEM_COLS = 128;
+constexpr uint32_t STACK_LBO = 24 * 128, PLANE_LBO = 8 * 128, SBO = 128;
+static_assert(STK == XP + 2 * PLANE && PL == STK + 3 * 64 * 64 * 2 && PL + 2 * PLANE <= BYTES, "regions");
+static_assert(2 * CH * STAGE_LD * 4 <= PL, "y staging ends below the H planes");
+}  // namespace h16
+
+// Byte offset of element (row, k) in a K-major, non-swizzled half operand
+// with `rows` rows: 8 x 8 core matrices of 128 bytes.
+__device__ __forceinline__ uint32_t koff16(int row, int k, int rows) {
+    return (uint32_t)((((k >> 3) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + ((k & 7) << 1));
+}
+// Raw rows of this kernel: 16-byte chunk j of token row l at chunk
+// j ^ 2 ((l >> 1) mod 4), so that the transform's reads (eight lanes: four
+// even rows, two neighbouring chunks) fall on eight distinct bank groups.
+__device__ __forceinline__ uint32_t raw_off16(int l, int j) {
+    return (uint32_t)(l * 512 + ((j ^ (((l >> 1) & 3) << 1)) << 4));
+}
+// Two values as a half pair, the first in the low 16 bits (the lower K).
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
+}
+__device__ __forceinline__ void st_u32(unsigned char* base, uint32_t off, uint32_t v) {
+    *reinterpret_cast<uint32_t*>(base + off) = v;
+}
+__device__ __forceinline__ unsigned abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
+__device__ __forceinline__ unsigned max4_bits(float4 v, unsigned m) {
+    return max(max(max(m, abs_bits(v.x)), abs_bits(v.y)), max(abs_bits(v.z), abs_bits(v.w)));
+}
+__device__ __forceinline__ unsigned warp_max(unsigned v) {
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// Scale 2^-e and its inverse 2^e for a tile whose largest component has the
+// fp32 bit pattern `bits` (e its exponent, kept within the normal range).
+struct Pow2 {
+    float s, inv;
+    __device__ __forceinline__ explicit Pow2(unsigned bits) {
+        int e = (int)((bits >> 23) & 0xffu) - 127;
+        e = max(-126, min(126, e));
+        s = __uint_as_float((unsigned)(127 - e) << 23);
+        inv = __uint_as_float((unsigned)(127 + e) << 23);
+    }
+};
+
+__global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p) {
+    constexpr int N = NS, NT = h16::NT, CPT = h16::CPT;
+    constexpr uint32_t RAW_B = h16::RAW_B, XP = h16::XP, STK = h16::STK, PL = h16::PL, PLANE = h16::PLANE;
+    constexpr uint32_t BLK = h16::BLK, COL_A = h16::COL_A, COL_B = h16::COL_B, TMEM_COLS = h16::TMEM_COLS;
+    constexpr uint32_t STACK_LBO = h16::STACK_LBO, PLANE_LBO = h16::PLANE_LBO, SBO = h16::SBO;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ float s_rho[CH];
+    __shared__ float2 s_rot[CH];
+    __shared__ float2 s_rot_last;
+    __shared__ __align__(8) uint64_t mbar[4];  // S, G, OFF, Y
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_ticket;
+    __shared__ int s_bad;
+    __shared__ unsigned s_max[4];  // largest |component| (fp32 bits) of x, B, C, H_c in this tile
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        s_ticket = atomicAdd(p.ticket, 1);
+        s_bad = 0;
+        for (int i = 0; i < 4; ++i) tc::mbar_init(&mbar[i], 1);
+        tc::mbar_fence_init();
+    }
+    if (tid < 4) s_max[tid] = 0u;
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    const int ticket = s_ticket;
+    if (ticket >= p.BH * p.nc) {
+        tc::fence_before_sync();
+        __syncthreads();
+        if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+        return;
+    }
+    const int c = ticket / p.BH, bh = ticket - c * p.BH;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int t0 = c * CH;
+    const long long row0 = ((long long)b * p.T + t0) * p.H + h;  // row of token t0; token l at row0 + l H
+    const long long H = p.H;
+    const uint32_t sb0 = tc::smem_u32(smem);
+
+    // This thread's items: 2 x 2 complex blocks, tokens (l0, l0 + 1) x
+    // columns (n, n + 1) with n = 16 i + 8 g + 2 bq, i < 4 (raw chunk n / 2).
+    // Lanes with g = 1 store the second row of each pair first, so that every
+    // 32-bit operand store of a warp covers 32 distinct banks.
+    const int aq = lane & 3, bq = (lane >> 2) & 3, g = (lane >> 4) & 1;
+    const int l0 = 8 * warp + 2 * aq;
+    const bool swp = g != 0;
+    auto jof = [&](int i) { return 8 * i + 4 * g + bq; };
+
+    // Rows of x, B and C of the tile half a wave of resident CTAs ahead into L2.
+    if (p.pf_dist > 0 && tid < 3 * CH) {
+        const int pt = ticket + p.pf_dist;
+        if (pt < p.BH * p.nc) {
+            const int pc = pt / p.BH, pbh = pt - pc * p.BH;
+            const int tok = pc * CH + (tid & (CH - 1));
+            if (tok < p.T) {
+                const size_t prow = ((size_t)(pbh / p.H) * p.T + tok) * p.H + pbh % p.H;
+                const int which = tid / CH;  // 0: x, 1: B, 2: C
+                if (which == 0) prefetch_l2(p.x + prow * (PD / 2), PD * 8);
+                else prefetch_l2((which == 1 ? p.B : p.C) + prow * (N / 2), N * 8);
+            }
+        }
+    }
+
+    // ---- 0. loads: dt tables, raw x and B rows by cp.async (warp w copies
+    // rows w + 8 r, one 16-byte chunk per lane), C into registers.
+    float2 tk = make_float2(0.f, 0.f);
+    float phi_c = 0.f;
+    if (tid < CH) {
+        tk = __ldcg(p.tok + ((size_t)bh * p.nc + c) * CH + tid);
+        phi_c = __ldcg(p.phi + (size_t)bh * p.nc + c);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        const int lr = warp + 8 * r;
+        const bool ok = t0 + lr < p.T;
+        const long long grow = row0 + (long long)lr * H;
+        const float4* gx = p.x + (ok ? grow * (PD / 2) + lane : 0);
+        const float4* gb = p.B + (ok ? grow * (N / 2) + lane : 0);
+        cp_async16(sb0 + raw_off16(lr, lane), gx, ok);
+        cp_async16(sb0 + RAW_B + raw_off16(lr, lane), gb, ok);
+    }
+    cp_async_commit();
+    float4 cv[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const int l = l0 + rr;
+            cv[i][rr] = (t0 + l < p.T) ? __ldg(p.C + (row0 + (long long)l * H) * (N / 2) + jof(i))
+                                       : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+
+    // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
+    if (tid < CH) {
+        float sn, cs;
+        sincosf(phi_c + tk.y, &sn, &cs);
+        s_rho[tid] = tk.x;
+        s_rot[tid] = make_float2(cs, sn);
+        if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
+    }
+    cp_async_wait_all();
+    __syncthreads();
+    const float rho_end = s_rho[CH - 1];
+    const float eend = __expf(rho_end);
+
+    const uint32_t ID = tc::idesc_f16(128, 64);
+    // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`;
+    // one MMA takes K = 16, so the start address steps by two core matrices.
+    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs) {
+        const uint64_t a_up = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
+        const uint64_t a_dn = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
+        const uint64_t b_re = tc::make_desc(bs, PLANE_LBO, SBO);
+        const uint64_t b_im = tc::make_desc(bs + PLANE, PLANE_LBO, SBO);
+        constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4, B_STEP = (2 * PLANE_LBO) >> 4;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            tc::mma_f16(d, a_up + ks * A_STEP, b_re + ks * B_STEP, ID, ks > 0 ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) tc::mma_f16(d, a_dn + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
+    };
+    auto issue = [&](uint32_t d, uint32_t as, uint32_t bs, uint64_t* bar) {
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        __syncthreads();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            cgemm(d, as, bs);
+            tc::commit(bar);
+        }
+    };
+    auto wait_bar = [&](uint64_t* bar) {
+        if (!tc::mbar_wait_bounded(bar, 0, kWaitCycles)) s_bad = 1;
+    };
+    constexpr uint32_t NEG2 = 0x80008000u;  // sign bits of a half pair
+
+    // ---- 2. X planes over raw x (rows p, K = l), scaled; the scales of x and
+    // C; Ct = e^{i Theta} C as scaled half pairs in registers.
+    uint32_t cw[4][2][2];  // [item][row l0 + rr][re, im]: columns (n, n + 1)
+    float inv_x, inv_c;
+    {
+        float4 xv[4][2];
+        unsigned mx = 0u, mc = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                xv[i][rr] = *reinterpret_cast<const float4*>(smem + raw_off16(l0 + rr, jof(i)));
+                mx = max4_bits(xv[i][rr], mx);
+                mc = max4_bits(cv[i][rr], mc);
+            }
+        mx = warp_max(mx);
+        mc = warp_max(mc);
+        if (lane == 0) {
+            atomicMax(&s_max[0], mx);
+            atomicMax(&s_max[2], mc);
+        }
+        __syncthreads();  // raw x is overwritten below; the maxima are complete
+        const Pow2 sx(s_max[0]), sc(s_max[2]);
+        inv_x = sx.inv;
+        inv_c = sc.inv;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int n = 16 * i + 8 * g + 2 * bq;
+            const uint32_t oa = XP + koff16(n, l0, 64), ob = XP + koff16(n + 1, l0, 64);
+            const float4 u = xv[i][0], w = xv[i][1];  // tokens l0, l0 + 1
+            const uint32_t ra = pack_h2(u.x * sx.s, w.x * sx.s), rb = pack_h2(u.z * sx.s, w.z * sx.s);
+            const uint32_t ia = pack_h2(u.y * sx.s, w.y * sx.s), ib = pack_h2(u.w * sx.s, w.w * sx.s);
+            st_u32(smem, swp ? ob : oa, swp ? rb : ra);
+            st_u32(smem, swp ? oa : ob, swp ? ra : rb);
+            st_u32(smem + PLANE, swp ? ob : oa, swp ? ib : ia);
+            st_u32(smem + PLANE, swp ? oa : ob, swp ? ia : ib);
+        }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const float2 rot = s_rot[l0 + rr];
+            const float s = sc.s;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const float4 v = cv[i][rr];
+                const float c0r = rot.x * v.x - rot.y * v.y, c0i = rot.x * v.y + rot.y * v.x;
+                const float c1r = rot.x * v.z - rot.y * v.w, c1i = rot.x * v.w + rot.y * v.z;
+                cw[i][rr][0] = pack_h2(c0r * s, c1r * s);
+                cw[i][rr][1] = pack_h2(c0i * s, c1i * s);
+            }
+        }
+    }
+
+    // ---- 3. Bt planes (rows l, K = n) and the F stack (rows n, K = l) over
+    // raw B, scaled by B's scale; S' = F X.
+    float inv_b;
+    {
+        float4 bv[4][2];
+        unsigned mb = 0u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                bv[i][rr] = *reinterpret_cast<const float4*>(smem + RAW_B + raw_off16(l0 + rr, jof(i)));
+                mb = max4_bits(bv[i][rr], mb);
+            }
+        mb = warp_max(mb);
+        if (lane == 0) atomicMax(&s_max[1], mb);
+        __syncthreads();  // raw B is overwritten below
+        const Pow2 sbk(s_max[1]);
+        inv_b = sbk.inv;
+        const float s = sbk.s;
+        const float ds0 = __expf(rho_end - s_rho[l0]) * s, ds1 = __expf(rho_end - s_rho[l0 + 1]) * s;
+        const float2 r0 = s_rot[l0], r1 = s_rot[l0 + 1];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int n = 16 * i + 8 * g + 2 * bq;
+            const float4 u = bv[i][0], w = bv[i][1];
+            // Bt = e^{-i Theta} B at (l0, n), (l0, n + 1), (l0 + 1, n), (l0 + 1, n + 1)
+            const float u0r = r0.x * u.x + r0.y * u.y, u0i = r0.x * u.y - r0.y * u.x;
+            const float u1r = r0.x * u.z + r0.y * u.w, u1i = r0.x * u.w - r0.y * u.z;
+            const float w0r = r1.x * w.x + r1.y * w.y, w0i = r1.x * w.y - r1.y * w.x;
+            const float w1r = r1.x * w.z + r1.y * w.w, w1i = r1.x * w.w - r1.y * w.z;
+            {
+                const uint32_t oa = PL + koff16(l0, n, 64), ob = PL + koff16(l0 + 1, n, 64);
+                const uint32_t ra = pack_h2(u0r * s, u1r * s), rb = pack_h2(w0r * s, w1r * s);
+                const uint32_t ia = pack_h2(u0i * s, u1i * s), ib = pack_h2(w0i * s, w1i * s);
+                st_u32(smem, swp ? ob : oa, swp ? rb : ra);
+                st_u32(smem, swp ? oa : ob, swp ? ra : rb);
+                st_u32(smem + PLANE, swp ? ob : oa, swp ? ib : ia);
+                st_u32(smem + PLANE, swp ? oa : ob, swp ? ia : ib);
+            }
+            {
+                // F[n][l] = exp(rho_end - rho_l) Bt[l][n]; row n holds K = (l0, l0 + 1)
+                const uint32_t oa = STK + koff16(n, l0, 192), ob = STK + koff16(n + 1, l0, 192);
+                const uint32_t ra = pack_h2(u0r * ds0, w0r * ds1), rb = pack_h2(u1r * ds0, w1r * ds1);
+                const uint32_t ia = pack_h2(u0i * ds0, w0i * ds1), ib = pack_h2(u1i * ds0, w1i * ds1);
+                const uint32_t o1 = swp ? ob : oa, o2 = swp ? oa : ob;
+                const uint32_t r1w = swp ? rb : ra, r2w = swp ? ra : rb, i1w = swp ? ib : ia, i2w = swp ? ia : ib;
+                st_u32(smem, o1, i1w ^ NEG2);
+                st_u32(smem, o2, i2w ^ NEG2);
+                st_u32(smem, o1 + BLK, r1w);
+                st_u32(smem, o2 + BLK, r2w);
+                st_u32(smem, o1 + 2 * BLK, i1w);
+                st_u32(smem, o2 + 2 * BLK, i2w);
+            }
+        }
+    }
+    issue(tmem + COL_A, sb0 + STK, sb0 + XP, &mbar[0]);
+
+    // ---- 4. Ct stack (rows l, K = n) over F once S' has read it; G = Ct Bt^T
+    wait_bar(&mbar[0]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int n = 16 * i + 8 * g + 2 * bq;
+        const uint32_t oa = STK + koff16(l0, n, 192), ob = STK + koff16(l0 + 1, n, 192);
+        const uint32_t o1 = swp ? ob : oa, o2 = swp ? oa : ob;
+        const uint32_t r1w = swp ? cw[i][1][0] : cw[i][0][0], r2w = swp ? cw[i][0][0] : cw[i][1][0];
+        const uint32_t i1w = swp ? cw[i][1][1] : cw[i][0][1], i2w = swp ? cw[i][0][1] : cw[i][1][1];
+        st_u32(smem, o1, i1w ^ NEG2);
+        st_u32(smem, o2, i2w ^ NEG2);
+        st_u32(smem, o1 + BLK, r1w);
+        st_u32(smem, o2 + BLK, r2w);
+        st_u32(smem, o1 + 2 * BLK, i1w);
+        st_u32(smem, o2 + 2 * BLK, i2w);
+    }
+    issue(tmem + COL_B, sb0 + STK, sb0 + PL, &mbar[1]);
+
+    // ---- 5. hand-off: the thread owns state row lrow of part `part` and the
+    // CPT columns from c0col of S'; it takes H_c from the cells the same thread
+    // position of chunk c-1 wrote and publishes H_{c+1} = e^{rho_end} H_c + S'
+    // in the true scale.
+    const int q = warp & 3, cblk = warp >> 2;
+    const int L = q * 32 + lane;
+    const int part = L >> 6, lrow = L & 63;
+    const int c0col = cblk * CPT;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+    float hv[CPT];
+    {
+        const size_t ring0 = (size_t)bh * RING;
+        const unsigned long long* cin =
+            p.ring + (ring0 + (c % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
+        unsigned long long* cout = p.ring + (ring0 + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
+        if (c > 0) {
+            const uint32_t want = (uint32_t)c;
+            const long long w0 = clock64();
+            if (lane == 0) {
+                while ((uint32_t)(ld_cell(cin + c0col * NS) >> 32) != want) {
+                    if (clock64() - w0 > p.wait_cycles) break;
+                    __nanosleep(128);
+                }
+            }
+            __syncwarp();
+            bool late = false;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                while (true) {
+                    // all 16 loads are issued before any tag is examined
+                    unsigned long long w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) w[j] = ld_cell(cin + (c0col + 16 * half + j) * NS);
+                    bool all = true;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        hv[16 * half + j] = __uint_as_float((uint32_t)w[j]);
+                        all = all && ((uint32_t)(w[j] >> 32) == want);
+                    }
+                    if (all) break;
+                    if (clock64() - w0 > p.wait_cycles) {
+                        late = true;
+                        break;
+                    }
+                    __nanosleep(128);
+                }
+            }
+            if (late) {
+                atomicOr(p.err, 1);
+                if (p.status) atomicOr(p.status, kStatusHandoff);
+            }
+        } else if (p.h0) {
+            const float* src = reinterpret_cast<const float*>(p.h0 + ((size_t)bh * N + lrow) * PD + c0col) + part;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) hv[j] = __ldg(src + 2 * j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) hv[j] = 0.f;
+        }
+        uint32_t r[CPT];
+        tc::fence_after_sync();
+        tc::tmem_ld16(tmem + lane_base + COL_A + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tc::tmem_ld16(tmem + lane_base + COL_A + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tc::tmem_wait_ld();
+        const uint32_t tag = (uint32_t)(c + 1);
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const float sv = __uint_as_float(r[j]) * inv_b * inv_x;
+            st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], sv), tag);
+        }
+        unsigned mh = 0u;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) mh = max(mh, abs_bits(hv[j]));
+        mh = warp_max(mh);
+        if (lane == 0) atomicMax(&s_max[3], mh);
+    }
+    tc::fence_before_sync();
+    __syncthreads();  // the scale of H_c is complete
+    const Pow2 shc(s_max[3]);
+    const float inv_h = shc.inv;
+
+    // ---- 6. H_c as the B operand of Y_off (rows p, K = n) over the Bt planes
+    // once G has read them.  A butterfly of shuffles transposes each warp's
+    // 32 (n) x 32 (p) block so that each lane owns one p and 32 consecutive n.
+    {
+#pragma unroll
+        for (int sbit = CPT / 2; sbit >= 1; sbit >>= 1) {
+            const bool upper = (lane & sbit) != 0;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) {
+                if ((j & sbit) == 0) {
+                    const float send = upper ? hv[j] : hv[j | sbit];
+                    const float recv = __shfl_xor_sync(0xffffffffu, send, sbit);
+                    if (upper) hv[j] = recv;
+                    else hv[j | sbit] = recv;
+                }
+            }
+        }
+        // now hv[j] = H_part[nb + j][c0col + lane]
+        const int nb = lrow - lane;
+        const float s = shc.s;
+        wait_bar(&mbar[1]);
+        unsigned char* plane = smem + PL + part * PLANE + koff16(c0col + lane, nb, 64);
+#pragma unroll
+        for (int k8 = 0; k8 < CPT / 8; ++k8) {  // K = nb + 8 k8: one core matrix (8 row groups) further per step
+            const uint4 v = make_uint4(pack_h2(hv[8 * k8] * s, hv[8 * k8 + 1] * s),
+                                       pack_h2(hv[8 * k8 + 2] * s, hv[8 * k8 + 3] * s),
+                                       pack_h2(hv[8 * k8 + 4] * s, hv[8 * k8 + 5] * s),
+                                       pack_h2(hv[8 * k8 + 6] * s, hv[8 * k8 + 7] * s));
+            *reinterpret_cast<uint4*>(plane + 1024 * k8) = v;
+        }
+    }
+    issue(tmem + COL_A, sb0 + STK, sb0 + PL, &mbar[2]);  // Y_off' = Ct H_c, over S'
+
+    // ---- 7. masked scores M = L o G (scaled like G) over Ct once Y_off has
+    // read it; Y_diag = M X over G.
+    {
+        uint32_t r[CPT];
+        tc::fence_after_sync();
+        tc::tmem_ld16(tmem + lane_base + COL_B + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tc::tmem_ld16(tmem + lane_base + COL_B + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tc::tmem_wait_ld();
+        const float rl = s_rho[lrow];
+        float m[CPT];
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+            const int sidx = c0col + j;
+            const float arg = (sidx <= lrow) ? rl - s_rho[sidx] : -INFINITY;
+            m[j] = __expf(arg) * __uint_as_float(r[j]);
+        }
+        wait_bar(&mbar[2]);
+        // 16-byte stores: eight consecutive K of one row fill one core-matrix
+        // row; K + 8 is one core matrix (24 row groups) further
+        unsigned char* mrow = smem + STK + koff16(lrow, c0col, 192);
+#pragma unroll
+        for (int k8 = 0; k8 < CPT / 8; ++k8) {
+            const uint4 v = make_uint4(pack_h2(m[8 * k8], m[8 * k8 + 1]), pack_h2(m[8 * k8 + 2], m[8 * k8 + 3]),
+                                       pack_h2(m[8 * k8 + 4], m[8 * k8 + 5]), pack_h2(m[8 * k8 + 6], m[8 * k8 + 7]));
+            if (part == 0) {
+                *reinterpret_cast<uint4*>(mrow + BLK + 3072 * k8) = v;
+            } else {
+                *reinterpret_cast<uint4*>(mrow + 2 * BLK + 3072 * k8) = v;
+                *reinterpret_cast<uint4*>(mrow + 3072 * k8) = make_uint4(v.x ^ NEG2, v.y ^ NEG2, v.z ^ NEG2, v.w ^ NEG2);
+            }
+        }
+    }
+    issue(tmem + COL_B, sb0 + STK, sb0 + XP, &mbar[3]);
+
+    // ---- 8. y = Y_diag + e^{rho_l} Y_off' + D x with the scales taken out.
+    // The skip term uses the exact fp32 input (an L2 hit, fetched while Y_diag
+    // runs).  The staging planes lie over the X planes and the stack, which
+    // Y_diag has finished reading.
+    constexpr int YI = CH * PD / NT;  // output elements per thread: rows ly + 4 k, column py
+    const int ly = tid >> 6, py = tid & 63;
+    const long long ystep = 4 * H * PD;
+    const long long yoff = (row0 + (long long)ly * H) * PD + py;
+    float2 xs[YI];
+#pragma unroll
+    for (int k = 0; k < YI; ++k)
+        xs[k] = (t0 + ly + 4 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
+                                        : make_float2(0.f, 0.f);
+    {
+        wait_bar(&mbar[3]);
+        tc::fence_after_sync();
+        const float el = __expf(s_rho[lrow]);
+        float* stage = reinterpret_cast<float*>(smem) + part * CH * STAGE_LD + lrow * STAGE_LD + c0col;
+#pragma unroll
+        for (int hh = 0; hh < CPT / 16; ++hh) {
+            uint32_t ry[16], ro[16];
+            tc::tmem_ld16(tmem + lane_base + COL_B + c0col + 16 * hh, ry);
+            tc::tmem_ld16(tmem + lane_base + COL_A + c0col + 16 * hh, ro);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float yd = __uint_as_float(ry[j]) * inv_c * inv_b * inv_x;
+                const float yo = __uint_as_float(ro[j]) * inv_c * inv_h;
+                stage[16 * hh + j] = fmaf(el, yo, yd);
+            }
+        }
+    }
+    __syncthreads();
+    {
+        const float Dh = p.D[h];
+        const float* stage = reinterpret_cast<const float*>(smem) + ly * STAGE_LD + py;
+#pragma unroll
+        for (int k = 0; k < YI; ++k) {
+            if (t0 + ly + 4 * k < p.T) {
+                const float yr = stage[4 * k * STAGE_LD], yi = stage[CH * STAGE_LD + 4 * k * STAGE_LD];
+                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
+            }
+        }
+    }
+
+    // ---- 9. final state of the sequence, rotated back to the original frame
+    if (c == p.nc - 1 && p.h_final) {
+        const float cs = s_rot_last.x, sn = s_rot_last.y;
+        for (int i = tid; i < N * PD; i += NT) {
+            const int n = i >> 6, pp = i & 63;
+            const unsigned long long* cell =
+                p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)pp * NS + n;
+            const float hr = __uint_as_float((uint32_t)ld_cell(cell));
+            const float hi = __uint_as_float((uint32_t)ld_cell(cell + PD * NS));
+            p.h_final[(size_t)bh * N * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
+        }
+    }
+
+    if (s_bad && tid == 0) {
+        atomicOr(p.err, 2);
+        if (p.status) atomicOr(p.status, kStatusChunkMma);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
 }  // namespace
 
 // The tensor-core kernel runs 64-token tiles with headdim 64 and dstate 64 or
@@ -854,6 +1414,37 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     return e;
 }
 
+// The half-operand kernel: three CTAs per SM by shared memory, each holding
+// 128 tensor-memory columns, so every resident CTA finds its columns free.
+static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStream_t st) {
+    constexpr int SMEM_BYTES = h16::BYTES;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static std::atomic<int> resident[128];
+    const bool cached = dev >= 0 && dev < 128;
+    int res = cached ? resident[dev].load(std::memory_order_relaxed) : 0;
+    if (res == 0) {
+        cudaError_t e =
+            cudaFuncSetAttribute(fused_chunk_kernel_h16, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        int per_sm = 0, sms = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel_h16, h16::NT, SMEM_BYTES);
+        if (e != cudaSuccess) return e;
+        if (per_sm * (int)h16::TMEM_COLS > 512) return cudaErrorNotSupported;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        res = per_sm * sms;
+        if (cached) resident[dev].store(res, std::memory_order_relaxed);
+    }
+    TcParams p = p_in;
+    p.pf_dist = res / 2;
+    if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
+    fused_chunk_kernel_h16<<<(unsigned)tiles, h16::NT, SMEM_BYTES, st>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (g_prof_end) cudaEventRecord(g_prof_end, st);
+    return e;
+}
+
 cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     TcParams p;
     const int64_t BH = a.Bz * a.H, nc = (a.T + CH - 1) / CH, NH = a.N / NS;
@@ -900,8 +1491,7 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
                             : launch_fused<1, false, true>(p, BH * nc, true, st);
     }
     if (a.split_tf32) return NH == 1 ? launch_fused<1, true, false>(p, BH * nc, true, st) : cudaErrorNotSupported;
-    return NH == 1 ? launch_fused<1, false, false>(p, BH * nc, true, st)
-                   : launch_fused<2, false, false>(p, BH * nc, true, st);
+    return NH == 1 ? launch_fused_h16(p, BH * nc, st) : launch_fused<2, false, false>(p, BH * nc, true, st);
 }
 
 // Failure-detection self-test: a two-sequence, two-chunk forward whose

@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the sm_100-family tensor-core path used by the
-// chunk kernels: tcgen05.mma (kind::tf32, one CTA), tensor-memory allocation
+// chunk kernels: tcgen05.mma (kind::tf32 and kind::f16, one CTA), tensor-memory allocation
 // and loads, mbarrier completion, and the shared-memory matrix descriptor for
 // the K-major, non-swizzled canonical layout.
 //
@@ -36,6 +36,24 @@ __device__ __forceinline__ uint64_t make_desc(uint32_t saddr, uint32_t lbo, uint
 __host__ __device__ constexpr uint32_t idesc_tf32(int M, int N, bool neg_a = false, bool neg_b = false) {
     return (1u << 4) | (2u << 7) | (2u << 10) | ((neg_a ? 1u : 0u) << 13) | ((neg_b ? 1u : 0u) << 14) |
            (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Instruction descriptor, kind::f16 with IEEE half operands: D fp32, A and B
+// f16 (format 0), both K-major, dense, shape M x N.  With 16-bit elements a
+// core matrix row of 16 bytes holds 8 K values and one MMA consumes K = 16
+// (again two column groups).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N) {
+    return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// D[tmem] (+)= A[smem] * B[smem]^T with half operands, issued by one thread.
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
 }
 
 // D[tmem] (+)= A[smem] * B[smem]^T, issued by one thread.
