@@ -839,9 +839,14 @@ __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
 __device__ __forceinline__ void st_u32(unsigned char* base, uint32_t off, uint32_t v) {
     *reinterpret_cast<uint32_t*>(base + off) = v;
 }
-__device__ __forceinline__ unsigned abs_bits(float v) { return __float_as_uint(v) & 0x7fffffffu; }
-__device__ __forceinline__ unsigned max4_bits(float4 v, unsigned m) {
-    return max(max(max(m, abs_bits(v.x)), abs_bits(v.y)), max(abs_bits(v.z), abs_bits(v.w)));
+__device__ __forceinline__ float maxabs4(float4 v, float m) {
+    return fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+}
+// 2^x for x <= 0 by the hardware's approximate base-2 exponential.
+__device__ __forceinline__ float ex2_approx(float x) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+    return r;
 }
 __device__ __forceinline__ unsigned warp_max(unsigned v) {
 #pragma unroll
@@ -867,6 +872,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     constexpr uint32_t STACK_LBO = h16::STACK_LBO, PLANE_LBO = h16::PLANE_LBO, SBO = h16::SBO;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ float s_rho[CH];
+    __shared__ __align__(16) float s_rho2[CH];  // rho_l log2(e)
     __shared__ float2 s_rot[CH];
     __shared__ float2 s_rot_last;
     __shared__ __align__(8) uint64_t mbar[4];  // S, G, OFF, Y
@@ -963,6 +969,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         float sn, cs;
         sincosf(phi_c + tk.y, &sn, &cs);
         s_rho[tid] = tk.x;
+        s_rho2[tid] = tk.x * 1.4426950408889634f;
         s_rot[tid] = make_float2(cs, sn);
         if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
     }
@@ -1007,17 +1014,16 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     float inv_x, inv_c;
     {
         float4 xv[4][2];
-        unsigned mx = 0u, mc = 0u;
+        float fx = 0.f, fc = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 xv[i][rr] = *reinterpret_cast<const float4*>(smem + raw_off16(l0 + rr, jof(i)));
-                mx = max4_bits(xv[i][rr], mx);
-                mc = max4_bits(cv[i][rr], mc);
+                fx = maxabs4(xv[i][rr], fx);
+                fc = maxabs4(cv[i][rr], fc);
             }
-        mx = warp_max(mx);
-        mc = warp_max(mc);
+        const unsigned mx = warp_max(__float_as_uint(fx)), mc = warp_max(__float_as_uint(fc));
         if (lane == 0) {
             atomicMax(&s_max[0], mx);
             atomicMax(&s_max[2], mc);
@@ -1040,15 +1046,15 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         }
 #pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
-            const float2 rot = s_rot[l0 + rr];
-            const float s = sc.s;
+            const float2 r0 = s_rot[l0 + rr];
+            const float2 rot = make_float2(r0.x * sc.s, r0.y * sc.s);  // the rotation with C's scale
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const float4 v = cv[i][rr];
                 const float c0r = rot.x * v.x - rot.y * v.y, c0i = rot.x * v.y + rot.y * v.x;
                 const float c1r = rot.x * v.z - rot.y * v.w, c1i = rot.x * v.w + rot.y * v.z;
-                cw[i][rr][0] = pack_h2(c0r * s, c1r * s);
-                cw[i][rr][1] = pack_h2(c0i * s, c1i * s);
+                cw[i][rr][0] = pack_h2(c0r, c1r);
+                cw[i][rr][1] = pack_h2(c0i, c1i);
             }
         }
     }
@@ -1058,22 +1064,23 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     float inv_b;
     {
         float4 bv[4][2];
-        unsigned mb = 0u;
+        float fb = 0.f;
 #pragma unroll
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
                 bv[i][rr] = *reinterpret_cast<const float4*>(smem + RAW_B + raw_off16(l0 + rr, jof(i)));
-                mb = max4_bits(bv[i][rr], mb);
+                fb = maxabs4(bv[i][rr], fb);
             }
-        mb = warp_max(mb);
+        const unsigned mb = warp_max(__float_as_uint(fb));
         if (lane == 0) atomicMax(&s_max[1], mb);
         __syncthreads();  // raw B is overwritten below
         const Pow2 sbk(s_max[1]);
         inv_b = sbk.inv;
-        const float s = sbk.s;
-        const float ds0 = __expf(rho_end - s_rho[l0]) * s, ds1 = __expf(rho_end - s_rho[l0 + 1]) * s;
-        const float2 r0 = s_rot[l0], r1 = s_rot[l0 + 1];
+        // rotations with B's scale: the Bt values below are scaled
+        const float ds0 = __expf(rho_end - s_rho[l0]), ds1 = __expf(rho_end - s_rho[l0 + 1]);
+        const float2 q0 = s_rot[l0], q1 = s_rot[l0 + 1];
+        const float2 r0 = make_float2(q0.x * sbk.s, q0.y * sbk.s), r1 = make_float2(q1.x * sbk.s, q1.y * sbk.s);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const int n = 16 * i + 8 * g + 2 * bq;
@@ -1085,8 +1092,8 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
             const float w1r = r1.x * w.z + r1.y * w.w, w1i = r1.x * w.w - r1.y * w.z;
             {
                 const uint32_t oa = PL + koff16(l0, n, 64), ob = PL + koff16(l0 + 1, n, 64);
-                const uint32_t ra = pack_h2(u0r * s, u1r * s), rb = pack_h2(w0r * s, w1r * s);
-                const uint32_t ia = pack_h2(u0i * s, u1i * s), ib = pack_h2(w0i * s, w1i * s);
+                const uint32_t ra = pack_h2(u0r, u1r), rb = pack_h2(w0r, w1r);
+                const uint32_t ia = pack_h2(u0i, u1i), ib = pack_h2(w0i, w1i);
                 st_u32(smem, swp ? ob : oa, swp ? rb : ra);
                 st_u32(smem, swp ? oa : ob, swp ? ra : rb);
                 st_u32(smem + PLANE, swp ? ob : oa, swp ? ib : ia);
@@ -1193,15 +1200,13 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         tc::tmem_ld16(tmem + lane_base + COL_A + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
         tc::tmem_wait_ld();
         const uint32_t tag = (uint32_t)(c + 1);
+        const float k_s = inv_b * inv_x;  // a product of powers of two: exact
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-            const float sv = __uint_as_float(r[j]) * inv_b * inv_x;
-            st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], sv), tag);
-        }
-        unsigned mh = 0u;
+        for (int j = 0; j < CPT; ++j) st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j]) * k_s), tag);
+        float fh = 0.f;
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) mh = max(mh, abs_bits(hv[j]));
-        mh = warp_max(mh);
+        for (int j = 0; j < CPT; ++j) fh = fmaxf(fh, fabsf(hv[j]));
+        const unsigned mh = warp_max(__float_as_uint(fh));
         if (lane == 0) atomicMax(&s_max[3], mh);
     }
     tc::fence_before_sync();
@@ -1245,18 +1250,32 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // ---- 7. masked scores M = L o G (scaled like G) over Ct once Y_off has
     // read it; Y_diag = M X over G.
     {
-        uint32_t r[CPT];
-        tc::fence_after_sync();
-        tc::tmem_ld16(tmem + lane_base + COL_B + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tc::tmem_ld16(tmem + lane_base + COL_B + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-        tc::tmem_wait_ld();
-        const float rl = s_rho[lrow];
         float m[CPT];
+        // a warp whose rows all precede its columns holds only masked scores
+        const bool all_masked = c0col > (lrow | 31);
+        if (all_masked) {
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) {
-            const int sidx = c0col + j;
-            const float arg = (sidx <= lrow) ? rl - s_rho[sidx] : -INFINITY;
-            m[j] = __expf(arg) * __uint_as_float(r[j]);
+            for (int j = 0; j < CPT; ++j) m[j] = 0.f;
+        } else {
+            uint32_t r[CPT];
+            tc::fence_after_sync();
+            tc::tmem_ld16(tmem + lane_base + COL_B + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+            tc::tmem_ld16(tmem + lane_base + COL_B + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+            tc::tmem_wait_ld();
+            const float rl2 = s_rho2[lrow];
+            const float4* rs = reinterpret_cast<const float4*>(s_rho2 + c0col);
+#pragma unroll
+            for (int j4 = 0; j4 < CPT / 4; ++j4) {
+                const float4 r4 = rs[j4];
+                const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = 4 * j4 + u;
+                    // causal mask as 2^-inf = 0: a select, not a branch around the exponential
+                    const float arg = (c0col + j <= lrow) ? rl2 - rv[u] : -INFINITY;
+                    m[j] = ex2_approx(arg) * __uint_as_float(r[j]);
+                }
+            }
         }
         wait_bar(&mbar[2]);
         // 16-byte stores: eight consecutive K of one row fill one core-matrix
@@ -1292,7 +1311,9 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     {
         wait_bar(&mbar[3]);
         tc::fence_after_sync();
-        const float el = __expf(s_rho[lrow]);
+        // exact products of powers of two; the row decay joins the second
+        const float k_d = inv_c * inv_b * inv_x;
+        const float k_o = __expf(s_rho[lrow]) * (inv_c * inv_h);
         float* stage = reinterpret_cast<float*>(smem) + part * CH * STAGE_LD + lrow * STAGE_LD + c0col;
 #pragma unroll
         for (int hh = 0; hh < CPT / 16; ++hh) {
@@ -1301,11 +1322,8 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
             tc::tmem_ld16(tmem + lane_base + COL_A + c0col + 16 * hh, ro);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                const float yd = __uint_as_float(ry[j]) * inv_c * inv_b * inv_x;
-                const float yo = __uint_as_float(ro[j]) * inv_c * inv_h;
-                stage[16 * hh + j] = fmaf(el, yo, yd);
-            }
+            for (int j = 0; j < 16; ++j)
+                stage[16 * hh + j] = fmaf(k_o, __uint_as_float(ro[j]), __uint_as_float(ry[j]) * k_d);
         }
     }
     __syncthreads();
