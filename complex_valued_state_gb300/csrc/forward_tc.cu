@@ -359,6 +359,8 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     const long long rstride = rev ? -(long long)p.H : (long long)p.H;
     const bool cj_x = (mode & kFwdConjX) != 0, cj_b = (mode & kFwdConjB) != 0, cj_c = (mode & kFwdConjC) != 0;
     const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
+    const bool skip = !MODES || p.D != nullptr;
+    const float Dh = skip ? __ldg(p.D + h) : 0.f;  // skip coefficient, needed only at the end: fetched now
 
     // This thread's items of a 64 x 64 complex tile: the column pair
     // (n0, n0 + 1) of rows l0 + 16 i, i < IT, so that 16 consecutive threads
@@ -727,7 +729,6 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     const int ly = tid >> 6, py = tid & 63;
     const long long ystep = 8 * rstride * PD;
     const long long yoff = (row0 + (long long)ly * rstride) * PD + py;
-    const bool skip = !MODES || p.D != nullptr;
     float2 xs[YI];
 #pragma unroll
     for (int k = 0; k < YI; ++k) {
@@ -749,7 +750,6 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     }
     __syncthreads();
     {
-        const float Dh = skip ? p.D[h] : 0.f;
         const float ysign = (mode & kFwdConjY) ? -1.f : 1.f;
         const float* stage = reinterpret_cast<const float*>(sm1) + ly * STAGE_LD + py;
 #pragma unroll
@@ -910,6 +910,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const long long row0 = ((long long)b * p.T + t0) * p.H + h;  // row of token t0; token l at row0 + l H
     const long long H = p.H;
     const uint32_t sb0 = tc::smem_u32(smem);
+    const float Dh = __ldg(p.D + h);  // skip coefficient, needed only at the end: fetched now
 
     // This thread's items: 2 x 2 complex blocks, tokens (l0, l0 + 1) x
     // columns (n, n + 1) with n = 16 i + 8 g + 2 bq, i < 4 (raw chunk n / 2).
@@ -1328,7 +1329,6 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     }
     __syncthreads();
     {
-        const float Dh = p.D[h];
         const float* stage = reinterpret_cast<const float*>(smem) + ly * STAGE_LD + py;
 #pragma unroll
         for (int k = 0; k < YI; ++k) {
