@@ -800,20 +800,20 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
 // out, which is exact.  The hand-off cells keep fp32 values in the true scale.
 //
 // Footprint.  Half operands need half the bytes.  A CTA of 256 threads uses
-// 64 KB of shared memory (raw x and B rows staged first, the operands written
+// 66 KB of shared memory (raw x and B rows staged first, the operands written
 // over them) and 128 tensor-memory columns (two accumulators, each reused:
 // S' then Y_off, G then Y_diag), so three CTAs share an SM.  The TF32 kernel
 // fits two CTAs of 512 threads.
 namespace h16 {
 constexpr int NT = 256;              // threads per CTA
 constexpr int CPT = 32;              // accumulator columns per thread
-constexpr uint32_t RAW_B = 32768;    // raw B rows (raw x rows at 0), 512 bytes per token each
+constexpr uint32_t RAW_B = 64 * 528;  // raw B rows (raw x rows at 0), 528 bytes per token each
 constexpr uint32_t XP = 0;           // X planes: rows p, K = l (re plane, then im plane)
 constexpr uint32_t STK = 16384;      // F, then Ct, then M: [-Ai; Ar; Ai], 192 rows x K 64
 constexpr uint32_t PL = 40960;       // Bt planes (rows l, K = n), then H planes (rows p, K = n)
 constexpr uint32_t PLANE = 64 * 64 * 2;
 constexpr uint32_t BLK = 1024;       // 64 rows further down a stack
-constexpr int BYTES = 65536;
+constexpr int BYTES = 2 * 64 * 528;  // 66 KB
 constexpr uint32_t COL_A = 0, COL_B = 64, TMEM_COLS = 128;
 constexpr uint32_t STACK_LBO = 24 * 128, PLANE_LBO = 8 * 128, SBO = 128;
 static_assert(STK == XP + 2 * PLANE && PL == STK + 3 * 64 * 64 * 2 && PL + 2 * PLANE <= BYTES, "regions");
@@ -825,12 +825,13 @@ static_assert(2 * CH * STAGE_LD * 4 <= PL, "y staging ends below the H planes");
 __device__ __forceinline__ uint32_t koff16(int row, int k, int rows) {
     return (uint32_t)((((k >> 3) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + ((k & 7) << 1));
 }
-// Raw rows of this kernel: 16-byte chunk j of token row l at chunk
-// j ^ 2 ((l >> 1) mod 4), so that the transform's reads (eight lanes: four
-// even rows, two neighbouring chunks) fall on eight distinct bank groups.
-__device__ __forceinline__ uint32_t raw_off16(int l, int j) {
-    return (uint32_t)(l * 512 + ((j ^ (((l >> 1) & 3) << 1)) << 4));
-}
+// Raw rows of this kernel, as the bulk copies leave them: token row l at
+// 528 l (512 bytes and 16 of padding), 16-byte chunk j at 16 j.  The padding
+// moves each row by one bank group, so that each eight-lane phase of the
+// transform's 16-byte reads (four even rows, two neighbouring chunks) falls on
+// eight distinct bank groups.
+constexpr int RAW_LD = 528;
+__device__ __forceinline__ uint32_t raw_at(int l, int j) { return (uint32_t)(l * RAW_LD + j * 16); }
 // Two values as a half pair, the first in the low 16 bits (the lower K).
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 v = __floats2half2_rn(lo, hi);
@@ -875,7 +876,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     __shared__ __align__(16) float s_rho2[CH];  // rho_l log2(e)
     __shared__ float2 s_rot[CH];
     __shared__ float2 s_rot_last;
-    __shared__ __align__(8) uint64_t mbar[4];  // S, G, OFF, Y
+    __shared__ __align__(8) uint64_t mbar[5];  // S, G, OFF, Y, raw rows
     __shared__ uint32_t s_tmem;
     __shared__ int s_ticket;
     __shared__ int s_bad;
@@ -889,7 +890,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     if (tid == 0) {
         s_ticket = atomicAdd(p.ticket, 1);
         s_bad = 0;
-        for (int i = 0; i < 4; ++i) tc::mbar_init(&mbar[i], 1);
+        for (int i = 0; i < 5; ++i) tc::mbar_init(&mbar[i], 1);
         tc::mbar_fence_init();
     }
     if (tid < 4) s_max[tid] = 0u;
@@ -936,25 +937,28 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         }
     }
 
-    // ---- 0. loads: dt tables, raw x and B rows by cp.async (warp w copies
-    // rows w + 8 r, one 16-byte chunk per lane), C into registers.
+    // ---- 0. loads: dt tables, raw x and B rows by bulk copies (one 512-byte
+    // row per thread of the first four warps, completing on mbar[4]; rows past
+    // the sequence end are zero-filled instead), C into registers.
     float2 tk = make_float2(0.f, 0.f);
     float phi_c = 0.f;
     if (tid < CH) {
         tk = __ldcg(p.tok + ((size_t)bh * p.nc + c) * CH + tid);
         phi_c = __ldcg(p.phi + (size_t)bh * p.nc + c);
     }
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-        const int lr = warp + 8 * r;
-        const bool ok = t0 + lr < p.T;
-        const long long grow = row0 + (long long)lr * H;
-        const float4* gx = p.x + (ok ? grow * (PD / 2) + lane : 0);
-        const float4* gb = p.B + (ok ? grow * (N / 2) + lane : 0);
-        cp_async16(sb0 + raw_off16(lr, lane), gx, ok);
-        cp_async16(sb0 + RAW_B + raw_off16(lr, lane), gb, ok);
+    const int rows = min(CH, p.T - t0);
+    if (tid == 0) tc::mbar_arrive_expect_tx(&mbar[4], (uint32_t)rows * 1024u);
+    if (tid < 2 * CH) {
+        const int lr = tid & (CH - 1), op = tid >> 6;  // op 0: x, 1: B (both 512 bytes per token)
+        const uint32_t off = (op ? RAW_B : 0u) + raw_at(lr, 0);
+        if (lr < rows) {
+            tc::bulk_g2s(sb0 + off, (op ? p.B : p.x) + (row0 + (long long)lr * H) * 32, 512u, &mbar[4]);
+        } else {
+            float4* z = reinterpret_cast<float4*>(smem + off);
+#pragma unroll 1
+            for (int k = 0; k < 32; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
     }
-    cp_async_commit();
     float4 cv[4][2];
 #pragma unroll
     for (int i = 0; i < 4; ++i)
@@ -974,7 +978,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         s_rot[tid] = make_float2(cs, sn);
         if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
     }
-    cp_async_wait_all();
+    if (!tc::mbar_wait_bounded(&mbar[4], 0, kWaitCycles)) s_bad = 1;
     __syncthreads();
     const float rho_end = s_rho[CH - 1];
     const float eend = __expf(rho_end);
@@ -1020,7 +1024,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                xv[i][rr] = *reinterpret_cast<const float4*>(smem + raw_off16(l0 + rr, jof(i)));
+                xv[i][rr] = *reinterpret_cast<const float4*>(smem + raw_at(l0 + rr, jof(i)));
                 fx = maxabs4(xv[i][rr], fx);
                 fc = maxabs4(cv[i][rr], fc);
             }
@@ -1070,7 +1074,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         for (int i = 0; i < 4; ++i)
 #pragma unroll
             for (int rr = 0; rr < 2; ++rr) {
-                bv[i][rr] = *reinterpret_cast<const float4*>(smem + RAW_B + raw_off16(l0 + rr, jof(i)));
+                bv[i][rr] = *reinterpret_cast<const float4*>(smem + RAW_B + raw_at(l0 + rr, jof(i)));
                 fb = maxabs4(bv[i][rr], fb);
             }
         const unsigned mb = warp_max(__float_as_uint(fb));
@@ -1454,8 +1458,12 @@ static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStr
         res = per_sm * sms;
         if (cached) resident[dev].store(res, std::memory_order_relaxed);
     }
+    // L2 prefetch half a wave ahead only when each sequence has many tiles in
+    // flight (at least 8 resident CTAs per sequence).  Measured: a 32-sequence
+    // run of 32768 tokens gains 1.6 % from it; mamba2_layer, 96 sequences of
+    // 2048 tokens, loses 1.4 % (its tiles' own loads compete with it).
     TcParams p = p_in;
-    p.pf_dist = res / 2;
+    p.pf_dist = ((int64_t)p.BH * 8 <= res) ? res / 2 : 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
     fused_chunk_kernel_h16<<<(unsigned)tiles, h16::NT, SMEM_BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
