@@ -800,24 +800,35 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
 // out, which is exact.  The hand-off cells keep fp32 values in the true scale.
 //
 // Footprint.  Half operands need half the bytes.  A CTA of 256 threads uses
-// 66 KB of shared memory (raw x and B rows staged first, the operands written
+// 72 KB of shared memory (raw x and B rows staged first, the operands written
 // over them) and 128 tensor-memory columns (two accumulators, each reused:
 // S' then Y_off, G then Y_diag), so three CTAs share an SM.  The TF32 kernel
 // fits two CTAs of 512 threads.
+//
+// Orientation.  S', Y_off and Y_diag are taken transposed, with the headdim p
+// in the accumulator lanes: S'^T = X^T F^T, Y_off^T = H_c^T Ct^T and
+// Y_diag^T = X^T M^T, all with the X^T (or H_c^T) stack as the A operand.  The
+// hand-off thread then holds consecutive state rows n of one p, which is the
+// K order of H_c^T, so the carried-in state goes to shared memory without a
+// transpose.
 namespace h16 {
 constexpr int NT = 256;              // threads per CTA
 constexpr int CPT = 32;              // accumulator columns per thread
 constexpr uint32_t RAW_B = 64 * 528;  // raw B rows (raw x rows at 0), 528 bytes per token each
-constexpr uint32_t XP = 0;           // X planes: rows p, K = l (re plane, then im plane)
-constexpr uint32_t STK = 16384;      // F, then Ct, then M: [-Ai; Ar; Ai], 192 rows x K 64
-constexpr uint32_t PL = 40960;       // Bt planes (rows l, K = n), then H planes (rows p, K = n)
-constexpr uint32_t PLANE = 64 * 64 * 2;
-constexpr uint32_t BLK = 1024;       // 64 rows further down a stack
-constexpr int BYTES = 2 * 64 * 528;  // 66 KB
+constexpr uint32_t PLANE = 64 * 64 * 2;  // one 64 x 64 half plane
+constexpr uint32_t STACK = 3 * PLANE;     // [-Ai; Ar; Ai]: 192 rows x K 64
+constexpr uint32_t BLK = 1024;            // 64 rows further down a stack
+constexpr uint32_t XS = 0;       // X^T stack (rows p, K = l), the whole tile
+constexpr uint32_t FP = STACK;   // F planes (rows n, K = l)
+constexpr uint32_t CS = STACK;   // then the Ct stack (rows l, K = n)
+constexpr uint32_t MP = STACK;   // then M planes (rows l, K = s)
+constexpr uint32_t BP = 2 * STACK;  // Bt planes (rows s, K = n)
+constexpr uint32_t HS = 2 * STACK;  // then the H_c^T stack (rows p, K = n)
+constexpr int BYTES = HS + STACK;   // 72 KB
 constexpr uint32_t COL_A = 0, COL_B = 64, TMEM_COLS = 128;
 constexpr uint32_t STACK_LBO = 24 * 128, PLANE_LBO = 8 * 128, SBO = 128;
-static_assert(STK == XP + 2 * PLANE && PL == STK + 3 * 64 * 64 * 2 && PL + 2 * PLANE <= BYTES, "regions");
-static_assert(2 * CH * STAGE_LD * 4 <= PL, "y staging ends below the H planes");
+static_assert(CS + STACK <= BP && BP + 2 * PLANE <= HS + STACK && 2 * RAW_B <= BYTES, "regions");
+static_assert(2 * CH * STAGE_LD * 4 <= HS, "y staging ends below the H stack");
 }  // namespace h16
 
 // Byte offset of element (row, k) in a K-major, non-swizzled half operand
@@ -868,12 +879,14 @@ struct Pow2 {
 
 __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p) {
     constexpr int N = NS, NT = h16::NT, CPT = h16::CPT;
-    constexpr uint32_t RAW_B = h16::RAW_B, XP = h16::XP, STK = h16::STK, PL = h16::PL, PLANE = h16::PLANE;
+    constexpr uint32_t RAW_B = h16::RAW_B, XS = h16::XS, FP = h16::FP, CS = h16::CS, MP = h16::MP, BP = h16::BP;
+    constexpr uint32_t HS = h16::HS, PLANE = h16::PLANE;
     constexpr uint32_t BLK = h16::BLK, COL_A = h16::COL_A, COL_B = h16::COL_B, TMEM_COLS = h16::TMEM_COLS;
     constexpr uint32_t STACK_LBO = h16::STACK_LBO, PLANE_LBO = h16::PLANE_LBO, SBO = h16::SBO;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ float s_rho[CH];
     __shared__ __align__(16) float s_rho2[CH];  // rho_l log2(e)
+    __shared__ __align__(16) float s_erho[CH];  // e^{rho_l}
     __shared__ float2 s_rot[CH];
     __shared__ float2 s_rot_last;
     __shared__ __align__(8) uint64_t mbar[5];  // S, G, OFF, Y, raw rows
@@ -975,6 +988,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         sincosf(phi_c + tk.y, &sn, &cs);
         s_rho[tid] = tk.x;
         s_rho2[tid] = tk.x * 1.4426950408889634f;
+        s_erho[tid] = __expf(tk.x);
         s_rot[tid] = make_float2(cs, sn);
         if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
     }
@@ -986,25 +1000,28 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const uint32_t ID = tc::idesc_f16(128, 64);
     // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`;
     // one MMA takes K = 16, so the start address steps by two core matrices.
-    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs) {
+    // B's real plane at `bs` and its imaginary plane `im_off` bytes further,
+    // K groups `b_lbo` bytes apart (plain planes, or two blocks of a stack).
+    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs, uint32_t b_lbo, uint32_t im_off) {
         const uint64_t a_up = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
         const uint64_t a_dn = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
-        const uint64_t b_re = tc::make_desc(bs, PLANE_LBO, SBO);
-        const uint64_t b_im = tc::make_desc(bs + PLANE, PLANE_LBO, SBO);
-        constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4, B_STEP = (2 * PLANE_LBO) >> 4;
+        const uint64_t b_re = tc::make_desc(bs, b_lbo, SBO);
+        const uint64_t b_im = tc::make_desc(bs + im_off, b_lbo, SBO);
+        constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4;
+        const uint64_t B_STEP = (2 * b_lbo) >> 4;
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks)
             tc::mma_f16(d, a_up + ks * A_STEP, b_re + ks * B_STEP, ID, ks > 0 ? 1u : 0u);
 #pragma unroll
         for (int ks = 0; ks < 4; ++ks) tc::mma_f16(d, a_dn + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
     };
-    auto issue = [&](uint32_t d, uint32_t as, uint32_t bs, uint64_t* bar) {
+    auto issue = [&](uint32_t d, uint32_t as, uint32_t bs, uint32_t b_lbo, uint32_t b_im, uint64_t* bar) {
         tc::fence_proxy_async();
         tc::fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc::fence_after_sync();
-            cgemm(d, as, bs);
+            cgemm(d, as, bs, b_lbo, b_im);
             tc::commit(bar);
         }
     };
@@ -1013,8 +1030,8 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     };
     constexpr uint32_t NEG2 = 0x80008000u;  // sign bits of a half pair
 
-    // ---- 2. X planes over raw x (rows p, K = l), scaled; the scales of x and
-    // C; Ct = e^{i Theta} C as scaled half pairs in registers.
+    // ---- 2. the X^T stack over raw x (rows p, K = l), scaled; the scales of
+    // x and C; Ct = e^{i Theta} C as scaled half pairs in registers.
     uint32_t cw[4][2][2];  // [item][row l0 + rr][re, im]: columns (n, n + 1)
     float inv_x, inv_c;
     {
@@ -1038,18 +1055,6 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         inv_x = sx.inv;
         inv_c = sc.inv;
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int n = 16 * i + 8 * g + 2 * bq;
-            const uint32_t oa = XP + koff16(n, l0, 64), ob = XP + koff16(n + 1, l0, 64);
-            const float4 u = xv[i][0], w = xv[i][1];  // tokens l0, l0 + 1
-            const uint32_t ra = pack_h2(u.x * sx.s, w.x * sx.s), rb = pack_h2(u.z * sx.s, w.z * sx.s);
-            const uint32_t ia = pack_h2(u.y * sx.s, w.y * sx.s), ib = pack_h2(u.w * sx.s, w.w * sx.s);
-            st_u32(smem, swp ? ob : oa, swp ? rb : ra);
-            st_u32(smem, swp ? oa : ob, swp ? ra : rb);
-            st_u32(smem + PLANE, swp ? ob : oa, swp ? ib : ia);
-            st_u32(smem + PLANE, swp ? oa : ob, swp ? ia : ib);
-        }
-#pragma unroll
         for (int rr = 0; rr < 2; ++rr) {
             const float2 r0 = s_rot[l0 + rr];
             const float2 rot = make_float2(r0.x * sc.s, r0.y * sc.s);  // the rotation with C's scale
@@ -1062,10 +1067,26 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
                 cw[i][rr][1] = pack_h2(c0i, c1i);
             }
         }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int n = 16 * i + 8 * g + 2 * bq;  // rows p = n, n + 1
+            const uint32_t oa = XS + koff16(n, l0, 192), ob = XS + koff16(n + 1, l0, 192);
+            const float4 u = xv[i][0], w = xv[i][1];  // tokens l0, l0 + 1
+            const uint32_t ra = pack_h2(u.x * sx.s, w.x * sx.s), rb = pack_h2(u.z * sx.s, w.z * sx.s);
+            const uint32_t ia = pack_h2(u.y * sx.s, w.y * sx.s), ib = pack_h2(u.w * sx.s, w.w * sx.s);
+            const uint32_t o1 = swp ? ob : oa, o2 = swp ? oa : ob;
+            const uint32_t r1w = swp ? rb : ra, r2w = swp ? ra : rb, i1w = swp ? ib : ia, i2w = swp ? ia : ib;
+            st_u32(smem, o1, i1w ^ NEG2);
+            st_u32(smem, o2, i2w ^ NEG2);
+            st_u32(smem, o1 + BLK, r1w);
+            st_u32(smem, o2 + BLK, r2w);
+            st_u32(smem, o1 + 2 * BLK, i1w);
+            st_u32(smem, o2 + 2 * BLK, i2w);
+        }
     }
 
-    // ---- 3. Bt planes (rows l, K = n) and the F stack (rows n, K = l) over
-    // raw B, scaled by B's scale; S' = F X.
+    // ---- 3. Bt planes (rows l, K = n) and F planes (rows n, K = l) over raw
+    // B, scaled by B's scale; S'^T = X^T F^T.
     float inv_b;
     {
         float4 bv[4][2];
@@ -1096,7 +1117,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
             const float w0r = r1.x * w.x + r1.y * w.y, w0i = r1.x * w.y - r1.y * w.x;
             const float w1r = r1.x * w.z + r1.y * w.w, w1i = r1.x * w.w - r1.y * w.z;
             {
-                const uint32_t oa = PL + koff16(l0, n, 64), ob = PL + koff16(l0 + 1, n, 64);
+                const uint32_t oa = BP + koff16(l0, n, 64), ob = BP + koff16(l0 + 1, n, 64);
                 const uint32_t ra = pack_h2(u0r, u1r), rb = pack_h2(w0r, w1r);
                 const uint32_t ia = pack_h2(u0i, u1i), ib = pack_h2(w0i, w1i);
                 st_u32(smem, swp ? ob : oa, swp ? rb : ra);
@@ -1106,28 +1127,24 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
             }
             {
                 // F[n][l] = exp(rho_end - rho_l) Bt[l][n]; row n holds K = (l0, l0 + 1)
-                const uint32_t oa = STK + koff16(n, l0, 192), ob = STK + koff16(n + 1, l0, 192);
+                const uint32_t oa = FP + koff16(n, l0, 64), ob = FP + koff16(n + 1, l0, 64);
                 const uint32_t ra = pack_h2(u0r * ds0, w0r * ds1), rb = pack_h2(u1r * ds0, w1r * ds1);
                 const uint32_t ia = pack_h2(u0i * ds0, w0i * ds1), ib = pack_h2(u1i * ds0, w1i * ds1);
-                const uint32_t o1 = swp ? ob : oa, o2 = swp ? oa : ob;
-                const uint32_t r1w = swp ? rb : ra, r2w = swp ? ra : rb, i1w = swp ? ib : ia, i2w = swp ? ia : ib;
-                st_u32(smem, o1, i1w ^ NEG2);
-                st_u32(smem, o2, i2w ^ NEG2);
-                st_u32(smem, o1 + BLK, r1w);
-                st_u32(smem, o2 + BLK, r2w);
-                st_u32(smem, o1 + 2 * BLK, i1w);
-                st_u32(smem, o2 + 2 * BLK, i2w);
+                st_u32(smem, swp ? ob : oa, swp ? rb : ra);
+                st_u32(smem, swp ? oa : ob, swp ? ra : rb);
+                st_u32(smem + PLANE, swp ? ob : oa, swp ? ib : ia);
+                st_u32(smem + PLANE, swp ? oa : ob, swp ? ia : ib);
             }
         }
     }
-    issue(tmem + COL_A, sb0 + STK, sb0 + XP, &mbar[0]);
+    issue(tmem + COL_A, sb0 + XS, sb0 + FP, PLANE_LBO, PLANE, &mbar[0]);
 
-    // ---- 4. Ct stack (rows l, K = n) over F once S' has read it; G = Ct Bt^T
+    // ---- 4. Ct stack (rows l, K = n) over F once S'^T has read it; G = Ct Bt^T
     wait_bar(&mbar[0]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         const int n = 16 * i + 8 * g + 2 * bq;
-        const uint32_t oa = STK + koff16(l0, n, 192), ob = STK + koff16(l0 + 1, n, 192);
+        const uint32_t oa = CS + koff16(l0, n, 192), ob = CS + koff16(l0 + 1, n, 192);
         const uint32_t o1 = swp ? ob : oa, o2 = swp ? oa : ob;
         const uint32_t r1w = swp ? cw[i][1][0] : cw[i][0][0], r2w = swp ? cw[i][0][0] : cw[i][1][0];
         const uint32_t i1w = swp ? cw[i][1][1] : cw[i][0][1], i2w = swp ? cw[i][0][1] : cw[i][1][1];
@@ -1138,12 +1155,13 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         st_u32(smem, o1 + 2 * BLK, i1w);
         st_u32(smem, o2 + 2 * BLK, i2w);
     }
-    issue(tmem + COL_B, sb0 + STK, sb0 + PL, &mbar[1]);
+    issue(tmem + COL_B, sb0 + CS, sb0 + BP, PLANE_LBO, PLANE, &mbar[1]);
 
-    // ---- 5. hand-off: the thread owns state row lrow of part `part` and the
-    // CPT columns from c0col of S'; it takes H_c from the cells the same thread
-    // position of chunk c-1 wrote and publishes H_{c+1} = e^{rho_end} H_c + S'
-    // in the true scale.
+    // ---- 5. hand-off: the thread owns headdim column p = lrow of part `part`
+    // and the CPT state rows n from c0col (S'^T holds p in its lanes).  It
+    // takes H_c from the cells the same thread position of chunk c-1 wrote and
+    // publishes H_{c+1} = e^{rho_end} H_c + S' in the true scale.  Cells are
+    // laid out [part][n][p], so a warp's accesses are contiguous.
     const int q = warp & 3, cblk = warp >> 2;
     const int L = q * 32 + lane;
     const int part = L >> 6, lrow = L & 63;
@@ -1192,9 +1210,9 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
                 if (p.status) atomicOr(p.status, kStatusHandoff);
             }
         } else if (p.h0) {
-            const float* src = reinterpret_cast<const float*>(p.h0 + ((size_t)bh * N + lrow) * PD + c0col) + part;
+            const float* src = reinterpret_cast<const float*>(p.h0 + ((size_t)bh * N + c0col) * PD + lrow) + part;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) hv[j] = __ldg(src + 2 * j);
+            for (int j = 0; j < CPT; ++j) hv[j] = __ldg(src + 2 * PD * j);
         } else {
 #pragma unroll
             for (int j = 0; j < CPT; ++j) hv[j] = 0.f;
@@ -1219,41 +1237,32 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const Pow2 shc(s_max[3]);
     const float inv_h = shc.inv;
 
-    // ---- 6. H_c as the B operand of Y_off (rows p, K = n) over the Bt planes
-    // once G has read them.  A butterfly of shuffles transposes each warp's
-    // 32 (n) x 32 (p) block so that each lane owns one p and 32 consecutive n.
+    // ---- 6. H_c^T as the A operand of Y_off^T (stack rows p, K = n) over the
+    // Bt planes once G has read them: this thread holds row p = lrow of part
+    // `part` at the CPT consecutive K = n from c0col.
     {
-#pragma unroll
-        for (int sbit = CPT / 2; sbit >= 1; sbit >>= 1) {
-            const bool upper = (lane & sbit) != 0;
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                if ((j & sbit) == 0) {
-                    const float send = upper ? hv[j] : hv[j | sbit];
-                    const float recv = __shfl_xor_sync(0xffffffffu, send, sbit);
-                    if (upper) hv[j] = recv;
-                    else hv[j | sbit] = recv;
-                }
-            }
-        }
-        // now hv[j] = H_part[nb + j][c0col + lane]
-        const int nb = lrow - lane;
         const float s = shc.s;
         wait_bar(&mbar[1]);
-        unsigned char* plane = smem + PL + part * PLANE + koff16(c0col + lane, nb, 64);
+        unsigned char* hrow = smem + HS + koff16(lrow, c0col, 192);
 #pragma unroll
-        for (int k8 = 0; k8 < CPT / 8; ++k8) {  // K = nb + 8 k8: one core matrix (8 row groups) further per step
+        for (int k8 = 0; k8 < CPT / 8; ++k8) {  // K + 8: one core matrix (24 row groups) further
             const uint4 v = make_uint4(pack_h2(hv[8 * k8] * s, hv[8 * k8 + 1] * s),
                                        pack_h2(hv[8 * k8 + 2] * s, hv[8 * k8 + 3] * s),
                                        pack_h2(hv[8 * k8 + 4] * s, hv[8 * k8 + 5] * s),
                                        pack_h2(hv[8 * k8 + 6] * s, hv[8 * k8 + 7] * s));
-            *reinterpret_cast<uint4*>(plane + 1024 * k8) = v;
+            if (part == 0) {
+                *reinterpret_cast<uint4*>(hrow + BLK + 3072 * k8) = v;
+            } else {
+                *reinterpret_cast<uint4*>(hrow + 2 * BLK + 3072 * k8) = v;
+                *reinterpret_cast<uint4*>(hrow + 3072 * k8) = make_uint4(v.x ^ NEG2, v.y ^ NEG2, v.z ^ NEG2, v.w ^ NEG2);
+            }
         }
     }
-    issue(tmem + COL_A, sb0 + STK, sb0 + PL, &mbar[2]);  // Y_off' = Ct H_c, over S'
+    // Y_off'^T = H_c^T Ct^T over S'^T; the Ct stack's blocks 1 and 2 serve as B planes
+    issue(tmem + COL_A, sb0 + HS, sb0 + CS + BLK, STACK_LBO, BLK, &mbar[2]);
 
-    // ---- 7. masked scores M = L o G (scaled like G) over Ct once Y_off has
-    // read it; Y_diag = M X over G.
+    // ---- 7. masked scores M = L o G (scaled like G) as planes (rows l, K = s)
+    // over Ct once Y_off has read it; Y_diag^T = X^T M^T over G.
     {
         float m[CPT];
         // a warp whose rows all precede its columns holds only masked scores
@@ -1284,21 +1293,15 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         }
         wait_bar(&mbar[2]);
         // 16-byte stores: eight consecutive K of one row fill one core-matrix
-        // row; K + 8 is one core matrix (24 row groups) further
-        unsigned char* mrow = smem + STK + koff16(lrow, c0col, 192);
+        // row; K + 8 is one core matrix (8 row groups) further
+        unsigned char* mrow = smem + MP + part * PLANE + koff16(lrow, c0col, 64);
 #pragma unroll
-        for (int k8 = 0; k8 < CPT / 8; ++k8) {
-            const uint4 v = make_uint4(pack_h2(m[8 * k8], m[8 * k8 + 1]), pack_h2(m[8 * k8 + 2], m[8 * k8 + 3]),
-                                       pack_h2(m[8 * k8 + 4], m[8 * k8 + 5]), pack_h2(m[8 * k8 + 6], m[8 * k8 + 7]));
-            if (part == 0) {
-                *reinterpret_cast<uint4*>(mrow + BLK + 3072 * k8) = v;
-            } else {
-                *reinterpret_cast<uint4*>(mrow + 2 * BLK + 3072 * k8) = v;
-                *reinterpret_cast<uint4*>(mrow + 3072 * k8) = make_uint4(v.x ^ NEG2, v.y ^ NEG2, v.z ^ NEG2, v.w ^ NEG2);
-            }
-        }
+        for (int k8 = 0; k8 < CPT / 8; ++k8)
+            *reinterpret_cast<uint4*>(mrow + 1024 * k8) =
+                make_uint4(pack_h2(m[8 * k8], m[8 * k8 + 1]), pack_h2(m[8 * k8 + 2], m[8 * k8 + 3]),
+                           pack_h2(m[8 * k8 + 4], m[8 * k8 + 5]), pack_h2(m[8 * k8 + 6], m[8 * k8 + 7]));
     }
-    issue(tmem + COL_B, sb0 + STK, sb0 + XP, &mbar[3]);
+    issue(tmem + COL_B, sb0 + XS, sb0 + MP, PLANE_LBO, PLANE, &mbar[3]);
 
     // ---- 8. y = Y_diag + e^{rho_l} Y_off' + D x with the scales taken out.
     // The skip term uses the exact fp32 input (an L2 hit, fetched while Y_diag
@@ -1316,10 +1319,12 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     {
         wait_bar(&mbar[3]);
         tc::fence_after_sync();
-        // exact products of powers of two; the row decay joins the second
+        // the accumulators hold column p = lrow at tokens l = c0col + j;
+        // exact products of powers of two, the token's decay e^{rho_l} per column
         const float k_d = inv_c * inv_b * inv_x;
-        const float k_o = __expf(s_rho[lrow]) * (inv_c * inv_h);
-        float* stage = reinterpret_cast<float*>(smem) + part * CH * STAGE_LD + lrow * STAGE_LD + c0col;
+        const float k_o = inv_c * inv_h;
+        float* stage = reinterpret_cast<float*>(smem) + part * CH * STAGE_LD + c0col * STAGE_LD + lrow;
+        const float4* er = reinterpret_cast<const float4*>(s_erho + c0col);
 #pragma unroll
         for (int hh = 0; hh < CPT / 16; ++hh) {
             uint32_t ry[16], ro[16];
@@ -1327,8 +1332,15 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
             tc::tmem_ld16(tmem + lane_base + COL_A + c0col + 16 * hh, ro);
             tc::tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                stage[16 * hh + j] = fmaf(k_o, __uint_as_float(ro[j]), __uint_as_float(ry[j]) * k_d);
+            for (int j4 = 0; j4 < 4; ++j4) {
+                const float4 e4 = er[4 * hh + j4];
+                const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = 4 * j4 + u;
+                    stage[(16 * hh + j) * STAGE_LD] = fmaf(ev[u] * k_o, __uint_as_float(ro[j]), __uint_as_float(ry[j]) * k_d);
+                }
+            }
         }
     }
     __syncthreads();
@@ -1346,10 +1358,8 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // ---- 9. final state of the sequence, rotated back to the original frame
     if (c == p.nc - 1 && p.h_final) {
         const float cs = s_rot_last.x, sn = s_rot_last.y;
-        for (int i = tid; i < N * PD; i += NT) {
-            const int n = i >> 6, pp = i & 63;
-            const unsigned long long* cell =
-                p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)pp * NS + n;
+        for (int i = tid; i < N * PD; i += NT) {  // element (n, p) = i of [n][p]; cells are [part][n][p]
+            const unsigned long long* cell = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + i;
             const float hr = __uint_as_float((uint32_t)ld_cell(cell));
             const float hi = __uint_as_float((uint32_t)ld_cell(cell + PD * NS));
             p.h_final[(size_t)bh * N * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
