@@ -34,6 +34,7 @@
 
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <atomic>
 #include <type_traits>
 
@@ -935,7 +936,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const bool swp = g != 0;
     auto jof = [&](int i) { return 8 * i + 4 * g + bq; };
 
-    // Rows of x, B and C of the tile half a wave of resident CTAs ahead into L2.
+    // Rows of x, B and C of a later tile into L2 (when the launch asks for it).
     if (p.pf_dist > 0 && tid < 3 * CH) {
         const int pt = ticket + p.pf_dist;
         if (pt < p.BH * p.nc) {
@@ -1459,21 +1460,36 @@ static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStr
         cudaError_t e =
             cudaFuncSetAttribute(fused_chunk_kernel_h16, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        int per_sm = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel_h16, h16::NT, SMEM_BYTES);
+        e = cudaFuncSetAttribute(fused_chunk_kernel_h16, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                 cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
-        if (per_sm * (int)h16::TMEM_COLS > 512) return cudaErrorNotSupported;
-        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-        if (e != cudaSuccess) return e;
+        // CTAs per SM from the shared-memory, register and thread limits.  The
+        // occupancy query answers one for this kernel, while the SMs hold three
+        // (measured), so the limits are applied here directly.
+        int smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0, sms = 0;
+        cudaFuncAttributes fa;
+        if ((e = cudaFuncGetAttributes(&fa, fused_chunk_kernel_h16)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return e;
+        const int per_cta_smem = SMEM_BYTES + (int)fa.sharedSizeBytes + reserved;
+        const int regs_per_warp = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated in units of 256
+        int per_sm = smem_sm / per_cta_smem;
+        per_sm = std::min(per_sm, regs_sm / (regs_per_warp * (h16::NT / 32)));
+        per_sm = std::min(per_sm, threads_sm / h16::NT);
+        // every resident CTA must find its tensor-memory columns free
+        if (per_sm < 1 || per_sm * (int)h16::TMEM_COLS > 512) return cudaErrorNotSupported;
         res = per_sm * sms;
         if (cached) resident[dev].store(res, std::memory_order_relaxed);
     }
-    // L2 prefetch half a wave ahead only when each sequence has many tiles in
-    // flight (at least 8 resident CTAs per sequence).  Measured: a 32-sequence
-    // run of 32768 tokens gains 1.6 % from it; mamba2_layer, 96 sequences of
-    // 2048 tokens, loses 1.4 % (its tiles' own loads compete with it).
+    // No L2 prefetch of later tiles: measured on this kernel, prefetching half
+    // the SM count of tickets ahead cost mamba2_layer 1.4 % and gained nothing
+    // on a 32-sequence run of 32768 tokens.
     TcParams p = p_in;
-    p.pf_dist = ((int64_t)p.BH * 8 <= res) ? res / 2 : 0;
+    p.pf_dist = 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
     fused_chunk_kernel_h16<<<(unsigned)tiles, h16::NT, SMEM_BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
