@@ -795,10 +795,12 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
 // TF32 value, so rounding an operand to either costs the same relative error.
 // Its exponent range is narrow, so every operand tile gets a power-of-two scale
 // taken from its largest component: x, B and C of the tile, and the carried-in
-// state H_c, each scaled so that its largest component lies in [1, 2).  The
-// masked scores inherit the scales of C and B (|L o G| <= 64 * 8 = 512).
-// Accumulators hold scaled sums and the epilogues multiply the scales back
-// out, which is exact.  The hand-off cells keep fp32 values in the true scale.
+// state H_c, each scaled so that its largest component lies in [2^14, 2^15)
+// (rotated components stay below 2^15.5 < 65504).  The accumulators stay far
+// inside fp32 (|G| <= 64 * 8 * 2^30); the masked scores take G times 2^-28,
+// folded into their exponential, so |L o G| 2^-28 <= 512.  The epilogues
+// multiply the scales back out, which is exact.  The hand-off cells keep fp32
+// values in the true scale.
 //
 // Footprint.  Half operands need half the bytes.  A CTA of 256 threads uses
 // 72 KB of shared memory (raw x and B rows staged first, the operands written
@@ -866,15 +868,19 @@ __device__ __forceinline__ unsigned warp_max(unsigned v) {
     for (int o = 16; o >= 1; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
-// Scale 2^-e and its inverse 2^e for a tile whose largest component has the
-// fp32 bit pattern `bits` (e its exponent, kept within the normal range).
+// Scale 2^(14-e) and its inverse 2^(e-14) for a tile whose largest component
+// has the fp32 bit pattern `bits` (e its exponent): the largest component goes
+// to [2^14, 2^15), the top of the half range, so that components far smaller
+// than it (down to about 4e-9 of it) still round to normal half values.  e is
+// kept where both factors are normal fp32 numbers.
+constexpr int kHalfTop = 14;
 struct Pow2 {
     float s, inv;
     __device__ __forceinline__ explicit Pow2(unsigned bits) {
         int e = (int)((bits >> 23) & 0xffu) - 127;
-        e = max(-126, min(126, e));
-        s = __uint_as_float((unsigned)(127 - e) << 23);
-        inv = __uint_as_float((unsigned)(127 + e) << 23);
+        e = max(-112, min(126, e));
+        s = __uint_as_float((unsigned)(127 + kHalfTop - e) << 23);
+        inv = __uint_as_float((unsigned)(127 - kHalfTop + e) << 23);
     }
 };
 
@@ -1286,8 +1292,9 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int j = 4 * j4 + u;
-                    // causal mask as 2^-inf = 0: a select, not a branch around the exponential
-                    const float arg = (c0col + j <= lrow) ? rl2 - rv[u] : -INFINITY;
+                    // causal mask as 2^-inf = 0: a select, not a branch around the
+                    // exponential; the 2^-28 that keeps M in the half range rides along
+                    const float arg = (c0col + j <= lrow) ? (rl2 - rv[u]) - 28.f : -INFINITY;
                     m[j] = ex2_approx(arg) * __uint_as_float(r[j]);
                 }
             }
@@ -1322,7 +1329,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         tc::fence_after_sync();
         // the accumulators hold column p = lrow at tokens l = c0col + j;
         // exact products of powers of two, the token's decay e^{rho_l} per column
-        const float k_d = inv_c * inv_b * inv_x;
+        const float k_d = inv_c * inv_b * inv_x * 268435456.f;  // and the masked scores' 2^-28
         const float k_o = inv_c * inv_h;
         float* stage = reinterpret_cast<float*>(smem) + part * CH * STAGE_LD + c0col * STAGE_LD + lrow;
         const float4* er = reinterpret_cast<const float4*>(s_erho + c0col);
