@@ -1556,8 +1556,10 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
 // Failure-detection self-test: a two-sequence, two-chunk forward whose
 // tickets start at the second chunk, so no CTA ever publishes the first
 // chunk's state and the hand-off wait of the second chunk must give up after
-// `wait_cycles`.  Returns the kernel's error bits (bit 0: a hand-off wait
-// timed out) through *err_bits after synchronising the stream.
+// `wait_cycles`.  Runs the TF32 kernel and then the half-operand kernel and
+// returns their error bits (bit 0: a hand-off wait timed out) through
+// *err_bits after synchronising the stream: the TF32 kernel's in bits 0-7,
+// the half-operand kernel's in bits 8-15.
 cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cudaStream_t st) {
     const int Bz = 1, T = 2 * CH, H = 2, N = NS, P = PD;
     const size_t nx = (size_t)Bz * T * H * P, nb = (size_t)Bz * T * H * N, nt = (size_t)Bz * T * H;
@@ -1622,13 +1624,18 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.status = status_word();
     p.pf_dist = 0;
     p.wait_cycles = wait_cycles;
+    // the TF32 kernel, then the half-operand kernel on the same problem (the
+    // prep resets the ticket to the second chunk and the error word each time)
     if (e == cudaSuccess) e = launch_prep(p, false, st);
     if (e == cudaSuccess) e = launch_fused<1, false, false>(p, BH * nc, false, st);
-    int bits = -1;
-    if (e == cudaSuccess) e = cudaMemcpyAsync(&bits, p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
+    int bits[2] = {-1, -1};
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&bits[0], p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = launch_prep(p, false, st);
+    if (e == cudaSuccess) e = launch_fused_h16(p, BH * nc, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&bits[1], p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
     cudaFreeAsync(buf, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (err_bits) *err_bits = bits;
+    if (err_bits) *err_bits = (bits[0] < 0 || bits[1] < 0) ? -1 : (bits[0] | (bits[1] << 8));
     return e;
 }
 

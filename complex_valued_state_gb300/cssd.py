@@ -172,8 +172,10 @@ def profile_events(begin=None, end=None):
 
 
 def selftest_handoff_timeout(wait_cycles: int = 2_000_000, stream=None) -> int:
-    """Run the forward with a predecessor chunk that never publishes; return the
-    kernel's error bits (bit 0 set = the bounded hand-off wait gave up)."""
+    """Run both tensor-core forward kernels with a predecessor chunk that never
+    publishes; return their error bits: the TF32 kernel's in bits 0-7, the
+    half-operand kernel's in bits 8-15 (bit 0 of each set = the bounded
+    hand-off wait gave up)."""
     import torch as _t
 
     bits = ctypes.c_int(-1)

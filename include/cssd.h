@@ -359,15 +359,17 @@ int cssd_device_status(unsigned* bits, int clear, cssd_stream_t stream);
 int cssd_profile_events(void* ev_begin, void* ev_end);
 
 /* Failure-detection self-test of the forward's inter-chunk hand-off.  Runs
- * the tensor-core forward on a small internal problem (two sequences, two
- * 64-token chunks, zero inputs) whose first chunk is never processed, so the
- * second chunk's bounded wait for its predecessor's state has to give up after
- * `wait_cycles` SM clocks.  The kernel then records bit 0 in its error word,
- * finishes, and frees its tensor memory; the device stays usable.  The call
- * allocates its buffers stream-ordered, synchronises `stream`, and returns the
- * error word in *err_bits (bit 0 = a hand-off wait timed out, bit 1 = any wait
- * timed out).  Returns CSSD_ERR_NULL / CSSD_ERR_DIMS for bad arguments,
- * CSSD_ERR_CUDA if a runtime call fails. */
+ * both tensor-core forward kernels (TF32 operands, then half operands) on a
+ * small internal problem (two sequences, two 64-token chunks, zero inputs)
+ * whose first chunk is never processed, so the second chunk's bounded wait for
+ * its predecessor's state has to give up after `wait_cycles` SM clocks.  Each
+ * kernel then records bit 0 in its error word, finishes, and frees its tensor
+ * memory; the device stays usable.  The call allocates its buffers
+ * stream-ordered, synchronises `stream`, and returns the two error words in
+ * *err_bits: the TF32 kernel's in bits 0-7, the half-operand kernel's in bits
+ * 8-15 (in each, bit 0 = a hand-off wait timed out, bit 1 = a tensor-core
+ * completion wait timed out).  Returns CSSD_ERR_NULL / CSSD_ERR_DIMS for bad
+ * arguments, CSSD_ERR_CUDA if a runtime call fails. */
 int cssd_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cssd_stream_t stream);
 
 /* Static, NUL-terminated description of a status code. */
