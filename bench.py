@@ -161,12 +161,38 @@ KERNEL_SOURCES = {
 }
 
 
+def strip_comments(src: str) -> str:
+    """C/C++/CUDA source without its comments (string and character literals
+    kept as they are), so that a comment-only edit leaves the hash alone."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        else:
+            out.append(c)
+            i += 1
+    return "".join(out)
+
+
 def kernel_source_sha(kernel: str) -> str:
+    """Hash of the kernel's sources without comments: the traffic record of a
+    kernel counts only while its code is the one the counters were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "complex_valued_state_gb300", "csrc")
     for name in sorted(KERNEL_SOURCES[kernel]):
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        with open(os.path.join(csrc, name), encoding="utf-8") as f:
+            h.update(name.encode() + strip_comments(f.read()).encode())
     return h.hexdigest()[:16]
 
 

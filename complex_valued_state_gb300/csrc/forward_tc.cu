@@ -1313,8 +1313,8 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
 
     // ---- 8. y = Y_diag + e^{rho_l} Y_off' + D x with the scales taken out.
     // The skip term uses the exact fp32 input (an L2 hit, fetched while Y_diag
-    // runs).  The staging planes lie over the X planes and the stack, which
-    // Y_diag has finished reading.
+    // runs).  The staging planes lie over the X^T stack and the M planes,
+    // which Y_diag has finished reading.
     constexpr int YI = CH * PD / NT;  // output elements per thread: rows ly + 4 k, column py
     const int ly = tid >> 6, py = tid & 63;
     const long long ystep = 4 * H * PD;
