@@ -186,13 +186,15 @@ def strip_comments(src: str) -> str:
 
 
 def kernel_source_sha(kernel: str) -> str:
-    """Hash of the kernel's sources without comments: the traffic record of a
-    kernel counts only while its code is the one the counters were taken on."""
+    """Hash of the kernel's sources without comments and with whitespace runs
+    collapsed: the traffic record of a kernel counts only while its code is the
+    one the counters were taken on."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "complex_valued_state_gb300", "csrc")
     for name in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(csrc, name), encoding="utf-8") as f:
-            h.update(name.encode() + strip_comments(f.read()).encode())
+            code = " ".join(strip_comments(f.read()).split())  # whitespace runs as one space
+            h.update(name.encode() + code.encode())
     return h.hexdigest()[:16]
 
 

@@ -1,5 +1,8 @@
-// Fused chunkwise forward on the tcgen05 tensor cores (TF32, fp32 accumulate),
-// for chunk = dstate = headdim = 64.
+// Fused chunkwise forward on the tcgen05 tensor cores for headdim 64 with
+// dstate 64 or 128, in 64-token tiles: fp32 accumulation in tensor memory,
+// with TF32 operands (fused_chunk_kernel: dstate 128, split precision, the
+// backward's runs) or IEEE half operands with per-tile power-of-two scales
+// (fused_chunk_kernel_h16: the dstate-64 forward).
 //
 // Method ("The Chunkwise Complex SSD Algorithm", Mamba-3-Lite docs, sections
 // 4.2-4.5; "SSD Theory" section 4.5).  For one (batch, head) with
@@ -23,8 +26,8 @@
 // One CTA per (chunk, batch*head), dispatched in chunk-major order through an
 // atomic ticket so that the CTA owning chunk c-1 of a sequence has always
 // started before the CTA owning chunk c waits for its state.  The state is
-// handed over through a two-slot ring in global memory (L2 resident) with a
-// per-sequence release/acquire counter; the wait is bounded.
+// handed over through a two-slot ring in global memory (L2 resident) of 8-byte
+// cells that carry the value with its chunk tag; the wait is bounded.
 //
 // Complex GEMMs run as real ones on stacked operands: with A = Ar + i Ai
 // stored as the three row blocks [-Ai; Ar; Ai] and B as planes Br, Bi,
@@ -797,8 +800,8 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
 // taken from its largest component: x, B and C of the tile, and the carried-in
 // state H_c, each scaled so that its largest component lies in [2^14, 2^15)
 // (rotated components stay below 2^15.5 < 65504).  The accumulators stay far
-// inside fp32 (|G| <= 64 * 8 * 2^30); the masked scores take G times 2^-28,
-// folded into their exponential, so |L o G| 2^-28 <= 512.  The epilogues
+// inside fp32 (|G| < 64 * 2^31); the masked scores take G times 2^-28, folded
+// into their exponential, so |L o G| 2^-28 < 512.  The epilogues
 // multiply the scales back out, which is exact.  The hand-off cells keep fp32
 // values in the true scale.
 //
