@@ -83,6 +83,16 @@ typedef struct {
 size_t cssd_workspace_bytes(const cssd_dims* dims, int chunk);
 
 /* Chunkwise forward over a whole sequence from a zero initial state.
+ *
+ * Precision: the tensor-core paths (headdim 64, dstate 64 or 128) round the
+ * GEMM operands to an 11-bit significand and accumulate in fp32.  dstate 64
+ * uses IEEE half operands with a power-of-two scale per tile and operand,
+ * dstate 128 uses TF32.  Decays, rotations, the inter-chunk state and the
+ * output are fp32.  Measured errors are 1e-4 to 5e-4 of the largest value of
+ * y and of h_final (the bar the tests hold is 2e-3).  The CUDA-core
+ * path (other shapes) is fp32 throughout.  cssd_chunked_forward_precise
+ * gives about fp32 accuracy on the tensor cores. */
+/* Arguments:
  *   x       complex64 [batch, seqlen, nheads, headdim]   token content
  *   dt      float32   [batch, seqlen, nheads]            raw step (softplus applied inside)
  *   A       complex64 [nheads]                           per-head rate
