@@ -49,6 +49,7 @@ def parse():
     ap.add_argument("--no-born", action="store_true", help="skip the causal Born attention measurement")
     ap.add_argument("--no-backward", action="store_true", help="skip the gradient (backward) measurement")
     ap.add_argument("--no-precise", action="store_true", help="skip the split-precision forward measurement")
+    ap.add_argument("--no-tf32", action="store_true", help="skip the TF32-operand forward measurement")
     ap.add_argument("--long-seqlen", type=int, default=0,
                     help="tokens of the long_seq forward (default: the workload's 65536; smaller for profiling)")
     return ap.parse_args()
@@ -155,6 +156,7 @@ KERNEL_SOURCES = {
     "fused_chunk_kernel_h16": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
     "fused_chunk_kernel_split": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
     "fused_chunk_kernel_dstate128": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
+    "fused_chunk_kernel_tf32": ("forward_tc.cu", "tcgen05.cuh", "cssd_common.cuh"),
     "step_kernel": ("step.cu", "cssd_common.cuh"),
     "cayley_scan_kernel": ("cayley.cu", "cssd_common.cuh"),
     "born_kernel": ("born.cu", "tcgen05.cuh", "cssd_common.cuh"),
@@ -315,6 +317,7 @@ def run_ours(args, rank, world, local):
     torch.cuda.synchronize(dev)
     e_ms = e0.elapsed_time(e1) / e_steps
     e_ms = reduce_max(pg, e_ms, dev)
+    link = host_link(dev, h2d, d2h, e_ms)
 
     decode = const_input = cayley = born = backward = None
     if not args.no_decode:
@@ -327,6 +330,7 @@ def run_ours(args, rank, world, local):
     if not args.no_backward:
         backward = bench_backward(args, dev)
     precise = None if args.no_precise else bench_precise(args, dev)
+    tf32 = None if args.no_tf32 else bench_tf32(args, dev)
     long_seq = None
     if not args.no_long:
         long_seq = bench_long_seq(args, dev)
@@ -357,7 +361,8 @@ def run_ours(args, rank, world, local):
         "roofline": roof,
         "e2e": {"value": round(whole_job_rate(world, units, e_ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e_ms, 5),
-                "path": "cssd_chunked_forward_host (pinned host tensors streamed in pieces) + cssd_step"},
+                "path": "cssd_chunked_forward_host (pinned host tensors streamed in pieces) + cssd_step",
+                "link": link},
         "gpu_launches": launches * args.steps,
         "clocks": clk.summary(),
     }
@@ -373,6 +378,8 @@ def run_ours(args, rank, world, local):
         out["backward"] = backward
     if precise:
         out["precise_forward"] = precise
+    if tf32:
+        out["tf32_forward"] = tf32
     if long_seq:
         out["long_seq"] = long_seq
     if world == 1 and not args.no_cpu_baseline:
@@ -380,6 +387,51 @@ def run_ours(args, rank, world, local):
     print(json.dumps(out), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def host_link(dev, h2d_bytes, d2h_bytes, e2e_ms):
+    """The host link alone on the step's bytes, timed in the same run as e2e:
+    one pinned-to-device copy of the step's inputs and one device-to-pinned copy
+    of its outputs, each alone and then both at once on two streams (what a
+    step that hides all compute under the copies would take).  `frac` = that
+    concurrent copy time / the e2e step time (1.0: e2e runs at the link's rate)."""
+    import torch
+
+    src = torch.empty(h2d_bytes, dtype=torch.uint8).pin_memory()
+    dst_h = torch.empty(d2h_bytes, dtype=torch.uint8).pin_memory()
+    d_in = torch.empty(h2d_bytes, dtype=torch.uint8, device=dev)
+    d_out = torch.empty(d2h_bytes, dtype=torch.uint8, device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+    def timed(fn, reps=5):
+        for _ in range(2):
+            fn()
+        torch.cuda.synchronize(dev)
+        best = float("inf")
+        for _ in range(reps):
+            t = time.perf_counter()
+            fn()
+            torch.cuda.synchronize(dev)
+            best = min(best, (time.perf_counter() - t) * 1e3)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s_in):
+            d_in.copy_(src, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s_out):
+            dst_h.copy_(d_out, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    h_ms, d_ms, b_ms = timed(h2d), timed(d2h), timed(both)
+    return {"h2d_gbs": round(h2d_bytes / h_ms / 1e6, 1), "d2h_gbs": round(d2h_bytes / d_ms / 1e6, 1),
+            "h2d_ms": round(h_ms, 4), "d2h_ms": round(d_ms, 4), "both_ms": round(b_ms, 4),
+            "link_gbs": round((h2d_bytes + d2h_bytes) / b_ms / 1e6, 1), "link_frac": round(b_ms / e2e_ms, 4),
+            "note": "pinned copies of the step's bytes, best of 5 host-timed reps; link_frac = both_ms / e2e ms"}
 
 
 def bench_decode(args, dev):
@@ -728,6 +780,16 @@ def fused_tensor(units, dstate, k_ms, passes=1, operand="tf32"):
 
 def bench_precise(args, dev):
     """Split-precision forward (cssd_chunked_forward_precise) on the mamba2_layer workload."""
+    return bench_operand_variant(args, dev, "precise")
+
+
+def bench_tf32(args, dev):
+    """TF32-operand forward (cssd_chunked_forward_tf32, the TF32 fused kernel at
+    dstate 64) on the mamba2_layer workload, beside the half-operand headline."""
+    return bench_operand_variant(args, dev, "tf32")
+
+
+def bench_operand_variant(args, dev, variant):
     import torch
 
     from complex_valued_state_gb300 import cssd
@@ -745,7 +807,7 @@ def bench_precise(args, dev):
 
     def fwd():
         cssd.chunked_forward(g["x"], g["dt"], g["A"], g["B"], g["C"], g["D"], chunk=ch, y=y, h_final=h, workspace=ws,
-                             precise=True)
+                             precise=variant == "precise", tf32=variant == "tf32")
 
     for _ in range(3):
         fwd()
@@ -770,12 +832,18 @@ def bench_precise(args, dev):
     alg = units * (8 * P + 16 * N + 4 + 8 * P)
     hbm, kind = peaks()
     gbs = alg / (k_ms / 1e3) / 1e9
-    tensor = fused_tensor(units, N, k_ms, passes=3)  # hi.hi, hi.lo, lo.hi
-    return {"workload": f"mamba2_layer Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch}, split-precision forward",
+    if variant == "precise":
+        tensor = fused_tensor(units, N, k_ms, passes=3)  # hi.hi, hi.lo, lo.hi
+        label, kname, tkey = "split-precision forward", "fused_chunk_kernel (split)", "fused_chunk_kernel_split"
+    else:
+        tensor = fused_tensor(units, N, k_ms)
+        label, kname, tkey = "TF32-operand forward", "fused_chunk_kernel (tf32)", "fused_chunk_kernel_tf32"
+    return {"workload": f"mamba2_layer Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch}, {label}",
             "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_call": round(ms, 4), "calls": n,
-            "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel (split)", "achieved": round(gbs, 1),
+            "dtype": "f32 (split TF32 operands)" if variant == "precise" else "tf32",
+            "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
-                         "traffic": recorded_traffic("fused_chunk_kernel_split", units),
+                         "traffic": recorded_traffic(tkey, units),
                          "kernel_ms": round(k_ms, 4), "alg_bytes_per_launch": alg},
             "tensor": tensor}
 

@@ -136,7 +136,7 @@ int step_common(const cssd_dims* d, void* h, const void* x, const float* dt, con
 // cssd_chunked_forward_h0.
 int forward_common(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B, const void* C,
                    const float* D, const void* h0, void* y, void* h_final, int chunk, void* workspace,
-                   size_t workspace_bytes, cssd_stream_t stream_, bool precise = false) {
+                   size_t workspace_bytes, cssd_stream_t stream_, bool precise = false, bool tf32 = false) {
     int s = check_dims(d, true);
     if (s != CSSD_OK) return s;
     if (!supported_chunk(chunk)) return CSSD_ERR_UNSUPPORTED;
@@ -179,6 +179,7 @@ int forward_common(const cssd_dims* d, const void* x, const float* dt, const voi
     a.h_final = static_cast<float2*>(h_final);
     a.h0 = static_cast<const float2*>(h0);
     a.split_tf32 = precise;
+    a.tf32_operands = tf32;
     const cudaError_t e = cssd::launch_forward(a, ws, stream);
     if (!workspace) cudaFreeAsync(ws, stream);
     return e == cudaSuccess ? CSSD_OK : CSSD_ERR_CUDA;
@@ -271,6 +272,13 @@ int cssd_chunked_forward_precise(const cssd_dims* d, const void* x, const float*
                                  const void* C, const float* D, const void* h0, void* y, void* h_final, int chunk,
                                  void* workspace, size_t workspace_bytes, cssd_stream_t stream_) {
     return forward_common(d, x, dt, A, B, C, D, h0, y, h_final, chunk, workspace, workspace_bytes, stream_, true);
+}
+
+int cssd_chunked_forward_tf32(const cssd_dims* d, const void* x, const float* dt, const void* A, const void* B,
+                              const void* C, const float* D, const void* h0, void* y, void* h_final, int chunk,
+                              void* workspace, size_t workspace_bytes, cssd_stream_t stream_) {
+    return forward_common(d, x, dt, A, B, C, D, h0, y, h_final, chunk, workspace, workspace_bytes, stream_, false,
+                          true);
 }
 
 int cssd_step(const cssd_dims* d, void* h, const void* x, const float* dt, const void* A, const void* B,

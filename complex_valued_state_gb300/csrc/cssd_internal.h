@@ -50,6 +50,9 @@ struct FwdArgs {
     // Tensor-core path only: split-precision operands (three TF32 products per
     // product, about fp32 accuracy, one CTA per SM) instead of plain TF32.
     bool split_tf32 = false;
+    // Tensor-core path only: plain TF32 operands on every tensor-core shape
+    // (dstate 64 otherwise runs half operands with per-tile scales).
+    bool tf32_operands = false;
     unsigned mode = 0;  // kFwd* bits (tensor-core path only); D may be null (no skip) when set
     // kFwdDump: the state chunk c hands to chunk c + 1, in the rotated frame,
     // at dump[((bh * NH + half) * (nc + 1) + c + 1) * 2 * 64 * 64 + part * 64 * 64 + p * 64 + n]

@@ -1553,6 +1553,9 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
                             : launch_fused<1, false, true>(p, BH * nc, true, st);
     }
     if (a.split_tf32) return NH == 1 ? launch_fused<1, true, false>(p, BH * nc, true, st) : cudaErrorNotSupported;
+    if (a.tf32_operands)
+        return NH == 1 ? launch_fused<1, false, false>(p, BH * nc, true, st)
+                       : launch_fused<2, false, false>(p, BH * nc, true, st);
     return NH == 1 ? launch_fused_h16(p, BH * nc, st) : launch_fused<2, false, false>(p, BH * nc, true, st);
 }
 

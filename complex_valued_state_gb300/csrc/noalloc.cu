@@ -36,7 +36,7 @@
 namespace {
 
 constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
-constexpr int kMaxDevices = 64;
+constexpr int kMaxDevices = 128;  // the bound the library's other per-device caches use
 
 // The scratch array.  In host code this name is only a stand-in for the
 // symbol; its device address comes from cudaGetSymbolAddress.

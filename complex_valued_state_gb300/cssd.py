@@ -32,7 +32,7 @@ STATUS = {
 
 # Every symbol include/cssd.h declares.
 EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward", "cssd_chunked_forward_h0",
-           "cssd_chunked_forward_precise",
+           "cssd_chunked_forward_precise", "cssd_chunked_forward_tf32",
            "cssd_host_forward_device_bytes", "cssd_chunked_forward_host",
            "cssd_backward_workspace_bytes", "cssd_chunked_backward",
            "cssd_chunked_forward_noalloc", "cssd_step", "cssd_step_n", "cssd_step_infinite", "cssd_cayley_scan", "cssd_born_attention",
@@ -76,6 +76,8 @@ def load(path: str = LIB_PATH):
             lib.cssd_chunked_forward_h0.restype = ctypes.c_int
             lib.cssd_chunked_forward_precise.argtypes = [dims_p] + [vp] * 9 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
             lib.cssd_chunked_forward_precise.restype = ctypes.c_int
+            lib.cssd_chunked_forward_tf32.argtypes = [dims_p] + [vp] * 9 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
+            lib.cssd_chunked_forward_tf32.restype = ctypes.c_int
             lib.cssd_host_forward_device_bytes.argtypes = [dims_p, ctypes.c_int, ctypes.c_int64]
             lib.cssd_host_forward_device_bytes.restype = ctypes.c_size_t
             lib.cssd_chunked_forward_host.argtypes = [dims_p] + [vp] * 9 + [ctypes.c_int, ctypes.c_int64, vp,
@@ -197,10 +199,10 @@ def forward_launches(batch: int, seqlen: int, nheads: int, dstate: int, headdim:
 
 
 def chunked_forward(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None, want_state: bool = True,
-                    workspace=None, stream=None, h0=None, precise: bool = False):
+                    workspace=None, stream=None, h0=None, precise: bool = False, tf32: bool = False):
     """cssd_chunked_forward (cssd_chunked_forward_h0 when `h0` is given,
-    cssd_chunked_forward_precise when `precise`) on device tensors; returns
-    (y, h_final or None).
+    cssd_chunked_forward_precise when `precise`, cssd_chunked_forward_tf32 when
+    `tf32`) on device tensors; returns (y, h_final or None).
 
     x complex64 [Bz,T,H,P]; dt float32 [Bz,T,H]; A complex64 [H];
     B, C complex64 [Bz,T,H,N]; D float32 [H]; h0 complex64 [Bz,H,N,P], the
@@ -231,14 +233,17 @@ def chunked_forward(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None,
             raise ValueError("workspace must be a contiguous tensor on the inputs' device")
         ws_bytes = workspace.numel() * workspace.element_size()
     d = Dims(Bz, T, H, N, P)
-    if precise:
+    if precise and tf32:
+        raise ValueError("precise and tf32 select different entry points; pass at most one")
+    if precise or tf32:
         if h0 is not None:
             _check(h0, "h0", c64, (Bz, H, N, P), dev)
-        st = lib.cssd_chunked_forward_precise(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C),
-                                              _ptr(D), _ptr(h0), _ptr(y), _ptr(h_final), int(chunk),
-                                              _ptr(workspace), ctypes.c_size_t(ws_bytes), _stream_handle(stream, dev))
+        name = "cssd_chunked_forward_precise" if precise else "cssd_chunked_forward_tf32"
+        st = getattr(lib, name)(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(h0),
+                                _ptr(y), _ptr(h_final), int(chunk), _ptr(workspace), ctypes.c_size_t(ws_bytes),
+                                _stream_handle(stream, dev))
         if st != CSSD_OK:
-            raise CssdError(st, "cssd_chunked_forward_precise")
+            raise CssdError(st, name)
         return y, h_final
     if h0 is None:
         st = lib.cssd_chunked_forward(ctypes.byref(d), _ptr(x), _ptr(dt), _ptr(A), _ptr(B), _ptr(C), _ptr(D),

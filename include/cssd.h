@@ -30,8 +30,9 @@
  *     the host before anything is launched and leave every output untouched.
  *     A launch failure returns CSSD_ERR_CUDA.  Faults during execution surface
  *     at the caller's next synchronisation.  Nothing aborts or traps.
- *   - CUDA graphs: every device-pointer entry point may be called while
- *     `stream` is being captured, and the graph's replays then redo the call's
+ *   - CUDA graphs: every device-pointer entry point except
+ *     cssd_chunked_forward_noalloc (about which this note says nothing) may
+ *     be called while `stream` is being captured, and the graph's replays then redo the call's
  *     work on the captured buffers.  Make one call of the same entry point on
  *     the device before the capture (it fills per-device caches of kernel
  *     attributes and occupancy), and pass a workspace where the call takes
@@ -178,6 +179,24 @@ int cssd_chunked_forward_precise(const cssd_dims* dims, const void* x, const flo
                                  const void* B, const void* C, const float* D, const void* h0, void* y,
                                  void* h_final, int chunk, void* workspace, size_t workspace_bytes,
                                  cssd_stream_t stream);
+
+/* cssd_chunked_forward_h0 with the tensor-core contractions taken on TF32
+ * operands (10 explicit mantissa bits, the fp32 exponent range, rounded to
+ * nearest) on every tensor-core shape, accumulation fp32.  The chunked form of
+ * "The Chunkwise Complex SSD Algorithm" (sections 4.3-4.5) is exact up to
+ * rounding; the pages fix no operand precision for its GEMMs.
+ * cssd_chunked_forward takes half operands with a power-of-two scale per tile
+ * and operand at dstate 64 (the same 11-bit significand, a narrower exponent
+ * range covered by the per-tile scales) and TF32 at dstate 128; this entry
+ * point keeps TF32 at dstate 64 too, for callers and measurements that want
+ * the wider operand exponent range without per-tile scaling.  Shapes the
+ * CUDA-core kernels take run them (fp32), as in cssd_chunked_forward.
+ * Arguments, workspace size (cssd_workspace_bytes) and status are those of
+ * cssd_chunked_forward_h0; h0 may be NULL. */
+int cssd_chunked_forward_tf32(const cssd_dims* dims, const void* x, const float* dt, const void* A,
+                              const void* B, const void* C, const float* D, const void* h0, void* y,
+                              void* h_final, int chunk, void* workspace, size_t workspace_bytes,
+                              cssd_stream_t stream);
 
 /* Forward over tensors that live in HOST memory, streamed through the device
  * in pieces of `piece_len` tokens: while one piece computes, the next one's

@@ -174,6 +174,14 @@ def test_initial_state_and_host_forward_argument_errors(lib):
     q[7] = None  # y
     assert f(ctypes.byref(ok), *q, 64, None, 0, None) == -1
     assert f(ctypes.byref(ok), *p, 64, ctypes.c_void_p(0x900000), 16, None) == -5
+    f = lib.cssd_chunked_forward_tf32  # same arguments and checks as the h0 forward
+    assert f(None, *p, 64, None, 0, None) == -1
+    assert f(ctypes.byref(ok), *p, 128 + 1, None, 0, None) == -3
+    assert f(ctypes.byref(cssd.Dims(1, 64, 1, 24, 16)), *p, 64, None, 0, None) == -3
+    q = list(p)
+    q[3] = ctypes.c_void_p(0x10308)  # B: 16-byte alignment
+    assert f(ctypes.byref(ok), *q, 64, None, 0, None) == -4
+    assert f(ctypes.byref(ok), *p, 64, ctypes.c_void_p(0x900000), 16, None) == -5
     f = lib.cssd_chunked_forward_precise  # same arguments and checks
     assert f(None, *p, 64, None, 0, None) == -1
     assert f(ctypes.byref(ok), *p, 128 + 1, None, 0, None) == -3
