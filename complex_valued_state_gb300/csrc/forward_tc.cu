@@ -205,6 +205,23 @@ __device__ __forceinline__ void st_cell(unsigned long long* q, float v, uint32_t
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(q), "l"(w) : "memory");
 }
 
+// Four consecutive cells (32 bytes, 32-byte aligned) as one vector access;
+// each 8-byte cell stays single-copy atomic.
+__device__ __forceinline__ void ld_cell4(const unsigned long long* q, unsigned long long* w) {
+    asm volatile("ld.relaxed.gpu.global.v4.b64 {%0, %1, %2, %3}, [%4];"
+                 : "=l"(w[0]), "=l"(w[1]), "=l"(w[2]), "=l"(w[3])
+                 : "l"(q)
+                 : "memory");
+}
+__device__ __forceinline__ unsigned long long cell_word(float v, uint32_t tag) {
+    return ((unsigned long long)tag << 32) | __float_as_uint(v);
+}
+__device__ __forceinline__ void st_cell4(unsigned long long* q, const unsigned long long* w) {
+    asm volatile("st.relaxed.gpu.global.v4.b64 [%0], {%1, %2, %3, %4};" ::"l"(q), "l"(w[0]), "l"(w[1]), "l"(w[2]),
+                 "l"(w[3])
+                 : "memory");
+}
+
 // CPT consecutive TMEM columns of this warp's lane quarter into registers.
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CPT]) {
 #pragma unroll
@@ -820,16 +837,16 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
 namespace h16 {
 constexpr int NT = 256;              // threads per CTA
 constexpr int CPT = 32;              // accumulator columns per thread
-constexpr uint32_t RAW_B = 64 * 528;  // raw B rows (raw x rows at 0), 528 bytes per token each
+constexpr uint32_t RAW_B = 64 * 576;  // raw B rows (raw x rows at 0), 576 bytes per token each
 constexpr uint32_t PLANE = 64 * 64 * 2;  // one 64 x 64 half plane
 constexpr uint32_t STACK = 3 * PLANE;     // [-Ai; Ar; Ai]: 192 rows x K 64
 constexpr uint32_t BLK = 1024;            // 64 rows further down a stack
 constexpr uint32_t XS = 0;       // X^T stack (rows p, K = l), the whole tile
 constexpr uint32_t FP = STACK;   // F planes (rows n, K = l)
 constexpr uint32_t CS = STACK;   // then the Ct stack (rows l, K = n)
-constexpr uint32_t MP = STACK;   // then M planes (rows l, K = s)
 constexpr uint32_t BP = 2 * STACK;  // Bt planes (rows s, K = n)
-constexpr uint32_t HS = 2 * STACK;  // then the H_c^T stack (rows p, K = n)
+constexpr uint32_t MP = 2 * STACK;  // then M planes (rows l, K = s), once G has read Bt
+constexpr uint32_t HS = 2 * STACK;  // then the H_c^T stack (rows p, K = n), once Y_diag has read M
 constexpr int BYTES = HS + STACK;   // 72 KB
 constexpr uint32_t COL_A = 0, COL_B = 64, TMEM_COLS = 128;
 constexpr uint32_t STACK_LBO = 24 * 128, PLANE_LBO = 8 * 128, SBO = 128;
@@ -843,19 +860,31 @@ __device__ __forceinline__ uint32_t koff16(int row, int k, int rows) {
     return (uint32_t)((((k >> 3) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + ((k & 7) << 1));
 }
 // Raw rows of this kernel, as the bulk copies leave them: token row l at
-// 528 l (512 bytes and 16 of padding), 16-byte chunk j at 16 j.  The padding
-// moves each row by one bank group, so that each eight-lane phase of the
-// transform's 16-byte reads (four even rows, two neighbouring chunks) falls on
-// eight distinct bank groups.
-constexpr int RAW_LD = 528;
+// 576 l (512 bytes and 64 of padding), 16-byte chunk j at 16 j.  The padding
+// moves consecutive rows half a bank cycle apart, so that each eight-lane
+// phase of the transform's 16-byte reads (two rows, four neighbouring chunks
+// each) falls on eight distinct bank groups.
+constexpr int RAW_LD = 576;
 __device__ __forceinline__ uint32_t raw_at(int l, int j) { return (uint32_t)(l * RAW_LD + j * 16); }
 // Two values as a half pair, the first in the low 16 bits (the lower K).
 __device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
     const __half2 v = __floats2half2_rn(lo, hi);
     return *reinterpret_cast<const uint32_t*>(&v);
 }
-__device__ __forceinline__ void st_u32(unsigned char* base, uint32_t off, uint32_t v) {
-    *reinterpret_cast<uint32_t*>(base + off) = v;
+// Four 8 x 8 half matrices from registers into shared memory: lanes 8m..8m+7
+// give the addresses of the eight 16-byte rows of matrix m; register m of lane
+// t holds the pair (row t/4, columns 2(t%4), 2(t%4)+1) of matrix m.  With
+// .trans each matrix is stored transposed (that pair lands in rows 2(t%4) and
+// 2(t%4)+1 at column t/4).
+__device__ __forceinline__ void stm4(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0), "r"(r1),
+                 "r"(r2), "r"(r3)
+                 : "memory");
+}
+__device__ __forceinline__ void stm4t(uint32_t addr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(r0),
+                 "r"(r1), "r"(r2), "r"(r3)
+                 : "memory");
 }
 __device__ __forceinline__ float maxabs4(float4 v, float m) {
     return fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
@@ -866,11 +895,8 @@ __device__ __forceinline__ float ex2_approx(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
     return r;
 }
-__device__ __forceinline__ unsigned warp_max(unsigned v) {
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
-}
+// Largest of a warp's values (non-negative fp32 bit patterns order as integers).
+__device__ __forceinline__ unsigned warp_max(unsigned v) { return __reduce_max_sync(0xffffffffu, v); }
 // Scale 2^(14-e) and its inverse 2^(e-14) for a tile whose largest component
 // has the fp32 bit pattern `bits` (e its exponent): the largest component goes
 // to [2^14, 2^15), the top of the half range, so that components far smaller
@@ -936,29 +962,14 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const uint32_t sb0 = tc::smem_u32(smem);
     const float Dh = __ldg(p.D + h);  // skip coefficient, needed only at the end: fetched now
 
-    // This thread's items: 2 x 2 complex blocks, tokens (l0, l0 + 1) x
-    // columns (n, n + 1) with n = 16 i + 8 g + 2 bq, i < 4 (raw chunk n / 2).
-    // Lanes with g = 1 store the second row of each pair first, so that every
-    // 32-bit operand store of a warp covers 32 distinct banks.
-    const int aq = lane & 3, bq = (lane >> 2) & 3, g = (lane >> 4) & 1;
-    const int l0 = 8 * warp + 2 * aq;
-    const bool swp = g != 0;
-    auto jof = [&](int i) { return 8 * i + 4 * g + bq; };
-
-    // Rows of x, B and C of a later tile into L2 (when the launch asks for it).
-    if (p.pf_dist > 0 && tid < 3 * CH) {
-        const int pt = ticket + p.pf_dist;
-        if (pt < p.BH * p.nc) {
-            const int pc = pt / p.BH, pbh = pt - pc * p.BH;
-            const int tok = pc * CH + (tid & (CH - 1));
-            if (tok < p.T) {
-                const size_t prow = ((size_t)(pbh / p.H) * p.T + tok) * p.H + pbh % p.H;
-                const int which = tid / CH;  // 0: x, 1: B, 2: C
-                if (which == 0) prefetch_l2(p.x + prow * (PD / 2), PD * 8);
-                else prefetch_l2((which == 1 ? p.B : p.C) + prow * (N / 2), N * 8);
-            }
-        }
-    }
+    // Lane t of warp w owns token l = 8 w + t/4 of the tile and, in each
+    // 8-column block b, the column pair 8 b + 2 (t%4), +1 of x, B and C:
+    // exactly its fragment of the 8 x 8 core matrix (tokens 8w.., columns
+    // 8b..) that stmatrix stores, untransposed for operands with rows l (Bt,
+    // Ct) and transposed for operands with K = l (X^T, F).
+    const int l = 8 * warp + (lane >> 2), jp = lane & 3;
+    const int mrow = lane >> 3;                      // the matrix this lane addresses in an x4 store
+    const uint32_t r16 = (uint32_t)(lane & 7) << 4;  // and its row within that matrix
 
     // ---- 0. loads: dt tables, raw x and B rows by bulk copies (one 512-byte
     // row per thread of the first four warps, completing on mbar[4]; rows past
@@ -982,15 +993,11 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
             for (int k = 0; k < 32; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
     }
-    float4 cv[4][2];
+    const bool lok = t0 + l < p.T;
+    float4 cv[8];
 #pragma unroll
-    for (int i = 0; i < 4; ++i)
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const int l = l0 + rr;
-            cv[i][rr] = (t0 + l < p.T) ? __ldg(p.C + (row0 + (long long)l * H) * (N / 2) + jof(i))
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
+    for (int bb = 0; bb < 8; ++bb)
+        cv[bb] = lok ? __ldg(p.C + (row0 + (long long)l * H) * (N / 2) + 4 * bb + jp) : make_float4(0.f, 0.f, 0.f, 0.f);
 
     // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
     if (tid < CH) {
@@ -1006,6 +1013,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     __syncthreads();
     const float rho_end = s_rho[CH - 1];
     const float eend = __expf(rho_end);
+    const float2 rot = s_rot[l];
 
     const uint32_t ID = tc::idesc_f16(128, 64);
     // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`;
@@ -1042,19 +1050,17 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
 
     // ---- 2. the X^T stack over raw x (rows p, K = l), scaled; the scales of
     // x and C; Ct = e^{i Theta} C as scaled half pairs in registers.
-    uint32_t cw[4][2][2];  // [item][row l0 + rr][re, im]: columns (n, n + 1)
+    uint32_t cre[8], cim[8];  // Ct of this lane's token, block bb: (real, imaginary) half pairs
     float inv_x, inv_c;
     {
-        float4 xv[4][2];
+        float4 xv[8];
         float fx = 0.f, fc = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                xv[i][rr] = *reinterpret_cast<const float4*>(smem + raw_at(l0 + rr, jof(i)));
-                fx = maxabs4(xv[i][rr], fx);
-                fc = maxabs4(cv[i][rr], fc);
-            }
+        for (int bb = 0; bb < 8; ++bb) {
+            xv[bb] = *reinterpret_cast<const float4*>(smem + raw_at(l, 4 * bb + jp));
+            fx = maxabs4(xv[bb], fx);
+            fc = maxabs4(cv[bb], fc);
+        }
         const unsigned mx = warp_max(__float_as_uint(fx)), mc = warp_max(__float_as_uint(fc));
         if (lane == 0) {
             atomicMax(&s_max[0], mx);
@@ -1064,34 +1070,29 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         const Pow2 sx(s_max[0]), sc(s_max[2]);
         inv_x = sx.inv;
         inv_c = sc.inv;
+        const float2 r0 = make_float2(rot.x * sc.s, rot.y * sc.s);  // the rotation with C's scale
 #pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            const float2 r0 = s_rot[l0 + rr];
-            const float2 rot = make_float2(r0.x * sc.s, r0.y * sc.s);  // the rotation with C's scale
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const float4 v = cv[i][rr];
-                const float c0r = rot.x * v.x - rot.y * v.y, c0i = rot.x * v.y + rot.y * v.x;
-                const float c1r = rot.x * v.z - rot.y * v.w, c1i = rot.x * v.w + rot.y * v.z;
-                cw[i][rr][0] = pack_h2(c0r, c1r);
-                cw[i][rr][1] = pack_h2(c0i, c1i);
-            }
+        for (int bb = 0; bb < 8; ++bb) {
+            const float4 v = cv[bb];
+            const float c0r = r0.x * v.x - r0.y * v.y, c0i = r0.x * v.y + r0.y * v.x;
+            const float c1r = r0.x * v.z - r0.y * v.w, c1i = r0.x * v.w + r0.y * v.z;
+            cre[bb] = pack_h2(c0r, c1r);
+            cim[bb] = pack_h2(c0i, c1i);
         }
+        // transposed stores: matrix q of the 24 (block b = q / 3 of 8 columns,
+        // stack block q % 3: -Xi, Xr, Xi)
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int n = 16 * i + 8 * g + 2 * bq;  // rows p = n, n + 1
-            const uint32_t oa = XS + koff16(n, l0, 192), ob = XS + koff16(n + 1, l0, 192);
-            const float4 u = xv[i][0], w = xv[i][1];  // tokens l0, l0 + 1
-            const uint32_t ra = pack_h2(u.x * sx.s, w.x * sx.s), rb = pack_h2(u.z * sx.s, w.z * sx.s);
-            const uint32_t ia = pack_h2(u.y * sx.s, w.y * sx.s), ib = pack_h2(u.w * sx.s, w.w * sx.s);
-            const uint32_t o1 = swp ? ob : oa, o2 = swp ? oa : ob;
-            const uint32_t r1w = swp ? rb : ra, r2w = swp ? ra : rb, i1w = swp ? ib : ia, i2w = swp ? ia : ib;
-            st_u32(smem, o1, i1w ^ NEG2);
-            st_u32(smem, o2, i2w ^ NEG2);
-            st_u32(smem, o1 + BLK, r1w);
-            st_u32(smem, o2 + BLK, r2w);
-            st_u32(smem, o1 + 2 * BLK, i1w);
-            st_u32(smem, o2 + 2 * BLK, i2w);
+        for (int i = 0; i < 6; ++i) {
+            uint32_t rg[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int q = 4 * i + k, bb = q / 3, blk = q % 3;  // compile-time
+                const float4 v = xv[bb];
+                const uint32_t im = pack_h2(v.y * sx.s, v.w * sx.s);
+                rg[k] = blk == 1 ? pack_h2(v.x * sx.s, v.z * sx.s) : blk == 0 ? (im ^ NEG2) : im;
+            }
+            const int q = 4 * i + mrow, bb = (q * 11) >> 5, blk = q - 3 * bb;  // q / 3 for q < 24
+            stm4t(sb0 + XS + ((uint32_t)(warp * 24 + 8 * blk + bb) << 7) + r16, rg[0], rg[1], rg[2], rg[3]);
         }
     }
 
@@ -1099,52 +1100,37 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // B, scaled by B's scale; S'^T = X^T F^T.
     float inv_b;
     {
-        float4 bv[4][2];
+        float4 bv[8];
         float fb = 0.f;
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-                bv[i][rr] = *reinterpret_cast<const float4*>(smem + RAW_B + raw_at(l0 + rr, jof(i)));
-                fb = maxabs4(bv[i][rr], fb);
-            }
+        for (int bb = 0; bb < 8; ++bb) {
+            bv[bb] = *reinterpret_cast<const float4*>(smem + RAW_B + raw_at(l, 4 * bb + jp));
+            fb = maxabs4(bv[bb], fb);
+        }
         const unsigned mb = warp_max(__float_as_uint(fb));
         if (lane == 0) atomicMax(&s_max[1], mb);
         __syncthreads();  // raw B is overwritten below
         const Pow2 sbk(s_max[1]);
         inv_b = sbk.inv;
-        // rotations with B's scale: the Bt values below are scaled
-        const float ds0 = __expf(rho_end - s_rho[l0]), ds1 = __expf(rho_end - s_rho[l0 + 1]);
-        const float2 q0 = s_rot[l0], q1 = s_rot[l0 + 1];
-        const float2 r0 = make_float2(q0.x * sbk.s, q0.y * sbk.s), r1 = make_float2(q1.x * sbk.s, q1.y * sbk.s);
+        // Bt = e^{-i Theta} B scaled, F = e^{rho_end - rho_l} Bt
+        const float ds = __expf(rho_end - s_rho[l]);
+        const float2 r0 = make_float2(rot.x * sbk.s, rot.y * sbk.s);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const int n = 16 * i + 8 * g + 2 * bq;
-            const float4 u = bv[i][0], w = bv[i][1];
-            // Bt = e^{-i Theta} B at (l0, n), (l0, n + 1), (l0 + 1, n), (l0 + 1, n + 1)
-            const float u0r = r0.x * u.x + r0.y * u.y, u0i = r0.x * u.y - r0.y * u.x;
-            const float u1r = r0.x * u.z + r0.y * u.w, u1i = r0.x * u.w - r0.y * u.z;
-            const float w0r = r1.x * w.x + r1.y * w.y, w0i = r1.x * w.y - r1.y * w.x;
-            const float w1r = r1.x * w.z + r1.y * w.w, w1i = r1.x * w.w - r1.y * w.z;
-            {
-                const uint32_t oa = BP + koff16(l0, n, 64), ob = BP + koff16(l0 + 1, n, 64);
-                const uint32_t ra = pack_h2(u0r, u1r), rb = pack_h2(w0r, w1r);
-                const uint32_t ia = pack_h2(u0i, u1i), ib = pack_h2(w0i, w1i);
-                st_u32(smem, swp ? ob : oa, swp ? rb : ra);
-                st_u32(smem, swp ? oa : ob, swp ? ra : rb);
-                st_u32(smem + PLANE, swp ? ob : oa, swp ? ib : ia);
-                st_u32(smem + PLANE, swp ? oa : ob, swp ? ia : ib);
+            uint32_t rb[4], rf[4];
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const float4 v = bv[2 * i + k];
+                const float u0r = r0.x * v.x + r0.y * v.y, u0i = r0.x * v.y - r0.y * v.x;
+                const float u1r = r0.x * v.z + r0.y * v.w, u1i = r0.x * v.w - r0.y * v.z;
+                rb[2 * k] = pack_h2(u0r, u1r);
+                rb[2 * k + 1] = pack_h2(u0i, u1i);
+                rf[2 * k] = pack_h2(u0r * ds, u1r * ds);
+                rf[2 * k + 1] = pack_h2(u0i * ds, u1i * ds);
             }
-            {
-                // F[n][l] = exp(rho_end - rho_l) Bt[l][n]; row n holds K = (l0, l0 + 1)
-                const uint32_t oa = FP + koff16(n, l0, 64), ob = FP + koff16(n + 1, l0, 64);
-                const uint32_t ra = pack_h2(u0r * ds0, w0r * ds1), rb = pack_h2(u1r * ds0, w1r * ds1);
-                const uint32_t ia = pack_h2(u0i * ds0, w0i * ds1), ib = pack_h2(u1i * ds0, w1i * ds1);
-                st_u32(smem, swp ? ob : oa, swp ? rb : ra);
-                st_u32(smem, swp ? oa : ob, swp ? ra : rb);
-                st_u32(smem + PLANE, swp ? ob : oa, swp ? ib : ia);
-                st_u32(smem + PLANE, swp ? oa : ob, swp ? ia : ib);
-            }
+            const int q = 4 * i + mrow, bb = q >> 1, pl = q & 1;  // matrix q: block bb, plane pl
+            stm4(sb0 + BP + pl * PLANE + ((uint32_t)(bb * 8 + warp) << 7) + r16, rb[0], rb[1], rb[2], rb[3]);
+            stm4t(sb0 + FP + pl * PLANE + ((uint32_t)(warp * 8 + bb) << 7) + r16, rf[0], rf[1], rf[2], rf[3]);
         }
     }
     issue(tmem + COL_A, sb0 + XS, sb0 + FP, PLANE_LBO, PLANE, &mbar[0]);
@@ -1152,131 +1138,36 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // ---- 4. Ct stack (rows l, K = n) over F once S'^T has read it; G = Ct Bt^T
     wait_bar(&mbar[0]);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const int n = 16 * i + 8 * g + 2 * bq;
-        const uint32_t oa = CS + koff16(l0, n, 192), ob = CS + koff16(l0 + 1, n, 192);
-        const uint32_t o1 = swp ? ob : oa, o2 = swp ? oa : ob;
-        const uint32_t r1w = swp ? cw[i][1][0] : cw[i][0][0], r2w = swp ? cw[i][0][0] : cw[i][1][0];
-        const uint32_t i1w = swp ? cw[i][1][1] : cw[i][0][1], i2w = swp ? cw[i][0][1] : cw[i][1][1];
-        st_u32(smem, o1, i1w ^ NEG2);
-        st_u32(smem, o2, i2w ^ NEG2);
-        st_u32(smem, o1 + BLK, r1w);
-        st_u32(smem, o2 + BLK, r2w);
-        st_u32(smem, o1 + 2 * BLK, i1w);
-        st_u32(smem, o2 + 2 * BLK, i2w);
+    for (int i = 0; i < 6; ++i) {
+        uint32_t rg[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q = 4 * i + k, bb = q / 3, blk = q % 3;  // compile-time
+            rg[k] = blk == 1 ? cre[bb] : blk == 0 ? (cim[bb] ^ NEG2) : cim[bb];
+        }
+        const int q = 4 * i + mrow, bb = (q * 11) >> 5, blk = q - 3 * bb;
+        stm4(sb0 + CS + ((uint32_t)(bb * 24 + 8 * blk + warp) << 7) + r16, rg[0], rg[1], rg[2], rg[3]);
     }
     issue(tmem + COL_B, sb0 + CS, sb0 + BP, PLANE_LBO, PLANE, &mbar[1]);
 
-    // ---- 5. hand-off: the thread owns headdim column p = lrow of part `part`
-    // and the CPT state rows n from c0col (S'^T holds p in its lanes).  It
-    // takes H_c from the cells the same thread position of chunk c-1 wrote and
-    // publishes H_{c+1} = e^{rho_end} H_c + S' in the true scale.  Cells are
-    // laid out [part][n][p], so a warp's accesses are contiguous.
+    // Accumulator roles: lane quarter q, column block of CPT columns;
+    // accumulator row L = 32 q + lane is the real part (L < 64) or the
+    // imaginary part (L >= 64) of row lrow = L mod 64 (token l for G, headdim
+    // p for S'^T, Y_off^T and Y_diag^T).
     const int q = warp & 3, cblk = warp >> 2;
     const int L = q * 32 + lane;
     const int part = L >> 6, lrow = L & 63;
     const int c0col = cblk * CPT;
     const uint32_t lane_base = (uint32_t)(q * 32) << 16;
-    float hv[CPT];
-    {
-        const size_t ring0 = (size_t)bh * RING;
-        const unsigned long long* cin =
-            p.ring + (ring0 + (c % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
-        unsigned long long* cout = p.ring + (ring0 + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)part * PD * NS + lrow;
-        if (c > 0) {
-            const uint32_t want = (uint32_t)c;
-            const long long w0 = clock64();
-            if (lane == 0) {
-                while ((uint32_t)(ld_cell(cin + c0col * NS) >> 32) != want) {
-                    if (clock64() - w0 > p.wait_cycles) break;
-                    __nanosleep(128);
-                }
-            }
-            __syncwarp();
-            bool late = false;
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                while (true) {
-                    // all 16 loads are issued before any tag is examined
-                    unsigned long long w[16];
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) w[j] = ld_cell(cin + (c0col + 16 * half + j) * NS);
-                    bool all = true;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        hv[16 * half + j] = __uint_as_float((uint32_t)w[j]);
-                        all = all && ((uint32_t)(w[j] >> 32) == want);
-                    }
-                    if (all) break;
-                    if (clock64() - w0 > p.wait_cycles) {
-                        late = true;
-                        break;
-                    }
-                    __nanosleep(128);
-                }
-            }
-            if (late) {
-                atomicOr(p.err, 1);
-                if (p.status) atomicOr(p.status, kStatusHandoff);
-            }
-        } else if (p.h0) {
-            const float* src = reinterpret_cast<const float*>(p.h0 + ((size_t)bh * N + c0col) * PD + lrow) + part;
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) hv[j] = __ldg(src + 2 * PD * j);
-        } else {
-#pragma unroll
-            for (int j = 0; j < CPT; ++j) hv[j] = 0.f;
-        }
-        uint32_t r[CPT];
-        tc::fence_after_sync();
-        tc::tmem_ld16(tmem + lane_base + COL_A + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
-        tc::tmem_ld16(tmem + lane_base + COL_A + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
-        tc::tmem_wait_ld();
-        const uint32_t tag = (uint32_t)(c + 1);
-        const float k_s = inv_b * inv_x;  // a product of powers of two: exact
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j]) * k_s), tag);
-        float fh = 0.f;
-#pragma unroll
-        for (int j = 0; j < CPT; ++j) fh = fmaxf(fh, fabsf(hv[j]));
-        const unsigned mh = warp_max(__float_as_uint(fh));
-        if (lane == 0) atomicMax(&s_max[3], mh);
-    }
-    tc::fence_before_sync();
-    __syncthreads();  // the scale of H_c is complete
-    const Pow2 shc(s_max[3]);
-    const float inv_h = shc.inv;
 
-    // ---- 6. H_c^T as the A operand of Y_off^T (stack rows p, K = n) over the
-    // Bt planes once G has read them: this thread holds row p = lrow of part
-    // `part` at the CPT consecutive K = n from c0col.
-    {
-        const float s = shc.s;
-        wait_bar(&mbar[1]);
-        unsigned char* hrow = smem + HS + koff16(lrow, c0col, 192);
-#pragma unroll
-        for (int k8 = 0; k8 < CPT / 8; ++k8) {  // K + 8: one core matrix (24 row groups) further
-            const uint4 v = make_uint4(pack_h2(hv[8 * k8] * s, hv[8 * k8 + 1] * s),
-                                       pack_h2(hv[8 * k8 + 2] * s, hv[8 * k8 + 3] * s),
-                                       pack_h2(hv[8 * k8 + 4] * s, hv[8 * k8 + 5] * s),
-                                       pack_h2(hv[8 * k8 + 6] * s, hv[8 * k8 + 7] * s));
-            if (part == 0) {
-                *reinterpret_cast<uint4*>(hrow + BLK + 3072 * k8) = v;
-            } else {
-                *reinterpret_cast<uint4*>(hrow + 2 * BLK + 3072 * k8) = v;
-                *reinterpret_cast<uint4*>(hrow + 3072 * k8) = make_uint4(v.x ^ NEG2, v.y ^ NEG2, v.z ^ NEG2, v.w ^ NEG2);
-            }
-        }
-    }
-    // Y_off'^T = H_c^T Ct^T over S'^T; the Ct stack's blocks 1 and 2 serve as B planes
-    issue(tmem + COL_A, sb0 + HS, sb0 + CS + BLK, STACK_LBO, BLK, &mbar[2]);
-
-    // ---- 7. masked scores M = L o G (scaled like G) as planes (rows l, K = s)
-    // over Ct once Y_off has read it; Y_diag^T = X^T M^T over G.
+    // ---- 5. masked scores M = L o G (scaled like G) as planes (rows l, K = s)
+    // over Bt once G has read it; Y_diag^T = X^T M^T over G.  Y_diag runs
+    // while the hand-off below waits for the previous chunk's state.
     {
         float m[CPT];
         // a warp whose rows all precede its columns holds only masked scores
         const bool all_masked = c0col > (lrow | 31);
+        wait_bar(&mbar[1]);
         if (all_masked) {
 #pragma unroll
             for (int j = 0; j < CPT; ++j) m[j] = 0.f;
@@ -1302,7 +1193,6 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
                 }
             }
         }
-        wait_bar(&mbar[2]);
         // 16-byte stores: eight consecutive K of one row fill one core-matrix
         // row; K + 8 is one core matrix (8 row groups) further
         unsigned char* mrow = smem + MP + part * PLANE + koff16(lrow, c0col, 64);
@@ -1314,10 +1204,117 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     }
     issue(tmem + COL_B, sb0 + XS, sb0 + MP, PLANE_LBO, PLANE, &mbar[3]);
 
+    // ---- 6. hand-off: the thread owns headdim column p = lrow of part `part`
+    // and the CPT state rows n from c0col (S'^T holds p in its lanes).  It
+    // takes H_c from the cells the same thread position of chunk c-1 wrote and
+    // publishes H_{c+1} = e^{rho_end} H_c + S' in the true scale.  Cells are
+    // laid out [part][n / 4][p][n mod 4], so a thread's cells come in 32-byte
+    // runs of four n (one vector access each, every cell single-copy atomic)
+    // and a warp's accesses are contiguous.
+    float hv[CPT];
+    {
+        const size_t qbase = ((size_t)part * (NS / 4) + (c0col >> 2)) * PD + lrow;  // quad index of n = c0col
+        const unsigned long long* cin = p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS) + 4 * qbase;
+        unsigned long long* cout = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + 4 * qbase;
+        constexpr int QS = 4 * PD;  // cells from one quad of n to the next
+        if (c > 0) {
+            const uint32_t want = (uint32_t)c;
+            const long long w0 = clock64();
+            // one lane per warp watches one cell until it carries this chunk's
+            // tag, then every lane reads all its cells at once
+            if (lane == 0) {
+                while ((uint32_t)(ld_cell(cin) >> 32) != want) {
+                    if (clock64() - w0 > p.wait_cycles) break;
+                    __nanosleep(64);
+                }
+            }
+            __syncwarp();
+            bool late = false;
+            while (true) {
+                unsigned long long w[CPT];
+#pragma unroll
+                for (int j4 = 0; j4 < CPT / 4; ++j4) ld_cell4(cin + QS * j4, w + 4 * j4);
+                bool all = true;
+#pragma unroll
+                for (int j = 0; j < CPT; ++j) {
+                    hv[j] = __uint_as_float((uint32_t)w[j]);
+                    all = all && ((uint32_t)(w[j] >> 32) == want);
+                }
+                if (all) break;
+                if (clock64() - w0 > p.wait_cycles) {
+                    late = true;
+                    break;
+                }
+                __nanosleep(64);
+            }
+            if (late) {
+                atomicOr(p.err, 1);
+                if (p.status) atomicOr(p.status, kStatusHandoff);
+            }
+        } else if (p.h0) {
+            const float* src = reinterpret_cast<const float*>(p.h0 + ((size_t)bh * N + c0col) * PD + lrow) + part;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) hv[j] = __ldg(src + 2 * PD * j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) hv[j] = 0.f;
+        }
+        uint32_t r[CPT];
+        tc::fence_after_sync();
+        tc::tmem_ld16(tmem + lane_base + COL_A + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+        tc::tmem_ld16(tmem + lane_base + COL_A + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+        tc::tmem_wait_ld();
+        const uint32_t tag = (uint32_t)(c + 1);
+        const float k_s = inv_b * inv_x;  // a product of powers of two: exact
+#pragma unroll
+        for (int j4 = 0; j4 < CPT / 4; ++j4) {
+            unsigned long long w[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int j = 4 * j4 + u;
+                w[u] = cell_word(fmaf(eend, hv[j], __uint_as_float(r[j]) * k_s), tag);
+            }
+            st_cell4(cout + QS * j4, w);
+        }
+        float fh = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) fh = fmaxf(fh, fabsf(hv[j]));
+        const unsigned mh = warp_max(__float_as_uint(fh));
+        if (lane == 0) atomicMax(&s_max[3], mh);
+    }
+    tc::fence_before_sync();
+    __syncthreads();  // the scale of H_c is complete
+    const Pow2 shc(s_max[3]);
+    const float inv_h = shc.inv;
+
+    // ---- 7. H_c^T as the A operand of Y_off^T (stack rows p, K = n) over the
+    // M planes once Y_diag has read them: this thread holds row p = lrow of
+    // part `part` at the CPT consecutive K = n from c0col.
+    {
+        const float s = shc.s;
+        wait_bar(&mbar[3]);
+        unsigned char* hrow = smem + HS + koff16(lrow, c0col, 192);
+#pragma unroll
+        for (int k8 = 0; k8 < CPT / 8; ++k8) {  // K + 8: one core matrix (24 row groups) further
+            const uint4 v = make_uint4(pack_h2(hv[8 * k8] * s, hv[8 * k8 + 1] * s),
+                                       pack_h2(hv[8 * k8 + 2] * s, hv[8 * k8 + 3] * s),
+                                       pack_h2(hv[8 * k8 + 4] * s, hv[8 * k8 + 5] * s),
+                                       pack_h2(hv[8 * k8 + 6] * s, hv[8 * k8 + 7] * s));
+            if (part == 0) {
+                *reinterpret_cast<uint4*>(hrow + BLK + 3072 * k8) = v;
+            } else {
+                *reinterpret_cast<uint4*>(hrow + 2 * BLK + 3072 * k8) = v;
+                *reinterpret_cast<uint4*>(hrow + 3072 * k8) = make_uint4(v.x ^ NEG2, v.y ^ NEG2, v.z ^ NEG2, v.w ^ NEG2);
+            }
+        }
+    }
+    // Y_off'^T = H_c^T Ct^T over S'^T; the Ct stack's blocks 1 and 2 serve as B planes
+    issue(tmem + COL_A, sb0 + HS, sb0 + CS + BLK, STACK_LBO, BLK, &mbar[2]);
+
     // ---- 8. y = Y_diag + e^{rho_l} Y_off' + D x with the scales taken out.
-    // The skip term uses the exact fp32 input (an L2 hit, fetched while Y_diag
-    // runs).  The staging planes lie over the X^T stack and the M planes,
-    // which Y_diag has finished reading.
+    // The skip term uses the exact fp32 input (an L2 hit, fetched while Y_off
+    // runs).  The staging planes lie over the X^T stack and the Ct stack,
+    // which Y_diag and Y_off have finished reading.
     constexpr int YI = CH * PD / NT;  // output elements per thread: rows ly + 4 k, column py
     const int ly = tid >> 6, py = tid & 63;
     const long long ystep = 4 * H * PD;
@@ -1328,7 +1325,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         xs[k] = (t0 + ly + 4 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
                                         : make_float2(0.f, 0.f);
     {
-        wait_bar(&mbar[3]);
+        wait_bar(&mbar[2]);
         tc::fence_after_sync();
         // the accumulators hold column p = lrow at tokens l = c0col + j;
         // exact products of powers of two, the token's decay e^{rho_l} per column
@@ -1369,8 +1366,10 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // ---- 9. final state of the sequence, rotated back to the original frame
     if (c == p.nc - 1 && p.h_final) {
         const float cs = s_rot_last.x, sn = s_rot_last.y;
-        for (int i = tid; i < N * PD; i += NT) {  // element (n, p) = i of [n][p]; cells are [part][n][p]
-            const unsigned long long* cell = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + i;
+        for (int i = tid; i < N * PD; i += NT) {  // element (n, p) = i of [n][p]; cells are [part][n / 4][p][n mod 4]
+            const int n = i >> 6, pp = i & 63;
+            const unsigned long long* cell = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) +
+                                             ((size_t)(n >> 2) * PD + pp) * 4 + (n & 3);
             const float hr = __uint_as_float((uint32_t)ld_cell(cell));
             const float hi = __uint_as_float((uint32_t)ld_cell(cell + PD * NS));
             p.h_final[(size_t)bh * N * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
