@@ -405,14 +405,15 @@ unsigned grid_rows(int64_t rows) { return (unsigned)(rows < 65535 * 8 ? rows : 6
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 // The forward to about fp32 accuracy: the split-precision tensor-core kernel
-// (three TF32 products per product) where its shape applies, else the fp32
-// CUDA-core chunk kernels.
+// (three TF32 products per product) where it is built (headdim 64, dstate
+// 64), else the fp32 CUDA-core chunk kernels (dstate 128 among them).
+bool precise_on_tc(int64_t N, int64_t P, int chunk) { return tc_forward_supported(N, P, chunk) && N == 64; }
 size_t precise_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
-    if (tc_forward_supported(N, P, chunk)) return tc_forward_workspace_bytes(Bz, T, H, N);
+    if (precise_on_tc(N, P, chunk)) return tc_forward_workspace_bytes(Bz, T, H, N);
     return seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);
 }
 cudaError_t launch_precise_forward(FwdArgs f, void* ws, cudaStream_t st) {
-    if (!tc_forward_supported(f.N, f.P, f.chunk)) return launch_seq_forward(f, ws, st);
+    if (!precise_on_tc(f.N, f.P, f.chunk)) return launch_seq_forward(f, ws, st);
     f.split_tf32 = true;
     return launch_tc_forward(f, ws, st);
 }
@@ -483,7 +484,7 @@ BwdLayout bwd_layout(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int
 
 bool backward_supported(int64_t N, int64_t P) {
     auto ok = [](int64_t v) { return v == 16 || v == 32 || v == 64; };
-    return ok(N) && ok(P);
+    return (ok(N) || N == 128) && ok(P);
 }
 
 size_t backward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {

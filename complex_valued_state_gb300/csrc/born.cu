@@ -77,7 +77,8 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
     using Cfg = BornCfg<D>;
     constexpr int NB = Cfg::NB, IT = Cfg::ITEMS, BK = Cfg::BK;
     extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t mbar[3];  // G done, (unused), ACC update done
+    __shared__ __align__(8) uint64_t mbar[3];  // G done, drain, ACC update done
+    __shared__ int s_gave_up;                   // some thread's completion wait gave up
     __shared__ uint32_t s_tmem;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -100,6 +101,7 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
         tc::tmem_relinquish();
     }
     if (tid == 0) {
+        s_gave_up = 0;
         for (int i = 0; i < 3; ++i) tc::mbar_init(&mbar[i], 1);
         tc::mbar_fence_init();
     }
@@ -304,7 +306,12 @@ __global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, 
             out[m] = make_float2((stage[m] + __uint_as_float(acc[m])) * inv,
                                  (stage[D + m] + __uint_as_float(acc[D + m])) * inv);
     }
-    if (!ok && tid == 0 && status) atomicOr(status, kStatusBornMma);  // a completion wait gave up
+    if (!ok) s_gave_up = 1;  // a completion wait gave up
+    __syncthreads();
+    if (s_gave_up && tid == 0) {
+        if (status) atomicOr(status, kStatusBornMma);
+        tc::drain_mmas(&mbar[1], kBornWait);
+    }
     tc::fence_before_sync();
     __syncthreads();
     if (warp == 0) tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);

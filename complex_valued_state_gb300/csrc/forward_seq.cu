@@ -182,6 +182,11 @@ cudaError_t launch_n(const FwdArgs& a, float2* S, float2* E, cudaStream_t st) {
         case 16: return launch_np<N, 16>(a, S, E, st);
         case 32: return launch_np<N, 32>(a, S, E, st);
         case 64: return launch_np<N, 64>(a, S, E, st);
+        case 128:
+            // headdim 128 with dstate up to 64: the gradient runs of dstate 128
+            // (their state is the transpose, headdim and dstate swapped)
+            if constexpr (N <= 64) return launch_np<N, 128>(a, S, E, st);
+            break;
     }
     return cudaErrorInvalidValue;
 }

@@ -339,7 +339,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     __shared__ float s_rho[CH];
     __shared__ float2 s_rot[CH];  // (cos, sin) of Theta_l; first used as scan scratch
     __shared__ float2 s_rot_last;
-    __shared__ __align__(8) uint64_t mbar[4];  // S, G, OFF, Y
+    __shared__ __align__(8) uint64_t mbar[5];  // S, G, OFF, Y, drain
     __shared__ uint32_t s_tmem;
     __shared__ int s_ticket;
     __shared__ int s_bad;
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     if (tid == 0) {
         s_ticket = atomicAdd(p.ticket, 1);
         s_bad = 0;
-        for (int i = 0; i < 4; ++i) tc::mbar_init(&mbar[i], 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
         tc::mbar_fence_init();
     }
     tc::fence_before_sync();
@@ -800,6 +800,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     if (s_bad && tid == 0) {
         atomicOr(p.err, 2);
         if (p.status) atomicOr(p.status, kStatusChunkMma);
+        tc::drain_mmas(&mbar[4], kWaitCycles);
     }
     tc::fence_before_sync();
     __syncthreads();
@@ -925,7 +926,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     __shared__ __align__(16) float s_erho[CH];  // e^{rho_l}
     __shared__ float2 s_rot[CH];
     __shared__ float2 s_rot_last;
-    __shared__ __align__(8) uint64_t mbar[5];  // S, G, OFF, Y, raw rows
+    __shared__ __align__(8) uint64_t mbar[6];  // S, G, OFF, Y, raw rows, drain
     __shared__ uint32_t s_tmem;
     __shared__ int s_ticket;
     __shared__ int s_bad;
@@ -939,7 +940,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     if (tid == 0) {
         s_ticket = atomicAdd(p.ticket, 1);
         s_bad = 0;
-        for (int i = 0; i < 5; ++i) tc::mbar_init(&mbar[i], 1);
+        for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
         tc::mbar_fence_init();
     }
     if (tid < 4) s_max[tid] = 0u;
@@ -1379,6 +1380,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     if (s_bad && tid == 0) {
         atomicOr(p.err, 2);
         if (p.status) atomicOr(p.status, kStatusChunkMma);
+        tc::drain_mmas(&mbar[5], kWaitCycles);
     }
     tc::fence_before_sync();
     __syncthreads();

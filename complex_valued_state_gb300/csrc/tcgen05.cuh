@@ -128,6 +128,16 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* m, uint32_t parity, 
     return true;
 }
 
+// Before tensor memory is released by a CTA whose completion wait gave up:
+// one more commit from the thread that issued the MMAs, on a barrier used for
+// nothing else, waited for with the same bound, so that the columns are not
+// freed while an MMA may still write them.  (If this wait gives up as well,
+// the MMA does not complete at all and nothing better is possible.)
+__device__ __forceinline__ void drain_mmas(uint64_t* fresh_mbar, long long max_cycles) {
+    commit(fresh_mbar);
+    mbar_wait_bounded(fresh_mbar, 0, max_cycles);
+}
+
 // Expect `bytes` of asynchronous copies on an mbarrier and arrive once.
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* m, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(m)), "r"(bytes) : "memory");

@@ -324,10 +324,13 @@ int cssd_cayley_scan(const cssd_dims* dims, const float* phi, const float* u, co
  * fp32 accuracy, because R_t is a small difference of large sums that plain
  * TF32 operands would spoil: by the tensor-core kernel with split-precision
  * operands (each value as two TF32 parts, three TF32 products per product)
- * where headdim is 64 and dstate 64, else by the fp32 CUDA-core chunk kernels.
- * gB and gC use the plain TF32 tensor-core kernel where it applies.
- *   dims, x, dt, A, B, C, D, chunk   as cssd_chunked_forward; dstate and
- *            headdim in {16, 32, 64} (else CSSD_ERR_UNSUPPORTED)
+ * where headdim is 64 and dstate 64, else by the fp32 CUDA-core chunk kernels
+ * (dstate 128 among them).  gB and gC use the tensor-core forward where it
+ * applies; with dstate 128 their runs (state transposed: headdim 128) take
+ * the CUDA-core kernels.
+ *   dims, x, dt, A, B, C, D, chunk   as cssd_chunked_forward; dstate in
+ *            {16, 32, 64, 128}, headdim in {16, 32, 64} (else
+ *            CSSD_ERR_UNSUPPORTED)
  *   dy       complex64 [batch, seqlen, nheads, headdim]  upstream gradient
  *   gx       complex64 like x;  gdt float32 like dt;  gA complex64 [nheads];
  *   gB, gC   complex64 like B, C;  gD float32 [nheads]     (all written)

@@ -133,7 +133,8 @@ def test_backward_argument_errors(lib):
     p = [ctypes.c_void_p(0x10000 + 0x100 * i) for i in range(14)]  # x dt A B C D dy gx gdt gA gB gC gD ws
     f = lib.cssd_chunked_backward
     assert f(None, *p[:13], 64, p[13], 1 << 40, None) == -1
-    assert f(ctypes.byref(cssd.Dims(1, 8, 2, 128, 64)), *p[:13], 64, p[13], 1 << 40, None) == -3
+    assert f(ctypes.byref(cssd.Dims(1, 8, 2, 48, 64)), *p[:13], 64, p[13], 1 << 40, None) == -3
+    assert f(ctypes.byref(cssd.Dims(1, 8, 2, 64, 128)), *p[:13], 64, p[13], 1 << 40, None) == -3
     assert f(ctypes.byref(ok), *p[:13], 32, p[13], 1 << 40, None) == -3  # chunk
     q = list(p)
     q[6] = None  # dy
@@ -143,7 +144,8 @@ def test_backward_argument_errors(lib):
     assert f(ctypes.byref(ok), *q[:13], 64, q[13], 1 << 40, None) == -4
     assert f(ctypes.byref(ok), *p[:13], 64, p[13], 16, None) == -5  # workspace too small
     assert lib.cssd_backward_workspace_bytes(ctypes.byref(ok), 64) > 0
-    assert lib.cssd_backward_workspace_bytes(ctypes.byref(cssd.Dims(1, 8, 2, 128, 64)), 64) == 0
+    assert lib.cssd_backward_workspace_bytes(ctypes.byref(cssd.Dims(1, 8, 2, 128, 64)), 64) > 0  # dstate 128
+    assert lib.cssd_backward_workspace_bytes(ctypes.byref(cssd.Dims(1, 8, 2, 64, 128)), 64) == 0  # headdim 128
 
 
 def test_born_attention_argument_errors(lib):

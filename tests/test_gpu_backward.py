@@ -109,7 +109,26 @@ def test_mamba2_layer_shape_two_heads(cs, orc):
         assert rel_err(got["gA"][h:h + 1], ref["gA"]) < TOL and rel_err(got["gD"][h:h + 1], ref["gD"]) < TOL
 
 
-def test_rejects_dstate_128(cs):
-    d = wl.random_case(10, 1, 8, 1, 128, 64)
-    with pytest.raises(cs.CssdError):
-        run(cs, d, upstream(11, (1, 8, 1, 64)), 64)
+@pytest.mark.parametrize("P", [64, 32])
+@pytest.mark.parametrize("T,chunk", [(1, 64), (65, 64), (200, 128), (257, 128)])
+def test_dstate_128(cs, orc, P, T, chunk):
+    """dstate 128: y and gx on the fp32 CUDA-core kernels, the transposed-state
+    runs of gB and gC with headdim 128 on the same kernels."""
+    d = wl.random_case(6000 + P + T, 2, T, 3, 128, P)
+    dy = upstream(6100 + T, (2, T, 3, P))
+    got = run(cs, d, dy, chunk)
+    ref = orc.cssd_backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], dy)
+    for k in KEYS:
+        assert rel_err(got[k], ref[k]) < TOL, k
+
+
+def test_long_seq_shape_dstate_128(cs, orc):
+    """The long_seq shape (dstate 128, headdim 64, chunk 128, slow decay) over
+    4096 tokens on two heads; the oracle keeps every state of the sequence."""
+    w = wl.LONG_SEQ.with_(seqlen=4096, nheads=2)
+    d = wl.make_inputs(w)
+    dy = upstream(12, (w.batch, w.seqlen, w.nheads, w.headdim))
+    got = run(cs, d, dy, w.chunk)
+    ref = orc.cssd_backward(d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], dy)
+    for k in KEYS:
+        assert rel_err(got[k], ref[k]) < TOL, k
