@@ -407,7 +407,9 @@ size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 // The forward to about fp32 accuracy: the split-precision tensor-core kernel
 // (three TF32 products per product) where it is built (headdim 64, dstate
 // 64), else the fp32 CUDA-core chunk kernels (dstate 128 among them).
-bool precise_on_tc(int64_t N, int64_t P, int chunk) { return tc_forward_supported(N, P, chunk) && N == 64; }
+bool precise_on_tc(int64_t N, int64_t P, int chunk) {
+    return tc_forward_supported(N, P, chunk) && tc_full_shape(N, P) && N == 64;
+}
 size_t precise_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
     if (precise_on_tc(N, P, chunk)) return tc_forward_workspace_bytes(Bz, T, H, N);
     return seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);
@@ -423,7 +425,7 @@ cudaError_t launch_precise_forward(FwdArgs f, void* ws, cudaStream_t st) {
 // its transpose are tensor-core shapes; otherwise they run on reversed and
 // conjugated copies of the inputs.
 bool folded_runs(int64_t N, int64_t P, int chunk) {
-    return tc_forward_supported(N, P, chunk) && tc_forward_supported(P, N, chunk);
+    return tc_forward_supported(N, P, chunk) && tc_full_shape(N, P) && tc_full_shape(P, N);
 }
 
 // With the folded runs and T a multiple of 64, R_t comes from chunk-local sums

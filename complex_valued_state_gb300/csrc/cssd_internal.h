@@ -101,6 +101,10 @@ cudaError_t launch_seq_forward(const FwdArgs& a, void* workspace, cudaStream_t s
 
 // Fused tensor-core kernel (forward_tc.cu).
 bool tc_forward_supported(int64_t N, int64_t P, int chunk);
+// The TF32 kernel's shapes (headdim 64, dstate 64 or 128): split precision,
+// TF32 operands and the index and sign modes need them; the other tensor-core
+// shapes (dstate and headdim up to 64) run the half-operand kernel, padded.
+bool tc_full_shape(int64_t N, int64_t P);
 // Shapes the split-precision forward serves: the tensor-core shapes with
 // dstate 64, and every shape the CUDA-core kernels take (fp32 already).
 bool precise_forward_supported(int64_t N, int64_t P, int chunk);

@@ -1,14 +1,20 @@
 // Chooses the kernels of the chunked forward by shape: the fused tensor-core
-// kernel for headdim 64 with dstate 64 or 128, the CUDA-core chunk kernels for
-// every other supported shape.  Both compute the same chunkwise decomposition.
+// kernels for headdim 64 with dstate 64 or 128 and, padded to 64, for dstate
+// and headdim up to 64; the CUDA-core chunk kernels for dstate 128 with a
+// smaller headdim, and for the split-precision and TF32 entry points on the
+// padded shapes.  All compute the same chunkwise decomposition.
 
 #include "cssd_internal.h"
 
 namespace cssd {
 
 size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk) {
-    if (tc_forward_supported(N, P, chunk)) return tc_forward_workspace_bytes(Bz, T, H, N);
-    return seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);
+    if (!tc_forward_supported(N, P, chunk)) return seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);
+    const size_t tc = tc_forward_workspace_bytes(Bz, T, H, N);
+    if (tc_full_shape(N, P)) return tc;
+    // padded shapes: the split-precision and TF32 entry points run the CUDA-core kernels there
+    const size_t seq = seq_forward_workspace_bytes(Bz, T, H, N, P, chunk);
+    return tc > seq ? tc : seq;
 }
 
 // Tensor-core path: two prep kernels and the chunk kernel; CUDA-core path:
@@ -16,7 +22,9 @@ size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int6
 int forward_launches(int64_t, int64_t, int64_t, int64_t, int64_t, int) { return 3; }
 
 cudaError_t launch_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
-    if (tc_forward_supported(a.N, a.P, a.chunk)) return launch_tc_forward(a, ws, st);
+    const bool plain = a.mode == 0 && !a.split_tf32 && !a.tf32_operands;
+    if (tc_forward_supported(a.N, a.P, a.chunk) && (tc_full_shape(a.N, a.P) || plain))
+        return launch_tc_forward(a, ws, st);
     if (a.mode != 0) return cudaErrorInvalidValue;  // index and sign modes: tensor-core path only
     return launch_seq_forward(a, ws, st);
 }

@@ -167,6 +167,7 @@ struct TcParams {
     int* err;          // [1] error bits of this call (workspace)
     unsigned* status;  // the library's status word (kStatus* bits), or null
     int T, H, BH, nc, NH;
+    int Nd, Pd;             // dstate and headdim of the call (the half-operand kernel pads them to 64)
     int first_ticket;       // tickets start here (0 in normal use)
     int pf_dist;            // L2 prefetch distance in tickets (0: none)
     long long wait_cycles;  // limit of the hand-off wait (SM clocks)
@@ -960,6 +961,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const int t0 = c * CH;
     const long long row0 = ((long long)b * p.T + t0) * p.H + h;  // row of token t0; token l at row0 + l H
     const long long H = p.H;
+    const int Nd = p.Nd, Pd = p.Pd;  // widths of the call; the tiles are padded with zeros to 64
     const uint32_t sb0 = tc::smem_u32(smem);
     const float Dh = __ldg(p.D + h);  // skip coefficient, needed only at the end: fetched now
 
@@ -972,9 +974,10 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const int mrow = lane >> 3;                      // the matrix this lane addresses in an x4 store
     const uint32_t r16 = (uint32_t)(lane & 7) << 4;  // and its row within that matrix
 
-    // ---- 0. loads: dt tables, raw x and B rows by bulk copies (one 512-byte
-    // row per thread of the first four warps, completing on mbar[4]; rows past
-    // the sequence end are zero-filled instead), C into registers.
+    // ---- 0. loads: dt tables, raw x and B rows by bulk copies (one row per
+    // thread of the first four warps, completing on mbar[4]; the columns past
+    // the call's width and the rows past the sequence end are zero-filled
+    // instead), C into registers.
     float2 tk = make_float2(0.f, 0.f);
     float phi_c = 0.f;
     if (tid < CH) {
@@ -982,14 +985,18 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         phi_c = __ldcg(p.phi + (size_t)bh * p.nc + c);
     }
     const int rows = min(CH, p.T - t0);
-    if (tid == 0) tc::mbar_arrive_expect_tx(&mbar[4], (uint32_t)rows * 1024u);
+    if (tid == 0) tc::mbar_arrive_expect_tx(&mbar[4], (uint32_t)rows * (uint32_t)(8 * (Pd + Nd)));
     if (tid < 2 * CH) {
-        const int lr = tid & (CH - 1), op = tid >> 6;  // op 0: x, 1: B (both 512 bytes per token)
+        const int lr = tid & (CH - 1), op = tid >> 6;  // op 0: x (Pd complex per token), 1: B (Nd)
+        const int wd = op ? Nd : Pd;
         const uint32_t off = (op ? RAW_B : 0u) + raw_at(lr, 0);
+        float4* z = reinterpret_cast<float4*>(smem + off);
         if (lr < rows) {
-            tc::bulk_g2s(sb0 + off, (op ? p.B : p.x) + (row0 + (long long)lr * H) * 32, 512u, &mbar[4]);
+            tc::bulk_g2s(sb0 + off, (op ? p.B : p.x) + (row0 + (long long)lr * H) * (wd / 2), (uint32_t)(8 * wd),
+                         &mbar[4]);
+#pragma unroll 1
+            for (int k = wd / 2; k < 32; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         } else {
-            float4* z = reinterpret_cast<float4*>(smem + off);
 #pragma unroll 1
             for (int k = 0; k < 32; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
@@ -998,7 +1005,8 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     float4 cv[8];
 #pragma unroll
     for (int bb = 0; bb < 8; ++bb)
-        cv[bb] = lok ? __ldg(p.C + (row0 + (long long)l * H) * (N / 2) + 4 * bb + jp) : make_float4(0.f, 0.f, 0.f, 0.f);
+        cv[bb] = (lok && 8 * bb + 2 * jp < Nd) ? __ldg(p.C + (row0 + (long long)l * H) * (Nd / 2) + 4 * bb + jp)
+                                               : make_float4(0.f, 0.f, 0.f, 0.f);
 
     // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
     if (tid < CH) {
@@ -1253,9 +1261,10 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
                 if (p.status) atomicOr(p.status, kStatusHandoff);
             }
         } else if (p.h0) {
-            const float* src = reinterpret_cast<const float*>(p.h0 + ((size_t)bh * N + c0col) * PD + lrow) + part;
+            // the caller's state, [Nd][Pd] per sequence; padded rows and columns are zero
+            const float* src = reinterpret_cast<const float*>(p.h0 + ((size_t)bh * Nd + c0col) * Pd + lrow) + part;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) hv[j] = __ldg(src + 2 * PD * j);
+            for (int j = 0; j < CPT; ++j) hv[j] = (lrow < Pd && c0col + j < Nd) ? __ldg(src + 2 * Pd * j) : 0.f;
         } else {
 #pragma unroll
             for (int j = 0; j < CPT; ++j) hv[j] = 0.f;
@@ -1318,13 +1327,14 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // which Y_diag and Y_off have finished reading.
     constexpr int YI = CH * PD / NT;  // output elements per thread: rows ly + 4 k, column py
     const int ly = tid >> 6, py = tid & 63;
-    const long long ystep = 4 * H * PD;
-    const long long yoff = (row0 + (long long)ly * H) * PD + py;
+    const bool pok = py < Pd;
+    const long long ystep = 4 * H * Pd;
+    const long long yoff = (row0 + (long long)ly * H) * Pd + py;
     float2 xs[YI];
 #pragma unroll
     for (int k = 0; k < YI; ++k)
-        xs[k] = (t0 + ly + 4 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
-                                        : make_float2(0.f, 0.f);
+        xs[k] = (pok && t0 + ly + 4 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
+                                               : make_float2(0.f, 0.f);
     {
         wait_bar(&mbar[2]);
         tc::fence_after_sync();
@@ -1357,7 +1367,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         const float* stage = reinterpret_cast<const float*>(smem) + ly * STAGE_LD + py;
 #pragma unroll
         for (int k = 0; k < YI; ++k) {
-            if (t0 + ly + 4 * k < p.T) {
+            if (pok && t0 + ly + 4 * k < p.T) {
                 const float yr = stage[4 * k * STAGE_LD], yi = stage[CH * STAGE_LD + 4 * k * STAGE_LD];
                 p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
             }
@@ -1367,13 +1377,13 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // ---- 9. final state of the sequence, rotated back to the original frame
     if (c == p.nc - 1 && p.h_final) {
         const float cs = s_rot_last.x, sn = s_rot_last.y;
-        for (int i = tid; i < N * PD; i += NT) {  // element (n, p) = i of [n][p]; cells are [part][n / 4][p][n mod 4]
-            const int n = i >> 6, pp = i & 63;
+        for (int i = tid; i < Nd * Pd; i += NT) {  // element (n, p) = i of [Nd][Pd]; cells are [part][n / 4][p][n mod 4]
+            const int n = i / Pd, pp = i - n * Pd;
             const unsigned long long* cell = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) +
                                              ((size_t)(n >> 2) * PD + pp) * 4 + (n & 3);
             const float hr = __uint_as_float((uint32_t)ld_cell(cell));
             const float hi = __uint_as_float((uint32_t)ld_cell(cell + PD * NS));
-            p.h_final[(size_t)bh * N * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
+            p.h_final[(size_t)bh * Nd * Pd + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
         }
     }
 
@@ -1392,14 +1402,22 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
 // The tensor-core kernel runs 64-token tiles with headdim 64 and dstate 64 or
 // 128; a requested chunk of 128 is computed as two consecutive 64-token tiles
 // with the state handed over between them, which is the same decomposition.
+//
+// Dstate and headdim below 64 (16 or 32, either or both) run the half-operand
+// kernel on tiles padded with zeros to 64: the padded state rows and columns
+// stay zero, and only the real ones are written out.
 bool tc_forward_supported(int64_t N, int64_t P, int chunk) {
-    return P == PD && (N == NS || N == 2 * NS) && (chunk == CH || chunk == 2 * CH);
+    if (chunk != CH && chunk != 2 * CH) return false;
+    if (N == 2 * NS) return P == PD;
+    return N <= NS && P <= PD;
 }
 
-bool precise_forward_supported(int64_t N, int64_t P, int chunk) { return !(tc_forward_supported(N, P, chunk) && N != NS); }
+bool tc_full_shape(int64_t N, int64_t P) { return P == PD && (N == NS || N == 2 * NS); }
+
+bool precise_forward_supported(int64_t N, int64_t P, int chunk) { return !(tc_forward_supported(N, P, chunk) && N > NS); }
 
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N) {
-    const int64_t BH = Bz * H, nc = (T + CH - 1) / CH, NH = N / NS;
+    const int64_t BH = Bz * H, nc = (T + CH - 1) / CH, NH = (N + NS - 1) / NS;
     size_t off = (size_t)BH * NH * RING * 2 * PD * NS * sizeof(unsigned long long);  // hand-off cells
     off += 256;                                                                       // ticket, err
     off += ((size_t)BH * nc * sizeof(float) + 255) / 256 * 256;                       // phi
@@ -1510,7 +1528,9 @@ static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStr
 
 cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     TcParams p;
-    const int64_t BH = a.Bz * a.H, nc = (a.T + CH - 1) / CH, NH = a.N / NS;
+    const int64_t BH = a.Bz * a.H, nc = (a.T + CH - 1) / CH, NH = (a.N + NS - 1) / NS;
+    const bool full = tc_full_shape(a.N, a.P);
+    if (!full && (a.mode != 0 || a.split_tf32 || a.tf32_operands)) return cudaErrorNotSupported;
     unsigned char* w = static_cast<unsigned char*>(ws);
     p.ring = reinterpret_cast<unsigned long long*>(w);
     w += (size_t)BH * NH * RING * 2 * PD * NS * sizeof(unsigned long long);
@@ -1537,6 +1557,8 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.BH = (int)BH;
     p.nc = (int)nc;
     p.NH = (int)NH;
+    p.Nd = (int)a.N;
+    p.Pd = (int)a.P;
     p.first_ticket = 0;
     p.status = status_word();
     p.pf_dist = 0;
@@ -1627,6 +1649,8 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.BH = (int)BH;
     p.nc = (int)nc;
     p.NH = 1;
+    p.Nd = N;
+    p.Pd = P;
     p.first_ticket = (int)BH;  // chunk 0 of every sequence is never taken
     p.status = status_word();
     p.pf_dist = 0;

@@ -85,14 +85,16 @@ size_t cssd_workspace_bytes(const cssd_dims* dims, int chunk);
 
 /* Chunkwise forward over a whole sequence from a zero initial state.
  *
- * Precision: the tensor-core paths (headdim 64, dstate 64 or 128) round the
- * GEMM operands to an 11-bit significand and accumulate in fp32.  dstate 64
- * uses IEEE half operands with a power-of-two scale per tile and operand,
- * dstate 128 uses TF32.  Decays, rotations, the inter-chunk state and the
- * output are fp32.  Measured errors are 1e-4 to 5e-4 of the largest value of
- * y and of h_final (the bar the tests hold is 2e-3).  The CUDA-core
- * path (other shapes) is fp32 throughout.  cssd_chunked_forward_precise
- * gives about fp32 accuracy on the tensor cores. */
+ * Kernels and precision: every shape except dstate 128 with headdim 16 or 32
+ * runs on the tensor cores, rounding the GEMM operands to an 11-bit
+ * significand and accumulating in fp32.  dstate and headdim up to 64 use IEEE
+ * half operands with a power-of-two scale per tile and operand (tiles below 64
+ * are padded with zeros to 64); dstate 128 with headdim 64 uses TF32.  Decays,
+ * rotations, the inter-chunk state and the output are fp32.  Measured errors
+ * are 1e-4 to 5e-4 of the largest value of y and of h_final (the bar the
+ * tests hold is 2e-3).  dstate 128 with headdim 16 or 32 runs the CUDA-core
+ * kernels, fp32 throughout.  cssd_chunked_forward_precise gives about fp32
+ * accuracy. */
 /* Arguments:
  *   x       complex64 [batch, seqlen, nheads, headdim]   token content
  *   dt      float32   [batch, seqlen, nheads]            raw step (softplus applied inside)
@@ -171,10 +173,10 @@ int cssd_chunked_forward_h0(const cssd_dims* dims, const void* x, const float* d
  * Measured ~1e-6 of the largest |y|, at about 1.8x the time of
  * cssd_chunked_forward (three times the tensor-core work and twice the shared
  * memory, one CTA per SM).  Built for headdim 64 with dstate 64; dstate 128
- * with headdim 64 returns CSSD_ERR_UNSUPPORTED.  Shapes the CUDA-core kernels
- * take (headdim or dstate 16 / 32) run them, fp32 already, as in
- * cssd_chunked_forward.  Arguments, workspace size (cssd_workspace_bytes) and
- * status are otherwise those of cssd_chunked_forward_h0; h0 may be NULL. */
+ * with headdim 64 returns CSSD_ERR_UNSUPPORTED.  The other shapes (headdim or
+ * dstate 16 / 32) run the fp32 CUDA-core chunk kernels.  Arguments,
+ * workspace size (cssd_workspace_bytes) and status are otherwise those of
+ * cssd_chunked_forward_h0; h0 may be NULL. */
 int cssd_chunked_forward_precise(const cssd_dims* dims, const void* x, const float* dt, const void* A,
                                  const void* B, const void* C, const float* D, const void* h0, void* y,
                                  void* h_final, int chunk, void* workspace, size_t workspace_bytes,
@@ -189,8 +191,9 @@ int cssd_chunked_forward_precise(const cssd_dims* dims, const void* x, const flo
  * and operand at dstate 64 (the same 11-bit significand, a narrower exponent
  * range covered by the per-tile scales) and TF32 at dstate 128; this entry
  * point keeps TF32 at dstate 64 too, for callers and measurements that want
- * the wider operand exponent range without per-tile scaling.  Shapes the
- * CUDA-core kernels take run them (fp32), as in cssd_chunked_forward.
+ * the wider operand exponent range without per-tile scaling.  The other shapes
+ * (dstate or headdim below 64, and dstate 128 with a smaller headdim) run the
+ * fp32 CUDA-core chunk kernels.
  * Arguments, workspace size (cssd_workspace_bytes) and status are those of
  * cssd_chunked_forward_h0; h0 may be NULL. */
 int cssd_chunked_forward_tf32(const cssd_dims* dims, const void* x, const float* dt, const void* A,

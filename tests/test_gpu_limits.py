@@ -41,7 +41,9 @@ def rows_of(d, rows):
     return {k: (v if k in ("A", "D") else v[rows]) for k, v in d.items()}
 
 
-@pytest.mark.parametrize("N,P,T", [(16, 16, 3), (64, 64, 2)])
+# (128, 16): the CUDA-core kernels (dstate 128 with a smaller headdim);
+# (16, 16): the half-operand kernel padded to 64; (64, 64): the same kernel unpadded
+@pytest.mark.parametrize("N,P,T", [(128, 16, 3), (16, 16, 3), (64, 64, 2)])
 def test_forward_at_batch_limit(cs, oracle_lib, N, P, T):
     d = wl.random_case(9100 + N, BMAX, T, 1, N, P)
     g = {k: torch.from_numpy(np.ascontiguousarray(d[k])).cuda() for k in KEYS}

@@ -2,12 +2,15 @@
 the CPU oracle, and the operand-precision comparison with the default forward.
 
 The default forward takes half operands with a power-of-two scale per tile and
-operand at dstate 64, TF32 operands at dstate 128, and fp32 on the CUDA-core
-shapes; cssd_chunked_forward_tf32 keeps TF32 on every tensor-core shape.  Both
-round each GEMM operand to an 11-bit significand, so on the pages' workloads
-the half-operand error must stay within twice the TF32 error (plus a floor of
-1e-5 of the largest magnitude for cases where both are tiny).  Tolerance of the
-parity checks: max |got - ref| <= 2e-3 * max |ref| per output tensor.
+operand at dstate and headdim up to 64 (padded to 64 below that), and TF32
+operands at dstate 128; cssd_chunked_forward_tf32 keeps TF32 on the TF32
+kernel's shapes (headdim 64, dstate 64 or 128) and runs the fp32 CUDA-core
+kernels on the others.  Where both are 11-bit operand paths the half-operand
+error must stay within twice the TF32 error (plus a floor of 1e-5 of the
+largest magnitude for cases where both are tiny); the tiny workload (dstate =
+headdim = 16) compares half operands with fp32 and is held to the parity bar
+only.  Tolerance of the parity checks: max |got - ref| <= 2e-3 * max |ref| per
+output tensor.
 
 Run with -s to see the per-workload error table.
 """
@@ -88,4 +91,5 @@ def test_half_operands_within_twice_tf32(cs, oracle_lib, name, heads):
     print(f"\nerror table {name}: " + " ".join(f"{k}={v:.3e}" for k, v in e.items()))
     for k in ("y", "h"):
         assert e[f"{k}_tf32"] < TOL and e[f"{k}_default"] < TOL
-        assert e[f"{k}_default"] <= 2 * e[f"{k}_tf32"] + 1e-5
+        if w.headdim == 64 and w.dstate in (64, 128):
+            assert e[f"{k}_default"] <= 2 * e[f"{k}_tf32"] + 1e-5
