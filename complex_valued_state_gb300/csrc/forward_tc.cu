@@ -315,13 +315,11 @@ __global__ void __launch_bounds__(256) phase_scan_kernel(TcParams p) {
             if (lane >= o) v += u;
         }
         const double excl = carry + v - th;
-        if (c < p.nc) {
-            double r = fmod(excl, two_pi);
-            if (r > 3.141592653589793) r -= two_pi;
-            if (r < -3.141592653589793) r += two_pi;
-            ph[c] = (float)r;
-        }
-        carry = fmod(carry + __shfl_sync(0xffffffffu, v, 31), two_pi);
+        // reduced to [-pi, pi] by subtracting the nearest multiple of 2 pi
+        // (exact enough in double for any angle a sequence accumulates)
+        if (c < p.nc) ph[c] = (float)fma(-rint(excl * (1.0 / two_pi)), two_pi, excl);
+        const double cs = carry + __shfl_sync(0xffffffffu, v, 31);
+        carry = fma(-rint(cs * (1.0 / two_pi)), two_pi, cs);
     }
 }
 
