@@ -140,13 +140,14 @@ int forward_common(const cssd_dims* d, const void* x, const float* dt, const voi
     int s = check_dims(d, true);
     if (s != CSSD_OK) return s;
     if (!supported_chunk(chunk)) return CSSD_ERR_UNSUPPORTED;
-    if (precise && !cssd::precise_forward_supported(d->dstate, d->headdim, chunk)) return CSSD_ERR_UNSUPPORTED;
     if (!x || !dt || !A || !B || !C || !D || !y) return CSSD_ERR_NULL;
     if (!aligned(x, 16) || !aligned(B, 16) || !aligned(C, 16) || !aligned(y, 16) ||
         (h_final && !aligned(h_final, 16)) || (h0 && !aligned(h0, 16)) || (workspace && !aligned(workspace, 16)) ||
         !aligned(A, 8) || !aligned(dt, 4) || !aligned(D, 4))
         return CSSD_ERR_ALIGN;
-    const size_t need = cssd::forward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
+    const size_t need =
+        precise ? cssd::forward_precise_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk)
+                : cssd::forward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
     if (workspace && workspace_bytes < need) return CSSD_ERR_WORKSPACE;
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     int dev = 0;
@@ -249,6 +250,11 @@ const char* cssd_status_string(int status) {
 size_t cssd_workspace_bytes(const cssd_dims* d, int chunk) {
     if (check_dims(d, true) != CSSD_OK || !supported_chunk(chunk)) return 0;
     return cssd::forward_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
+}
+
+size_t cssd_precise_workspace_bytes(const cssd_dims* d, int chunk) {
+    if (check_dims(d, true) != CSSD_OK || !supported_chunk(chunk)) return 0;
+    return cssd::forward_precise_workspace_bytes(d->batch, d->seqlen, d->nheads, d->dstate, d->headdim, chunk);
 }
 
 int cssd_forward_launches(const cssd_dims* d, int chunk) {

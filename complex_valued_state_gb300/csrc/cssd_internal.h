@@ -92,6 +92,7 @@ extern thread_local cudaEvent_t g_prof_end;
 // (headdim 64, dstate 64 or 128; split-precision operands when
 // FwdArgs::split_tf32), else the CUDA-core chunk kernels.
 size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
+size_t forward_precise_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
 int forward_launches(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
 cudaError_t launch_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
 
@@ -105,9 +106,6 @@ bool tc_forward_supported(int64_t N, int64_t P, int chunk);
 // TF32 operands and the index and sign modes need them; the other tensor-core
 // shapes (dstate and headdim up to 64) run the half-operand kernel, padded.
 bool tc_full_shape(int64_t N, int64_t P);
-// Shapes the split-precision forward serves: the tensor-core shapes with
-// dstate 64, and every shape the CUDA-core kernels take (fp32 already).
-bool precise_forward_supported(int64_t N, int64_t P, int chunk);
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N);
 cudaError_t launch_tc_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
 cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cudaStream_t stream);

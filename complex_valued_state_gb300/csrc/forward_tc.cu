@@ -206,23 +206,6 @@ __device__ __forceinline__ void st_cell(unsigned long long* q, float v, uint32_t
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(q), "l"(w) : "memory");
 }
 
-// Four consecutive cells (32 bytes, 32-byte aligned) as one vector access;
-// each 8-byte cell stays single-copy atomic.
-__device__ __forceinline__ void ld_cell4(const unsigned long long* q, unsigned long long* w) {
-    asm volatile("ld.relaxed.gpu.global.v4.b64 {%0, %1, %2, %3}, [%4];"
-                 : "=l"(w[0]), "=l"(w[1]), "=l"(w[2]), "=l"(w[3])
-                 : "l"(q)
-                 : "memory");
-}
-__device__ __forceinline__ unsigned long long cell_word(float v, uint32_t tag) {
-    return ((unsigned long long)tag << 32) | __float_as_uint(v);
-}
-__device__ __forceinline__ void st_cell4(unsigned long long* q, const unsigned long long* w) {
-    asm volatile("st.relaxed.gpu.global.v4.b64 [%0], {%1, %2, %3, %4};" ::"l"(q), "l"(w[0]), "l"(w[1]), "l"(w[2]),
-                 "l"(w[3])
-                 : "memory");
-}
-
 // CPT consecutive TMEM columns of this warp's lane quarter into registers.
 __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CPT]) {
 #pragma unroll
@@ -1215,44 +1198,45 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // and the CPT state rows n from c0col (S'^T holds p in its lanes).  It
     // takes H_c from the cells the same thread position of chunk c-1 wrote and
     // publishes H_{c+1} = e^{rho_end} H_c + S' in the true scale.  Cells are
-    // laid out [part][n / 4][p][n mod 4], so a thread's cells come in 32-byte
-    // runs of four n (one vector access each, every cell single-copy atomic)
-    // and a warp's accesses are contiguous.
+    // laid out [part][n][p], so a warp's access to one n is 256 contiguous
+    // bytes.  (32-byte vector cells, [part][n / 4][p][n mod 4], measured 4 %
+    // slower.)
     float hv[CPT];
     {
-        const size_t qbase = ((size_t)part * (NS / 4) + (c0col >> 2)) * PD + lrow;  // quad index of n = c0col
-        const unsigned long long* cin = p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS) + 4 * qbase;
-        unsigned long long* cout = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + 4 * qbase;
-        constexpr int QS = 4 * PD;  // cells from one quad of n to the next
+        const size_t slot = (size_t)part * NS * PD + (size_t)c0col * PD + lrow;
+        const unsigned long long* cin = p.ring + ((size_t)bh * RING + (c % RING)) * (2 * PD * NS) + slot;
+        unsigned long long* cout = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) + slot;
         if (c > 0) {
             const uint32_t want = (uint32_t)c;
             const long long w0 = clock64();
             // one lane per warp watches one cell until it carries this chunk's
-            // tag, then every lane reads all its cells at once
+            // tag, then every lane reads its cells, 16 loads in flight at a time
             if (lane == 0) {
                 while ((uint32_t)(ld_cell(cin) >> 32) != want) {
                     if (clock64() - w0 > p.wait_cycles) break;
-                    __nanosleep(64);
+                    __nanosleep(128);
                 }
             }
             __syncwarp();
             bool late = false;
-            while (true) {
-                unsigned long long w[CPT];
+            for (int half = 0; half < 2 && !late; ++half) {
+                while (true) {
+                    unsigned long long w[16];
 #pragma unroll
-                for (int j4 = 0; j4 < CPT / 4; ++j4) ld_cell4(cin + QS * j4, w + 4 * j4);
-                bool all = true;
+                    for (int j = 0; j < 16; ++j) w[j] = ld_cell(cin + (size_t)(16 * half + j) * PD);
+                    bool all = true;
 #pragma unroll
-                for (int j = 0; j < CPT; ++j) {
-                    hv[j] = __uint_as_float((uint32_t)w[j]);
-                    all = all && ((uint32_t)(w[j] >> 32) == want);
+                    for (int j = 0; j < 16; ++j) {
+                        hv[16 * half + j] = __uint_as_float((uint32_t)w[j]);
+                        all = all && ((uint32_t)(w[j] >> 32) == want);
+                    }
+                    if (all) break;
+                    if (clock64() - w0 > p.wait_cycles) {
+                        late = true;
+                        break;
+                    }
+                    __nanosleep(128);
                 }
-                if (all) break;
-                if (clock64() - w0 > p.wait_cycles) {
-                    late = true;
-                    break;
-                }
-                __nanosleep(64);
             }
             if (late) {
                 atomicOr(p.err, 1);
@@ -1275,15 +1259,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         const uint32_t tag = (uint32_t)(c + 1);
         const float k_s = inv_b * inv_x;  // a product of powers of two: exact
 #pragma unroll
-        for (int j4 = 0; j4 < CPT / 4; ++j4) {
-            unsigned long long w[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int j = 4 * j4 + u;
-                w[u] = cell_word(fmaf(eend, hv[j], __uint_as_float(r[j]) * k_s), tag);
-            }
-            st_cell4(cout + QS * j4, w);
-        }
+        for (int j = 0; j < CPT; ++j) st_cell(cout + (size_t)j * PD, fmaf(eend, hv[j], __uint_as_float(r[j]) * k_s), tag);
         float fh = 0.f;
 #pragma unroll
         for (int j = 0; j < CPT; ++j) fh = fmaxf(fh, fabsf(hv[j]));
@@ -1375,10 +1351,10 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // ---- 9. final state of the sequence, rotated back to the original frame
     if (c == p.nc - 1 && p.h_final) {
         const float cs = s_rot_last.x, sn = s_rot_last.y;
-        for (int i = tid; i < Nd * Pd; i += NT) {  // element (n, p) = i of [Nd][Pd]; cells are [part][n / 4][p][n mod 4]
+        for (int i = tid; i < Nd * Pd; i += NT) {  // element (n, p) = i of [Nd][Pd]; cells are [part][n][p]
             const int n = i / Pd, pp = i - n * Pd;
             const unsigned long long* cell = p.ring + ((size_t)bh * RING + ((c + 1) % RING)) * (2 * PD * NS) +
-                                             ((size_t)(n >> 2) * PD + pp) * 4 + (n & 3);
+                                             (size_t)n * PD + pp;
             const float hr = __uint_as_float((uint32_t)ld_cell(cell));
             const float hi = __uint_as_float((uint32_t)ld_cell(cell + PD * NS));
             p.h_final[(size_t)bh * Nd * Pd + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
@@ -1411,8 +1387,6 @@ bool tc_forward_supported(int64_t N, int64_t P, int chunk) {
 }
 
 bool tc_full_shape(int64_t N, int64_t P) { return P == PD && (N == NS || N == 2 * NS); }
-
-bool precise_forward_supported(int64_t N, int64_t P, int chunk) { return !(tc_forward_supported(N, P, chunk) && N > NS); }
 
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N) {
     const int64_t BH = Bz * H, nc = (T + CH - 1) / CH, NH = (N + NS - 1) / NS;

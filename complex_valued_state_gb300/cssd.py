@@ -31,7 +31,7 @@ STATUS = {
 }
 
 # Every symbol include/cssd.h declares.
-EXPORTS = ("cssd_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward", "cssd_chunked_forward_h0",
+EXPORTS = ("cssd_workspace_bytes", "cssd_precise_workspace_bytes", "cssd_forward_launches", "cssd_chunked_forward", "cssd_chunked_forward_h0",
            "cssd_chunked_forward_precise", "cssd_chunked_forward_tf32",
            "cssd_host_forward_device_bytes", "cssd_chunked_forward_host",
            "cssd_backward_workspace_bytes", "cssd_chunked_backward",
@@ -68,6 +68,8 @@ def load(path: str = LIB_PATH):
             vp, dims_p = ctypes.c_void_p, ctypes.POINTER(Dims)
             lib.cssd_workspace_bytes.argtypes = [dims_p, ctypes.c_int]
             lib.cssd_workspace_bytes.restype = ctypes.c_size_t
+            lib.cssd_precise_workspace_bytes.argtypes = [dims_p, ctypes.c_int]
+            lib.cssd_precise_workspace_bytes.restype = ctypes.c_size_t
             lib.cssd_forward_launches.argtypes = [dims_p, ctypes.c_int]
             lib.cssd_forward_launches.restype = ctypes.c_int
             lib.cssd_chunked_forward.argtypes = [dims_p] + [vp] * 8 + [ctypes.c_int, vp, ctypes.c_size_t, vp]
@@ -193,6 +195,11 @@ def workspace_bytes(batch: int, seqlen: int, nheads: int, dstate: int, headdim: 
     return int(load().cssd_workspace_bytes(ctypes.byref(d), int(chunk)))
 
 
+def precise_workspace_bytes(batch: int, seqlen: int, nheads: int, dstate: int, headdim: int, chunk: int) -> int:
+    d = Dims(batch, seqlen, nheads, dstate, headdim)
+    return int(load().cssd_precise_workspace_bytes(ctypes.byref(d), int(chunk)))
+
+
 def forward_launches(batch: int, seqlen: int, nheads: int, dstate: int, headdim: int, chunk: int) -> int:
     d = Dims(batch, seqlen, nheads, dstate, headdim)
     return int(load().cssd_forward_launches(ctypes.byref(d), int(chunk)))
@@ -207,7 +214,8 @@ def chunked_forward(x, dt, A, B, C, D, *, chunk: int = 64, y=None, h_final=None,
     x complex64 [Bz,T,H,P]; dt float32 [Bz,T,H]; A complex64 [H];
     B, C complex64 [Bz,T,H,N]; D float32 [H]; h0 complex64 [Bz,H,N,P], the
     state before the first token (zero when None).  `workspace` is an optional
-    uint8 device tensor of at least workspace_bytes(...) bytes.
+    uint8 device tensor of at least workspace_bytes(...) bytes
+    (precise_workspace_bytes(...) with `precise`).
     """
     lib = load()
     dev = x.device

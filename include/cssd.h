@@ -83,6 +83,13 @@ typedef struct {
  * Returns 0 when the sizes or the chunk are invalid. */
 size_t cssd_workspace_bytes(const cssd_dims* dims, int chunk);
 
+/* Bytes of device workspace cssd_chunked_forward_precise needs for these
+ * sizes: cssd_workspace_bytes, except at dstate 128, where that entry point
+ * runs the CUDA-core chunk kernels and keeps every chunk's state (8 dstate
+ * headdim bytes per chunk and sequence).  Returns 0 when the sizes or the
+ * chunk are invalid. */
+size_t cssd_precise_workspace_bytes(const cssd_dims* dims, int chunk);
+
 /* Chunkwise forward over a whole sequence from a zero initial state.
  *
  * Kernels and precision: every shape except dstate 128 with headdim 16 or 32
@@ -172,11 +179,11 @@ int cssd_chunked_forward_h0(const cssd_dims* dims, const void* x, const float* d
  * accurate expf and the within-chunk cumulative log-steps are summed in double.
  * Measured ~1e-6 of the largest |y|, at about 1.8x the time of
  * cssd_chunked_forward (three times the tensor-core work and twice the shared
- * memory, one CTA per SM).  Built for headdim 64 with dstate 64; dstate 128
- * with headdim 64 returns CSSD_ERR_UNSUPPORTED.  The other shapes (headdim or
- * dstate 16 / 32) run the fp32 CUDA-core chunk kernels.  Arguments,
- * workspace size (cssd_workspace_bytes) and status are otherwise those of
- * cssd_chunked_forward_h0; h0 may be NULL. */
+ * memory, one CTA per SM).  Built for headdim 64 with dstate 64; every other
+ * shape (dstate 128, and headdim or dstate 16 / 32) runs the fp32 CUDA-core
+ * chunk kernels, fp32 throughout (~1e-6 too, slower).  The workspace is
+ * cssd_precise_workspace_bytes(dims, chunk) bytes.  Arguments and status are
+ * otherwise those of cssd_chunked_forward_h0; h0 may be NULL. */
 int cssd_chunked_forward_precise(const cssd_dims* dims, const void* x, const float* dt, const void* A,
                                  const void* B, const void* C, const float* D, const void* h0, void* y,
                                  void* h_final, int chunk, void* workspace, size_t workspace_bytes,

@@ -57,6 +57,12 @@ def test_workspace_bytes(lib):
     assert cssd.workspace_bytes(1, 64, 1, 16, 16, 96) == 0  # unsupported chunk
     assert cssd.workspace_bytes(1, 0, 1, 16, 16, 64) == 0  # empty sequence
     assert cssd.workspace_bytes(1, 64, 1, 48, 16, 64) == 0  # unsupported N
+    # split precision: the forward's workspace, except at dstate 128 (the
+    # CUDA-core kernels keep every chunk's state)
+    assert cssd.precise_workspace_bytes(4, 2048, 24, 64, 64, 64) == cssd.workspace_bytes(4, 2048, 24, 64, 64, 64)
+    assert cssd.precise_workspace_bytes(1, 4096, 8, 32, 32, 128) == cssd.workspace_bytes(1, 4096, 8, 32, 32, 128)
+    assert cssd.precise_workspace_bytes(1, 8192, 32, 128, 64, 128) >= 32 * 64 * 128 * 64 * 8
+    assert cssd.precise_workspace_bytes(1, 64, 1, 48, 16, 64) == 0
 
 
 def _fwd(lib, dims, ptrs=None, chunk=64, ws=None, ws_bytes=0):
@@ -187,7 +193,9 @@ def test_initial_state_and_host_forward_argument_errors(lib):
     f = lib.cssd_chunked_forward_precise  # same arguments and checks
     assert f(None, *p, 64, None, 0, None) == -1
     assert f(ctypes.byref(ok), *p, 128 + 1, None, 0, None) == -3
-    assert f(ctypes.byref(cssd.Dims(1, 64, 1, 128, 64)), *p, 64, None, 0, None) == -3  # dstate 128, headdim 64
+    # dstate 128 with headdim 64 is accepted (the fp32 CUDA-core kernels): the
+    # call gets as far as the workspace check
+    assert f(ctypes.byref(cssd.Dims(1, 64, 1, 128, 64)), *p, 64, ctypes.c_void_p(0x900000), 16, None) == -5
     q = list(p)
     q[6] = ctypes.c_void_p(0x10604)
     assert f(ctypes.byref(ok), *q, 64, None, 0, None) == -4

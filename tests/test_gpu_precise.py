@@ -92,10 +92,32 @@ def test_precise_slow_decay_long_sequence(cs, oracle_lib):
     assert rel_err(hf.cpu().numpy()[:, heads], h_ref) < TOL
 
 
-def test_precise_rejects_dstate_128_tensor_core_shape(cs):
-    d = wl.random_case(8400, 1, 64, 1, 128, 64)
-    with pytest.raises(cs.CssdError):
-        cs.chunked_forward(**dev(d), chunk=64, precise=True)
+@pytest.mark.parametrize("chunk", (64, 128))
+@pytest.mark.parametrize("T", (1, 65, 300))
+def test_precise_dstate_128(cs, oracle_lib, T, chunk):
+    """dstate 128 with headdim 64 (the fp32 CUDA-core chunk kernels), from a
+    given initial state."""
+    d = wl.random_case(8400 + T + chunk, 2, T, 3, 128, 64)
+    h0 = wl.random_state(8500 + T, 2, 3, 128, 64)
+    y, hf = cs.chunked_forward(**dev(d), chunk=chunk, precise=True, h0=torch.from_numpy(h0).cuda())
+    torch.cuda.synchronize()
+    y_ref, h_ref = oracle_lib.cssd_naive(**d, h0=h0)
+    assert rel_err(y.cpu().numpy(), y_ref) < TOL
+    assert rel_err(hf.cpu().numpy(), h_ref) < TOL
+
+
+def test_precise_long_seq_sampled_heads(cs, oracle_lib):
+    """The long_seq shape (dstate 128, headdim 64, chunk 128, slow decay) over
+    8192 tokens; heads 0 and 31 against the oracle."""
+    w = wl.LONG_SEQ.with_(seqlen=8192)
+    d = wl.make_inputs(w)
+    y, hf = cs.chunked_forward(**dev(d), chunk=w.chunk, precise=True)
+    torch.cuda.synchronize()
+    heads = [0, w.nheads - 1]
+    sub = {k: (d[k][heads] if k in ("A", "D") else d[k][:, :, heads]) for k in KEYS}
+    y_ref, h_ref = oracle_lib.cssd_naive(**sub)
+    assert rel_err(y.cpu().numpy()[:, :, heads], y_ref) < TOL
+    assert rel_err(hf.cpu().numpy()[:, heads], h_ref) < TOL
 
 
 def test_precise_is_deterministic(cs):
