@@ -697,9 +697,10 @@ def bench_born(args, dev):
 
 def bench_backward(args, dev):
     """Gradients of the mamba2_layer forward (cssd_chunked_backward: y and the
-    x-gradient run on the fp32 CUDA-core chunk kernels, the B and C gradients
-    on the tensor-core kernel).  HBM roofline on the algorithmic bytes: x, dt,
-    B, C, dy in and gx, gdt, gB, gC out."""
+    x-gradient run on the split-precision half-operand kernel, the B and C
+    gradients on the plain half-operand kernel, each with the index and sign
+    modes).  HBM roofline on the algorithmic bytes: x, dt, B, C, dy in and gx,
+    gdt, gB, gC out."""
     import numpy as np
     import torch
 
@@ -734,7 +735,7 @@ def bench_backward(args, dev):
     gbs = alg / (ms / 1e3) / 1e9
     return {"workload": f"mamba2_layer backward Bz{w.batch} T{w.seqlen} H{w.nheads} N{N} P{P} chunk{w.chunk}",
             "ms_per_call": round(ms, 4), "calls": n, "value": round(w.units / (ms / 1e3), 1), "unit": "token-heads/s",
-            "roofline": {"bound": "hbm", "kernel": "whole backward (24 launches)", "achieved": round(gbs, 1),
+            "roofline": {"bound": "hbm", "kernel": "whole backward (16 launches)", "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
                          "alg_bytes_per_call": alg},
             "workspace_bytes": int(ws.numel())}
@@ -924,14 +925,14 @@ def bench_operand_variant(args, dev, variant):
     hbm, kind = peaks()
     gbs = alg / (k_ms / 1e3) / 1e9
     if variant == "precise":
-        tensor = fused_tensor(units, N, k_ms, passes=3)  # hi.hi, hi.lo, lo.hi
-        label, kname, tkey = "split-precision forward", "fused_chunk_kernel (split)", "fused_chunk_kernel_split"
+        tensor = fused_tensor(units, N, k_ms, passes=3, operand="f16")  # hi.hi, hi.lo, lo.hi of half parts
+        label, kname, tkey = "split-precision forward", "fused_chunk_kernel_h16 (split)", "fused_chunk_kernel_split"
     else:
         tensor = fused_tensor(units, N, k_ms)
         label, kname, tkey = "TF32-operand forward", "fused_chunk_kernel (tf32)", "fused_chunk_kernel_tf32"
     return {"workload": f"mamba2_layer Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch}, {label}",
             "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_call": round(ms, 4), "calls": n,
-            "dtype": "f32 (split TF32 operands)" if variant == "precise" else "tf32",
+            "dtype": "f32 (split half operands)" if variant == "precise" else "tf32",
             "roofline": {"bound": "hbm", "kernel": kname, "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
                          "traffic": recorded_traffic(tkey, units),

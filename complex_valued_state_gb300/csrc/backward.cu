@@ -23,8 +23,8 @@
 // and gD = sum_{b,t,p} Re(conj(dy) x).  The total of r vanishes (R_0 = 0: the
 // first step multiplies the zero initial state), so R_t = -sum_{u < t} r_u too.
 // r_t is a small difference of two sums of P products, so y and gx, which it
-// is formed from, are computed to about fp32 accuracy (with the plain TF32
-// tensor-core forward the error reached 1e-2 of the largest gdt): by the
+// is formed from, are computed to about fp32 accuracy (with operands rounded
+// to 11 significant bits the error reached 1e-2 of the largest gdt): by the
 // split-precision tensor-core kernel where its shape applies, else by the
 // fp32 CUDA-core chunk kernels.  gB and gC, read directly, take the plain
 // tensor-core kernel where it applies.
@@ -264,6 +264,8 @@ __global__ void __launch_bounds__(EB) boundary_kernel(const float* __restrict__ 
     const int64_t bh = q / (nc - 1), b = bh / H, h = bh - b * H;
     const float* hs = Hd + ((size_t)bh * (nc + 1) + c) * (2 * S);
     const float* gs = Gd + ((size_t)bh * (nc + 1) + (nc - c)) * (2 * S);
+    // element i of both dumps is the same (n, p): the sum does not depend on
+    // their layout.
     // per-thread partial sums of 16 products in fp32 (the states themselves
     // carry ~22 significant bits; FP64 arithmetic is slow on this part), the
     // block reduction in double
@@ -405,8 +407,9 @@ unsigned grid_rows(int64_t rows) { return (unsigned)(rows < 65535 * 8 ? rows : 6
 size_t align256(size_t v) { return (v + 255) / 256 * 256; }
 
 // The forward to about fp32 accuracy: the split-precision tensor-core kernel
-// (three TF32 products per product) where it is built (headdim 64, dstate
-// 64), else the fp32 CUDA-core chunk kernels (dstate 128 among them).
+// (each operand as two half parts, three products per product) where it is
+// built (headdim 64, dstate 64), else the fp32 CUDA-core chunk kernels
+// (dstate 128 among them).
 bool precise_on_tc(int64_t N, int64_t P, int chunk) {
     return tc_forward_supported(N, P, chunk) && tc_full_shape(N, P) && N == 64;
 }
@@ -416,7 +419,7 @@ size_t precise_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t
 }
 cudaError_t launch_precise_forward(FwdArgs f, void* ws, cudaStream_t st) {
     if (!precise_on_tc(f.N, f.P, f.chunk)) return launch_seq_forward(f, ws, st);
-    f.split_tf32 = true;
+    f.split_operands = true;
     return launch_tc_forward(f, ws, st);
 }
 

@@ -179,7 +179,7 @@ int forward_common(const cssd_dims* d, const void* x, const float* dt, const voi
     a.y = static_cast<float2*>(y);
     a.h_final = static_cast<float2*>(h_final);
     a.h0 = static_cast<const float2*>(h0);
-    a.split_tf32 = precise;
+    a.split_operands = precise;
     a.tf32_operands = tf32;
     const cudaError_t e = cssd::launch_forward(a, ws, stream);
     if (!workspace) cudaFreeAsync(ws, stream);

@@ -47,17 +47,18 @@ struct FwdArgs {
     float2* y;
     float2* h_final;             // may be null
     const float2* h0 = nullptr;  // state before the first token [Bz,H,N,P]; null = zero
-    // Tensor-core path only: split-precision operands (three TF32 products per
-    // product, about fp32 accuracy, one CTA per SM) instead of plain TF32.
-    bool split_tf32 = false;
+    // Tensor-core path only: split-precision operands (each value as two half
+    // parts, three products per product, about fp32 accuracy, one CTA per SM).
+    bool split_operands = false;
     // Tensor-core path only: plain TF32 operands on every tensor-core shape
     // (dstate 64 otherwise runs half operands with per-tile scales).
     bool tf32_operands = false;
     unsigned mode = 0;  // kFwd* bits (tensor-core path only); D may be null (no skip) when set
-    // kFwdDump: the state chunk c hands to chunk c + 1, in the rotated frame,
-    // at dump[((bh * NH + half) * (nc + 1) + c + 1) * 2 * 64 * 64 + part * 64 * 64 + p * 64 + n]
-    // (part 0 real, 1 imaginary; NH = dstate / 64, nc = 64-token chunks), and
-    // (cos, sin) of that frame's angle at rot_dump[bh * (nc + 1) + c + 1].
+    // kFwdDump (dstate = headdim = 64): the state chunk c hands to chunk c + 1,
+    // in the rotated frame, at dump[(bh * (nc + 1) + c + 1) * 2 * 64 * 64 +
+    // part * 64 * 64 + n * 64 + p] (part 0 real, 1 imaginary; nc = 64-token
+    // chunks), and (cos, sin) of that frame's angle at
+    // rot_dump[bh * (nc + 1) + c + 1].
     float* dump = nullptr;
     float2* rot_dump = nullptr;
 };
@@ -90,7 +91,7 @@ extern thread_local cudaEvent_t g_prof_end;
 
 // The chunked forward: the fused tensor-core kernel where its shape applies
 // (headdim 64, dstate 64 or 128; split-precision operands when
-// FwdArgs::split_tf32), else the CUDA-core chunk kernels.
+// FwdArgs::split_operands, dstate 64 only), else the CUDA-core chunk kernels.
 size_t forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
 size_t forward_precise_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
 int forward_launches(int64_t Bz, int64_t T, int64_t H, int64_t N, int64_t P, int chunk);
@@ -102,8 +103,8 @@ cudaError_t launch_seq_forward(const FwdArgs& a, void* workspace, cudaStream_t s
 
 // Fused tensor-core kernel (forward_tc.cu).
 bool tc_forward_supported(int64_t N, int64_t P, int chunk);
-// The TF32 kernel's shapes (headdim 64, dstate 64 or 128): split precision,
-// TF32 operands and the index and sign modes need them; the other tensor-core
+// The unpadded shapes (headdim 64, dstate 64 or 128): split precision, TF32
+// operands and the index and sign modes need them; the other tensor-core
 // shapes (dstate and headdim up to 64) run the half-operand kernel, padded.
 bool tc_full_shape(int64_t N, int64_t P);
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N);

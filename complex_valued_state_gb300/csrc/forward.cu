@@ -32,8 +32,8 @@ size_t forward_precise_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t
 int forward_launches(int64_t, int64_t, int64_t, int64_t, int64_t, int) { return 3; }
 
 cudaError_t launch_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
-    const bool plain = a.mode == 0 && !a.split_tf32 && !a.tf32_operands;
-    const bool tc_split = !a.split_tf32 || a.N == 64;  // the split instance is built for dstate 64 only
+    const bool plain = a.mode == 0 && !a.split_operands && !a.tf32_operands;
+    const bool tc_split = !a.split_operands || a.N == 64;  // split precision is built for dstate 64 only
     if (tc_forward_supported(a.N, a.P, a.chunk) && ((tc_full_shape(a.N, a.P) && tc_split) || plain))
         return launch_tc_forward(a, ws, st);
     if (a.mode != 0) return cudaErrorInvalidValue;  // index and sign modes: tensor-core path only

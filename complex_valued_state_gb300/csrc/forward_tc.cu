@@ -1,8 +1,9 @@
 // Fused chunkwise forward on the tcgen05 tensor cores for headdim 64 with
 // dstate 64 or 128, in 64-token tiles: fp32 accumulation in tensor memory,
-// with TF32 operands (fused_chunk_kernel: dstate 128, split precision, the
-// backward's runs) or IEEE half operands with per-tile power-of-two scales
-// (fused_chunk_kernel_h16: the dstate-64 forward).
+// with TF32 operands (fused_chunk_kernel: dstate 128 and the TF32 entry
+// point) or IEEE half operands with per-tile power-of-two scales
+// (fused_chunk_kernel_h16: the dstate-64 forward, its split-precision
+// variant and the backward's runs).
 //
 // Method ("The Chunkwise Complex SSD Algorithm", Mamba-3-Lite docs, sections
 // 4.2-4.5; "SSD Theory" section 4.5).  For one (batch, head) with
@@ -56,22 +57,15 @@ constexpr int IT = 2048 / NT;       // tile items (float4) per thread
 constexpr int CPT = 64 / (NT / 128);  // accumulator columns per thread
 constexpr int RING = 2;   // state slots per sequence
 
-// Shared memory regions (bytes).  With split precision every operand is held
-// twice, its TF32 value (hi) and the TF32 value of the remainder (lo), the lo
-// copy right after the hi one.
+// Shared memory regions of the TF32 kernel (bytes).
 constexpr int STACK_BYTES = 3 * 64 * 64 * 4;  // [-Ai; Ar; Ai], 192 rows x 64 K
 constexpr int PLANE_BYTES = 64 * 64 * 4;      // one 64 x 64 fp32 plane
-template <bool SPLIT>
 struct Smem {
-    static constexpr int K = SPLIT ? 2 : 1;
-    static constexpr int S1 = 0;                           // F, then Ct, then M, then y staging
-    static constexpr int S2 = S1 + K * STACK_BYTES;        // X planes (Xr, Xi)
-    static constexpr int S3 = S2 + K * 2 * PLANE_BYTES;    // Bt planes, then H planes
-    static constexpr int BYTES = S3 + K * 2 * PLANE_BYTES;  // 112 KB, or 224 KB split
-    static constexpr uint32_t LO1 = STACK_BYTES;           // lo copy of the S1 stack
-    static constexpr uint32_t LO23 = 2 * PLANE_BYTES;      // lo copy of an S2 / S3 plane pair
+    static constexpr int S1 = 0;                        // F, then Ct, then M, then y staging
+    static constexpr int S2 = S1 + STACK_BYTES;         // X planes (Xr, Xi)
+    static constexpr int S3 = S2 + 2 * PLANE_BYTES;     // Bt planes, then H planes
+    static constexpr int BYTES = S3 + 2 * PLANE_BYTES;  // 112 KB
 };
-static_assert(Smem<true>::BYTES + 2048 <= 227 * 1024, "split operands fit in one CTA's shared memory");
 // y staging: a real and an imaginary 64 x 64 plane with an odd row stride, so
 // that both the column-wise writes from tensor-memory lanes and the row-wise
 // reads of the output pass fall on 32 distinct banks.
@@ -107,44 +101,22 @@ __device__ __forceinline__ void st_f32x2(unsigned char* base, uint32_t off, floa
     *reinterpret_cast<float2*>(base + off) = make_float2(a, b);
 }
 
-// An fp32 operand value as the TF32 pair hi + lo (hi = v rounded to TF32, lo =
-// the remainder rounded to TF32): the three products hi.hi + hi.lo + lo.hi of
-// two such pairs carry about 21 significant bits, the fp32 product up to
-// rounding.  Without SPLIT only hi is formed.
-template <bool SPLIT>
-struct Tf {
-    float hi, lo;
-    __device__ __forceinline__ explicit Tf(float v) {
-        hi = tf32r(v);
-        lo = SPLIT ? tf32r(v - hi) : 0.f;
-    }
-};
-// e^x for the decay factors: the fast exponential for plain TF32 (its error is
-// far below TF32 rounding), CUDA's accurate expf with split precision (the fast
-// one scales its argument in fp32 and loses ~1e-6 relative at |x| ~ 40).
+// e^x for the decay factors: the fast exponential for operands rounded to 11
+// significant bits (its error is far below that rounding), CUDA's accurate
+// expf with split precision (the fast one scales its argument in fp32 and
+// loses ~1e-6 relative at |x| ~ 40).
 template <bool SPLIT>
 __device__ __forceinline__ float kexp(float x) {
     return SPLIT ? expf(x) : __expf(x);
 }
 
-// Store one operand value (hi at `off`, lo `lo_delta` bytes further).
-template <bool SPLIT>
-__device__ __forceinline__ void st_op(unsigned char* base, uint32_t off, uint32_t lo_delta, float v) {
-    const Tf<SPLIT> t(v);
-    st_f32(base, off, t.hi);
-    if (SPLIT) st_f32(base, off + lo_delta, t.lo);
+// TF32 operand stores: the values rounded to TF32, one, two or four at a time.
+__device__ __forceinline__ void st_op(unsigned char* base, uint32_t off, float v) { st_f32(base, off, tf32r(v)); }
+__device__ __forceinline__ void st_op2(unsigned char* base, uint32_t off, float a, float b) {
+    st_f32x2(base, off, tf32r(a), tf32r(b));
 }
-template <bool SPLIT>
-__device__ __forceinline__ void st_op2(unsigned char* base, uint32_t off, uint32_t lo_delta, float a, float b) {
-    const Tf<SPLIT> ta(a), tb(b);
-    st_f32x2(base, off, ta.hi, tb.hi);
-    if (SPLIT) st_f32x2(base, off + lo_delta, ta.lo, tb.lo);
-}
-template <bool SPLIT>
-__device__ __forceinline__ void st_op4(unsigned char* base, uint32_t off, uint32_t lo_delta, float4 v) {
-    const Tf<SPLIT> a(v.x), b(v.y), c(v.z), d(v.w);
-    *reinterpret_cast<float4*>(base + off) = make_float4(a.hi, b.hi, c.hi, d.hi);
-    if (SPLIT) *reinterpret_cast<float4*>(base + off + lo_delta) = make_float4(a.lo, b.lo, c.lo, d.lo);
+__device__ __forceinline__ void st_op4(unsigned char* base, uint32_t off, float4 v) {
+    *reinterpret_cast<float4*>(base + off) = make_float4(tf32r(v.x), tf32r(v.y), tf32r(v.z), tf32r(v.w));
 }
 
 struct TcParams {
@@ -157,10 +129,10 @@ struct TcParams {
     float2* y;         // [Bz,T,H,P]
     float2* h_final;   // [Bz,H,N,P] or null
     const float2* h0;  // [Bz,H,N,P] state before the first token, or null (zero)
-    unsigned mode;     // kFwd* index and sign modes; D is null when there is no skip term
+    unsigned mode;     // kFwd* index and sign modes (half-operand kernel); D is null when there is no skip term
     float* dump;       // kFwdDump: published chunk states (layout in FwdArgs)
     float2* rot_dump;  // kFwdDump: (cos, sin) of each published state's frame
-    unsigned long long* ring;  // [BH][RING][2][P][N] tagged cells
+    unsigned long long* ring;  // [BH][NH][RING][2][64][64] tagged cells: [p][n] (TF32 kernel) or [n][p] (half)
     int* ticket;       // [1]
     float* phi;        // [BH][nc] phase before each chunk, in [-pi, pi]
     float2* tok;       // [BH][nc][CH] per token: (rho_l, theta_l) within the chunk
@@ -311,17 +283,16 @@ __global__ void __launch_bounds__(256) phase_scan_kernel(TcParams p) {
 // NH halves of 64 (dstate = 64 NH): the state GEMM, the hand-off and the
 // carried-in readout run once per half, the score GEMM accumulates over the
 // halves, and the masked scores and Y_diag run once.
-template <int NH, bool SPLIT, bool MODES>
-__global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams p) {
-    using SM = Smem<SPLIT>;
-    const unsigned mode = MODES ? p.mode : 0u;  // index and sign modes (compiled out for the plain forward)
+template <int NH>
+__global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
+    using SM = Smem;
     constexpr int N = NS * NH;  // dstate
-    constexpr uint32_t LO1 = SM::LO1, LO23 = SM::LO23;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ float s_rho[CH];
     __shared__ float2 s_rot[CH];  // (cos, sin) of Theta_l; first used as scan scratch
     __shared__ float2 s_rot_last;
-    __shared__ __align__(8) uint64_t mbar[5];  // S, G, OFF, Y, drain
+    constexpr int NBAR = 5;
+    __shared__ __align__(8) uint64_t mbar[NBAR];  // S, G, OFF, Y, drain
     __shared__ uint32_t s_tmem;
     __shared__ int s_ticket;
     __shared__ int s_bad;
@@ -338,7 +309,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     if (tid == 0) {
         s_ticket = atomicAdd(p.ticket, 1);
         s_bad = 0;
-        for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
+        for (int i = 0; i < NBAR; ++i) tc::mbar_init(&mbar[i], 1);
         tc::mbar_fence_init();
     }
     tc::fence_before_sync();
@@ -355,15 +326,12 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     const int c = ticket / p.BH, bh = ticket - c * p.BH;
     const int b = bh / p.H, h = bh - b * p.H;
     const int t0 = c * CH;
-    // Row of token l of the tile: row0 + l * rstride (time-reversed runs walk
-    // the original rows backwards).  Only rows of real tokens are formed.
-    const bool rev = (mode & kFwdReverse) != 0;
-    const long long row0 = ((long long)b * p.T + (rev ? p.T - 1 - t0 : t0)) * p.H + h;
-    const long long rstride = rev ? -(long long)p.H : (long long)p.H;
-    const bool cj_x = (mode & kFwdConjX) != 0, cj_b = (mode & kFwdConjB) != 0, cj_c = (mode & kFwdConjC) != 0;
+    // Row of token l of the tile: row0 + l * rstride.  Only rows of real
+    // tokens are formed.
+    const long long row0 = ((long long)b * p.T + t0) * p.H + h;
+    const long long rstride = p.H;
     const uint32_t a1 = tc::smem_u32(sm1), a2 = tc::smem_u32(sm2), a3 = tc::smem_u32(sm3);
-    const bool skip = !MODES || p.D != nullptr;
-    const float Dh = skip ? __ldg(p.D + h) : 0.f;  // skip coefficient, needed only at the end: fetched now
+    const float Dh = __ldg(p.D + h);  // skip coefficient, needed only at the end: fetched now
 
     // This thread's items of a 64 x 64 complex tile: the column pair
     // (n0, n0 + 1) of rows l0 + 16 i, i < IT, so that 16 consecutive threads
@@ -384,17 +352,12 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     const bool swap_rows = ((l0 >> 2) & 1) != 0;
     const uint32_t sx = swap_rows ? 16u : 0u;
     // 64 columns (half hf) of a token-major [.., N] complex tile, into registers.
-    auto load_half = [&](const float4* src, int hf, bool cj, float4 (&v)[IT]) {
+    auto load_half = [&](const float4* src, int hf, float4 (&v)[IT]) {
         const long long g = (row0 + (long long)l0 * rstride) * (N / 2) + hf * 32 + (n0 >> 1);
         const long long step = 16 * rstride * (N / 2);
 #pragma unroll
-        for (int i = 0; i < IT; ++i) {
+        for (int i = 0; i < IT; ++i)
             v[i] = (t0 + l0 + 16 * i < p.T) ? __ldg(src + g + i * step) : make_float4(0.f, 0.f, 0.f, 0.f);
-            if (cj) {
-                v[i].y = -v[i].y;
-                v[i].w = -v[i].w;
-            }
-        }
     };
 
     // Rows of x, B and C of the tile one wave of resident CTAs ahead are
@@ -406,8 +369,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             const int pc = pt / p.BH, pbh = pt - pc * p.BH;
             const int tok = pc * CH + (tid & (CH - 1));
             if (tok < p.T) {
-                const int otok = (mode & kFwdReverse) ? p.T - 1 - tok : tok;  // original token
-                const size_t prow = ((size_t)(pbh / p.H) * p.T + otok) * p.H + pbh % p.H;
+                const size_t prow = ((size_t)(pbh / p.H) * p.T + tok) * p.H + pbh % p.H;
                 const int which = tid / CH;  // 0: x, 1: B, 2: C
                 if (which == 0) prefetch_l2(p.x + prow * (PD / 2), PD * 8);
                 else prefetch_l2((which == 1 ? p.B : p.C) + prow * (N / 2), N * 8);
@@ -441,7 +403,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     }
     cp_async_commit();
     float4 cv[IT];
-    load_half(p.C, 0, cj_c, cv);  // C (its first half when dstate is 128) in registers, in flight with the rest
+    load_half(p.C, 0, cv);  // C (its first half when dstate is 128) in registers, in flight with the rest
 
     // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
     if (tid < CH) {
@@ -454,31 +416,23 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     cp_async_wait_all();
     __syncthreads();
     const float rho_end = s_rho[CH - 1];
-    const float eend = kexp<SPLIT>(rho_end);
+    const float eend = __expf(rho_end);
 
     const uint32_t ID = tc::idesc_tf32(128, 64);
     // Complex GEMM into one accumulator: A stack at `as`, B planes at `bs`.
     // Descriptors are built once; stepping K by 8 advances the start-address
     // field (bytes / 16) by 2 * LBO / 16.
-    // With SPLIT the product is taken three times: hi x hi, hi x lo, lo x hi
-    // (the operands' lo copies sit LO1 / LO23 bytes after the hi ones).
-    auto cgemm = [&](uint32_t d, uint32_t as0, uint32_t bs0, bool accumulate) {
-        constexpr int PASSES = SPLIT ? 3 : 1;
+    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs, bool accumulate) {
+        const uint64_t a_up = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
+        const uint64_t a_dn = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
+        const uint64_t b_re = tc::make_desc(bs, PLANE_LBO, SBO);
+        const uint64_t b_im = tc::make_desc(bs + PLANE_BYTES, PLANE_LBO, SBO);
+        constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4, B_STEP = (2 * PLANE_LBO) >> 4;
 #pragma unroll
-        for (int pass = 0; pass < PASSES; ++pass) {
-            const uint32_t as = as0 + (pass == 2 ? LO1 : 0u), bs = bs0 + (pass == 1 ? LO23 : 0u);
-            const uint64_t a_up = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
-            const uint64_t a_dn = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
-            const uint64_t b_re = tc::make_desc(bs, PLANE_LBO, SBO);
-            const uint64_t b_im = tc::make_desc(bs + PLANE_BYTES, PLANE_LBO, SBO);
-            constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4, B_STEP = (2 * PLANE_LBO) >> 4;
+        for (int ks = 0; ks < 8; ++ks)
+            tc::mma_tf32(d, a_up + ks * A_STEP, b_re + ks * B_STEP, ID, (accumulate || ks > 0) ? 1u : 0u);
 #pragma unroll
-            for (int ks = 0; ks < 8; ++ks)
-                tc::mma_tf32(d, a_up + ks * A_STEP, b_re + ks * B_STEP, ID,
-                             (accumulate || pass > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-            for (int ks = 0; ks < 8; ++ks) tc::mma_tf32(d, a_dn + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
-        }
+        for (int ks = 0; ks < 8; ++ks) tc::mma_tf32(d, a_dn + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
     };
     auto issue = [&](uint32_t d, uint32_t as, uint32_t bs, bool accumulate, uint64_t* bar) {
         tc::fence_proxy_async();
@@ -507,22 +461,16 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     {
         float4 xv[IT];
 #pragma unroll
-        for (int i = 0; i < IT; ++i) {
-            xv[i] = *reinterpret_cast<const float4*>(sm2 + o_raw + 8192 * i);
-            if (cj_x) {
-                xv[i].y = -xv[i].y;
-                xv[i].w = -xv[i].w;
-            }
-        }
+        for (int i = 0; i < IT; ++i) xv[i] = *reinterpret_cast<const float4*>(sm2 + o_raw + 8192 * i);
         __syncthreads();  // raw X is overwritten below
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
             const uint32_t o = o_kl64 + 4096 * i;  // rows p = n0, n0 + 1; K = l
             const float r0 = xv[i].x, r1 = xv[i].z, m0 = xv[i].y, m1 = xv[i].w;
-            st_op<SPLIT>(sm2, o + sx, LO23, swap_rows ? r1 : r0);
-            st_op<SPLIT>(sm2, o + (sx ^ 16), LO23, swap_rows ? r0 : r1);
-            st_op<SPLIT>(sm2 + PLANE_BYTES, o + sx, LO23, swap_rows ? m1 : m0);
-            st_op<SPLIT>(sm2 + PLANE_BYTES, o + (sx ^ 16), LO23, swap_rows ? m0 : m1);
+            st_op(sm2, o + sx, swap_rows ? r1 : r0);
+            st_op(sm2, o + (sx ^ 16), swap_rows ? r0 : r1);
+            st_op(sm2 + PLANE_BYTES, o + sx, swap_rows ? m1 : m0);
+            st_op(sm2 + PLANE_BYTES, o + (sx ^ 16), swap_rows ? m0 : m1);
         }
     }
 
@@ -534,15 +482,9 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             float4 bv[IT];
             if (hf == 0) {
 #pragma unroll
-                for (int i = 0; i < IT; ++i) {
-                    bv[i] = *reinterpret_cast<const float4*>(sm3 + o_raw + 8192 * i);
-                    if (cj_b) {
-                        bv[i].y = -bv[i].y;
-                        bv[i].w = -bv[i].w;
-                    }
-                }
+                for (int i = 0; i < IT; ++i) bv[i] = *reinterpret_cast<const float4*>(sm3 + o_raw + 8192 * i);
             } else {
-                load_half(p.B, hf, cj_b, bv);
+                load_half(p.B, hf, bv);
                 wait_bar(&mbar[2], ph ^ 1);  // Y_off of the previous half has read Ct and H
             }
             __syncthreads();  // raw B (half 0) and last half's operands are overwritten below
@@ -554,26 +496,26 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
                 const float b0r = cs * bv[i].x + sn * bv[i].y, b0i = cs * bv[i].y - sn * bv[i].x;
                 const float b1r = cs * bv[i].z + sn * bv[i].w, b1i = cs * bv[i].w - sn * bv[i].z;
                 const uint32_t ob = o_lk64 + 256 * i;
-                st_op2<SPLIT>(sm3, ob, LO23, b0r, b1r);
-                st_op2<SPLIT>(sm3 + PLANE_BYTES, ob, LO23, b0i, b1i);
+                st_op2(sm3, ob, b0r, b1r);
+                st_op2(sm3 + PLANE_BYTES, ob, b0i, b1i);
                 // F[n][l] = exp(rho_end - rho_l) Bt[l][n]
-                const float ds = kexp<SPLIT>(rho_end - s_rho[l]);
+                const float ds = __expf(rho_end - s_rho[l]);
                 const float f0r = ds * b0r, f0i = ds * b0i, f1r = ds * b1r, f1i = ds * b1i;
                 const uint32_t of = o_kl192 + 12288 * i;
                 const float fAr = swap_rows ? f1r : f0r, fAi = swap_rows ? f1i : f0i;  // row written first
                 const float fBr = swap_rows ? f0r : f1r, fBi = swap_rows ? f0i : f1i;
-                st_op<SPLIT>(sm1, of + sx, LO1, -fAi);
-                st_op<SPLIT>(sm1, of + (sx ^ 16), LO1, -fBi);
-                st_op<SPLIT>(sm1, of + BLK + sx, LO1, fAr);
-                st_op<SPLIT>(sm1, of + BLK + (sx ^ 16), LO1, fBr);
-                st_op<SPLIT>(sm1, of + 2 * BLK + sx, LO1, fAi);
-                st_op<SPLIT>(sm1, of + 2 * BLK + (sx ^ 16), LO1, fBi);
+                st_op(sm1, of + sx, -fAi);
+                st_op(sm1, of + (sx ^ 16), -fBi);
+                st_op(sm1, of + BLK + sx, fAr);
+                st_op(sm1, of + BLK + (sx ^ 16), fBr);
+                st_op(sm1, of + 2 * BLK + sx, fAi);
+                st_op(sm1, of + 2 * BLK + (sx ^ 16), fBi);
             }
         }
         issue(tmem + COL_S, a1, a2, false, &mbar[0]);
 
         // ---- 4. Ct half stack into S1 once the state GEMM has read F; G += Ct Bt^T
-        if (NH > 1 && hf > 0) load_half(p.C, hf, cj_c, cv);
+        if (NH > 1 && hf > 0) load_half(p.C, hf, cv);
         wait_bar(&mbar[0], ph);
 #pragma unroll
         for (int i = 0; i < IT; ++i) {
@@ -582,9 +524,9 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             const float c0r = cs * cv[i].x - sn * cv[i].y, c0i = cs * cv[i].y + sn * cv[i].x;
             const float c1r = cs * cv[i].z - sn * cv[i].w, c1i = cs * cv[i].w + sn * cv[i].z;
             const uint32_t oc = o_lk192 + 256 * i;
-            st_op2<SPLIT>(sm1, oc, LO1, -c0i, -c1i);
-            st_op2<SPLIT>(sm1, oc + BLK, LO1, c0r, c1r);
-            st_op2<SPLIT>(sm1, oc + 2 * BLK, LO1, c0i, c1i);
+            st_op2(sm1, oc, -c0i, -c1i);
+            st_op2(sm1, oc + BLK, c0r, c1r);
+            st_op2(sm1, oc + 2 * BLK, c0i, c1i);
         }
         issue(tmem + COL_G, a1, a3, hf > 0, &mbar[1]);
 
@@ -648,16 +590,8 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             tmem_ld_cols(tmem + lane_base + COL_S + c0col, r);
             tc::tmem_wait_ld();
             const uint32_t tag = (uint32_t)(c + 1);
-            float* dmp = (mode & kFwdDump) ? p.dump + (((size_t)bh * NH + hf) * (p.nc + 1) + c + 1) * (2 * PD * NS) +
-                                                 (size_t)part * PD * NS + lrow
-                                           : nullptr;
 #pragma unroll
-            for (int j = 0; j < CPT; ++j) {
-                const float v = fmaf(eend, hv[j], __uint_as_float(r[j]));
-                st_cell(cout + (c0col + j) * NS, v, tag);
-                if (dmp) dmp[(c0col + j) * NS] = v;
-            }
-            if ((mode & kFwdDump) && hf == 0 && tid == 0) p.rot_dump[(size_t)bh * (p.nc + 1) + c + 1] = s_rot_last;
+            for (int j = 0; j < CPT; ++j) st_cell(cout + (c0col + j) * NS, fmaf(eend, hv[j], __uint_as_float(r[j])), tag);
         }
 
         // ---- 6. H_c of this half as the B operand of Y_off (rows p, K = n) in
@@ -685,8 +619,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             unsigned char* plane = sm3 + part * PLANE_BYTES + koff(pcol, nb, 64);
 #pragma unroll
             for (int k4 = 0; k4 < CPT / 4; ++k4)  // K = nb + 4 k4: one core matrix further per step
-                st_op4<SPLIT>(plane, 1024 * k4, LO23,
-                              make_float4(hv[4 * k4], hv[4 * k4 + 1], hv[4 * k4 + 2], hv[4 * k4 + 3]));
+                st_op4(plane, 1024 * k4, make_float4(hv[4 * k4], hv[4 * k4 + 1], hv[4 * k4 + 2], hv[4 * k4 + 3]));
         }
         issue(tmem + COL_OFF, a1, a3, hf > 0, &mbar[2]);  // Y_off' += Ct H_c
     }
@@ -706,7 +639,7 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
             // causal mask as exp(-inf) = 0: a select, not a branch around exp
             const int sidx = c0col + j;
             const float arg = (sidx <= lrow) ? rl - s_rho[sidx] : -INFINITY;
-            m[j] = kexp<SPLIT>(arg) * __uint_as_float(r[j]);
+            m[j] = __expf(arg) * __uint_as_float(r[j]);
         }
         wait_bar(&mbar[2], (NH - 1) & 1);
         // 16-byte stores: four consecutive K of one row fill one core-matrix
@@ -716,10 +649,10 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
         for (int k4 = 0; k4 < CPT / 4; ++k4) {
             const float4 v = make_float4(m[4 * k4], m[4 * k4 + 1], m[4 * k4 + 2], m[4 * k4 + 3]);
             if (part == 0) {
-                st_op4<SPLIT>(mrow, BLK + 3072 * k4, LO1, v);
+                st_op4(mrow, BLK + 3072 * k4, v);
             } else {
-                st_op4<SPLIT>(mrow, 2 * BLK + 3072 * k4, LO1, v);
-                st_op4<SPLIT>(mrow, 3072 * k4, LO1, make_float4(-v.x, -v.y, -v.z, -v.w));
+                st_op4(mrow, 2 * BLK + 3072 * k4, v);
+                st_op4(mrow, 3072 * k4, make_float4(-v.x, -v.y, -v.z, -v.w));
             }
         }
     }
@@ -734,11 +667,9 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
     const long long yoff = (row0 + (long long)ly * rstride) * PD + py;
     float2 xs[YI];
 #pragma unroll
-    for (int k = 0; k < YI; ++k) {
-        xs[k] = (skip && t0 + ly + 8 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
-                                                : make_float2(0.f, 0.f);
-        if (cj_x) xs[k].y = -xs[k].y;
-    }
+    for (int k = 0; k < YI; ++k)
+        xs[k] = (t0 + ly + 8 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
+                                        : make_float2(0.f, 0.f);
     {
         wait_bar(&mbar[3], 0);
         tc::fence_after_sync();
@@ -746,20 +677,19 @@ __global__ void __launch_bounds__(NT, SPLIT ? 1 : 2) fused_chunk_kernel(TcParams
         tmem_ld_cols(tmem + lane_base + COL_Y + c0col, ry);
         tmem_ld_cols(tmem + lane_base + COL_OFF + c0col, ro);
         tc::tmem_wait_ld();
-        const float el = kexp<SPLIT>(s_rho[lrow]);
+        const float el = __expf(s_rho[lrow]);
         float* stage = reinterpret_cast<float*>(sm1) + part * CH * STAGE_LD + lrow * STAGE_LD + c0col;
 #pragma unroll
         for (int j = 0; j < CPT; ++j) stage[j] = fmaf(el, __uint_as_float(ro[j]), __uint_as_float(ry[j]));
     }
     __syncthreads();
     {
-        const float ysign = (mode & kFwdConjY) ? -1.f : 1.f;
         const float* stage = reinterpret_cast<const float*>(sm1) + ly * STAGE_LD + py;
 #pragma unroll
         for (int k = 0; k < YI; ++k) {
             if (t0 + ly + 8 * k < p.T) {
                 const float yr = stage[8 * k * STAGE_LD], yi = stage[CH * STAGE_LD + 8 * k * STAGE_LD];
-                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), ysign * fmaf(Dh, xs[k].y, yi));
+                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
             }
         }
     }
@@ -869,6 +799,17 @@ __device__ __forceinline__ void stm4t(uint32_t addr, uint32_t r0, uint32_t r1, u
                  "r"(r1), "r"(r2), "r"(r3)
                  : "memory");
 }
+// Split precision: a pair of fp32 values as two half pairs, hi = half(v) and
+// lo = half(v - hi), so that hi + lo keeps ~22 significant bits.
+struct SplitH2 {
+    uint32_t hi, lo;
+};
+__device__ __forceinline__ SplitH2 split_h2(float a, float b) {
+    const __half2 h = __floats2half2_rn(a, b);
+    const float2 f = __half22float2(h);
+    const __half2 l = __floats2half2_rn(a - f.x, b - f.y);
+    return {*reinterpret_cast<const uint32_t*>(&h), *reinterpret_cast<const uint32_t*>(&l)};
+}
 __device__ __forceinline__ float maxabs4(float4 v, float m) {
     return fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
 }
@@ -896,8 +837,11 @@ struct Pow2 {
     }
 };
 
-__global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p) {
-    constexpr int N = NS, NT = h16::NT, CPT = h16::CPT;
+template <bool SPLIT, bool MODES>
+__global__ void __launch_bounds__(h16::NT, SPLIT ? 1 : 3) fused_chunk_kernel_h16(TcParams p) {
+    constexpr int NT = h16::NT, CPT = h16::CPT;
+    constexpr uint32_t LO = h16::BYTES;  // SPLIT: each operand's lo copy, this many bytes after the hi one
+    const unsigned mode = MODES ? p.mode : 0u;  // index and sign modes (compiled out for the plain forward)
     constexpr uint32_t RAW_B = h16::RAW_B, XS = h16::XS, FP = h16::FP, CS = h16::CS, MP = h16::MP, BP = h16::BP;
     constexpr uint32_t HS = h16::HS, PLANE = h16::PLANE;
     constexpr uint32_t BLK = h16::BLK, COL_A = h16::COL_A, COL_B = h16::COL_B, TMEM_COLS = h16::TMEM_COLS;
@@ -908,7 +852,8 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     __shared__ __align__(16) float s_erho[CH];  // e^{rho_l}
     __shared__ float2 s_rot[CH];
     __shared__ float2 s_rot_last;
-    __shared__ __align__(8) uint64_t mbar[6];  // S, G, OFF, Y, raw rows, drain
+    constexpr int NBAR = 6;
+    __shared__ __align__(8) uint64_t mbar[NBAR];  // S, G, OFF, Y, raw rows, drain
     __shared__ uint32_t s_tmem;
     __shared__ int s_ticket;
     __shared__ int s_bad;
@@ -922,7 +867,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     if (tid == 0) {
         s_ticket = atomicAdd(p.ticket, 1);
         s_bad = 0;
-        for (int i = 0; i < 6; ++i) tc::mbar_init(&mbar[i], 1);
+        for (int i = 0; i < NBAR; ++i) tc::mbar_init(&mbar[i], 1);
         tc::mbar_fence_init();
     }
     if (tid < 4) s_max[tid] = 0u;
@@ -940,11 +885,16 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const int c = ticket / p.BH, bh = ticket - c * p.BH;
     const int b = bh / p.H, h = bh - b * p.H;
     const int t0 = c * CH;
-    const long long row0 = ((long long)b * p.T + t0) * p.H + h;  // row of token t0; token l at row0 + l H
-    const long long H = p.H;
+    // Row of token l of the tile: row0 + l H (time-reversed runs walk the
+    // original rows backwards, H < 0).  Only rows of real tokens are read.
+    const bool rev = (mode & kFwdReverse) != 0;
+    const long long row0 = ((long long)b * p.T + (rev ? p.T - 1 - t0 : t0)) * p.H + h;
+    const long long H = rev ? -(long long)p.H : (long long)p.H;
+    const bool cj_x = (mode & kFwdConjX) != 0, cj_b = (mode & kFwdConjB) != 0, cj_c = (mode & kFwdConjC) != 0;
     const int Nd = p.Nd, Pd = p.Pd;  // widths of the call; the tiles are padded with zeros to 64
     const uint32_t sb0 = tc::smem_u32(smem);
-    const float Dh = __ldg(p.D + h);  // skip coefficient, needed only at the end: fetched now
+    const bool skip = !MODES || p.D != nullptr;
+    const float Dh = skip ? __ldg(p.D + h) : 0.f;  // skip coefficient, needed only at the end: fetched now
 
     // Lane t of warp w owns token l = 8 w + t/4 of the tile and, in each
     // 8-column block b, the column pair 8 b + 2 (t%4), +1 of x, B and C:
@@ -985,9 +935,14 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const bool lok = t0 + l < p.T;
     float4 cv[8];
 #pragma unroll
-    for (int bb = 0; bb < 8; ++bb)
+    for (int bb = 0; bb < 8; ++bb) {
         cv[bb] = (lok && 8 * bb + 2 * jp < Nd) ? __ldg(p.C + (row0 + (long long)l * H) * (Nd / 2) + 4 * bb + jp)
                                                : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (cj_c) {
+            cv[bb].y = -cv[bb].y;
+            cv[bb].w = -cv[bb].w;
+        }
+    }
 
     // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
     if (tid < CH) {
@@ -995,14 +950,14 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         sincosf(phi_c + tk.y, &sn, &cs);
         s_rho[tid] = tk.x;
         s_rho2[tid] = tk.x * 1.4426950408889634f;
-        s_erho[tid] = __expf(tk.x);
+        s_erho[tid] = kexp<SPLIT>(tk.x);
         s_rot[tid] = make_float2(cs, sn);
         if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
     }
     if (!tc::mbar_wait_bounded(&mbar[4], 0, kWaitCycles)) s_bad = 1;
     __syncthreads();
     const float rho_end = s_rho[CH - 1];
-    const float eend = __expf(rho_end);
+    const float eend = kexp<SPLIT>(rho_end);
     const float2 rot = s_rot[l];
 
     const uint32_t ID = tc::idesc_f16(128, 64);
@@ -1010,18 +965,24 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // one MMA takes K = 16, so the start address steps by two core matrices.
     // B's real plane at `bs` and its imaginary plane `im_off` bytes further,
     // K groups `b_lbo` bytes apart (plain planes, or two blocks of a stack).
-    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs, uint32_t b_lbo, uint32_t im_off) {
-        const uint64_t a_up = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
-        const uint64_t a_dn = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
-        const uint64_t b_re = tc::make_desc(bs, b_lbo, SBO);
-        const uint64_t b_im = tc::make_desc(bs + im_off, b_lbo, SBO);
-        constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4;
-        const uint64_t B_STEP = (2 * b_lbo) >> 4;
+    // With SPLIT the product is taken three times: hi x hi, hi x lo, lo x hi.
+    auto cgemm = [&](uint32_t d, uint32_t as0, uint32_t bs0, uint32_t b_lbo, uint32_t im_off) {
+        constexpr int PASSES = SPLIT ? 3 : 1;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
-            tc::mma_f16(d, a_up + ks * A_STEP, b_re + ks * B_STEP, ID, ks > 0 ? 1u : 0u);
+        for (int pass = 0; pass < PASSES; ++pass) {
+            const uint32_t as = as0 + (pass == 2 ? LO : 0u), bs = bs0 + (pass == 1 ? LO : 0u);
+            const uint64_t a_up = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
+            const uint64_t a_dn = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
+            const uint64_t b_re = tc::make_desc(bs, b_lbo, SBO);
+            const uint64_t b_im = tc::make_desc(bs + im_off, b_lbo, SBO);
+            constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4;
+            const uint64_t B_STEP = (2 * b_lbo) >> 4;
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks) tc::mma_f16(d, a_dn + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
+            for (int ks = 0; ks < 4; ++ks)
+                tc::mma_f16(d, a_up + ks * A_STEP, b_re + ks * B_STEP, ID, (pass > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < 4; ++ks) tc::mma_f16(d, a_dn + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
+        }
     };
     auto issue = [&](uint32_t d, uint32_t as, uint32_t bs, uint32_t b_lbo, uint32_t b_im, uint64_t* bar) {
         tc::fence_proxy_async();
@@ -1041,6 +1002,7 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     // ---- 2. the X^T stack over raw x (rows p, K = l), scaled; the scales of
     // x and C; Ct = e^{i Theta} C as scaled half pairs in registers.
     uint32_t cre[8], cim[8];  // Ct of this lane's token, block bb: (real, imaginary) half pairs
+    uint32_t crl[SPLIT ? 8 : 1], cil[SPLIT ? 8 : 1];  // SPLIT: their lo parts
     float inv_x, inv_c;
     {
         float4 xv[8];
@@ -1048,6 +1010,10 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
 #pragma unroll
         for (int bb = 0; bb < 8; ++bb) {
             xv[bb] = *reinterpret_cast<const float4*>(smem + raw_at(l, 4 * bb + jp));
+            if (cj_x) {
+                xv[bb].y = -xv[bb].y;
+                xv[bb].w = -xv[bb].w;
+            }
             fx = maxabs4(xv[bb], fx);
             fc = maxabs4(cv[bb], fc);
         }
@@ -1066,23 +1032,39 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
             const float4 v = cv[bb];
             const float c0r = r0.x * v.x - r0.y * v.y, c0i = r0.x * v.y + r0.y * v.x;
             const float c1r = r0.x * v.z - r0.y * v.w, c1i = r0.x * v.w + r0.y * v.z;
-            cre[bb] = pack_h2(c0r, c1r);
-            cim[bb] = pack_h2(c0i, c1i);
+            if constexpr (SPLIT) {
+                const SplitH2 sr = split_h2(c0r, c1r), si = split_h2(c0i, c1i);
+                cre[bb] = sr.hi;
+                cim[bb] = si.hi;
+                crl[bb] = sr.lo;
+                cil[bb] = si.lo;
+            } else {
+                cre[bb] = pack_h2(c0r, c1r);
+                cim[bb] = pack_h2(c0i, c1i);
+            }
         }
         // transposed stores: matrix q of the 24 (block b = q / 3 of 8 columns,
         // stack block q % 3: -Xi, Xr, Xi)
 #pragma unroll
         for (int i = 0; i < 6; ++i) {
-            uint32_t rg[4];
+            uint32_t rg[4], rl[4];
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int q = 4 * i + k, bb = q / 3, blk = q % 3;  // compile-time
                 const float4 v = xv[bb];
-                const uint32_t im = pack_h2(v.y * sx.s, v.w * sx.s);
-                rg[k] = blk == 1 ? pack_h2(v.x * sx.s, v.z * sx.s) : blk == 0 ? (im ^ NEG2) : im;
+                if constexpr (SPLIT) {
+                    const SplitH2 re = split_h2(v.x * sx.s, v.z * sx.s), im = split_h2(v.y * sx.s, v.w * sx.s);
+                    rg[k] = blk == 1 ? re.hi : blk == 0 ? (im.hi ^ NEG2) : im.hi;
+                    rl[k] = blk == 1 ? re.lo : blk == 0 ? (im.lo ^ NEG2) : im.lo;
+                } else {
+                    const uint32_t im = pack_h2(v.y * sx.s, v.w * sx.s);
+                    rg[k] = blk == 1 ? pack_h2(v.x * sx.s, v.z * sx.s) : blk == 0 ? (im ^ NEG2) : im;
+                }
             }
             const int q = 4 * i + mrow, bb = (q * 11) >> 5, blk = q - 3 * bb;  // q / 3 for q < 24
-            stm4t(sb0 + XS + ((uint32_t)(warp * 24 + 8 * blk + bb) << 7) + r16, rg[0], rg[1], rg[2], rg[3]);
+            const uint32_t a = sb0 + XS + ((uint32_t)(warp * 24 + 8 * blk + bb) << 7) + r16;
+            stm4t(a, rg[0], rg[1], rg[2], rg[3]);
+            if constexpr (SPLIT) stm4t(a + LO, rl[0], rl[1], rl[2], rl[3]);
         }
     }
 
@@ -1095,6 +1077,10 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
 #pragma unroll
         for (int bb = 0; bb < 8; ++bb) {
             bv[bb] = *reinterpret_cast<const float4*>(smem + RAW_B + raw_at(l, 4 * bb + jp));
+            if (cj_b) {
+                bv[bb].y = -bv[bb].y;
+                bv[bb].w = -bv[bb].w;
+            }
             fb = maxabs4(bv[bb], fb);
         }
         const unsigned mb = warp_max(__float_as_uint(fb));
@@ -1103,24 +1089,43 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         const Pow2 sbk(s_max[1]);
         inv_b = sbk.inv;
         // Bt = e^{-i Theta} B scaled, F = e^{rho_end - rho_l} Bt
-        const float ds = __expf(rho_end - s_rho[l]);
+        const float ds = kexp<SPLIT>(rho_end - s_rho[l]);
         const float2 r0 = make_float2(rot.x * sbk.s, rot.y * sbk.s);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            uint32_t rb[4], rf[4];
+            uint32_t rb[4], rf[4], lb[4], lf[4];
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
                 const float4 v = bv[2 * i + k];
                 const float u0r = r0.x * v.x + r0.y * v.y, u0i = r0.x * v.y - r0.y * v.x;
                 const float u1r = r0.x * v.z + r0.y * v.w, u1i = r0.x * v.w - r0.y * v.z;
-                rb[2 * k] = pack_h2(u0r, u1r);
-                rb[2 * k + 1] = pack_h2(u0i, u1i);
-                rf[2 * k] = pack_h2(u0r * ds, u1r * ds);
-                rf[2 * k + 1] = pack_h2(u0i * ds, u1i * ds);
+                if constexpr (SPLIT) {
+                    const SplitH2 br = split_h2(u0r, u1r), bi = split_h2(u0i, u1i);
+                    const SplitH2 fr = split_h2(u0r * ds, u1r * ds), fi = split_h2(u0i * ds, u1i * ds);
+                    rb[2 * k] = br.hi;
+                    rb[2 * k + 1] = bi.hi;
+                    rf[2 * k] = fr.hi;
+                    rf[2 * k + 1] = fi.hi;
+                    lb[2 * k] = br.lo;
+                    lb[2 * k + 1] = bi.lo;
+                    lf[2 * k] = fr.lo;
+                    lf[2 * k + 1] = fi.lo;
+                } else {
+                    rb[2 * k] = pack_h2(u0r, u1r);
+                    rb[2 * k + 1] = pack_h2(u0i, u1i);
+                    rf[2 * k] = pack_h2(u0r * ds, u1r * ds);
+                    rf[2 * k + 1] = pack_h2(u0i * ds, u1i * ds);
+                }
             }
             const int q = 4 * i + mrow, bb = q >> 1, pl = q & 1;  // matrix q: block bb, plane pl
-            stm4(sb0 + BP + pl * PLANE + ((uint32_t)(bb * 8 + warp) << 7) + r16, rb[0], rb[1], rb[2], rb[3]);
-            stm4t(sb0 + FP + pl * PLANE + ((uint32_t)(warp * 8 + bb) << 7) + r16, rf[0], rf[1], rf[2], rf[3]);
+            const uint32_t ab = sb0 + BP + pl * PLANE + ((uint32_t)(bb * 8 + warp) << 7) + r16;
+            const uint32_t af = sb0 + FP + pl * PLANE + ((uint32_t)(warp * 8 + bb) << 7) + r16;
+            stm4(ab, rb[0], rb[1], rb[2], rb[3]);
+            stm4t(af, rf[0], rf[1], rf[2], rf[3]);
+            if constexpr (SPLIT) {
+                stm4(ab + LO, lb[0], lb[1], lb[2], lb[3]);
+                stm4t(af + LO, lf[0], lf[1], lf[2], lf[3]);
+            }
         }
     }
     issue(tmem + COL_A, sb0 + XS, sb0 + FP, PLANE_LBO, PLANE, &mbar[0]);
@@ -1129,14 +1134,17 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     wait_bar(&mbar[0]);
 #pragma unroll
     for (int i = 0; i < 6; ++i) {
-        uint32_t rg[4];
+        uint32_t rg[4], rl[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int q = 4 * i + k, bb = q / 3, blk = q % 3;  // compile-time
             rg[k] = blk == 1 ? cre[bb] : blk == 0 ? (cim[bb] ^ NEG2) : cim[bb];
+            if constexpr (SPLIT) rl[k] = blk == 1 ? crl[bb] : blk == 0 ? (cil[bb] ^ NEG2) : cil[bb];
         }
         const int q = 4 * i + mrow, bb = (q * 11) >> 5, blk = q - 3 * bb;
-        stm4(sb0 + CS + ((uint32_t)(bb * 24 + 8 * blk + warp) << 7) + r16, rg[0], rg[1], rg[2], rg[3]);
+        const uint32_t a = sb0 + CS + ((uint32_t)(bb * 24 + 8 * blk + warp) << 7) + r16;
+        stm4(a, rg[0], rg[1], rg[2], rg[3]);
+        if constexpr (SPLIT) stm4(a + LO, rl[0], rl[1], rl[2], rl[3]);
     }
     issue(tmem + COL_B, sb0 + CS, sb0 + BP, PLANE_LBO, PLANE, &mbar[1]);
 
@@ -1187,10 +1195,19 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         // row; K + 8 is one core matrix (8 row groups) further
         unsigned char* mrow = smem + MP + part * PLANE + koff16(lrow, c0col, 64);
 #pragma unroll
-        for (int k8 = 0; k8 < CPT / 8; ++k8)
-            *reinterpret_cast<uint4*>(mrow + 1024 * k8) =
-                make_uint4(pack_h2(m[8 * k8], m[8 * k8 + 1]), pack_h2(m[8 * k8 + 2], m[8 * k8 + 3]),
-                           pack_h2(m[8 * k8 + 4], m[8 * k8 + 5]), pack_h2(m[8 * k8 + 6], m[8 * k8 + 7]));
+        for (int k8 = 0; k8 < CPT / 8; ++k8) {
+            if constexpr (SPLIT) {
+                SplitH2 sp[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) sp[u] = split_h2(m[8 * k8 + 2 * u], m[8 * k8 + 2 * u + 1]);
+                *reinterpret_cast<uint4*>(mrow + 1024 * k8) = make_uint4(sp[0].hi, sp[1].hi, sp[2].hi, sp[3].hi);
+                *reinterpret_cast<uint4*>(mrow + LO + 1024 * k8) = make_uint4(sp[0].lo, sp[1].lo, sp[2].lo, sp[3].lo);
+            } else {
+                *reinterpret_cast<uint4*>(mrow + 1024 * k8) =
+                    make_uint4(pack_h2(m[8 * k8], m[8 * k8 + 1]), pack_h2(m[8 * k8 + 2], m[8 * k8 + 3]),
+                               pack_h2(m[8 * k8 + 4], m[8 * k8 + 5]), pack_h2(m[8 * k8 + 6], m[8 * k8 + 7]));
+            }
+        }
     }
     issue(tmem + COL_B, sb0 + XS, sb0 + MP, PLANE_LBO, PLANE, &mbar[3]);
 
@@ -1258,8 +1275,17 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         tc::tmem_wait_ld();
         const uint32_t tag = (uint32_t)(c + 1);
         const float k_s = inv_b * inv_x;  // a product of powers of two: exact
+        // kFwdDump: the published state also goes to [bh][c + 1][part][n][p]
+        float* dmp = (mode & kFwdDump) ? p.dump + ((size_t)bh * (p.nc + 1) + c + 1) * (2 * PD * NS) +
+                                             (size_t)part * PD * NS + (size_t)c0col * PD + lrow
+                                       : nullptr;
 #pragma unroll
-        for (int j = 0; j < CPT; ++j) st_cell(cout + (size_t)j * PD, fmaf(eend, hv[j], __uint_as_float(r[j]) * k_s), tag);
+        for (int j = 0; j < CPT; ++j) {
+            const float v = fmaf(eend, hv[j], __uint_as_float(r[j]) * k_s);
+            st_cell(cout + (size_t)j * PD, v, tag);
+            if (dmp) dmp[(size_t)j * PD] = v;
+        }
+        if ((mode & kFwdDump) && tid == 0) p.rot_dump[(size_t)bh * (p.nc + 1) + c + 1] = s_rot_last;
         float fh = 0.f;
 #pragma unroll
         for (int j = 0; j < CPT; ++j) fh = fmaxf(fh, fabsf(hv[j]));
@@ -1280,15 +1306,28 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
         unsigned char* hrow = smem + HS + koff16(lrow, c0col, 192);
 #pragma unroll
         for (int k8 = 0; k8 < CPT / 8; ++k8) {  // K + 8: one core matrix (24 row groups) further
-            const uint4 v = make_uint4(pack_h2(hv[8 * k8] * s, hv[8 * k8 + 1] * s),
-                                       pack_h2(hv[8 * k8 + 2] * s, hv[8 * k8 + 3] * s),
-                                       pack_h2(hv[8 * k8 + 4] * s, hv[8 * k8 + 5] * s),
-                                       pack_h2(hv[8 * k8 + 6] * s, hv[8 * k8 + 7] * s));
+            uint4 v, w;  // hi (and with SPLIT lo) half pairs of the eight K
+            if constexpr (SPLIT) {
+                SplitH2 sp[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) sp[u] = split_h2(hv[8 * k8 + 2 * u] * s, hv[8 * k8 + 2 * u + 1] * s);
+                v = make_uint4(sp[0].hi, sp[1].hi, sp[2].hi, sp[3].hi);
+                w = make_uint4(sp[0].lo, sp[1].lo, sp[2].lo, sp[3].lo);
+            } else {
+                v = make_uint4(pack_h2(hv[8 * k8] * s, hv[8 * k8 + 1] * s), pack_h2(hv[8 * k8 + 2] * s, hv[8 * k8 + 3] * s),
+                               pack_h2(hv[8 * k8 + 4] * s, hv[8 * k8 + 5] * s), pack_h2(hv[8 * k8 + 6] * s, hv[8 * k8 + 7] * s));
+            }
             if (part == 0) {
                 *reinterpret_cast<uint4*>(hrow + BLK + 3072 * k8) = v;
+                if constexpr (SPLIT) *reinterpret_cast<uint4*>(hrow + LO + BLK + 3072 * k8) = w;
             } else {
                 *reinterpret_cast<uint4*>(hrow + 2 * BLK + 3072 * k8) = v;
                 *reinterpret_cast<uint4*>(hrow + 3072 * k8) = make_uint4(v.x ^ NEG2, v.y ^ NEG2, v.z ^ NEG2, v.w ^ NEG2);
+                if constexpr (SPLIT) {
+                    *reinterpret_cast<uint4*>(hrow + LO + 2 * BLK + 3072 * k8) = w;
+                    *reinterpret_cast<uint4*>(hrow + LO + 3072 * k8) =
+                        make_uint4(w.x ^ NEG2, w.y ^ NEG2, w.z ^ NEG2, w.w ^ NEG2);
+                }
             }
         }
     }
@@ -1306,9 +1345,12 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     const long long yoff = (row0 + (long long)ly * H) * Pd + py;
     float2 xs[YI];
 #pragma unroll
-    for (int k = 0; k < YI; ++k)
-        xs[k] = (pok && t0 + ly + 4 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
-                                               : make_float2(0.f, 0.f);
+    for (int k = 0; k < YI; ++k) {
+        xs[k] = (skip && pok && t0 + ly + 4 * k < p.T)
+                    ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
+                    : make_float2(0.f, 0.f);
+        if (cj_x) xs[k].y = -xs[k].y;
+    }
     {
         wait_bar(&mbar[2]);
         tc::fence_after_sync();
@@ -1338,12 +1380,13 @@ __global__ void __launch_bounds__(h16::NT, 3) fused_chunk_kernel_h16(TcParams p)
     }
     __syncthreads();
     {
+        const float ysign = (mode & kFwdConjY) ? -1.f : 1.f;
         const float* stage = reinterpret_cast<const float*>(smem) + ly * STAGE_LD + py;
 #pragma unroll
         for (int k = 0; k < YI; ++k) {
             if (pok && t0 + ly + 4 * k < p.T) {
                 const float yr = stage[4 * k * STAGE_LD], yi = stage[CH * STAGE_LD + 4 * k * STAGE_LD];
-                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
+                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), ysign * fmaf(Dh, xs[k].y, yi));
             }
         }
     }
@@ -1414,9 +1457,9 @@ static cudaError_t launch_prep(const TcParams& p, bool precise, cudaStream_t st)
 // sequence forward by ~4 %, the others gained nothing).
 
 // `prefetch`: whether CTAs prefetch the inputs of the tile one wave ahead.
-template <int NH, bool SPLIT, bool MODES>
+template <int NH>
 static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefetch, cudaStream_t st) {
-    constexpr int SMEM_BYTES = Smem<SPLIT>::BYTES;
+    constexpr int SMEM_BYTES = Smem::BYTES;
     int dev = 0;
     cudaGetDevice(&dev);
     // CTAs of this kernel resident on the whole device, per device; nonzero
@@ -1427,11 +1470,11 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     int res = cached ? resident[dev].load(std::memory_order_relaxed) : 0;
     if (res == 0) {
         cudaError_t e =
-            cudaFuncSetAttribute(fused_chunk_kernel<NH, SPLIT, MODES>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+            cudaFuncSetAttribute(fused_chunk_kernel<NH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  SMEM_BYTES);
         if (e != cudaSuccess) return e;
         int per_sm = 0, sms = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel<NH, SPLIT, MODES>, NT,
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fused_chunk_kernel<NH>, NT,
                                                           SMEM_BYTES);
         if (e != cudaSuccess) return e;
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -1442,7 +1485,7 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     TcParams p = p_in;
     p.pf_dist = prefetch ? res / 2 : 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
-    fused_chunk_kernel<NH, SPLIT, MODES><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
+    fused_chunk_kernel<NH><<<(unsigned)tiles, NT, SMEM_BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (g_prof_end) cudaEventRecord(g_prof_end, st);
     return e;
@@ -1450,8 +1493,9 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
 
 // The half-operand kernel: three CTAs per SM by shared memory, each holding
 // 128 tensor-memory columns, so every resident CTA finds its columns free.
+template <bool SPLIT, bool MODES>
 static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStream_t st) {
-    constexpr int SMEM_BYTES = h16::BYTES;
+    constexpr int SMEM_BYTES = SPLIT ? 2 * h16::BYTES : h16::BYTES;
     int dev = 0;
     cudaGetDevice(&dev);
     static std::atomic<int> resident[128];
@@ -1459,9 +1503,9 @@ static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStr
     int res = cached ? resident[dev].load(std::memory_order_relaxed) : 0;
     if (res == 0) {
         cudaError_t e =
-            cudaFuncSetAttribute(fused_chunk_kernel_h16, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+            cudaFuncSetAttribute(fused_chunk_kernel_h16<SPLIT, MODES>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(fused_chunk_kernel_h16, cudaFuncAttributePreferredSharedMemoryCarveout,
+        e = cudaFuncSetAttribute(fused_chunk_kernel_h16<SPLIT, MODES>, cudaFuncAttributePreferredSharedMemoryCarveout,
                                  cudaSharedmemCarveoutMaxShared);
         if (e != cudaSuccess) return e;
         // CTAs per SM from the shared-memory, register and thread limits.  The
@@ -1469,7 +1513,7 @@ static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStr
         // (measured), so the limits are applied here directly.
         int smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0, sms = 0;
         cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, fused_chunk_kernel_h16)) != cudaSuccess ||
+        if ((e = cudaFuncGetAttributes(&fa, fused_chunk_kernel_h16<SPLIT, MODES>)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
             (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess ||
@@ -1492,7 +1536,7 @@ static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStr
     TcParams p = p_in;
     p.pf_dist = 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
-    fused_chunk_kernel_h16<<<(unsigned)tiles, h16::NT, SMEM_BYTES, st>>>(p);
+    fused_chunk_kernel_h16<SPLIT, MODES><<<(unsigned)tiles, h16::NT, SMEM_BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (g_prof_end) cudaEventRecord(g_prof_end, st);
     return e;
@@ -1502,7 +1546,7 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     TcParams p;
     const int64_t BH = a.Bz * a.H, nc = (a.T + CH - 1) / CH, NH = (a.N + NS - 1) / NS;
     const bool full = tc_full_shape(a.N, a.P);
-    if (!full && (a.mode != 0 || a.split_tf32 || a.tf32_operands)) return cudaErrorNotSupported;
+    if (!full && (a.mode != 0 || a.split_operands || a.tf32_operands)) return cudaErrorNotSupported;
     unsigned char* w = static_cast<unsigned char*>(ws);
     p.ring = reinterpret_cast<unsigned long long*>(w);
     w += (size_t)BH * NH * RING * 2 * PD * NS * sizeof(unsigned long long);
@@ -1535,23 +1579,21 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     p.status = status_word();
     p.pf_dist = 0;
     p.wait_cycles = kWaitCycles;
-    cudaError_t e = launch_prep(p, a.split_tf32, st);
+    cudaError_t e = launch_prep(p, a.split_operands, st);
     if (e != cudaSuccess) return e;
-    // Split precision is built for dstate 64 only: the dstate-128 variant
-    // stalled in its first multi-chunk run and stays out until the cause is
-    // known (callers reject that shape first).
-    // The index and sign modes (the backward's runs) take their own dstate-64
-    // instances, so the plain forward is compiled without them.
+    // Split precision and the index and sign modes (the backward's runs) are
+    // instances of the half-operand kernel for dstate = headdim = 64, so the
+    // plain forward is compiled without them; callers route other shapes to
+    // the CUDA-core kernels first.
     if (a.mode != 0) {
         if (NH != 1) return cudaErrorNotSupported;
-        return a.split_tf32 ? launch_fused<1, true, true>(p, BH * nc, true, st)
-                            : launch_fused<1, false, true>(p, BH * nc, true, st);
+        return a.split_operands ? launch_fused_h16<true, true>(p, BH * nc, st) : launch_fused_h16<false, true>(p, BH * nc, st);
     }
-    if (a.split_tf32) return NH == 1 ? launch_fused<1, true, false>(p, BH * nc, true, st) : cudaErrorNotSupported;
+    if (a.split_operands) return NH == 1 ? launch_fused_h16<true, false>(p, BH * nc, st) : cudaErrorNotSupported;
     if (a.tf32_operands)
-        return NH == 1 ? launch_fused<1, false, false>(p, BH * nc, true, st)
-                       : launch_fused<2, false, false>(p, BH * nc, true, st);
-    return NH == 1 ? launch_fused_h16(p, BH * nc, st) : launch_fused<2, false, false>(p, BH * nc, true, st);
+        return NH == 1 ? launch_fused<1>(p, BH * nc, true, st)
+                       : launch_fused<2>(p, BH * nc, true, st);
+    return NH == 1 ? launch_fused_h16<false, false>(p, BH * nc, st) : launch_fused<2>(p, BH * nc, true, st);
 }
 
 // Failure-detection self-test: a two-sequence, two-chunk forward whose
@@ -1630,11 +1672,11 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     // the TF32 kernel, then the half-operand kernel on the same problem (the
     // prep resets the ticket to the second chunk and the error word each time)
     if (e == cudaSuccess) e = launch_prep(p, false, st);
-    if (e == cudaSuccess) e = launch_fused<1, false, false>(p, BH * nc, false, st);
+    if (e == cudaSuccess) e = launch_fused<1>(p, BH * nc, false, st);
     int bits[2] = {-1, -1};
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bits[0], p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = launch_prep(p, false, st);
-    if (e == cudaSuccess) e = launch_fused_h16(p, BH * nc, st);
+    if (e == cudaSuccess) e = launch_fused_h16<false, false>(p, BH * nc, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bits[1], p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
     cudaFreeAsync(buf, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);

@@ -170,16 +170,17 @@ int cssd_chunked_forward_h0(const cssd_dims* dims, const void* x, const float* d
                             cssd_stream_t stream);
 
 /* cssd_chunked_forward_h0 to about fp32 accuracy.  The chunked form is exact
- * up to rounding, and on the tensor-core path (headdim 64, dstate 64 or 128)
- * the rounding of cssd_chunked_forward is that of TF32 operands (~1e-4 of the
- * largest |y| on the pages' workloads).  Here every operand is held as two
- * TF32 parts hi + lo (hi = the value rounded to TF32, lo = the remainder
- * rounded to TF32) and every product is taken as hi.hi + hi.lo + lo.hi, which
- * keeps ~21 significant bits per product; the decay exponentials use the
- * accurate expf and the within-chunk cumulative log-steps are summed in double.
- * Measured ~1e-6 of the largest |y|, at about 1.8x the time of
- * cssd_chunked_forward (three times the tensor-core work and twice the shared
- * memory, one CTA per SM).  Built for headdim 64 with dstate 64; every other
+ * up to rounding, and on the tensor-core path the rounding of
+ * cssd_chunked_forward is that of operands with an 11-bit significand (~1e-4
+ * of the largest |y| on the pages' workloads).  Here every operand, scaled by
+ * its tile's power of two, is held as two IEEE half parts hi + lo (hi = the
+ * value rounded to half, lo = the remainder rounded to half) and every product
+ * is taken as hi.hi + hi.lo + lo.hi, which keeps ~22 significant bits per
+ * product; the decay exponentials use the accurate expf and the within-chunk
+ * cumulative log-steps are summed in double.  Measured ~1e-6 of the largest
+ * |y|, at about 2x the time of cssd_chunked_forward (three times the
+ * tensor-core work and twice the shared memory, one CTA per SM).  Built for
+ * headdim 64 with dstate 64; every other
  * shape (dstate 128, and headdim or dstate 16 / 32) runs the fp32 CUDA-core
  * chunk kernels, fp32 throughout (~1e-6 too, slower).  The workspace is
  * cssd_precise_workspace_bytes(dims, chunk) bytes.  Arguments and status are
@@ -331,10 +332,11 @@ int cssd_cayley_scan(const cssd_dims* dims, const float* phi, const float* u, co
  * product of the two runs' states and summed only within chunks, otherwise
  * summed over the sequence from its shorter end; gD = sum Re(conj(dy) x).
  * The forward output y is recomputed, and it and gx are computed to about
- * fp32 accuracy, because R_t is a small difference of large sums that plain
- * TF32 operands would spoil: by the tensor-core kernel with split-precision
- * operands (each value as two TF32 parts, three TF32 products per product)
- * where headdim is 64 and dstate 64, else by the fp32 CUDA-core chunk kernels
+ * fp32 accuracy, because R_t is a small difference of large sums that
+ * operands rounded to 11 significant bits would spoil: by the tensor-core
+ * kernel with split-precision operands (each value as two half parts, three
+ * products per product) where headdim is 64 and dstate 64, else by the fp32
+ * CUDA-core chunk kernels
  * (dstate 128 among them).  gB and gC use the tensor-core forward where it
  * applies; with dstate 128 their runs (state transposed: headdim 128) take
  * the CUDA-core kernels.
