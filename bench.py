@@ -786,10 +786,11 @@ def bench_long_seq(args, dev):
     gbs = alg / (k_ms / 1e3) / 1e9
     return {"workload": f"long_seq Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch}, forward only",
             "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_step": round(ms, 4), "steps": n,
-            "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel (dstate 128, TF32)", "achieved": round(gbs, 1), "peak": hbm,
+            "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel_h16w (dstate 128, half operands)",
+                         "achieved": round(gbs, 1), "peak": hbm,
                          "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind, "kernel_ms": round(k_ms, 4),
                          "traffic": recorded_traffic("fused_chunk_kernel_dstate128", units),
-                         "alg_bytes_per_launch": alg, "tensor": fused_tensor(units, N, k_ms)}}
+                         "alg_bytes_per_launch": alg, "tensor": fused_tensor(units, N, k_ms, operand="f16")}}
 
 
 def f16_peak():

@@ -1,9 +1,9 @@
 // Fused chunkwise forward on the tcgen05 tensor cores for headdim 64 with
 // dstate 64 or 128, in 64-token tiles: fp32 accumulation in tensor memory,
-// with TF32 operands (fused_chunk_kernel: dstate 128 and the TF32 entry
-// point) or IEEE half operands with per-tile power-of-two scales
+// with IEEE half operands with per-tile power-of-two scales
 // (fused_chunk_kernel_h16: the dstate-64 forward, its split-precision
-// variant and the backward's runs).
+// variant and the backward's runs; fused_chunk_kernel_h16w: the dstate-128
+// forward) or TF32 operands (fused_chunk_kernel: the TF32 entry point).
 //
 // Method ("The Chunkwise Complex SSD Algorithm", Mamba-3-Lite docs, sections
 // 4.2-4.5; "SSD Theory" section 4.5).  For one (batch, head) with
@@ -289,7 +289,7 @@ __global__ void __launch_bounds__(NT, 2) fused_chunk_kernel(TcParams p) {
     constexpr int N = NS * NH;  // dstate
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ float s_rho[CH];
-    __shared__ float2 s_rot[CH];  // (cos, sin) of Theta_l; first used as scan scratch
+    __shared__ float2 s_rot[CH];  // (cos, sin) of Theta_l
     __shared__ float2 s_rot_last;
     constexpr int NBAR = 5;
     __shared__ __align__(8) uint64_t mbar[NBAR];  // S, G, OFF, Y, drain
@@ -1414,6 +1414,532 @@ __global__ void __launch_bounds__(h16::NT, SPLIT ? 1 : 3) fused_chunk_kernel_h16
     if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
 }
 
+
+// ------------------------------------------------------------------ dstate 128, half operands
+// fused_chunk_kernel_h16w: the half-operand tile computation for dstate 128
+// and headdim 64 (plain forward).  The state is handled in two 64-row halves
+// hf, as by the TF32 kernel, but with both halves' operands resident at once:
+//     S'_hf^T = X^T F_hf^T,   G = sum_hf Ct_hf Bt_hf^T,
+//     Y_diag^T = X^T M^T,     Y_off^T = sum_hf e^{rho_l} H_hf^T Ct_hf^T.
+// x, B and C take one power-of-two scale per tile each (the two halves'
+// products meet in G), the carried-in state one per half (each half's Y_off
+// has its own accumulator, over its S').  A CTA has 256 threads, 108 KB of
+// shared memory and 256 tensor-memory columns: two per SM.
+namespace h16w {
+constexpr int NT = 256;                       // threads per CTA
+constexpr int CPT = 32;                       // accumulator columns per thread
+constexpr uint32_t PLANE = 64 * 64 * 2;       // one 64 x 64 half plane
+constexpr uint32_t STACK = 3 * PLANE;         // [-Ai; Ar; Ai]: 192 rows x K 64
+constexpr uint32_t BLK = 1024;                // 64 rows further down a stack
+constexpr uint32_t RAW_ROWS = 64 * 576;       // raw rows of one 64-column operand: x, B half 0, B half 1
+constexpr uint32_t XS = 0;                    // X^T stack (rows p, K = l) until Y_diag has read it
+constexpr uint32_t BT0 = STACK;               // Bt planes of half 0 and 1 (rows s, K = n) until G
+constexpr uint32_t BT1 = STACK + 2 * PLANE;
+constexpr uint32_t F0 = STACK + 4 * PLANE;    // F planes (rows n, K = l) until S'
+constexpr uint32_t F1 = STACK + 6 * PLANE;
+constexpr uint32_t CS0 = F0;                  // Ct stacks (rows l, K = n) over F once S' has read it
+constexpr uint32_t CS1 = F0 + STACK;
+constexpr uint32_t MP = BT0;                  // M planes (rows l, K = s) over Bt once G has read it
+constexpr uint32_t HS0 = 0;                   // H_hf^T stacks (rows p, K = n) over X^T, M and Bt1
+constexpr uint32_t HS1 = STACK;               //   once Y_diag has read them
+constexpr int BYTES = 3 * RAW_ROWS;           // 108 KB: the raw rows are the largest footprint
+constexpr uint32_t COL_S0 = 0, COL_S1 = 64, COL_G = 128, TMEM_COLS = 256;  // Y_off_hf over S'_hf, Y_diag over G
+constexpr uint32_t STACK_LBO = 24 * 128, PLANE_LBO = 8 * 128, SBO = 128;
+// Each operand goes over raw rows that every thread has read before it is written:
+// X^T over raw x; F_0 over raw B half 0 and F_1 over raw B half 1; the Bt planes
+// over raw x and raw B half 0.
+static_assert(XS + STACK <= RAW_ROWS, "X^T stack over the raw x rows");
+static_assert(F0 >= RAW_ROWS && F0 + 2 * PLANE <= 2 * RAW_ROWS && F1 >= 2 * RAW_ROWS, "F planes over their half");
+static_assert(BT0 >= XS + STACK && BT1 + 2 * PLANE <= F0, "Bt planes between X^T and F");
+static_assert(CS1 + STACK <= (uint32_t)BYTES && HS1 + STACK <= CS0, "Ct stacks above the H stacks");
+static_assert(2 * CH * STAGE_LD * 4 <= CS0, "y staging ends below the Ct stacks");
+}  // namespace h16w
+
+__global__ void __launch_bounds__(h16w::NT, 2) fused_chunk_kernel_h16w(TcParams p) {
+    constexpr int NT = h16w::NT, CPT = h16w::CPT;
+    constexpr uint32_t PLANE = h16w::PLANE, BLK = h16w::BLK, RAW_ROWS = h16w::RAW_ROWS;
+    constexpr uint32_t XS = h16w::XS, MP = h16w::MP;
+    constexpr uint32_t STACK_LBO = h16w::STACK_LBO, PLANE_LBO = h16w::PLANE_LBO, SBO = h16w::SBO;
+    constexpr uint32_t COL_G = h16w::COL_G, TMEM_COLS = h16w::TMEM_COLS;
+    constexpr int NBAR = 7;
+    extern __shared__ __align__(1024) unsigned char smem[];
+    __shared__ float s_rho[CH];
+    __shared__ __align__(16) float s_rho2[CH];  // rho_l log2(e)
+    __shared__ __align__(16) float s_erho[CH];  // e^{rho_l}
+    __shared__ float2 s_rot[CH];
+    __shared__ float2 s_rot_last;
+    __shared__ __align__(8) uint64_t mbar[NBAR];  // S, G, Y, OFF half 0, OFF half 1, raw rows, drain
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_ticket;
+    __shared__ int s_bad;
+    __shared__ unsigned s_max[5];  // largest |component| (fp32 bits) of x, B, C, H_c half 0, H_c half 1
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    if (warp == 0) {
+        tc::tmem_alloc(&s_tmem, TMEM_COLS);
+        tc::tmem_relinquish();
+    }
+    if (tid == 0) {
+        s_ticket = atomicAdd(p.ticket, 1);
+        s_bad = 0;
+        for (int i = 0; i < NBAR; ++i) tc::mbar_init(&mbar[i], 1);
+        tc::mbar_fence_init();
+    }
+    if (tid < 5) s_max[tid] = 0u;
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = s_tmem;
+    const int ticket = s_ticket;
+    if (ticket >= p.BH * p.nc) {
+        tc::fence_before_sync();
+        __syncthreads();
+        if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+        return;
+    }
+    const int c = ticket / p.BH, bh = ticket - c * p.BH;
+    const int b = bh / p.H, h = bh - b * p.H;
+    const int t0 = c * CH;
+    const long long row0 = ((long long)b * p.T + t0) * p.H + h;  // row of token t0; token l at row0 + l H
+    const long long H = p.H;
+    const uint32_t sb0 = tc::smem_u32(smem);
+    const float Dh = __ldg(p.D + h);  // skip coefficient, needed only at the end: fetched now
+
+    // Lane t of warp w owns token l = 8 w + t/4 of the tile and, in each
+    // 8-column block, the column pair 2 (t%4), +1, as in the dstate-64 kernel.
+    const int l = 8 * warp + (lane >> 2), jp = lane & 3;
+    const int mrow = lane >> 3;
+    const uint32_t r16 = (uint32_t)(lane & 7) << 4;
+
+    // ---- 0. loads: dt tables; raw x rows and the two 64-column halves of
+    // the raw B rows by bulk copies (one row per thread of the first six
+    // warps, completing on mbar[5]; rows past the sequence end are
+    // zero-filled); C into registers, both halves.
+    float2 tk = make_float2(0.f, 0.f);
+    float phi_c = 0.f;
+    if (tid < CH) {
+        tk = __ldcg(p.tok + ((size_t)bh * p.nc + c) * CH + tid);
+        phi_c = __ldcg(p.phi + (size_t)bh * p.nc + c);
+    }
+    const int rows = min(CH, p.T - t0);
+    if (tid == 0) tc::mbar_arrive_expect_tx(&mbar[5], (uint32_t)rows * (uint32_t)(8 * (PD + 2 * NS)));
+    if (tid < 3 * CH) {
+        const int lr = tid & (CH - 1), op = tid >> 6;  // op 0: x, 1: B columns 0-63, 2: B columns 64-127
+        const uint32_t off = op * RAW_ROWS + raw_at(lr, 0);
+        if (lr < rows) {
+            const long long row = row0 + (long long)lr * H;
+            const float4* src = op == 0 ? p.x + row * (PD / 2) : p.B + row * NS + (op - 1) * (NS / 2);
+            tc::bulk_g2s(sb0 + off, src, 8u * NS, &mbar[5]);
+        } else {
+            float4* z = reinterpret_cast<float4*>(smem + off);
+#pragma unroll 1
+            for (int k = 0; k < 32; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+    const bool lok = t0 + l < p.T;
+    float4 cv[16];  // blocks 0-7: columns 0-63, 8-15: columns 64-127
+#pragma unroll
+    for (int bb = 0; bb < 16; ++bb)
+        cv[bb] = lok ? __ldg(p.C + (row0 + (long long)l * H) * NS + 4 * bb + jp) : make_float4(0.f, 0.f, 0.f, 0.f);
+
+    // ---- 1. per-token log-steps and rotations of Theta_l = Phi_c + theta_l
+    if (tid < CH) {
+        float sn, cs;
+        sincosf(phi_c + tk.y, &sn, &cs);
+        s_rho[tid] = tk.x;
+        s_rho2[tid] = tk.x * 1.4426950408889634f;
+        s_erho[tid] = __expf(tk.x);
+        s_rot[tid] = make_float2(cs, sn);
+        if (tid == CH - 1) s_rot_last = make_float2(cs, sn);
+    }
+    if (!tc::mbar_wait_bounded(&mbar[5], 0, kWaitCycles)) s_bad = 1;
+    __syncthreads();
+    const float rho_end = s_rho[CH - 1];
+    const float eend = __expf(rho_end);
+    const float2 rot = s_rot[l];
+
+    const uint32_t ID = tc::idesc_f16(128, 64);
+    // Complex GEMM into one accumulator (as in the dstate-64 kernel), adding
+    // to it when `acc`.
+    auto cgemm = [&](uint32_t d, uint32_t as, uint32_t bs, uint32_t b_lbo, uint32_t im_off, bool acc) {
+        const uint64_t a_up = tc::make_desc(as + 8 * SBO, STACK_LBO, SBO);  // [Ar; Ai]
+        const uint64_t a_dn = tc::make_desc(as, STACK_LBO, SBO);            // [-Ai; Ar]
+        const uint64_t b_re = tc::make_desc(bs, b_lbo, SBO);
+        const uint64_t b_im = tc::make_desc(bs + im_off, b_lbo, SBO);
+        constexpr uint64_t A_STEP = (2 * STACK_LBO) >> 4;
+        const uint64_t B_STEP = (2 * b_lbo) >> 4;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks)
+            tc::mma_f16(d, a_up + ks * A_STEP, b_re + ks * B_STEP, ID, (acc || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) tc::mma_f16(d, a_dn + ks * A_STEP, b_im + ks * B_STEP, ID, 1u);
+    };
+    auto sync_for_mma = [&]() {
+        tc::fence_proxy_async();
+        tc::fence_before_sync();
+        __syncthreads();
+    };
+    auto wait_bar = [&](uint64_t* bar) {
+        if (!tc::mbar_wait_bounded(bar, 0, kWaitCycles)) s_bad = 1;
+    };
+    constexpr uint32_t NEG2 = 0x80008000u;  // sign bits of a half pair
+
+    // ---- 2. the scales of x, B (both halves) and C (both halves); the X^T
+    // stack over raw x; Ct = e^{i Theta} C as scaled half pairs in registers.
+    uint32_t cre[16], cim[16];
+    float inv_x, inv_b, inv_c, scale_b;
+    {
+        float4 xv[8];
+        float fx = 0.f, fb = 0.f, fc = 0.f;
+#pragma unroll
+        for (int bb = 0; bb < 8; ++bb) {
+            xv[bb] = *reinterpret_cast<const float4*>(smem + raw_at(l, 4 * bb + jp));
+            fx = maxabs4(xv[bb], fx);
+            fb = maxabs4(*reinterpret_cast<const float4*>(smem + RAW_ROWS + raw_at(l, 4 * bb + jp)), fb);
+            fb = maxabs4(*reinterpret_cast<const float4*>(smem + 2 * RAW_ROWS + raw_at(l, 4 * bb + jp)), fb);
+        }
+#pragma unroll
+        for (int bb = 0; bb < 16; ++bb) fc = maxabs4(cv[bb], fc);
+        const unsigned mx = warp_max(__float_as_uint(fx)), mb = warp_max(__float_as_uint(fb));
+        const unsigned mc = warp_max(__float_as_uint(fc));
+        if (lane == 0) {
+            atomicMax(&s_max[0], mx);
+            atomicMax(&s_max[1], mb);
+            atomicMax(&s_max[2], mc);
+        }
+        __syncthreads();  // raw x is overwritten below; the maxima are complete
+        const Pow2 sx(s_max[0]), sbk(s_max[1]), sc(s_max[2]);
+        inv_x = sx.inv;
+        inv_b = sbk.inv;
+        inv_c = sc.inv;
+        scale_b = sbk.s;
+        const float2 r0 = make_float2(rot.x * sc.s, rot.y * sc.s);  // the rotation with C's scale
+#pragma unroll
+        for (int bb = 0; bb < 16; ++bb) {
+            const float4 v = cv[bb];
+            cre[bb] = pack_h2(r0.x * v.x - r0.y * v.y, r0.x * v.z - r0.y * v.w);
+            cim[bb] = pack_h2(r0.x * v.y + r0.y * v.x, r0.x * v.w + r0.y * v.z);
+        }
+        // transposed stores: matrix q of the 24 (block b = q / 3 of 8 columns,
+        // stack block q % 3: -Xi, Xr, Xi)
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            uint32_t rg[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int q = 4 * i + k, bb = q / 3, blk = q % 3;  // compile-time
+                const float4 v = xv[bb];
+                const uint32_t im = pack_h2(v.y * sx.s, v.w * sx.s);
+                rg[k] = blk == 1 ? pack_h2(v.x * sx.s, v.z * sx.s) : blk == 0 ? (im ^ NEG2) : im;
+            }
+            const int q = 4 * i + mrow, bb = (q * 11) >> 5, blk = q - 3 * bb;  // q / 3 for q < 24
+            stm4t(sb0 + XS + ((uint32_t)(warp * 24 + 8 * blk + bb) << 7) + r16, rg[0], rg[1], rg[2], rg[3]);
+        }
+    }
+
+    // ---- 3. per half: Bt planes (rows l, K = n) and F planes (rows n, K =
+    // l), written once every thread has read that half's raw rows (they lie
+    // over them); then S'_hf^T = X^T F_hf^T for both halves.
+    {
+        const float ds = __expf(rho_end - s_rho[l]);
+        const float2 r0 = make_float2(rot.x * scale_b, rot.y * scale_b);
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+            float4 bv[8];
+#pragma unroll
+            for (int bb = 0; bb < 8; ++bb)
+                bv[bb] = *reinterpret_cast<const float4*>(smem + (1 + hf) * RAW_ROWS + raw_at(l, 4 * bb + jp));
+            __syncthreads();  // this half's raw B rows are overwritten below
+            const uint32_t bt = hf ? h16w::BT1 : h16w::BT0, f = hf ? h16w::F1 : h16w::F0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                uint32_t rb[4], rf[4];
+#pragma unroll
+                for (int k = 0; k < 2; ++k) {
+                    const float4 v = bv[2 * i + k];
+                    const float u0r = r0.x * v.x + r0.y * v.y, u0i = r0.x * v.y - r0.y * v.x;
+                    const float u1r = r0.x * v.z + r0.y * v.w, u1i = r0.x * v.w - r0.y * v.z;
+                    rb[2 * k] = pack_h2(u0r, u1r);
+                    rb[2 * k + 1] = pack_h2(u0i, u1i);
+                    rf[2 * k] = pack_h2(u0r * ds, u1r * ds);
+                    rf[2 * k + 1] = pack_h2(u0i * ds, u1i * ds);
+                }
+                const int q = 4 * i + mrow, bb = q >> 1, pl = q & 1;  // matrix q: block bb, plane pl
+                stm4(sb0 + bt + pl * PLANE + ((uint32_t)(bb * 8 + warp) << 7) + r16, rb[0], rb[1], rb[2], rb[3]);
+                stm4t(sb0 + f + pl * PLANE + ((uint32_t)(warp * 8 + bb) << 7) + r16, rf[0], rf[1], rf[2], rf[3]);
+            }
+        }
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        tc::fence_after_sync();
+        cgemm(tmem + h16w::COL_S0, sb0 + XS, sb0 + h16w::F0, PLANE_LBO, PLANE, false);
+        cgemm(tmem + h16w::COL_S1, sb0 + XS, sb0 + h16w::F1, PLANE_LBO, PLANE, false);
+        tc::commit(&mbar[0]);
+    }
+
+    // ---- 4. Ct stacks of both halves over F once S' has read it;
+    // G = Ct_0 Bt_0^T + Ct_1 Bt_1^T
+    wait_bar(&mbar[0]);
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const uint32_t cs = hf ? h16w::CS1 : h16w::CS0;
+#pragma unroll
+        for (int i = 0; i < 6; ++i) {
+            uint32_t rg[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int q = 4 * i + k, bb = q / 3 + 8 * hf, blk = q % 3;  // compile-time
+                rg[k] = blk == 1 ? cre[bb] : blk == 0 ? (cim[bb] ^ NEG2) : cim[bb];
+            }
+            const int q = 4 * i + mrow, bb = (q * 11) >> 5, blk = q - 3 * bb;
+            stm4(sb0 + cs + ((uint32_t)(bb * 24 + 8 * blk + warp) << 7) + r16, rg[0], rg[1], rg[2], rg[3]);
+        }
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        tc::fence_after_sync();
+        cgemm(tmem + COL_G, sb0 + h16w::CS0, sb0 + h16w::BT0, PLANE_LBO, PLANE, false);
+        cgemm(tmem + COL_G, sb0 + h16w::CS1, sb0 + h16w::BT1, PLANE_LBO, PLANE, true);
+        tc::commit(&mbar[1]);
+    }
+
+    // Accumulator roles: lane quarter q, column block of CPT columns;
+    // accumulator row L = 32 q + lane is the real part (L < 64) or the
+    // imaginary part (L >= 64) of row lrow = L mod 64 (token l for G, headdim
+    // p for S'_hf^T, Y_off^T and Y_diag^T).
+    const int q = warp & 3, cblk = warp >> 2;
+    const int L = q * 32 + lane;
+    const int part = L >> 6, lrow = L & 63;
+    const int c0col = cblk * CPT;
+    const uint32_t lane_base = (uint32_t)(q * 32) << 16;
+
+    // ---- 5. masked scores M = L o G (scaled like G, times 2^-28) as planes
+    // over Bt once G has read it; Y_diag^T = X^T M^T over G.
+    {
+        float m[CPT];
+        const bool all_masked = c0col > (lrow | 31);
+        wait_bar(&mbar[1]);
+        if (all_masked) {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) m[j] = 0.f;
+        } else {
+            uint32_t r[CPT];
+            tc::fence_after_sync();
+            tc::tmem_ld16(tmem + lane_base + COL_G + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+            tc::tmem_ld16(tmem + lane_base + COL_G + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+            tc::tmem_wait_ld();
+            const float rl2 = s_rho2[lrow];
+            const float4* rs = reinterpret_cast<const float4*>(s_rho2 + c0col);
+#pragma unroll
+            for (int j4 = 0; j4 < CPT / 4; ++j4) {
+                const float4 r4 = rs[j4];
+                const float rv[4] = {r4.x, r4.y, r4.z, r4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = 4 * j4 + u;
+                    const float arg = (c0col + j <= lrow) ? (rl2 - rv[u]) - 28.f : -INFINITY;
+                    m[j] = ex2_approx(arg) * __uint_as_float(r[j]);
+                }
+            }
+        }
+        unsigned char* mrow_p = smem + MP + part * PLANE + koff16(lrow, c0col, 64);
+#pragma unroll
+        for (int k8 = 0; k8 < CPT / 8; ++k8)
+            *reinterpret_cast<uint4*>(mrow_p + 1024 * k8) =
+                make_uint4(pack_h2(m[8 * k8], m[8 * k8 + 1]), pack_h2(m[8 * k8 + 2], m[8 * k8 + 3]),
+                           pack_h2(m[8 * k8 + 4], m[8 * k8 + 5]), pack_h2(m[8 * k8 + 6], m[8 * k8 + 7]));
+    }
+    sync_for_mma();
+    if (tid == 0) {
+        tc::fence_after_sync();
+        cgemm(tmem + COL_G, sb0 + XS, sb0 + MP, PLANE_LBO, PLANE, false);
+        tc::commit(&mbar[2]);
+    }
+
+    // ---- 6. hand-off, one half after the other: the thread owns headdim
+    // column p = lrow of part `part` and the CPT state rows n from c0col of
+    // half hf; each half has its own ring of cells [part][n][p].  It takes
+    // H_c,hf from the cells chunk c-1 wrote and publishes H_{c+1},hf =
+    // e^{rho_end} H_c,hf + S'_hf in the true scale; then H_c,hf^T goes to
+    // shared memory (its own scale) and Y_off_hf^T = H_hf^T Ct_hf^T
+    // accumulates over S'_hf.
+    float inv_h0 = 0.f, inv_h1 = 0.f;
+#pragma unroll 1
+    for (int hf = 0; hf < 2; ++hf) {
+        float hv[CPT];
+        const size_t slot = (size_t)part * NS * PD + (size_t)c0col * PD + lrow;
+        const size_t ring_hf = ((size_t)bh * 2 + hf) * RING;
+        const unsigned long long* cin = p.ring + (ring_hf + (c % RING)) * (2 * PD * NS) + slot;
+        unsigned long long* cout = p.ring + (ring_hf + ((c + 1) % RING)) * (2 * PD * NS) + slot;
+        if (c > 0) {
+            const uint32_t want = (uint32_t)c;
+            const long long w0 = clock64();
+            if (lane == 0) {
+                while ((uint32_t)(ld_cell(cin) >> 32) != want) {
+                    if (clock64() - w0 > p.wait_cycles) break;
+                    __nanosleep(128);
+                }
+            }
+            __syncwarp();
+            bool late = false;
+            for (int half = 0; half < 2 && !late; ++half) {
+                while (true) {
+                    unsigned long long w[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) w[j] = ld_cell(cin + (size_t)(16 * half + j) * PD);
+                    bool all = true;
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        hv[16 * half + j] = __uint_as_float((uint32_t)w[j]);
+                        all = all && ((uint32_t)(w[j] >> 32) == want);
+                    }
+                    if (all) break;
+                    if (clock64() - w0 > p.wait_cycles) {
+                        late = true;
+                        break;
+                    }
+                    __nanosleep(128);
+                }
+            }
+            if (late) {
+                atomicOr(p.err, 1);
+                if (p.status) atomicOr(p.status, kStatusHandoff);
+            }
+        } else if (p.h0) {
+            // the caller's state, [128][64] per sequence: rows 64 hf + c0col + j
+            const float* src =
+                reinterpret_cast<const float*>(p.h0 + ((size_t)bh * 2 * NS + hf * NS + c0col) * PD + lrow) + part;
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) hv[j] = __ldg(src + 2 * PD * j);
+        } else {
+#pragma unroll
+            for (int j = 0; j < CPT; ++j) hv[j] = 0.f;
+        }
+        const uint32_t col_s = hf ? h16w::COL_S1 : h16w::COL_S0;
+        {
+            uint32_t r[CPT];
+            tc::fence_after_sync();
+            tc::tmem_ld16(tmem + lane_base + col_s + c0col, *reinterpret_cast<uint32_t(*)[16]>(r));
+            tc::tmem_ld16(tmem + lane_base + col_s + c0col + 16, *reinterpret_cast<uint32_t(*)[16]>(r + 16));
+            tc::tmem_wait_ld();
+            const uint32_t tag = (uint32_t)(c + 1);
+            const float k_s = inv_b * inv_x;  // a product of powers of two: exact
+#pragma unroll
+            for (int j = 0; j < CPT; ++j)
+                st_cell(cout + (size_t)j * PD, fmaf(eend, hv[j], __uint_as_float(r[j]) * k_s), tag);
+        }
+        float fh = 0.f;
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) fh = fmaxf(fh, fabsf(hv[j]));
+        const unsigned mh = warp_max(__float_as_uint(fh));
+        if (lane == 0) atomicMax(&s_max[3 + hf], mh);
+        tc::fence_before_sync();
+        __syncthreads();  // the scale of H_c,hf is complete; every thread has read S'_hf
+        const Pow2 shc(s_max[3 + hf]);
+        if (hf == 0) inv_h0 = shc.inv;
+        else inv_h1 = shc.inv;
+        const float s = shc.s;
+        if (hf == 0) wait_bar(&mbar[2]);  // Y_diag has read X^T and M: both H stacks may go over them
+        unsigned char* hrow = smem + (hf ? h16w::HS1 : h16w::HS0) + koff16(lrow, c0col, 192);
+#pragma unroll
+        for (int k8 = 0; k8 < CPT / 8; ++k8) {  // K + 8: one core matrix (24 row groups) further
+            const uint4 v = make_uint4(pack_h2(hv[8 * k8] * s, hv[8 * k8 + 1] * s),
+                                       pack_h2(hv[8 * k8 + 2] * s, hv[8 * k8 + 3] * s),
+                                       pack_h2(hv[8 * k8 + 4] * s, hv[8 * k8 + 5] * s),
+                                       pack_h2(hv[8 * k8 + 6] * s, hv[8 * k8 + 7] * s));
+            if (part == 0) {
+                *reinterpret_cast<uint4*>(hrow + BLK + 3072 * k8) = v;
+            } else {
+                *reinterpret_cast<uint4*>(hrow + 2 * BLK + 3072 * k8) = v;
+                *reinterpret_cast<uint4*>(hrow + 3072 * k8) = make_uint4(v.x ^ NEG2, v.y ^ NEG2, v.z ^ NEG2, v.w ^ NEG2);
+            }
+        }
+        sync_for_mma();
+        if (tid == 0) {
+            tc::fence_after_sync();
+            // Y_off_hf^T = H_hf^T Ct_hf^T over S'_hf; the Ct stack's blocks 1 and 2 serve as B planes
+            cgemm(tmem + col_s, sb0 + (hf ? h16w::HS1 : h16w::HS0), sb0 + (hf ? h16w::CS1 : h16w::CS0) + BLK, STACK_LBO,
+                  BLK, false);
+            tc::commit(&mbar[3 + hf]);
+        }
+    }
+
+    // ---- 7. y = Y_diag + e^{rho_l} (Y_off_0 + Y_off_1) + D x with the scales
+    // taken out; the skip term uses the exact fp32 input.  The staging planes
+    // lie over the H stacks, which both Y_off GEMMs have finished reading.
+    constexpr int YI = CH * PD / NT;  // output elements per thread: rows ly + 4 k, column py
+    const int ly = tid >> 6, py = tid & 63;
+    const long long ystep = 4 * H * PD;
+    const long long yoff = (row0 + (long long)ly * H) * PD + py;
+    float2 xs[YI];
+#pragma unroll
+    for (int k = 0; k < YI; ++k)
+        xs[k] = (t0 + ly + 4 * k < p.T) ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
+                                        : make_float2(0.f, 0.f);
+    {
+        wait_bar(&mbar[3]);
+        wait_bar(&mbar[4]);
+        tc::fence_after_sync();
+        const float k_d = inv_c * inv_b * inv_x * 268435456.f;  // and the masked scores' 2^-28
+        const float k_o0 = inv_c * inv_h0, k_o1 = inv_c * inv_h1;
+        float* stage = reinterpret_cast<float*>(smem) + part * CH * STAGE_LD + c0col * STAGE_LD + lrow;
+        const float4* er = reinterpret_cast<const float4*>(s_erho + c0col);
+#pragma unroll
+        for (int hh = 0; hh < CPT / 16; ++hh) {
+            uint32_t ry[16], ro0[16], ro1[16];
+            tc::tmem_ld16(tmem + lane_base + COL_G + c0col + 16 * hh, ry);
+            tc::tmem_ld16(tmem + lane_base + h16w::COL_S0 + c0col + 16 * hh, ro0);
+            tc::tmem_ld16(tmem + lane_base + h16w::COL_S1 + c0col + 16 * hh, ro1);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int j4 = 0; j4 < 4; ++j4) {
+                const float4 e4 = er[4 * hh + j4];
+                const float ev[4] = {e4.x, e4.y, e4.z, e4.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int j = 4 * j4 + u;
+                    const float off = fmaf(k_o0, __uint_as_float(ro0[j]), k_o1 * __uint_as_float(ro1[j]));
+                    stage[(16 * hh + j) * STAGE_LD] = fmaf(ev[u], off, __uint_as_float(ry[j]) * k_d);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    {
+        const float* stage = reinterpret_cast<const float*>(smem) + ly * STAGE_LD + py;
+#pragma unroll
+        for (int k = 0; k < YI; ++k) {
+            if (t0 + ly + 4 * k < p.T) {
+                const float yr = stage[4 * k * STAGE_LD], yi = stage[CH * STAGE_LD + 4 * k * STAGE_LD];
+                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), fmaf(Dh, xs[k].y, yi));
+            }
+        }
+    }
+
+    // ---- 8. final state of the sequence, rotated back to the original frame
+    if (c == p.nc - 1 && p.h_final) {
+        const float cs = s_rot_last.x, sn = s_rot_last.y;
+        for (int i = tid; i < 2 * NS * PD; i += NT) {  // element (n, p) = i of [128][64]
+            const int n = i / PD, pp = i - n * PD, hf = n / NS, nn = n - hf * NS;
+            const unsigned long long* cell =
+                p.ring + (((size_t)bh * 2 + hf) * RING + ((c + 1) % RING)) * (2 * PD * NS) + (size_t)nn * PD + pp;
+            const float hr = __uint_as_float((uint32_t)ld_cell(cell));
+            const float hi = __uint_as_float((uint32_t)ld_cell(cell + PD * NS));
+            p.h_final[(size_t)bh * 2 * NS * PD + i] = make_float2(cs * hr - sn * hi, cs * hi + sn * hr);
+        }
+    }
+
+    if (s_bad && tid == 0) {
+        atomicOr(p.err, 2);
+        if (p.status) atomicOr(p.status, kStatusChunkMma);
+        tc::drain_mmas(&mbar[6], kWaitCycles);
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tc::tmem_dealloc(tmem, TMEM_COLS);
+}
+
 }  // namespace
 
 // The tensor-core kernel runs 64-token tiles with headdim 64 and dstate 64 or
@@ -1491,8 +2017,41 @@ static cudaError_t launch_fused(const TcParams& p_in, int64_t tiles, bool prefet
     return e;
 }
 
-// The half-operand kernel: three CTAs per SM by shared memory, each holding
-// 128 tensor-memory columns, so every resident CTA finds its columns free.
+// First launch of a half-operand kernel on a device: its shared-memory
+// attributes, and the CTAs the whole device holds at once, from the
+// shared-memory, register and thread limits of one SM (the occupancy query
+// answers one CTA per SM for these kernels, while the SMs hold more,
+// measured).  Every resident CTA must find its tensor-memory columns free.
+template <typename Kernel>
+static cudaError_t half_kernel_setup(Kernel kern, int smem_bytes, int nt, int tmem_cols, int* resident) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_bytes)) != cudaSuccess ||
+        (e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                  cudaSharedmemCarveoutMaxShared)) != cudaSuccess)
+        return e;
+    int smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0, sms = 0;
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) != cudaSuccess ||
+        (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+        return e;
+    const int per_cta_smem = smem_bytes + (int)fa.sharedSizeBytes + reserved;
+    const int regs_per_warp = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated in units of 256
+    int per_sm = smem_sm / per_cta_smem;
+    per_sm = std::min(per_sm, regs_sm / (regs_per_warp * (nt / 32)));
+    per_sm = std::min(per_sm, threads_sm / nt);
+    if (per_sm < 1 || per_sm * tmem_cols > 512) return cudaErrorNotSupported;
+    *resident = per_sm * sms;
+    return cudaSuccess;
+}
+
+// The dstate-64 half-operand kernel: three CTAs per SM by shared memory, each
+// holding 128 tensor-memory columns (one with split precision).
 template <bool SPLIT, bool MODES>
 static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStream_t st) {
     constexpr int SMEM_BYTES = SPLIT ? 2 * h16::BYTES : h16::BYTES;
@@ -1500,34 +2059,11 @@ static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStr
     cudaGetDevice(&dev);
     static std::atomic<int> resident[128];
     const bool cached = dev >= 0 && dev < 128;
-    int res = cached ? resident[dev].load(std::memory_order_relaxed) : 0;
-    if (res == 0) {
-        cudaError_t e =
-            cudaFuncSetAttribute(fused_chunk_kernel_h16<SPLIT, MODES>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (!cached || resident[dev].load(std::memory_order_relaxed) == 0) {
+        int res = 0;
+        const cudaError_t e = half_kernel_setup(fused_chunk_kernel_h16<SPLIT, MODES>, SMEM_BYTES, h16::NT,
+                                                (int)h16::TMEM_COLS, &res);
         if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(fused_chunk_kernel_h16<SPLIT, MODES>, cudaFuncAttributePreferredSharedMemoryCarveout,
-                                 cudaSharedmemCarveoutMaxShared);
-        if (e != cudaSuccess) return e;
-        // CTAs per SM from the shared-memory, register and thread limits.  The
-        // occupancy query answers one for this kernel, while the SMs hold three
-        // (measured), so the limits are applied here directly.
-        int smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0, sms = 0;
-        cudaFuncAttributes fa;
-        if ((e = cudaFuncGetAttributes(&fa, fused_chunk_kernel_h16<SPLIT, MODES>)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-            return e;
-        const int per_cta_smem = SMEM_BYTES + (int)fa.sharedSizeBytes + reserved;
-        const int regs_per_warp = (fa.numRegs * 32 + 255) / 256 * 256;  // allocated in units of 256
-        int per_sm = smem_sm / per_cta_smem;
-        per_sm = std::min(per_sm, regs_sm / (regs_per_warp * (h16::NT / 32)));
-        per_sm = std::min(per_sm, threads_sm / h16::NT);
-        // every resident CTA must find its tensor-memory columns free
-        if (per_sm < 1 || per_sm * (int)h16::TMEM_COLS > 512) return cudaErrorNotSupported;
-        res = per_sm * sms;
         if (cached) resident[dev].store(res, std::memory_order_relaxed);
     }
     // No L2 prefetch of later tiles: measured on this kernel, prefetching half
@@ -1537,6 +2073,29 @@ static cudaError_t launch_fused_h16(const TcParams& p_in, int64_t tiles, cudaStr
     p.pf_dist = 0;
     if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
     fused_chunk_kernel_h16<SPLIT, MODES><<<(unsigned)tiles, h16::NT, SMEM_BYTES, st>>>(p);
+    const cudaError_t e = cudaGetLastError();
+    if (g_prof_end) cudaEventRecord(g_prof_end, st);
+    return e;
+}
+
+// The dstate-128 half-operand kernel: two CTAs per SM, each holding 256
+// tensor-memory columns.
+static cudaError_t launch_fused_h16w(const TcParams& p_in, int64_t tiles, cudaStream_t st) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    static std::atomic<int> resident[128];
+    const bool cached = dev >= 0 && dev < 128;
+    if (!cached || resident[dev].load(std::memory_order_relaxed) == 0) {
+        int res = 0;
+        const cudaError_t e =
+            half_kernel_setup(fused_chunk_kernel_h16w, h16w::BYTES, h16w::NT, (int)h16w::TMEM_COLS, &res);
+        if (e != cudaSuccess) return e;
+        if (cached) resident[dev].store(res, std::memory_order_relaxed);
+    }
+    TcParams p = p_in;
+    p.pf_dist = 0;
+    if (g_prof_begin) cudaEventRecord(g_prof_begin, st);
+    fused_chunk_kernel_h16w<<<(unsigned)tiles, h16w::NT, h16w::BYTES, st>>>(p);
     const cudaError_t e = cudaGetLastError();
     if (g_prof_end) cudaEventRecord(g_prof_end, st);
     return e;
@@ -1593,18 +2152,19 @@ cudaError_t launch_tc_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     if (a.tf32_operands)
         return NH == 1 ? launch_fused<1>(p, BH * nc, true, st)
                        : launch_fused<2>(p, BH * nc, true, st);
-    return NH == 1 ? launch_fused_h16<false, false>(p, BH * nc, st) : launch_fused<2>(p, BH * nc, true, st);
+    return NH == 1 ? launch_fused_h16<false, false>(p, BH * nc, st) : launch_fused_h16w(p, BH * nc, st);
 }
 
 // Failure-detection self-test: a two-sequence, two-chunk forward whose
 // tickets start at the second chunk, so no CTA ever publishes the first
 // chunk's state and the hand-off wait of the second chunk must give up after
-// `wait_cycles`.  Runs the TF32 kernel and then the half-operand kernel and
-// returns their error bits (bit 0: a hand-off wait timed out) through
-// *err_bits after synchronising the stream: the TF32 kernel's in bits 0-7,
-// the half-operand kernel's in bits 8-15.
+// `wait_cycles`.  Runs the TF32 kernel, the half-operand kernel at dstate 64
+// and the one at dstate 128, and returns their error bits (bit 0: a hand-off
+// wait timed out) through *err_bits after synchronising the stream: bits
+// 0-7, 8-15 and 16-23 in that order.
 cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cudaStream_t st) {
-    const int Bz = 1, T = 2 * CH, H = 2, N = NS, P = PD;
+    // buffers sized for dstate 128; the dstate-64 runs use their first part
+    const int Bz = 1, T = 2 * CH, H = 2, N = 2 * NS, P = PD;
     const size_t nx = (size_t)Bz * T * H * P, nb = (size_t)Bz * T * H * N, nt = (size_t)Bz * T * H;
     const size_t ws_bytes = tc_forward_workspace_bytes(Bz, T, H, N);
     const size_t total = (2 * nx + 2 * nb) * sizeof(float2) + nt * sizeof(float) + H * (sizeof(float2) + sizeof(float)) +
@@ -1639,7 +2199,7 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     const int64_t BH = Bz * H, nc = 2;
     unsigned char* w = ws;
     p.ring = reinterpret_cast<unsigned long long*>(w);
-    w += (size_t)BH * 1 * RING * 2 * PD * NS * sizeof(unsigned long long);
+    w += (size_t)BH * 2 * RING * 2 * PD * NS * sizeof(unsigned long long);
     p.ticket = reinterpret_cast<int*>(w);
     p.err = reinterpret_cast<int*>(w) + 1;
     w += 256;
@@ -1663,24 +2223,31 @@ cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cu
     p.BH = (int)BH;
     p.nc = (int)nc;
     p.NH = 1;
-    p.Nd = N;
+    p.Nd = NS;
     p.Pd = P;
     p.first_ticket = (int)BH;  // chunk 0 of every sequence is never taken
     p.status = status_word();
     p.pf_dist = 0;
     p.wait_cycles = wait_cycles;
-    // the TF32 kernel, then the half-operand kernel on the same problem (the
-    // prep resets the ticket to the second chunk and the error word each time)
+    // the TF32 kernel and the half-operand kernel at dstate 64, then the
+    // half-operand kernel at dstate 128, on the same problem (the prep resets
+    // the ticket to the second chunk and the error word each time)
     if (e == cudaSuccess) e = launch_prep(p, false, st);
     if (e == cudaSuccess) e = launch_fused<1>(p, BH * nc, false, st);
-    int bits[2] = {-1, -1};
+    int bits[3] = {-1, -1, -1};
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bits[0], p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
     if (e == cudaSuccess) e = launch_prep(p, false, st);
     if (e == cudaSuccess) e = launch_fused_h16<false, false>(p, BH * nc, st);
     if (e == cudaSuccess) e = cudaMemcpyAsync(&bits[1], p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
+    p.NH = 2;
+    p.Nd = N;
+    if (e == cudaSuccess) e = launch_prep(p, false, st);
+    if (e == cudaSuccess) e = launch_fused_h16w(p, BH * nc, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(&bits[2], p.err, sizeof(int), cudaMemcpyDeviceToHost, st);
     cudaFreeAsync(buf, st);
     if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (err_bits) *err_bits = (bits[0] < 0 || bits[1] < 0) ? -1 : (bits[0] | (bits[1] << 8));
+    if (err_bits)
+        *err_bits = (bits[0] < 0 || bits[1] < 0 || bits[2] < 0) ? -1 : (bits[0] | (bits[1] << 8) | (bits[2] << 16));
     return e;
 }
 

@@ -176,10 +176,10 @@ def profile_events(begin=None, end=None):
 
 
 def selftest_handoff_timeout(wait_cycles: int = 2_000_000, stream=None) -> int:
-    """Run both tensor-core forward kernels with a predecessor chunk that never
+    """Run the tensor-core forward kernels with a predecessor chunk that never
     publishes; return their error bits: the TF32 kernel's in bits 0-7, the
-    half-operand kernel's in bits 8-15 (bit 0 of each set = the bounded
-    hand-off wait gave up)."""
+    dstate-64 half-operand kernel's in bits 8-15, the dstate-128 one's in bits
+    16-23 (bit 0 of each set = the bounded hand-off wait gave up)."""
     import torch as _t
 
     bits = ctypes.c_int(-1)

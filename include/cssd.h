@@ -94,9 +94,10 @@ size_t cssd_precise_workspace_bytes(const cssd_dims* dims, int chunk);
  *
  * Kernels and precision: every shape except dstate 128 with headdim 16 or 32
  * runs on the tensor cores, rounding the GEMM operands to an 11-bit
- * significand and accumulating in fp32.  dstate and headdim up to 64 use IEEE
- * half operands with a power-of-two scale per tile and operand (tiles below 64
- * are padded with zeros to 64); dstate 128 with headdim 64 uses TF32.  Decays,
+ * significand and accumulating in fp32: IEEE half operands with a
+ * power-of-two scale per tile and operand (dstate and headdim up to 64, tiles
+ * below 64 padded with zeros to 64; dstate 128 with headdim 64 in two 64-row
+ * state halves, the carried-in state scaled per half).  Decays,
  * rotations, the inter-chunk state and the output are fp32.  Measured errors
  * are 1e-4 to 5e-4 of the largest value of y and of h_final (the bar the
  * tests hold is 2e-3).  dstate 128 with headdim 16 or 32 runs the CUDA-core
@@ -196,10 +197,10 @@ int cssd_chunked_forward_precise(const cssd_dims* dims, const void* x, const flo
  * "The Chunkwise Complex SSD Algorithm" (sections 4.3-4.5) is exact up to
  * rounding; the pages fix no operand precision for its GEMMs.
  * cssd_chunked_forward takes half operands with a power-of-two scale per tile
- * and operand at dstate 64 (the same 11-bit significand, a narrower exponent
- * range covered by the per-tile scales) and TF32 at dstate 128; this entry
- * point keeps TF32 at dstate 64 too, for callers and measurements that want
- * the wider operand exponent range without per-tile scaling.  The other shapes
+ * and operand (the same 11-bit significand, a narrower exponent range covered
+ * by the per-tile scales); this entry point keeps TF32 at dstate 64 and 128,
+ * for callers and measurements that want the wider operand exponent range
+ * without per-tile scaling.  The other shapes
  * (dstate or headdim below 64, and dstate 128 with a smaller headdim) run the
  * fp32 CUDA-core chunk kernels.
  * Arguments, workspace size (cssd_workspace_bytes) and status are those of
@@ -403,16 +404,18 @@ int cssd_device_status(unsigned* bits, int clear, cssd_stream_t stream);
 int cssd_profile_events(void* ev_begin, void* ev_end);
 
 /* Failure-detection self-test of the forward's inter-chunk hand-off.  Runs
- * both tensor-core forward kernels (TF32 operands, then half operands) on a
- * small internal problem (two sequences, two 64-token chunks, zero inputs)
+ * the tensor-core forward kernels (TF32 operands, half operands at dstate 64,
+ * half operands at dstate 128) on a small internal problem (two sequences,
+ * two 64-token chunks, zero inputs)
  * whose first chunk is never processed, so the second chunk's bounded wait for
  * its predecessor's state has to give up after `wait_cycles` SM clocks.  Each
  * kernel then records bit 0 in its error word, finishes, and frees its tensor
  * memory; the device stays usable.  The call allocates its buffers
- * stream-ordered, synchronises `stream`, and returns the two error words in
- * *err_bits: the TF32 kernel's in bits 0-7, the half-operand kernel's in bits
- * 8-15 (in each, bit 0 = a hand-off wait timed out, bit 1 = a tensor-core
- * completion wait timed out).  Returns CSSD_ERR_NULL / CSSD_ERR_DIMS for bad
+ * stream-ordered, synchronises `stream`, and returns the three error words in
+ * *err_bits: the TF32 kernel's in bits 0-7, the dstate-64 half-operand
+ * kernel's in bits 8-15, the dstate-128 one's in bits 16-23 (in each, bit 0 =
+ * a hand-off wait timed out, bit 1 = a tensor-core completion wait timed
+ * out).  Returns CSSD_ERR_NULL / CSSD_ERR_DIMS for bad
  * arguments, CSSD_ERR_CUDA if a runtime call fails. */
 int cssd_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cssd_stream_t stream);
 

@@ -2,10 +2,10 @@
 the CPU oracle, and the operand-precision comparison with the default forward.
 
 The default forward takes half operands with a power-of-two scale per tile and
-operand at dstate and headdim up to 64 (padded to 64 below that), and TF32
-operands at dstate 128; cssd_chunked_forward_tf32 keeps TF32 on the TF32
-kernel's shapes (headdim 64, dstate 64 or 128) and runs the fp32 CUDA-core
-kernels on the others.  Where both are 11-bit operand paths the half-operand
+operand on every tensor-core shape (dstate and headdim up to 64, padded to 64
+below that, and dstate 128 with headdim 64); cssd_chunked_forward_tf32 keeps
+TF32 on the unpadded shapes (headdim 64, dstate 64 or 128) and runs the fp32
+CUDA-core kernels on the others.  Where both are 11-bit operand paths the half-operand
 error must stay within twice the TF32 error (plus a floor of 1e-5 of the
 largest magnitude for cases where both are tiny); the tiny workload (dstate =
 headdim = 16) compares half operands with fp32 and is held to the parity bar
