@@ -384,7 +384,7 @@ def run_ours(args, rank, world, local):
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "step_launch": "one CUDA graph per step (forward prep, phase scan, chunk kernel, decode step), replayed",
+        "step_launch": "one CUDA graph per step (forward prep, chunk kernel, decode step), replayed",
         "ms_per_step_stream_launches": round(ms_stream, 5),
         "vs_baseline": None, "dtype": "f16", "data": "synthetic",
         "precision": "GEMM operands IEEE half with a power-of-two scale per tile and operand, fp32 accumulation; "

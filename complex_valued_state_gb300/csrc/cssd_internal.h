@@ -107,6 +107,9 @@ bool tc_forward_supported(int64_t N, int64_t P, int chunk);
 // operands and the index and sign modes need them; the other tensor-core
 // shapes (dstate and headdim up to 64) run the half-operand kernel, padded.
 bool tc_full_shape(int64_t N, int64_t P);
+// Launches of one tensor-core forward: the prep (one kernel, or two for
+// sequences of more than 64 chunks) and the chunk kernel.
+int tc_forward_launches(int64_t T);
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N);
 cudaError_t launch_tc_forward(const FwdArgs& a, void* workspace, cudaStream_t stream);
 cudaError_t tc_selftest_handoff_timeout(long long wait_cycles, int* err_bits, cudaStream_t stream);

@@ -27,9 +27,11 @@ size_t forward_precise_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t
     return forward_workspace_bytes(Bz, T, H, N, P, chunk);
 }
 
-// Tensor-core path: two prep kernels and the chunk kernel; CUDA-core path:
-// chunk states, scan, readout.
-int forward_launches(int64_t, int64_t, int64_t, int64_t, int64_t, int) { return 3; }
+// Tensor-core path: the prep and the chunk kernel (tc_forward_launches);
+// CUDA-core path: chunk states, scan, readout.
+int forward_launches(int64_t, int64_t T, int64_t, int64_t N, int64_t P, int chunk) {
+    return tc_forward_supported(N, P, chunk) ? tc_forward_launches(T) : 3;
+}
 
 cudaError_t launch_forward(const FwdArgs& a, void* ws, cudaStream_t st) {
     const bool plain = a.mode == 0 && !a.split_operands && !a.tf32_operands;

@@ -185,7 +185,8 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CPT])
 }
 
 // ------------------------------------------------------------------ prep
-// Two small kernels before the chunk kernel.
+// Two small kernels before the chunk kernel (one, seq_prep_kernel, for
+// sequences of up to 64 chunks).
 //
 // chunk_prep_kernel: one warp per (sequence, 64-token chunk).  Inclusive
 // cumsum of softplus(dt) over the chunk's tokens (padded tokens add nothing),
@@ -196,21 +197,11 @@ __device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, uint32_t (&r)[CPT])
 // rotates by stays within 2 pi and carries ~2e-7 of rounding instead of the
 // ~1e-5 a float cumsum to |theta| ~ 60 leaves; plain TF32 rounding is far
 // coarser than either.  The same CTAs clear the hand-off words.
+// The per-token tables of chunk c of sequence bh, computed by one warp
+// (lane: its lane); returns the chunk's phase total (in lane 31).
 template <bool PRECISE>
-__global__ void __launch_bounds__(256) chunk_prep_kernel(TcParams p) {
+__device__ __forceinline__ float chunk_tables(const TcParams& p, int bh, int c, int lane) {
     using Real = typename std::conditional<PRECISE, double, float>::type;
-    const int lane = threadIdx.x & 31;
-    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);  // global warp = bh * nc + c
-    {
-        // hand-off words: NH * RING * 2 * 64 * 64 per sequence, spread over all threads
-        const size_t words = (size_t)p.BH * p.NH * RING * 2 * PD * NS;
-        ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring);
-        const size_t nthreads = (size_t)gridDim.x * blockDim.x;
-        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < words / 2; i += nthreads)
-            cells[i] = make_ulonglong2(0ull, 0ull);
-    }
-    if (gw >= p.BH * p.nc) return;
-    const int bh = gw / p.nc, c = gw - bh * p.nc;
     const int b = bh / p.H, h = bh % p.H;
     const Real alpha = p.A[h].x, beta = (p.mode & kFwdConjA) ? -p.A[h].y : p.A[h].y;
     const float* dtb = p.dt + (size_t)b * p.T * p.H + h;  // token t at dtb[t * H]
@@ -230,7 +221,7 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(TcParams p) {
         }
     }
     v[1] += __shfl_sync(0xffffffffu, v[0], 31);
-    float2* out = p.tok + (size_t)gw * CH;
+    float2* out = p.tok + ((size_t)bh * p.nc + c) * CH;
     float th[2];
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
@@ -243,12 +234,50 @@ __global__ void __launch_bounds__(256) chunk_prep_kernel(TcParams p) {
         }
         out[hh * 32 + lane] = make_float2((float)(alpha * v[hh]), th[hh]);
     }
-    if (lane == 31) p.phi[gw] = th[1];  // phase total, turned into Phi_c below
+    return th[1];
+}
+
+// One warp's step of the phase prefix of a sequence: lane l holds the phase
+// total `th` of chunk c0 + l; writes Phi_c (the sum of the totals before c,
+// in double, reduced mod 2 pi) for the chunks below nc and advances `carry`
+// (the sum before c0, reduced likewise) past the 32 chunks.
+__device__ __forceinline__ void phase_prefix_step(float* ph, int c0, int nc, double th, int lane, double& carry) {
+    const double two_pi = 6.283185307179586476925286766559;
+    double v = th;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const double u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
+    }
+    const double excl = carry + v - th;
+    // reduced to [-pi, pi] by subtracting the nearest multiple of 2 pi
+    // (exact enough in double for any angle a sequence accumulates)
+    if (c0 + lane < nc) ph[c0 + lane] = (float)fma(-rint(excl * (1.0 / two_pi)), two_pi, excl);
+    const double cs = carry + __shfl_sync(0xffffffffu, v, 31);
+    carry = fma(-rint(cs * (1.0 / two_pi)), two_pi, cs);
+}
+
+template <bool PRECISE>
+__global__ void __launch_bounds__(256) chunk_prep_kernel(TcParams p) {
+    const int lane = threadIdx.x & 31;
+    const int gw = blockIdx.x * 8 + (threadIdx.x >> 5);  // global warp = bh * nc + c
+    {
+        // hand-off words: NH * RING * 2 * 64 * 64 per sequence, spread over all threads
+        const size_t words = (size_t)p.BH * p.NH * RING * 2 * PD * NS;
+        ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring);
+        const size_t nthreads = (size_t)gridDim.x * blockDim.x;
+        for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < words / 2; i += nthreads)
+            cells[i] = make_ulonglong2(0ull, 0ull);
+    }
+    if (gw >= p.BH * p.nc) return;
+    const int bh = gw / p.nc, c = gw - bh * p.nc;
+    const float total = chunk_tables<PRECISE>(p, bh, c, lane);
+    if (lane == 31) p.phi[gw] = total;  // phase total, turned into Phi_c below
 }
 
 // phase_scan_kernel: one warp per sequence.  Phi_c = sum of the phase totals of
-// the chunks before c, accumulated in double and reduced mod 2 pi, written over
-// the totals; resets the ticket and the error word.
+// the chunks before c, written over the totals; resets the ticket and the
+// error word.
 __global__ void __launch_bounds__(256) phase_scan_kernel(TcParams p) {
     const int lane = threadIdx.x & 31;
     const int bh = blockIdx.x * 8 + (threadIdx.x >> 5);
@@ -257,24 +286,47 @@ __global__ void __launch_bounds__(256) phase_scan_kernel(TcParams p) {
         *p.err = 0;
     }
     if (bh >= p.BH) return;
-    const double two_pi = 6.283185307179586476925286766559;
     float* ph = p.phi + (size_t)bh * p.nc;
     double carry = 0.0;
     for (int c0 = 0; c0 < p.nc; c0 += 32) {
-        const int c = c0 + lane;
-        const double th = (c < p.nc) ? (double)ph[c] : 0.0;
-        double v = th;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const double u = __shfl_up_sync(0xffffffffu, v, o);
-            if (lane >= o) v += u;
+        const double th = (c0 + lane < p.nc) ? (double)ph[c0 + lane] : 0.0;
+        phase_prefix_step(ph, c0, p.nc, th, lane, carry);
+    }
+}
+
+// seq_prep_kernel: both of the above in one launch for sequences of up to
+// kSeqPrepChunks chunks: one CTA of 32 warps per sequence clears the
+// sequence's hand-off words, forms 32 chunks' tables at a time (a warp per
+// chunk), and its first warp turns their phase totals into Phi_c.  The same
+// arithmetic in the same order as the two kernels, so the same tables.
+constexpr int kSeqPrepChunks = 64;
+template <bool PRECISE>
+__global__ void __launch_bounds__(1024) seq_prep_kernel(TcParams p) {
+    __shared__ float s_tot[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int bh = blockIdx.x;
+    if (bh == 0 && threadIdx.x == 0) {
+        *p.ticket = p.first_ticket;
+        *p.err = 0;
+    }
+    {
+        const size_t words = (size_t)p.NH * RING * 2 * PD * NS;  // this sequence's hand-off words
+        ulonglong2* cells = reinterpret_cast<ulonglong2*>(p.ring + (size_t)bh * words);
+        for (size_t i = threadIdx.x; i < words / 2; i += blockDim.x) cells[i] = make_ulonglong2(0ull, 0ull);
+    }
+    float* ph = p.phi + (size_t)bh * p.nc;
+    double carry = 0.0;
+    for (int c0 = 0; c0 < p.nc; c0 += 32) {
+        if (c0 + warp < p.nc) {
+            const float total = chunk_tables<PRECISE>(p, bh, c0 + warp, lane);
+            if (lane == 31) s_tot[warp] = total;
         }
-        const double excl = carry + v - th;
-        // reduced to [-pi, pi] by subtracting the nearest multiple of 2 pi
-        // (exact enough in double for any angle a sequence accumulates)
-        if (c < p.nc) ph[c] = (float)fma(-rint(excl * (1.0 / two_pi)), two_pi, excl);
-        const double cs = carry + __shfl_sync(0xffffffffu, v, 31);
-        carry = fma(-rint(cs * (1.0 / two_pi)), two_pi, cs);
+        __syncthreads();
+        if (warp == 0) {
+            const double th = (c0 + lane < p.nc) ? (double)s_tot[lane] : 0.0;
+            phase_prefix_step(ph, c0, p.nc, th, lane, carry);
+        }
+        __syncthreads();  // s_tot is refilled by the next 32 chunks
     }
 }
 
@@ -1957,6 +2009,8 @@ bool tc_forward_supported(int64_t N, int64_t P, int chunk) {
 
 bool tc_full_shape(int64_t N, int64_t P) { return P == PD && (N == NS || N == 2 * NS); }
 
+int tc_forward_launches(int64_t T) { return (T + CH - 1) / CH <= kSeqPrepChunks ? 2 : 3; }
+
 size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N) {
     const int64_t BH = Bz * H, nc = (T + CH - 1) / CH, NH = (N + NS - 1) / NS;
     size_t off = (size_t)BH * NH * RING * 2 * PD * NS * sizeof(unsigned long long);  // hand-off cells
@@ -1967,6 +2021,14 @@ size_t tc_forward_workspace_bytes(int64_t Bz, int64_t T, int64_t H, int64_t N) {
 }
 
 static cudaError_t launch_prep(const TcParams& p, bool precise, cudaStream_t st) {
+    if (p.nc <= kSeqPrepChunks) {
+        // one launch; longer sequences would walk their chunks serially in one CTA
+        if (precise)
+            seq_prep_kernel<true><<<(unsigned)p.BH, 1024, 0, st>>>(p);
+        else
+            seq_prep_kernel<false><<<(unsigned)p.BH, 1024, 0, st>>>(p);
+        return cudaGetLastError();
+    }
     const int64_t warps = (int64_t)p.BH * p.nc;
     if (precise)
         chunk_prep_kernel<true><<<(unsigned)((warps + 7) / 8), 256, 0, st>>>(p);

@@ -50,9 +50,13 @@ def test_workspace_bytes(lib):
     # CUDA-core path: every chunk's end state plus per-chunk decay totals
     got = cssd.workspace_bytes(1, 4096, 8, 32, 32, 128)
     assert got >= 8 * 32 * 32 * 32 * 8
-    assert cssd.forward_launches(4, 2048, 24, 64, 64, 64) == 3
+    # tensor cores: one prep launch up to 64 chunks of 64 tokens, two beyond, then the chunk kernel
+    assert cssd.forward_launches(4, 2048, 24, 64, 64, 64) == 2
+    assert cssd.forward_launches(4, 4096, 24, 64, 64, 64) == 2
+    assert cssd.forward_launches(4, 4097, 24, 64, 64, 64) == 3
     assert cssd.forward_launches(1, 65536, 32, 128, 64, 128) == 3
-    assert cssd.forward_launches(1, 4096, 8, 32, 32, 128) == 3
+    assert cssd.forward_launches(1, 4096, 8, 32, 32, 128) == 2  # padded to the tensor-core tile
+    assert cssd.forward_launches(1, 4096, 8, 128, 32, 128) == 3  # CUDA-core kernels
     assert cssd.workspace_bytes(1, 65, 1, 16, 16, 64) > cssd.workspace_bytes(1, 64, 1, 16, 16, 64)
     assert cssd.workspace_bytes(1, 64, 1, 16, 16, 96) == 0  # unsupported chunk
     assert cssd.workspace_bytes(1, 0, 1, 16, 16, 64) == 0  # empty sequence
