@@ -687,7 +687,7 @@ def bench_born(args, dev):
     tf = minimal / (ms / 1e3) / 1e12
     return {"workload": f"htransformer_attn Bz{Bz} T{T} H{H} D{D}", "ms_per_call": round(ms, 4), "calls": n,
             "value": round(Bz * T * H / (ms / 1e3), 1), "unit": "token-heads/s",
-            "roofline": {"bound": "tensor", "kernel": "born_kernel_w16", "achieved": round(tf, 1),
+            "roofline": {"bound": "tensor", "kernel": "born_kernel_q128<16>", "achieved": round(tf, 1),
                          "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_kind": kind,
                          "flops_per_launch": minimal, "flops": "algorithmic: the causal pairs",
                          "executed_flops_per_launch": executed,

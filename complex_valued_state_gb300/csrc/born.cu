@@ -6,20 +6,13 @@
 // The factor 1/(D tau_i) is common to a row's numerator and denominator and is
 // left out (psi does not depend on it).
 //
-// Width 16 runs born_kernel_w16 (below): 128 queries per CTA, the real and
-// imaginary scores in two accumulators.  Width 32 runs born_kernel:
-// one CTA (128 threads, one per tensor-memory lane) owns 64 queries of one
-// head and walks the key blocks of 64 up to the diagonal (a head's CTAs are
-// launched together, so its keys and values are read from DRAM about once):
-//   G = conj(Q) K^T     stacked real form: A = [-Ai; Ar; Ai] of A = conj(Q),
-//                       B = planes Kr, Ki, so lanes 0-63 hold Re G and lanes
-//                       64-127 Im G (the chunk kernels' complex GEMM)
-//   S = G o G           squared in place in tensor memory by the thread that
-//                       owns the lane (Re^2 on lanes 0-63, Im^2 on 64-127),
-//                       causal mask on the diagonal block
-//   ACC += S [Vr; Vi; 1]^T   A = S read from tensor memory; the row of ones
-//                       makes the last column the running sum of scores
-// and at the end sums the two lane halves (|g|^2 = Re^2 + Im^2) and divides.
+// One CTA of 256 threads owns 128 queries of one head, one per tensor-memory
+// lane, and walks the key blocks of 64 up to the diagonal (a head's CTAs are
+// launched together, its longest first, so its keys and values are read from
+// DRAM about once).  Per key block the real and imaginary scores are real
+// GEMMs into two accumulators, the threads square them in place, and the
+// value GEMM reads the squared scores from tensor memory; a row of ones in
+// the value operand makes one accumulator column the running sum of scores.
 // Scores need no rescaling between key blocks: they are non-negative and the
 // normalisation is a plain sum, so numerator and denominator accumulate in
 // fp32 in tensor memory across all blocks.
@@ -33,10 +26,7 @@
 namespace cssd {
 namespace {
 
-constexpr int BQ = 64;   // queries per CTA
-constexpr int BT = 128;  // threads: one per tensor-memory lane
 constexpr long long kBornWait = 4000000000LL;  // ~2 s at 2 GHz
-
 
 __device__ __forceinline__ uint32_t kofs(int row, int k, int rows) {
     return (uint32_t)((((k >> 2) * (rows >> 3) + (row >> 3)) << 7) + ((row & 7) << 4) + ((k & 3) << 2));
@@ -53,307 +43,44 @@ __device__ __forceinline__ void sts2(unsigned char* base, uint32_t off, float a,
     *reinterpret_cast<float2*>(base + off) = make_float2(a, b);
 }
 
-template <int D>
-struct BornCfg {
-    static constexpr int BK = 64;                     // keys per block
-    static constexpr int NB = 2 * D + 16;             // value operand rows: Vr, Vi, ones, zeros
-    static constexpr int Q_BYTES = 3 * BQ * D * 4;    // conj(Q) stack, 192 rows x D
-    static constexpr int KP_BYTES = BK * D * 4;       // one key plane, BK rows x D
-    static constexpr int V_BYTES = NB * BK * 4;       // value operand, NB rows x BK keys
-    static constexpr int KV_BYTES = 2 * KP_BYTES + V_BYTES;  // one key block's operands
-    static constexpr int SMEM = Q_BYTES + 2 * KV_BYTES;        // two key blocks in flight
-    static constexpr int ITEMS = BK * D / 2 / BT;     // float4 (two complex) per thread per key block
-    static constexpr int STAGE_LD = 2 * D + 1;        // staged floats per query row
-    // One score buffer and the sums: 128 columns at width 16 (four CTAs per SM).
-    static constexpr uint32_t COL_G = 0, COL_ACC = BK;
-    static constexpr uint32_t TMEM_COLS = COL_ACC + NB <= 128 ? 128 : 256;
-    static_assert(COL_ACC + NB <= TMEM_COLS, "tensor-memory budget");
-    static_assert(BQ * STAGE_LD * 4 <= SMEM, "staging fits in shared memory");
-    static_assert(ITEMS * BT * 2 == BK * D, "item mapping covers a key block");
-};
-
-template <int D>
-__global__ void __launch_bounds__(BT) born_kernel(const float4* __restrict__ q, const float4* __restrict__ k,
-                                                  const float4* __restrict__ v, float2* __restrict__ psi, int T,
-                                                  int H, int BH, int nqb, unsigned* status) {
-    using Cfg = BornCfg<D>;
-    constexpr int NB = Cfg::NB, IT = Cfg::ITEMS, BK = Cfg::BK;
-    extern __shared__ __align__(1024) unsigned char smem[];
-    __shared__ __align__(8) uint64_t mbar[3];  // G done, drain, ACC update done
-    __shared__ int s_gave_up;                   // some thread's completion wait gave up
-    __shared__ uint32_t s_tmem;
-
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    unsigned char* sq = smem;
-    // key block kb's operands live in buffer kb & 1: planes Kr, Ki, then the value operand
-    auto skb = [&](int buf) { return smem + Cfg::Q_BYTES + buf * Cfg::KV_BYTES; };
-    auto svb = [&](int buf) { return skb(buf) + 2 * Cfg::KP_BYTES; };
-    // The query blocks of one head are consecutive CTAs (its latest, longest
-    // block first), so they run close together and read the head's keys and
-    // values from L2 rather than each from DRAM.
-    const int bh = (int)(blockIdx.x / nqb);
-    const int qb = nqb - 1 - (int)(blockIdx.x % nqb);
-    const int b = bh / H, h = bh - b * H;
-    const int i0 = qb * BQ;
-    // float4 pointer to token t of this head (D / 2 float4 per token)
-    auto tok = [&](const float4* base, int t) { return base + ((size_t)((size_t)b * T + t) * H + h) * (D / 2); };
-
-    if (warp == 0) {
-        tc::tmem_alloc(&s_tmem, Cfg::TMEM_COLS);
-        tc::tmem_relinquish();
-    }
-    if (tid == 0) {
-        s_gave_up = 0;
-        for (int i = 0; i < 3; ++i) tc::mbar_init(&mbar[i], 1);
-        tc::mbar_fence_init();
-    }
-    // Rows 2D.. of both value operands: ones (the score sum), then zeros.
-    for (int e = tid; e < 2 * (NB - 2 * D) * BK; e += BT) {
-        const int buf = e / ((NB - 2 * D) * BK), f = e % ((NB - 2 * D) * BK);
-        const int r = 2 * D + f / BK, j = f % BK;
-        sts(svb(buf), kofs(r, j, NB), r == 2 * D ? 1.f : 0.f);
-    }
-    // Key and value rows of a block: item e = tid + BT i is float4 c (two
-    // complex) of key j, so that consecutive lanes read consecutive 16-byte
-    // pieces of a row.
-    auto item_j = [&](int e) { return e / (D / 2); };
-    auto item_c = [&](int e) { return e % (D / 2); };
-    // conj(Q) as the stack [-Ai; Ar; Ai] with Ar = Re q, Ai = -Im q.
-    for (int e = tid; e < BQ * D / 2; e += BT) {
-        const int i = item_j(e), c = item_c(e);
-        const float4 x = (i0 + i < T) ? __ldg(tok(q, i0 + i) + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        const float r0 = rna_tf32(x.x), m0 = rna_tf32(x.y), r1 = rna_tf32(x.z), m1 = rna_tf32(x.w);
-        sts2(sq, kofs(i, 2 * c, 3 * BQ), m0, m1);
-        sts2(sq, kofs(BQ + i, 2 * c, 3 * BQ), r0, r1);
-        sts2(sq, kofs(2 * BQ + i, 2 * c, 3 * BQ), -m0, -m1);
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    tc::fence_after_sync();
-    const uint32_t tmem = s_tmem;
-
-    // Tensor-memory lane of this thread: L = 32 warp + lane, part 0 (lanes 0-63)
-    // or 1 (64-127) of query row lrow.
-    const int L = warp * 32 + lane;
-    const int part = L >> 6, lrow = L & 63;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-
-    // This thread's items: float4 c of keys j0 + JS i (c and the key step are
-    // the same for every item), so each address below is a per-thread base
-    // plus a constant step in i, computed once.
-    constexpr int JS = BT / (D / 2);
-    const int j0 = item_j(tid), c0 = item_c(tid);
-    const size_t tok_stride = (size_t)H * (D / 2);  // float4 between consecutive tokens of the head
-    const float4* kbase = tok(k, 0) + (size_t)j0 * tok_stride + c0;
-    const float4* vbase = tok(v, 0) + (size_t)j0 * tok_stride + c0;
-    float4 kr[IT], vr[IT];
-    auto load_kv = [&](int kb) {
-#pragma unroll
-        for (int i = 0; i < IT; ++i) {
-            const int t = kb * BK + j0 + JS * i;
-            const size_t o = (size_t)(kb * BK + JS * i) * tok_stride;
-            kr[i] = t < T ? __ldg(kbase + o) : make_float4(0.f, 0.f, 0.f, 0.f);
-            vr[i] = t < T ? __ldg(vbase + o) : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-    };
-
-    const uint32_t ID_G = tc::idesc_tf32(128, BK), ID_V = tc::idesc_tf32(128, NB);
-    constexpr uint32_t Q_LBO = (3 * BQ / 8) * 128, K_LBO = (BK / 8) * 128, V_LBO = (NB / 8) * 128, SBO = 128;
-    const uint64_t a_hi = tc::make_desc(tc::smem_u32(sq) + 8 * SBO, Q_LBO, SBO);  // [Ar; Ai]
-    const uint64_t a_lo = tc::make_desc(tc::smem_u32(sq), Q_LBO, SBO);            // [-Ai; Ar]
-    bool ok = true;
-
-    // Key planes (rows j, K = a) and value operand (rows m, K = j) of the
-    // block held in registers, into buffer buf.  Rows 2c and 2c + 1 of the
-    // value operand: lanes with c & 4 write row 2c + 1 first, so each store
-    // covers all eight rows of a core matrix and the 32 lanes hit 32 distinct
-    // banks.
-    const bool sw = (c0 & 4) != 0;
-    const uint32_t k_off = kofs(j0, 2 * c0, BK);
-    const uint32_t v_off0 = kofs(2 * c0 + (sw ? 1 : 0), j0, NB), v_off1 = kofs(2 * c0 + (sw ? 0 : 1), j0, NB);
-    constexpr uint32_t K_ISTEP = (JS / 8) * 128;                // JS keys further: JS / 8 row groups
-    constexpr uint32_t V_ISTEP = (JS / 4) * (NB / 8) * 128;     // JS keys further: JS / 4 K groups
-    constexpr uint32_t V_IM = (D / 8) * 128;                    // rows D.. (imaginary parts)
-    static_assert(JS % 8 == 0, "key step keeps the row within its core matrix");
-    auto write_kv = [&](int buf) {
-        unsigned char* sk = skb(buf);
-        unsigned char* sv = svb(buf);
-#pragma unroll
-        for (int i = 0; i < IT; ++i) {
-            const uint32_t ko = k_off + K_ISTEP * i;
-            sts2(sk, ko, rna_tf32(kr[i].x), rna_tf32(kr[i].z));
-            sts2(sk + Cfg::KP_BYTES, ko, rna_tf32(kr[i].y), rna_tf32(kr[i].w));
-            const float r0 = rna_tf32(vr[i].x), r1 = rna_tf32(vr[i].z), m0 = rna_tf32(vr[i].y), m1 = rna_tf32(vr[i].w);
-            sts(sv, v_off0 + V_ISTEP * i, sw ? r1 : r0);
-            sts(sv, v_off1 + V_ISTEP * i, sw ? r0 : r1);
-            sts(sv, v_off0 + V_IM + V_ISTEP * i, sw ? m1 : m0);
-            sts(sv, v_off1 + V_IM + V_ISTEP * i, sw ? m0 : m1);
-        }
-        tc::fence_proxy_async();
-    };
-    // G of block kb (operands in buffer kb & 1) into the score columns.
-    auto issue_g = [&](int kb) {
-        const uint32_t kbase = tc::smem_u32(skb(kb & 1));
-        const uint64_t b_re = tc::make_desc(kbase, K_LBO, SBO);
-        const uint64_t b_im = tc::make_desc(kbase + Cfg::KP_BYTES, K_LBO, SBO);
-        const uint32_t d = tmem + Cfg::COL_G;
-        constexpr uint64_t A_STEP = (2 * Q_LBO) >> 4, B_STEP = (2 * K_LBO) >> 4;
-#pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks) tc::mma_tf32(d, a_hi + ks * A_STEP, b_re + ks * B_STEP, ID_G, ks > 0 ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < D / 8; ++ks) tc::mma_tf32(d, a_lo + ks * A_STEP, b_im + ks * B_STEP, ID_G, 1u);
-        tc::commit(&mbar[0]);
-    };
-
-    // Per key block kb: G (tensor cores) -> S = G o G in place (threads) ->
-    // ACC += S V (tensor cores), and while the ACC update runs the threads
-    // write block kb + 1's operands into the other buffer and fetch block
-    // kb + 2's rows.  mbar[0] completes once per G, mbar[2] once per ACC
-    // update, in block order, and every wait comes before the next commit to
-    // the same barrier.  Key blocks 0 .. last cover every key up to the query
-    // block's last position.
-    const int last = (i0 + BQ) / BK - 1;
-    load_kv(0);
-    write_kv(0);
-    if (last > 0) load_kv(1);
-    tc::fence_before_sync();
-    __syncthreads();
-    if (tid == 0) {
-        tc::fence_after_sync();
-        issue_g(0);
-    }
-#pragma unroll 1
-    for (int kb = 0; kb <= last; ++kb) {
-        const int buf = kb & 1;
-        ok = tc::mbar_wait_bounded(&mbar[0], (uint32_t)(kb & 1), kBornWait) && ok;
-        tc::fence_after_sync();
-        // S = G o G in place.
-        const int kq = i0 + lrow - kb * BK;  // last key of this block the row may see
-        const uint32_t gcol = tmem + lane_base + Cfg::COL_G;
-        uint32_t r[BK];
-#pragma unroll
-        for (int cb = 0; cb < BK / 16; ++cb) tc::tmem_ld16(gcol + 16 * cb, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * cb));
-        tc::tmem_wait_ld();
-        if (kb == last) {  // the diagonal block: keys after the query are masked
-#pragma unroll
-            for (int j = 0; j < BK; ++j) {
-                const float g = __uint_as_float(r[j]);
-                r[j] = __float_as_uint(j <= kq ? g * g : 0.f);
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < BK; ++j) {
-                const float g = __uint_as_float(r[j]);
-                r[j] = __float_as_uint(g * g);
-            }
-        }
-#pragma unroll
-        for (int cb = 0; cb < BK / 16; ++cb) tc::tmem_st16(gcol + 16 * cb, *reinterpret_cast<uint32_t(*)[16]>(r + 16 * cb));
-        tc::tmem_wait_st();
-        tc::fence_before_sync();
-        __syncthreads();
-        if (tid == 0) {
-            tc::fence_after_sync();
-            const uint64_t b_v = tc::make_desc(tc::smem_u32(svb(buf)), V_LBO, SBO);
-            constexpr uint64_t V_STEP = (2 * V_LBO) >> 4;
-#pragma unroll
-            for (int ks = 0; ks < BK / 8; ++ks)
-                tc::mma_tf32_ts(tmem + Cfg::COL_ACC, tmem + Cfg::COL_G + 8 * ks, b_v + ks * V_STEP, ID_V,
-                                (kb > 0 || ks > 0) ? 1u : 0u);
-            tc::commit(&mbar[2]);
-        }
-        if (kb < last) {
-            // The other buffer was last read by G and the ACC update of block
-            // kb - 1, both complete.
-            write_kv(buf ^ 1);
-            if (kb + 1 < last) load_kv(kb + 2);
-            // The score columns are free once this block's ACC update is done.
-            ok = tc::mbar_wait_bounded(&mbar[2], (uint32_t)(kb & 1), kBornWait) && ok;
-            tc::fence_before_sync();
-            __syncthreads();
-            if (tid == 0) {
-                tc::fence_after_sync();
-                issue_g(kb + 1);
-            }
-        }
-    }
-    ok = tc::mbar_wait_bounded(&mbar[2], (uint32_t)(last & 1), kBornWait) && ok;
-    tc::fence_after_sync();
-
-    // Epilogue: lanes 0-63 hold the Re^2-weighted sums, lanes 64-127 the
-    // Im^2-weighted ones; columns [0, D) real parts, [D, 2D) imaginary parts,
-    // 2D the score sum.  Part 0 stages its row, part 1 adds and divides.
-    float* stage = reinterpret_cast<float*>(smem) + lrow * Cfg::STAGE_LD;
-    uint32_t acc[(2 * D + 16) / 16 * 16];
-#pragma unroll
-    for (int cb = 0; cb < (2 * D + 16) / 16; ++cb) {
-        uint32_t r[16];
-        tc::tmem_ld16(tmem + lane_base + Cfg::COL_ACC + 16 * cb, r);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) acc[16 * cb + j] = r[j];
-    }
-    tc::tmem_wait_ld();
-    __syncthreads();  // every MMA has read the conj(Q) stack: the staging may overwrite it
-    if (part == 0) {
-#pragma unroll
-        for (int m = 0; m <= 2 * D; ++m) stage[m] = __uint_as_float(acc[m]);
-    }
-    __syncthreads();
-    if (part == 1 && i0 + lrow < T) {
-        const float den = stage[2 * D] + __uint_as_float(acc[2 * D]);
-        const float inv = den != 0.f ? 1.f / den : 0.f;
-        float2* out = psi + ((size_t)((size_t)b * T + i0 + lrow) * H + h) * D;
-#pragma unroll
-        for (int m = 0; m < D; ++m)
-            out[m] = make_float2((stage[m] + __uint_as_float(acc[m])) * inv,
-                                 (stage[D + m] + __uint_as_float(acc[D + m])) * inv);
-    }
-    if (!ok) s_gave_up = 1;  // a completion wait gave up
-    __syncthreads();
-    if (s_gave_up && tid == 0) {
-        if (status) atomicOr(status, kStatusBornMma);
-        tc::drain_mmas(&mbar[1], kBornWait);
-    }
-    tc::fence_before_sync();
-    __syncthreads();
-    if (warp == 0) tc::tmem_dealloc(tmem, Cfg::TMEM_COLS);
-}
-
-// ------------------------------------------------------------------ width 16, 128 queries per CTA
-// born_kernel_w16: the same computation for head width 16 with 128 queries
-// per CTA, one per tensor-memory lane, and the real and imaginary scores in
-// two accumulators instead of two lane halves:
-//   Re G = [Qr | Qi] [Kr | Ki]^T            (K = 32)
-//   Im G = Qr Ki^T - Qi Kr^T                (two K = 16 halves of the same
+// ------------------------------------------------------------------ 128 queries per CTA
+// born_kernel_q128<D>: 128 queries per CTA, one per tensor-memory lane, the
+// real and imaginary scores in two accumulators:
+//   Re G = [Qr | Qi] [Kr | Ki]^T            (K = 2D)
+//   Im G = Qr Ki^T - Qi Kr^T                (the two K = D halves of the same
 //                                            operands, the second negated)
 //   S = (Re G)^2 + (Im G)^2                  over Re G in tensor memory
 //   ACC += S [Vr; Vi; 1]^T                   (A = S from tensor memory)
 // so each lane ends with its query's numerator and score sum.  256 threads
-// (two per lane, one column half each), 56 KB of shared memory and 256
-// tensor-memory columns: two CTAs per SM, each with twice the queries of
-// the 64-query CTA.
-namespace bw {
-constexpr int D = 16;
-constexpr int BQ = 128;                    // queries per CTA
-constexpr int NT = 256;                    // threads
-constexpr int BK = 64;                     // keys per block
-constexpr int K2 = 2 * D;                  // K of the score GEMM
-constexpr int NB = 2 * D + 16;             // value operand rows: Vr, Vi, ones, zeros
-constexpr int Q_BYTES = BQ * K2 * 4;       // rows q, K = [qr | qi]
-constexpr int K_BYTES = BK * K2 * 4;       // rows j, K = [kr | ki]
-constexpr int V_BYTES = NB * BK * 4;       // rows m, K = j
-constexpr int KV_BYTES = K_BYTES + V_BYTES;
-constexpr int SMEM = Q_BYTES + 2 * KV_BYTES;  // two key blocks in flight
-constexpr int ITEMS = BK * D / 2 / NT;     // float4 of keys (and of values) per thread per key block
-constexpr uint32_t COL_RE = 0, COL_IM = BK, COL_ACC = 2 * BK, TMEM_COLS = 256;  // S over Re G
-constexpr uint32_t Q_LBO = (BQ / 8) * 128, K_LBO = (BK / 8) * 128, V_LBO = (NB / 8) * 128, SBO = 128;
+// (two per lane, one column half each) and 256 tensor-memory columns; 56 KB
+// of shared memory at width 16, 104 KB at 32: two CTAs per SM.
+template <int D>
+struct BornQ {
+static constexpr int BQ = 128;                    // queries per CTA
+static constexpr int NT = 256;                    // threads
+static constexpr int BK = 64;                     // keys per block
+static constexpr int K2 = 2 * D;                  // K of the score GEMM
+static constexpr int NB = 2 * D + 16;             // value operand rows: Vr, Vi, ones, zeros
+static constexpr int Q_BYTES = BQ * K2 * 4;       // rows q, K = [qr | qi]
+static constexpr int K_BYTES = BK * K2 * 4;       // rows j, K = [kr | ki]
+static constexpr int V_BYTES = NB * BK * 4;       // rows m, K = j
+static constexpr int KV_BYTES = K_BYTES + V_BYTES;
+static constexpr int SMEM = Q_BYTES + 2 * KV_BYTES;  // two key blocks in flight
+static constexpr int ITEMS = BK * D / 2 / NT;     // float4 of keys (and of values) per thread per key block
+static constexpr uint32_t COL_RE = 0, COL_IM = BK, COL_ACC = 2 * BK, TMEM_COLS = 256;  // S over Re G
+static constexpr uint32_t Q_LBO = (BQ / 8) * 128, K_LBO = (BK / 8) * 128, V_LBO = (NB / 8) * 128, SBO = 128;
+static constexpr int KSTEPS = K2 / 8;             // MMAs of K = 8 over [Re | Im]
+static constexpr int NACC = (NB + 15) / 16 * 16;  // accumulator columns read back
 static_assert(COL_ACC + NB <= TMEM_COLS && ITEMS * NT * 2 == BK * D, "budget and item mapping");
-}  // namespace bw
+static_assert(2 * (SMEM + 2048) <= 227 * 1024, "two CTAs per SM");
+};
 
-__global__ void __launch_bounds__(bw::NT, 2) born_kernel_w16(const float4* __restrict__ q, const float4* __restrict__ k,
-                                                            const float4* __restrict__ v, float2* __restrict__ psi,
-                                                            int T, int H, int nqb, unsigned* status) {
-    constexpr int D = bw::D, BQ2 = bw::BQ, BK = bw::BK, NB = bw::NB, IT = bw::ITEMS;
+template <int D>
+__global__ void __launch_bounds__(256, 2) born_kernel_q128(const float4* __restrict__ q, const float4* __restrict__ k,
+                                                          const float4* __restrict__ v, float2* __restrict__ psi,
+                                                          int T, int H, int nqb, unsigned* status) {
+    using bw = BornQ<D>;
+    constexpr int BQ2 = bw::BQ, BK = bw::BK, NB = bw::NB, IT = bw::ITEMS;
     extern __shared__ __align__(1024) unsigned char smem[];
     __shared__ __align__(8) uint64_t mbar[3];  // G done, drain, ACC update done
     __shared__ int s_gave_up;
@@ -438,18 +165,20 @@ __global__ void __launch_bounds__(bw::NT, 2) born_kernel_w16(const float4* __res
     constexpr uint64_t Q_STEP = (2 * bw::Q_LBO) >> 4, K_STEP = (2 * bw::K_LBO) >> 4, V_STEP = (2 * bw::V_LBO) >> 4;
     const uint64_t a_q = tc::make_desc(tc::smem_u32(sq), bw::Q_LBO, bw::SBO);
     // Re G and Im G of block kb (operands in buffer kb & 1).  One MMA takes
-    // K = 8: steps 0-1 cover the real parts (K 0-15), 2-3 the imaginary ones.
+    // K = 8: the first half of the steps covers the real parts, the second
+    // the imaginary ones.
     auto issue_g = [&](int kb) {
         const uint64_t b_k = tc::make_desc(tc::smem_u32(skb(kb & 1)), bw::K_LBO, bw::SBO);
+        constexpr int HS = bw::KSTEPS / 2;  // steps over one half (the real or the imaginary parts)
 #pragma unroll
-        for (int ks = 0; ks < 4; ++ks)
+        for (int ks = 0; ks < bw::KSTEPS; ++ks)
             tc::mma_tf32(tmem + bw::COL_RE, a_q + ks * Q_STEP, b_k + ks * K_STEP, ID_G, ks > 0 ? 1u : 0u);
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks)  // Qr Ki^T
-            tc::mma_tf32(tmem + bw::COL_IM, a_q + ks * Q_STEP, b_k + (2 + ks) * K_STEP, ID_G, ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < HS; ++ks)  // Qr Ki^T
+            tc::mma_tf32(tmem + bw::COL_IM, a_q + ks * Q_STEP, b_k + (HS + ks) * K_STEP, ID_G, ks > 0 ? 1u : 0u);
 #pragma unroll
-        for (int ks = 0; ks < 2; ++ks)  // - Qi Kr^T
-            tc::mma_tf32(tmem + bw::COL_IM, a_q + (2 + ks) * Q_STEP, b_k + ks * K_STEP, ID_GN, 1u);
+        for (int ks = 0; ks < HS; ++ks)  // - Qi Kr^T
+            tc::mma_tf32(tmem + bw::COL_IM, a_q + (HS + ks) * Q_STEP, b_k + ks * K_STEP, ID_GN, 1u);
         tc::commit(&mbar[0]);
     };
 
@@ -526,12 +255,12 @@ __global__ void __launch_bounds__(bw::NT, 2) born_kernel_w16(const float4* __res
     ok = tc::mbar_wait_bounded(&mbar[2], (uint32_t)(last & 1), kBornWait) && ok;
     tc::fence_after_sync();
 
-    // Epilogue: lane L holds its query's numerator (columns 0-15 real, 16-31
-    // imaginary parts) and score sum (column 32).
-    uint32_t acc[48];
+    // Epilogue: lane L holds its query's numerator (columns 0 to D-1 real,
+    // D to 2D-1 imaginary parts) and score sum (column 2D).
+    uint32_t acc[bw::NACC];
     if (ch == 0) {  // warp-uniform: the tensor-memory loads are collective over the warp
 #pragma unroll
-        for (int cb = 0; cb < 3; ++cb)
+        for (int cb = 0; cb < bw::NACC / 16; ++cb)
             tc::tmem_ld16(tmem + lane_base + bw::COL_ACC + 16 * cb, *reinterpret_cast<uint32_t(*)[16]>(acc + 16 * cb));
         tc::tmem_wait_ld();
     }
@@ -556,41 +285,23 @@ __global__ void __launch_bounds__(bw::NT, 2) born_kernel_w16(const float4* __res
     if (warp == 0) tc::tmem_dealloc(tmem, bw::TMEM_COLS);
 }
 
-static cudaError_t launch_born_w16(const BornArgs& a, cudaStream_t st) {
+template <int D>
+static cudaError_t launch_born_q128(const BornArgs& a, cudaStream_t st) {
+    using bw = BornQ<D>;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
     static std::atomic<bool> attr_set[128];
     if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
     if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        e = cudaFuncSetAttribute(born_kernel_w16, cudaFuncAttributeMaxDynamicSharedMemorySize, bw::SMEM);
+        e = cudaFuncSetAttribute(born_kernel_q128<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, bw::SMEM);
         if (e != cudaSuccess) return e;
         attr_set[dev].store(true, std::memory_order_relaxed);
     }
     const int64_t BH = a.Bz * a.H, nqb = (a.T + bw::BQ - 1) / bw::BQ;
-    born_kernel_w16<<<(unsigned)(BH * nqb), bw::NT, bw::SMEM, st>>>(
+    born_kernel_q128<D><<<(unsigned)(BH * nqb), bw::NT, bw::SMEM, st>>>(
         reinterpret_cast<const float4*>(a.q), reinterpret_cast<const float4*>(a.k), reinterpret_cast<const float4*>(a.v),
         a.psi, (int)a.T, (int)a.H, (int)nqb, status_word());
-    return cudaGetLastError();
-}
-
-template <int D>
-cudaError_t launch_born_d(const BornArgs& a, cudaStream_t st) {
-    using Cfg = BornCfg<D>;
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return e;
-    static std::atomic<bool> attr_set[128];  // per device; setting the attribute twice is harmless
-    if (dev < 0 || dev >= 128) return cudaErrorInvalidDevice;
-    if (!attr_set[dev].load(std::memory_order_relaxed)) {
-        e = cudaFuncSetAttribute(born_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::SMEM);
-        if (e != cudaSuccess) return e;
-        attr_set[dev].store(true, std::memory_order_relaxed);
-    }
-    const int64_t BH = a.Bz * a.H, nqb = (a.T + BQ - 1) / BQ;
-    born_kernel<D><<<(unsigned)(BH * nqb), BT, Cfg::SMEM, st>>>(
-        reinterpret_cast<const float4*>(a.q), reinterpret_cast<const float4*>(a.k), reinterpret_cast<const float4*>(a.v),
-        a.psi, (int)a.T, (int)a.H, (int)BH, (int)nqb, status_word());
     return cudaGetLastError();
 }
 
@@ -599,7 +310,7 @@ cudaError_t launch_born_d(const BornArgs& a, cudaStream_t st) {
 bool born_supported(int64_t D) { return D == 16 || D == 32; }
 
 cudaError_t launch_born(const BornArgs& a, cudaStream_t st) {
-    return a.D == 16 ? launch_born_w16(a, st) : launch_born_d<32>(a, st);
+    return a.D == 16 ? launch_born_q128<16>(a, st) : launch_born_q128<32>(a, st);
 }
 
 }  // namespace cssd
