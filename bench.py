@@ -652,9 +652,9 @@ def bench_born(args, dev):
     """Causal Born attention at the H-Transformer shapes (batch 256, T 1024,
     16 heads of width 16).  Tensor-bound: the roofline counts the algorithmic
     flops of the causal pairs (<q|k>, its squared modulus, s v and the score
-    sum); the MMA flops the kernel executes (128-query blocks against 64-key
-    blocks up to the diagonal: Re G and Im G 128x64x32 each, the value GEMM
-    128x(2D+16)x64) are reported beside them."""
+    sum); the MMA flops the kernel executes (128-query blocks against 32-key
+    blocks up to the diagonal: Re G and Im G together 128x64x(2D), the value
+    GEMM 128x(2D+16)x32 with its row of ones) are reported beside them."""
     import torch
 
     from complex_valued_state_gb300 import cssd
@@ -678,16 +678,16 @@ def bench_born(args, dev):
     e1.record(stream)
     torch.cuda.synchronize(dev)
     ms = e0.elapsed_time(e1) / n
-    nqb, nkb = (T + 127) // 128, (T + 63) // 64
-    blocks = Bz * H * sum(min(2 * (qb + 1), nkb) for qb in range(nqb))  # (128 queries, 64 keys) pairs visited
-    executed = blocks * (2 * 2 * 128 * 64 * (2 * D) + 2 * 128 * (2 * D + 16) * 64)
+    nqb, nkb = (T + 127) // 128, (T + 31) // 32
+    blocks = Bz * H * sum(min(4 * (qb + 1), nkb) for qb in range(nqb))  # (128 queries, 32 keys) pairs visited
+    executed = blocks * (2 * 128 * 64 * (2 * D) + 2 * 128 * (2 * D + 16) * 32)
     pairs = Bz * H * T * (T + 1) // 2
     minimal = pairs * (8 * D + 3 + 4 * D + 1)  # <q|k>, |.|^2, s v and the score sum
     peak, kind = tf32_peak()
     tf = minimal / (ms / 1e3) / 1e12
     return {"workload": f"htransformer_attn Bz{Bz} T{T} H{H} D{D}", "ms_per_call": round(ms, 4), "calls": n,
             "value": round(Bz * T * H / (ms / 1e3), 1), "unit": "token-heads/s",
-            "roofline": {"bound": "tensor", "kernel": "born_kernel_q128<16>", "achieved": round(tf, 1),
+            "roofline": {"bound": "tensor", "kernel": "born_kernel_ws<16>", "achieved": round(tf, 1),
                          "peak": round(peak, 1), "unit": "TFLOP/s", "frac": round(tf / peak, 4), "peak_kind": kind,
                          "flops_per_launch": minimal, "flops": "algorithmic: the causal pairs",
                          "executed_flops_per_launch": executed,

@@ -372,8 +372,9 @@ int cssd_chunked_backward(const cssd_dims* dims, const void* x, const float* dt,
  *   q, k, v  complex64 [batch, seqlen, nheads, D]  queries, keys, values
  *            (any phase rotation of q and k is applied by the caller)
  *   psi      complex64 [batch, seqlen, nheads, D]  output (written)
- * Scores and values enter the tensor cores as TF32 (round to nearest),
- * accumulation is fp32.  All four pointers are device pointers, 16-byte
+ * Queries, keys and values enter the tensor cores rounded to TF32 (round to
+ * nearest); the squared scores are read by the tensor cores at TF32 precision
+ * for the numerator and the score sum alike; accumulation is fp32.  All four pointers are device pointers, 16-byte
  * aligned.  Other D return CSSD_ERR_UNSUPPORTED.  Returns a cssd_status. */
 int cssd_born_attention(const cssd_dims* dims, const void* q, const void* k, const void* v, void* psi,
                         cssd_stream_t stream);
