@@ -37,8 +37,9 @@ __device__ __forceinline__ void sts(unsigned char* base, uint32_t off, float v) 
 
 // ------------------------------------------------------------------ the kernel
 // born_kernel_ws<D>: 128 queries per CTA, blocks of 32 keys.  Eight math
-// warps (two per lane quarter, one half of the key block each) and one warp
-// that runs the MMA loop, one elected lane issuing:
+// warps (two per lane quarter, one half of the key block each), one warp
+// that runs the MMA loop (one elected lane issuing) and, at width 16, four
+// loader warps:
 //   G  = Q [K; K']^T          A = Q from tensor memory (the query rows as
 //                             stored: re, im interleaved), B = the key block
 //                             as stored and as (im, -re), so that columns
@@ -53,17 +54,26 @@ __device__ __forceinline__ void sts(unsigned char* base, uint32_t off, float v) 
 // The score accumulator is double-buffered: the MMA warp queues G of block
 // kb + 2 as soon as the value GEMM of block kb has read its scores, so the
 // tensor core works on one block while the math warps square the next.  Key
-// and value blocks go through shared-memory slots written by the math warps
-// two blocks ahead, from registers loaded two blocks before that.
+// and value blocks go through shared-memory operand slots.  At width 16 the
+// loader warps fill them: raw rows by cp.async six blocks ahead, rounded and
+// stored by the thread that copied them.  At width 32 the math warps fill
+// them two blocks ahead, from registers loaded two blocks before that.
 template <int D>
 struct BornW {
     static constexpr int BQ = 128;         // queries per CTA
     static constexpr int NMATH = 256;      // math threads: two per tensor-memory lane
-    static constexpr int NT = NMATH + 32;  // and the MMA warp
+    // Width 16: four loader warps stage the key/value blocks.  Width 32: the
+    // math warps do (its raw blocks are twice the size, and a ring deep
+    // enough for the loaders does not fit beside the operand slots).
+    static constexpr bool LOADERS = D == 16;
+    static constexpr int NLOAD = LOADERS ? 128 : 0;
+    static constexpr int NT = NMATH + 32 + NLOAD;  // math warps 0-7, the MMA warp 8, loader warps 9-12
     static constexpr int BK = 32;          // keys per block
     static constexpr int K2 = 2 * D;       // K of the score GEMM
-    static constexpr int NR = D == 16 ? 4 : 3;  // key/value slots
-    static constexpr int IT = D / 16;      // float4 of keys (and of values) per math thread per block
+    static constexpr int NR = D == 16 ? 4 : 3;     // operand slots
+    static constexpr int NRAW = LOADERS ? 6 : 0;   // raw key/value slots: blocks in flight from global memory
+    static constexpr int IT = D / 16;      // float4 of keys (and of values) per math thread per block (math staging)
+    static constexpr int LIT = LOADERS ? BK * D / 2 / NLOAD : 0;  // the same per loader thread
     // [K; K'] operand: 2 BK rows, K2 columns.  The k-group stride is one row
     // group set plus 16 bytes, so the eight lanes that store one key row's
     // eight 16-byte groups hit eight different bank groups.
@@ -79,15 +89,20 @@ struct BornW {
     static constexpr uint32_t V_SBO = 144, V_LBO = (NB / 8) * V_SBO;
     static constexpr uint32_t V_BYTES = (BK / 4) * V_LBO;
     static constexpr uint32_t SLOT = K_BYTES + V_BYTES;
-    // 80 KB requested so that no third CTA shares an SM (its tensor-memory
+    // Raw slot (loader staging): the block's key rows then its value rows as stored.
+    static constexpr uint32_t RAW_HALF = BK * (D / 2) * 16, RAW = 2 * RAW_HALF;
+    static constexpr uint32_t RAW0 = NR * SLOT;
+    // At least 80 KB, so that no third CTA shares an SM (its tensor-memory
     // allocation would have to wait for one of the other two to finish).
-    static constexpr uint32_t SMEM = 80 * 1024;
+    static constexpr uint32_t SMEM_NEED = (RAW0 + NRAW * RAW + 1023) / 1024 * 1024;
+    static constexpr uint32_t SMEM = SMEM_NEED > 80 * 1024 ? SMEM_NEED : 80 * 1024;
     // Tensor memory: G buffers at 0 and 64 (Re then Im, S over Re), ACC at
     // 128, Q in the last K2 columns.
     static constexpr uint32_t COL_G = 0, COL_ACC = 128, TMEM_COLS = 256, COL_Q = TMEM_COLS - K2;
-    static_assert(NR * SLOT <= SMEM && 2 * (SMEM + 2048) <= 227 * 1024 && 3 * (SMEM + 1024) > 228 * 1024, "two CTAs per SM");
+    static_assert(2 * (SMEM + 2048) <= 227 * 1024 && 3 * (SMEM + 1024) > 228 * 1024, "two CTAs per SM");
     static_assert(COL_ACC + NB <= COL_Q && V_LBO >= (NB / 8 - 1) * V_SBO + 128 && SLOT % 16 == 0, "layout");
-    static_assert(NMATH == 8 * BK && (D == 16 || D == 32), "item mapping: eight threads per key row");
+    static_assert(NMATH == 8 * BK && (D == 16 || D == 32) && (!LOADERS || LIT * NLOAD * 2 == BK * D),
+                  "item mappings: eight threads per key row");
 };
 
 // Wait for a phase parity with the thread suspended (not spinning) until the
@@ -133,16 +148,27 @@ __device__ __forceinline__ void sts4(unsigned char* base, uint32_t off, float a,
     *reinterpret_cast<float4*>(base + off) = make_float4(a, b, c, d);
 }
 
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory"); }
+__device__ __forceinline__ float4 lds4(const unsigned char* base, uint32_t off) {
+    return *reinterpret_cast<const float4*>(base + off);
+}
+
 template <int D>
 __global__ void __launch_bounds__(BornW<D>::NT, 2) born_kernel_ws(const float4* __restrict__ q, const float4* __restrict__ k,
                                                                  const float4* __restrict__ v, float2* __restrict__ psi,
                                                                  int T, int H, int nqb, unsigned* status) {
     using bw = BornW<D>;
-    constexpr int BK = bw::BK, NR = bw::NR, IT = bw::IT;
+    constexpr int BK = bw::BK, NR = bw::NR, IT = bw::IT, NRAW = bw::NRAW;
     extern __shared__ __align__(1024) unsigned char smem[];
     // G complete (per buffer), S stored (per buffer, one arrival per math
-    // warp), slot written (one arrival per math warp), slot read (the value
-    // GEMM of the slot's block, and everything before it, complete), drain.
+    // warp), operand slot written (one arrival per staging warp), operand
+    // slot read (the value GEMM of the slot's block, and everything before
+    // it, complete), drain.
     __shared__ __align__(8) uint64_t mb_g[2], mb_s[2], mb_kv[NR], mb_free[NR], mb_drain;
     __shared__ float s_den[2][bw::BQ];
     __shared__ int s_gave_up;
@@ -169,7 +195,7 @@ __global__ void __launch_bounds__(BornW<D>::NT, 2) born_kernel_ws(const float4* 
             tc::mbar_init(&mb_s[i], 8);
         }
         for (int i = 0; i < NR; ++i) {
-            tc::mbar_init(&mb_kv[i], 8);
+            tc::mbar_init(&mb_kv[i], bw::LOADERS ? bw::NLOAD / 32 : 8);
             tc::mbar_init(&mb_free[i], 1);
         }
         tc::mbar_init(&mb_drain, 1);
@@ -212,8 +238,8 @@ __global__ void __launch_bounds__(BornW<D>::NT, 2) born_kernel_ws(const float4* 
                               *reinterpret_cast<const uint32_t(*)[16]>(qv + 16 * cb));
             tc::tmem_wait_st();
         }
-        // Keys and values: thread tid reads float4 (tid mod 8) + 8 i of key
-        // tid / 8 of each block, so eight lanes read one 128-byte row piece.
+        // Math staging (width 32): thread tid reads float4 (tid mod 8) + 8 i of
+        // key tid / 8 of each block, so eight lanes read one 128-byte row piece.
         const int j = tid >> 3, c0 = tid & 7;
         const float4* kbase = k + head0 + (size_t)j * tok_stride + c0;
         const float4* vbase = v + head0 + (size_t)j * tok_stride + c0;
@@ -250,14 +276,16 @@ __global__ void __launch_bounds__(BornW<D>::NT, 2) born_kernel_ws(const float4* 
             if (lane == 0) mbar_arrive1(&mb_kv[kb % NR]);
         };
         float4 ka[IT], va[IT], kb2[IT], vb2[IT];
-        load(0, ka, va);
-        write(0, ka, va);
-        if (last >= 1) {
-            load(1, ka, va);
-            write(1, ka, va);
+        if constexpr (!bw::LOADERS) {
+            load(0, ka, va);
+            write(0, ka, va);
+            if (last >= 1) {
+                load(1, ka, va);
+                write(1, ka, va);
+            }
+            if (last >= 2) load(2, ka, va);
+            if (last >= 3) load(3, kb2, vb2);
         }
-        if (last >= 2) load(2, ka, va);
-        if (last >= 3) load(3, kb2, vb2);
         tc::fence_before_sync();
         __syncthreads();  // Q stored
 
@@ -302,7 +330,7 @@ __global__ void __launch_bounds__(BornW<D>::NT, 2) born_kernel_ws(const float4* 
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive1(&mb_s[g]);
-            if (kb + 2 <= last) {
+            if (!bw::LOADERS && kb + 2 <= last) {
                 // Block kb + 2 goes into the slot of block kb + 2 - NR.  With
                 // four slots that is block kb - 2, free already: G of block
                 // kb, complete, was issued after the value GEMM of block kb - 2
@@ -346,6 +374,64 @@ __global__ void __launch_bounds__(BornW<D>::NT, 2) born_kernel_ws(const float4* 
             for (int m = 0; m < D / 4; ++m)
                 out[m] = make_float4(__uint_as_float(acc[4 * m]) * inv, __uint_as_float(acc[4 * m + 1]) * inv,
                                      __uint_as_float(acc[4 * m + 2]) * inv, __uint_as_float(acc[4 * m + 3]) * inv);
+        }
+    } else if (warp >= 9) {
+        if constexpr (bw::LOADERS) {
+            // Loader warps: raw key and value rows by cp.async NRAW blocks ahead
+            // into the raw slots; each thread then rounds exactly the pieces it
+            // copied to TF32 and stores them into the block's operand slot.
+            // Item n = lt + NLOAD i is float4 c = n mod (D/2) of key n / (D/2),
+            // so eight lanes read one 128-byte row piece.
+            const int lt = tid - (bw::NMATH + 32);
+            const uint32_t s0 = tc::smem_u32(smem);
+            auto copy_block = [&](int kb) {
+                if (kb <= last) {
+                    const uint32_t rs = s0 + bw::RAW0 + (kb % NRAW) * bw::RAW;
+#pragma unroll
+                    for (int i = 0; i < bw::LIT; ++i) {
+                        const int n = lt + bw::NLOAD * i, j = n / (D / 2), c = n % (D / 2);
+                        const bool in = kb * BK + j < T;
+                        // past the end: read nothing (the head's first token as the address), write zeros
+                        const size_t o = in ? (size_t)(kb * BK + j) * tok_stride + c : (size_t)c;
+                        cp_async16(rs + n * 16, k + head0 + o, in ? 16u : 0u);
+                        cp_async16(rs + bw::RAW_HALF + n * 16, v + head0 + o, in ? 16u : 0u);
+                    }
+                }
+                cp_async_commit();  // one group per block, empty past the last
+            };
+            for (int kb = 0; kb < NRAW; ++kb) copy_block(kb);
+            __syncthreads();  // Q and the constant rows stored (the math warps' barrier)
+#pragma unroll 1
+            for (int kb = 0; kb <= last; ++kb) {
+                cp_async_wait<NRAW - 1>();  // this thread's copies of block kb have landed
+                // Operand slot kb mod NR last held block kb - NR: its value GEMM must be done.
+                if (kb >= NR)
+                    ok = mbar_wait_sleep(&mb_free[(kb - NR) % NR], (uint32_t)(((kb - NR) / NR) & 1), kBornWait) && ok;
+                const unsigned char* rs = smem + bw::RAW0 + (kb % NRAW) * bw::RAW;
+                unsigned char* sk = smem + (kb % NR) * bw::SLOT;
+                unsigned char* sv = sk + bw::K_BYTES;
+#pragma unroll
+                for (int i = 0; i < bw::LIT; ++i) {
+                    const int n = lt + bw::NLOAD * i, j = n / (D / 2), c = n % (D / 2);
+                    const float4 kr = lds4(rs, n * 16), vr = lds4(rs + bw::RAW_HALF, n * 16);
+                    const float kx = rna_tf32(kr.x), ky = rna_tf32(kr.y), kz = rna_tf32(kr.z), kw = rna_tf32(kr.w);
+                    const uint32_t ko = c * bw::K_LBO + (j & 7) * 16;
+                    sts4(sk, ko + (j >> 3) * bw::K_SBO, kx, ky, kz, kw);            // row j: (re, im, re, im)
+                    sts4(sk, ko + ((BK + j) >> 3) * bw::K_SBO, ky, -kx, kw, -kz);  // row BK + j: (im, -re, ...)
+                    const uint32_t vo = (j >> 2) * bw::V_LBO + (j & 3) * 4;
+                    const float vv[4] = {vr.x, vr.y, vr.z, vr.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int m = 4 * c + e;
+                        sts(sv, vo + (m >> 3) * bw::V_SBO + (m & 7) * 16, rna_tf32(vv[e]));
+                    }
+                }
+                tc::fence_proxy_async();
+                __syncwarp();
+                if (lane == 0) mbar_arrive1(&mb_kv[kb % NR]);
+                copy_block(kb + NRAW);  // into the raw slot just read (its values are in registers already)
+            }
+            cp_async_wait<0>();
         }
     } else {
         __syncthreads();  // Q stored
