@@ -738,7 +738,7 @@ def bench_backward(args, dev):
     gbs = alg / (ms / 1e3) / 1e9
     return {"workload": f"mamba2_layer backward Bz{w.batch} T{w.seqlen} H{w.nheads} N{N} P{P} chunk{w.chunk}",
             "ms_per_call": round(ms, 4), "calls": n, "value": round(w.units / (ms / 1e3), 1), "unit": "token-heads/s",
-            "roofline": {"bound": "hbm", "kernel": "whole backward (16 launches)", "achieved": round(gbs, 1),
+            "roofline": {"bound": "hbm", "kernel": "whole backward (12 launches)", "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
                          "alg_bytes_per_call": alg},
             "workspace_bytes": int(ws.numel())}
