@@ -142,8 +142,7 @@ int cssd_forward_launches(const cssd_dims* dims, int chunk);
  *   - Sizes whose workspace (cssd_workspace_bytes) exceeds 16 MiB return
  *     CSSD_ERR_WORKSPACE without launching.
  *   - The first call on a device looks up the array's device address (with
- *     that device current) and caches it; make that first call before any
- *     stream capture.
+ *     that device current) and caches it.
  *   - All calls share the array and it keeps the last call's contents; the
  *     kernels clear what must start at zero on every call, but calls whose
  *     executions overlap on the GPU race on it and must be serialised. */
