@@ -52,6 +52,7 @@ def parse():
     ap.add_argument("--no-precise", action="store_true", help="skip the split-precision forward measurement")
     ap.add_argument("--no-tf32", action="store_true", help="skip the TF32-operand forward measurement")
     ap.add_argument("--no-small", action="store_true", help="skip the dstate = headdim = 32 forward measurement")
+    ap.add_argument("--no-pam", action="store_true", help="skip the PAM-workload forward measurement")
     ap.add_argument("--long-seqlen", type=int, default=0,
                     help="tokens of the long_seq forward (default: the workload's 65536; smaller for profiling)")
     return ap.parse_args()
@@ -364,6 +365,7 @@ def run_ours(args, rank, world, local):
     precise = None if args.no_precise else bench_precise(args, dev)
     tf32 = None if args.no_tf32 else bench_tf32(args, dev)
     small = None if args.no_small else bench_small(args, dev)
+    pam = None if args.no_pam else bench_pam(args, dev)
     long_seq = None
     if not args.no_long:
         long_seq = bench_long_seq(args, dev)
@@ -417,6 +419,8 @@ def run_ours(args, rank, world, local):
         out["tf32_forward"] = tf32
     if small:
         out["small_widths"] = small
+    if pam:
+        out["pam_forward"] = pam
     if long_seq:
         out["long_seq"] = long_seq
     if world == 1 and not args.no_cpu_baseline:
@@ -835,12 +839,35 @@ def bench_small(args, dev):
     """dstate = headdim = 32 at the mamba2_layer's batch, length and heads: the
     half-operand chunk kernel on tiles padded to 64 (the tensor-core path of the
     widths below 64)."""
+    from complex_valued_state_gb300 import workloads as wl
+
+    w = wl.MAMBA2_LAYER.with_(dstate=32, headdim=32)
+    return bench_forward_shape(
+        dev, w, f"mamba2_layer batch, length and heads at Bz{w.batch} T{w.seqlen} H{w.nheads} N{w.dstate} P{w.headdim} "
+        f"chunk{w.chunk}", "fused_chunk_kernel_h16 on tiles padded to 64", "fused_chunk_kernel_h16 (padded)")
+
+
+def bench_pam(args, dev):
+    """The PAM workload (Bz 8, T 1024, H 12, N = P = 64; queries, keys and values
+    mapped onto C, B and x, decay from the retention rates): the default
+    forward, the half-operand chunk kernel."""
+    from complex_valued_state_gb300 import workloads as wl
+
+    w = wl.PAM
+    return bench_forward_shape(
+        dev, w, f"pam Bz{w.batch} T{w.seqlen} H{w.nheads} N{w.dstate} P{w.headdim} chunk{w.chunk}",
+        "fused_chunk_kernel_h16", "fused_chunk_kernel_h16")
+
+
+def bench_forward_shape(dev, w, workload, kernel, roof_kernel):
+    """cssd_chunked_forward on one workload's inputs: whole-call time and the
+    chunk kernel's own time (the library's event hook), HBM roofline on the
+    algorithmic bytes (x, B, C, dt in; y out)."""
     import torch
 
     from complex_valued_state_gb300 import cssd
     from complex_valued_state_gb300 import workloads as wl
 
-    w = wl.MAMBA2_LAYER.with_(dstate=32, headdim=32)
     host = wl.make_inputs(w)
     g = {k: torch.from_numpy(host[k]).to(dev) for k in ("x", "dt", "A", "B", "C", "D")}
     del host
@@ -876,10 +903,10 @@ def bench_small(args, dev):
     alg = units * (8 * P + 16 * N + 4 + 8 * P)
     hbm, kind = peaks()
     gbs = alg / (k_ms / 1e3) / 1e9
-    return {"workload": f"mamba2_layer batch, length and heads at Bz{Bz} T{T} H{H} N{N} P{P} chunk{ch}",
+    return {"workload": workload,
             "value": round(units / (ms / 1e3), 1), "unit": UNIT, "ms_per_call": round(ms, 4), "calls": n,
-            "kernel": "fused_chunk_kernel_h16 on tiles padded to 64",
-            "roofline": {"bound": "hbm", "kernel": "fused_chunk_kernel_h16 (padded)", "achieved": round(gbs, 1),
+            "kernel": kernel,
+            "roofline": {"bound": "hbm", "kernel": roof_kernel, "achieved": round(gbs, 1),
                          "peak": hbm, "unit": "GB/s", "frac": round(gbs / hbm, 4), "peak_kind": kind,
                          "kernel_ms": round(k_ms, 4), "alg_bytes_per_launch": alg},
             "tensor": fused_tensor(units, 64, k_ms, operand="f16")}
