@@ -916,8 +916,8 @@ __global__ void __launch_bounds__(h16::NT, SPLIT ? 1 : 3) fused_chunk_kernel_h16
         tc::tmem_alloc(&s_tmem, TMEM_COLS);
         tc::tmem_relinquish();
     }
+    if (tid == 32) s_ticket = atomicAdd(p.ticket, 1);  // its round trip overlaps the allocation
     if (tid == 0) {
-        s_ticket = atomicAdd(p.ticket, 1);
         s_bad = 0;
         for (int i = 0; i < NBAR; ++i) tc::mbar_init(&mbar[i], 1);
         tc::mbar_fence_init();
@@ -1390,18 +1390,24 @@ __global__ void __launch_bounds__(h16::NT, SPLIT ? 1 : 3) fused_chunk_kernel_h16
     // The skip term uses the exact fp32 input (an L2 hit, fetched while Y_off
     // runs).  The staging planes lie over the X^T stack and the Ct stack,
     // which Y_diag and Y_off have finished reading.
-    constexpr int YI = CH * PD / NT;  // output elements per thread: rows ly + 4 k, column py
-    const int ly = tid >> 6, py = tid & 63;
-    const bool pok = py < Pd;
-    const long long ystep = 4 * H * Pd;
-    const long long yoff = (row0 + (long long)ly * H) * Pd + py;
-    float2 xs[YI];
+    // Output pairs per thread: rows ly + 8 k, columns 2 pp and 2 pp + 1 (the
+    // widths are even, so a pair is wholly inside or outside), one 16-byte
+    // access each.
+    constexpr int YI = CH * PD / 2 / NT;
+    const int ly = tid >> 5, pp = tid & 31;
+    const bool pok = 2 * pp < Pd;
+    const long long ystep = 8 * H * Pd;
+    const long long yoff = (row0 + (long long)ly * H) * Pd + 2 * pp;
+    float4 xs[YI];
 #pragma unroll
     for (int k = 0; k < YI; ++k) {
-        xs[k] = (skip && pok && t0 + ly + 4 * k < p.T)
-                    ? __ldg(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep)
-                    : make_float2(0.f, 0.f);
-        if (cj_x) xs[k].y = -xs[k].y;
+        xs[k] = (skip && pok && t0 + ly + 8 * k < p.T)
+                    ? __ldg(reinterpret_cast<const float4*>(reinterpret_cast<const float2*>(p.x) + yoff + k * ystep))
+                    : make_float4(0.f, 0.f, 0.f, 0.f);
+        if (cj_x) {
+            xs[k].y = -xs[k].y;
+            xs[k].w = -xs[k].w;
+        }
     }
     {
         wait_bar(&mbar[2]);
@@ -1433,12 +1439,15 @@ __global__ void __launch_bounds__(h16::NT, SPLIT ? 1 : 3) fused_chunk_kernel_h16
     __syncthreads();
     {
         const float ysign = (mode & kFwdConjY) ? -1.f : 1.f;
-        const float* stage = reinterpret_cast<const float*>(smem) + ly * STAGE_LD + py;
+        const float* stage = reinterpret_cast<const float*>(smem) + ly * STAGE_LD + 2 * pp;
 #pragma unroll
         for (int k = 0; k < YI; ++k) {
-            if (pok && t0 + ly + 4 * k < p.T) {
-                const float yr = stage[4 * k * STAGE_LD], yi = stage[CH * STAGE_LD + 4 * k * STAGE_LD];
-                p.y[yoff + k * ystep] = make_float2(fmaf(Dh, xs[k].x, yr), ysign * fmaf(Dh, xs[k].y, yi));
+            if (pok && t0 + ly + 8 * k < p.T) {
+                const float* st = stage + 8 * k * STAGE_LD;
+                const float yr0 = st[0], yr1 = st[1], yi0 = st[CH * STAGE_LD], yi1 = st[CH * STAGE_LD + 1];
+                *reinterpret_cast<float4*>(p.y + yoff + k * ystep) =
+                    make_float4(fmaf(Dh, xs[k].x, yr0), ysign * fmaf(Dh, xs[k].y, yi0), fmaf(Dh, xs[k].z, yr1),
+                                ysign * fmaf(Dh, xs[k].w, yi1));
             }
         }
     }
